@@ -1,0 +1,389 @@
+"""Benchmark: ConvTranspose3d + fused epilogue, useful TFLOP/s and ms/forward on GB300.
+
+One step = one pass of the whole hot path over one batch: weight pack/split,
+input staging, the implicit-GEMM kernel with its fused epilogue, statistics
+finalisation and (GroupNorm) the normalise pass -- every kernel of
+convt3d_pack_weights + convt3d_forward.  Inputs are resident in HBM; L2 is
+flushed (a 256 MiB write) before every timed step.  Each step is timed with
+CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--precision 3xtf32|ffma] [--impl gpu|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the path shards by batch with no collective on the data path);
+`value` is the useful flop of all ranks over the slowest rank's time.
+`--impl reference` times the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = workloads.GN.name
+TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 / BF16 tensor rates (GB300)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP32_FMA_PER_CLK_PER_SM = 128
+SMS = 152
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.BY_NAME))
+    ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "ffma"])
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the CPU baseline sample")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "sm_max_mhz": float(p.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu = str(gpu_id)
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", self.gpu], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "power": float(f[3]),
+                             "hw": f[5], "hw_thermal": f[6], "sw_thermal": f[7], "sw_power": f[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        peak_power = max(r["power"] for r in rows)
+        loaded = [r for r in rows if r["power"] >= 0.5 * peak_power] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded), "power_w_max": peak_power}
+
+
+# ------------------------------------------------------- traffic from ncu ----
+
+def kernel_source_sha(precision):
+    src = "tc.cu" if precision == "3xtf32" else "ffma.cu"
+    path = os.path.join(ROOT, "transposed_convolution_convt3d_gb300", "csrc", src)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(precision, workload):
+    """DRAM bytes per launch of the main kernel from a committed ncu summary, if the
+    summary was taken on the current kernel source (else None)."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    want = kernel_source_sha(precision)
+    for name in sorted(os.listdir(d)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        text = open(os.path.join(d, name)).read()
+        m_sha = re.search(r"kernel_source_sha\s*[:=]\s*([0-9a-f]{16})", text)
+        m_w = re.search(r"workload\s*[:=]\s*(\S+)", text)
+        m_t = re.search(r"traffic_bytes_per_launch\s*[:=]\s*([0-9.eE+]+)", text)
+        m_p = re.search(r"precision\s*[:=]\s*(\S+)", text)
+        if m_sha and m_t and m_w and m_sha.group(1) == want and m_w.group(1) == workload and \
+                (not m_p or m_p.group(1) == precision):
+            return float(m_t.group(1))
+    return None
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def cpu_oracle_sample(spec, inputs, target_s, max_samples=None):
+    """Time the oracle on a bounded sample of the batch: whole samples of the
+    per-sample epilogues (for BatchNorm the first n samples form a smaller
+    batch).  Returns (useful TFLOP/s, seconds, samples, cores)."""
+    import oracle
+    f = lambda t: None if t is None else t.numpy()  # noqa: E731
+    done, elapsed, n = 0, 0.0, 0
+    limit = spec.N if max_samples is None else min(spec.N, max_samples)
+    step = 1
+    while n < limit:
+        m = min(step, limit - n)
+        sub = workloads.sample_slice(inputs, n, n + m)
+        s = spec.replace(N=m)
+        t0 = time.perf_counter()
+        oracle.forward(f(sub["x"]), f(sub["w"]), f(sub["bias"]), stride=s.stride, pad=s.pad, out_pad=s.out_pad,
+                       epilogue=s.epilogue, groups=s.groups, eps=s.eps, scale=s.scale, gamma=f(sub["gamma"]),
+                       beta=f(sub["beta"]))
+        elapsed += time.perf_counter() - t0
+        done += s.useful_flop()
+        n += m
+        if elapsed >= target_s:
+            break
+    return done / elapsed / 1e12, elapsed, n, oracle.num_threads()
+
+
+def run_reference(args, spec):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inputs = workloads.make_inputs(spec)
+    f = lambda t: None if t is None else t.numpy()  # noqa: E731
+    sub = workloads.sample_slice(inputs, 0, 1)
+    s = spec.replace(N=1)
+
+    def step():
+        oracle.forward(f(sub["x"]), f(sub["w"]), f(sub["bias"]), stride=s.stride, pad=s.pad, out_pad=s.out_pad,
+                       epilogue=s.epilogue, groups=s.groups, eps=s.eps, scale=s.scale, gamma=f(sub["gamma"]),
+                       beta=f(sub["beta"]))
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = s.useful_flop() / dt / 1e12
+    sample = f"1 of {spec.N} batch samples per step ({s.useful_flop():.3e} useful flop)"
+    line = {
+        "impl": "reference", "metric": "useful_tflops", "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "sample": sample, "oracle": "CPU scatter-form fp64 loop nest (OpenMP)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU ----
+
+def run_gpu(args, spec):
+    import torch
+    import torch.distributed as dist
+
+    from transposed_convolution_convt3d_gb300 import PREC_3XTF32, PREC_FFMA, Plan
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    prec = PREC_3XTF32 if args.precision == "3xtf32" else PREC_FFMA
+
+    inputs = workloads.make_inputs(spec)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inputs.items()}
+    plan = Plan.from_spec(spec, precision=prec)
+    info = plan.info
+    ws = plan.new_workspace(dev)
+    y = plan.new_output(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        plan.pack_weights(d["w"], ws, stream)
+        plan.forward(d["x"], y, ws, d["bias"], d["gamma"], d["beta"], stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    plan.check(ws, stream)
+    torch.cuda.synchronize()
+
+    plan.profile_enable(True)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    step_ms, gemm_ms = [], []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))  # evict x, y and the packed weights from L2 between steps
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        gemm_ms.append(plan.profile_read())  # synchronises on the GEMM's end event
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    plan.profile_enable(False)
+    plan.check(ws, stream)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    useful = spec.useful_flop()
+    value = useful * world / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {k: (v.pin_memory() if v is not None else None) for k, v in inputs.items()}
+        y_host = torch.empty(plan.out_shape, dtype=torch.float32).pin_memory()
+        h2d = sum(v.numel() * 4 for v in host.values() if v is not None)
+        d2h = y_host.numel() * 4
+        e2e_ms = []
+        for i in range(args.e2e_steps + 1):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k, v in host.items():
+                if v is not None:
+                    d[k].copy_(v, non_blocking=True)
+            step()
+            y_host.copy_(y, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i > 0:
+                e2e_ms.append(a.elapsed_time(b))
+        e2e_t = sum(e2e_ms) / len(e2e_ms)
+        if world > 1:
+            t = torch.tensor([e2e_t], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_t = float(t.item())
+        e2e = {"value": useful * world / (e2e_t * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_t,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    gemm_avg = sum(gemm_ms) / len(gemm_ms)
+    if prec == PREC_3XTF32:
+        peak = pk["bf16_tflops"] * TF32_OVER_BF16
+        achieved = useful / (gemm_avg * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{pk['source']} bf16 burst x nominal TF32/BF16 ratio {TF32_OVER_BF16:.4f}",
+                "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak,
+                "frac_of_3xtf32_peak": achieved / (peak / 3.0)}
+    else:
+        peak = SMS * FP32_FMA_PER_CLK_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+        achieved = useful / (gemm_avg * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 flop x max SM clock",
+                "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak}
+    roof["kernel"] = "convt3d_tc_gemm" if prec == PREC_3XTF32 else "ffma_conv_kernel"
+    roof["kernel_ms"] = gemm_avg
+    roof["kernel_share_of_step"] = gemm_avg / ms_per_step
+    roof["traffic"] = committed_traffic(args.precision, spec.name)
+    roof["min_bytes"] = info["gemm_min_bytes"]
+    hbm_frac = info["forward_min_bytes"] / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"]
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, secs, nsamp, cores = cpu_oracle_sample(spec, inputs, args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{nsamp} of {spec.N} batch samples ({secs:.1f} s)"}
+
+    line = {
+        "metric": "useful_tflops", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": spec.name, "precision": args.precision, "x": [spec.N, spec.Cin, spec.D, spec.H, spec.W],
+                   "w": [spec.Cin, spec.Cout, spec.k, spec.k, spec.k], "stride": spec.stride, "pad": spec.pad,
+                   "out_pad": spec.out_pad, "out": list(plan.out_shape), "epilogue": spec.epilogue,
+                   "step": "pack_weights + forward (all kernels)", "l2": "flushed (256 MiB write) before each step",
+                   "useful_flop_per_step": useful, "parallelism": f"replicas x{world}"},
+        "hbm_frac_whole_step": hbm_frac,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": (info["launches_per_forward"] + info["launches_per_pack"]) * args.steps,
+        "clocks": clk,
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    spec = workloads.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, spec)
+    else:
+        run_gpu(args, spec)
+
+
+if __name__ == "__main__":
+    main()

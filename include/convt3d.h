@@ -1,0 +1,181 @@
+/*
+ * convt3d -- dense fp32 3-D transposed convolution with fused epilogues for
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation (the three POPCORNBENCH "Kimi-K2.6" transcript pages
+ * l2_p77, l2_p61 and l2_p49; each page's opening problem statement and its
+ * derivation of the transposed-convolution index mapping):
+ *
+ *   Y[n,co,od,oh,ow] = bias[co] + sum over ci, kd, kh, kw of
+ *                      x[n,ci,id,ih,iw] * w[ci,co,kd,kh,kw]
+ *   where od = id*stride - pad + kd (likewise oh, ow), restricted to
+ *   0 <= od < Do, and Do = (Din - 1)*stride - 2*pad + k + out_pad.
+ *
+ * followed by one epilogue:
+ *   IDENTITY                  y = Y                                     (no page; bare op)
+ *   RELU_GROUPNORM            v = max(Y,0); GroupNorm(groups) with biased
+ *                             variance over (channels of the group, all
+ *                             positions) per sample; affine gamma/beta    (page l2_p61)
+ *   SCALE_BATCHNORM_AVGPOOL   z = scale*Y; BatchNorm3d with batch statistics
+ *                             (biased variance over n and positions, per
+ *                             channel); affine; mean over positions
+ *                             -> [N, Cout, 1, 1, 1]                       (page l2_p77)
+ *   SOFTMAX_SIGMOID           softmax over channels, then elementwise
+ *                             sigmoid                                     (page l2_p49)
+ *
+ * Computation: an output-stationary implicit GEMM, M = output positions,
+ * N = Cout, K = Cin x taps.  Stride 2 is split into the 8 output-parity
+ * classes, each a dense stride-1 correlation over only the taps that reach
+ * it, so no zero-inserted taps are multiplied.  CONVT3D_PREC_3XTF32 runs the
+ * products on the tcgen05 tensor cores in split TF32 (a_hi*b_hi + a_hi*b_lo +
+ * a_lo*b_hi, fp32 accumulation); CONVT3D_PREC_FFMA runs them as fp32 FMAs on
+ * the CUDA cores (kept as an ablation).
+ *
+ * Conventions for every entry point:
+ *   - Layouts: x [N,Cin,Din,Hin,Win], y [N,Cout,Do,Ho,Wo] (BN+pool: [N,Cout]),
+ *     w [Cin,Cout,k,k,k] (PyTorch ConvTranspose3d), bias/gamma/beta [Cout];
+ *     all fp32, contiguous, device memory, 16-byte aligned.
+ *   - Ownership: the caller allocates and owns every device buffer (input,
+ *     output, workspace).  The library never allocates or frees device memory
+ *     and never synchronises a stream except in convt3d_check and
+ *     convt3d_profile_read.  A plan owns host metadata only.
+ *   - Streams: `stream` is a cudaStream_t (NULL = legacy default stream); all
+ *     device work of a call is issued on it, in order.
+ *   - Errors: a status code is returned, never an exception.  Arguments and
+ *     shapes are validated on the host before anything is launched; nothing is
+ *     launched when validation fails.  A failed launch returns
+ *     CONVT3D_ERR_CUDA (convt3d_last_error gives the CUDA message).  Device-side
+ *     conditions (a bounded wait that ran out) are recorded in the workspace
+ *     and reported by convt3d_check.
+ *   - y must not alias x.  Results are bitwise reproducible run to run (no
+ *     floating-point atomics).
+ */
+#ifndef CONVT3D_H
+#define CONVT3D_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CONVT3D_EPI_IDENTITY = 0,
+    CONVT3D_EPI_RELU_GROUPNORM = 1,
+    CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL = 2,
+    CONVT3D_EPI_SOFTMAX_SIGMOID = 3
+} convt3d_epilogue_t;
+
+typedef enum {
+    CONVT3D_PREC_3XTF32 = 0, /* tcgen05 tensor cores, split TF32 (default)  */
+    CONVT3D_PREC_FFMA = 1    /* CUDA-core fp32 FMA implicit GEMM (ablation) */
+} convt3d_precision_t;
+
+typedef enum {
+    CONVT3D_OK = 0,
+    CONVT3D_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, misaligned buffer       */
+    CONVT3D_ERR_UNSUPPORTED = 2,   /* valid operation outside what this build runs    */
+    CONVT3D_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than workspace_bytes  */
+    CONVT3D_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed                */
+    CONVT3D_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out (check only)  */
+    CONVT3D_ERR_DEVICE_ASSERT = 6, /* a device-side consistency check failed           */
+    CONVT3D_ERR_NOT_PACKED = 7     /* forward before pack_weights on this workspace    */
+} convt3d_status_t;
+
+/* Problem description.  Enumerations are carried as int for a stable ABI. */
+typedef struct {
+    int N, Cin, Cout;     /* batch, input channels, output channels (>= 1)             */
+    int Din, Hin, Win;    /* input extent (>= 1)                                        */
+    int k;                /* cubic kernel size, 1..7                                    */
+    int stride;           /* 1 or 2                                                     */
+    int pad;              /* 0 <= pad < k                                               */
+    int out_pad;          /* 0 <= out_pad < stride                                      */
+    int has_bias;         /* bias pointer is read iff non-zero                          */
+    int epilogue;         /* convt3d_epilogue_t                                         */
+    int groups;           /* GroupNorm groups; Cout % groups == 0 (RELU_GROUPNORM only) */
+    float eps;            /* GroupNorm / BatchNorm epsilon (> 0)                        */
+    float scale;          /* multiplier before BatchNorm (SCALE_BATCHNORM_AVGPOOL)      */
+    int precision;        /* convt3d_precision_t                                        */
+} convt3d_desc_t;
+
+typedef struct convt3d_plan_s *convt3d_plan_t;
+
+/* Plan facts, for callers that report or size things. */
+typedef struct {
+    int64_t out_shape[5];        /* y shape ([N,Cout,1,1,1] for BN+pool)                */
+    int num_classes;             /* stride^3 output-parity classes                      */
+    int64_t gemm_m;              /* output positions (N*Do*Ho*Wo)                        */
+    int64_t gemm_n;              /* Cout                                                */
+    int64_t gemm_k_total;        /* sum over classes of Cin * taps(class)                */
+    int64_t tiles;               /* GEMM output tiles per forward                        */
+    int tile_m;                  /* output positions per tile                            */
+    int launches_per_forward;    /* kernels convt3d_forward launches                     */
+    int launches_per_pack;       /* kernels convt3d_pack_weights launches                */
+    double useful_flop;          /* 2*N*Cout*Cin*k^3*Din*Hin*Win                         */
+    double issued_mma_flop;      /* tensor/FMA flop the main kernel issues per forward   */
+    double gemm_min_bytes;       /* algorithmic HBM bytes of the main kernel             */
+    double forward_min_bytes;    /* algorithmic HBM bytes of the whole forward           */
+} convt3d_info_t;
+
+/* Validate `desc` and build a plan (host only: no CUDA call, no GPU needed).
+ * Returns INVALID_ARG for malformed descriptions, UNSUPPORTED for valid ones
+ * this build does not run (for example 3XTF32 with Cout > 256).  *out is set
+ * to NULL on failure. */
+convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t *out);
+
+/* Release a plan (NULL is ignored). */
+void convt3d_plan_destroy(convt3d_plan_t plan);
+
+/* Output shape: [N,Cout,Do,Ho,Wo], or [N,Cout,1,1,1] for BN+pool. Host only. */
+convt3d_status_t convt3d_output_shape(convt3d_plan_t plan, int64_t shape[5]);
+
+/* Plan facts (see convt3d_info_t). Host only. */
+convt3d_status_t convt3d_plan_info(convt3d_plan_t plan, convt3d_info_t *info);
+
+/* Bytes of device workspace the caller must provide to pack_weights and
+ * forward (packed weights, the staged split input, statistics partials and a
+ * status word).  0 on a NULL plan.  Host only. */
+size_t convt3d_workspace_bytes(convt3d_plan_t plan);
+
+/* Re-lay the weight w [Cin,Cout,k,k,k] into the workspace: per parity class
+ * and tap, Cout rows by Cin columns, split into TF32 hi and lo planes
+ * (3XTF32) or kept fp32 (FFMA).  Call whenever w changes; forward reads only
+ * the packed copy.  Also clears the workspace status word.  Asynchronous on
+ * `stream`. */
+convt3d_status_t convt3d_pack_weights(convt3d_plan_t plan, const float *w, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* One forward pass: y = epilogue(convT(x, w) + bias).  bias may be NULL when
+ * has_bias is 0; gamma/beta are required for RELU_GROUPNORM and
+ * SCALE_BATCHNORM_AVGPOOL and ignored otherwise.  Uses the weights packed by
+ * the last convt3d_pack_weights on the same workspace.  Asynchronous on
+ * `stream`; y is complete when the stream reaches this point. */
+convt3d_status_t convt3d_forward(convt3d_plan_t plan, const float *x, const float *bias,
+                                 const float *gamma, const float *beta, float *y,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream`, read and clear the workspace status word: returns OK,
+ * TIMEOUT (a device-side bounded wait ran out) or DEVICE_ASSERT. */
+convt3d_status_t convt3d_check(convt3d_plan_t plan, void *workspace, void *stream);
+
+/* Optional timing of the main GEMM kernel: when enabled, forward records two
+ * CUDA events on `stream` around that launch; profile_read synchronises on
+ * the second and returns the elapsed milliseconds of the last forward. */
+convt3d_status_t convt3d_profile_enable(convt3d_plan_t plan, int enable);
+convt3d_status_t convt3d_profile_read(convt3d_plan_t plan, float *gemm_ms);
+
+/* Static text for a status code. */
+const char *convt3d_status_string(convt3d_status_t status);
+
+/* Detail of the most recent failure in this thread (empty string if none). */
+const char *convt3d_last_error(void);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int convt3d_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVT3D_H */

@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and validates descriptions on the host (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import workloads
+from transposed_convolution_convt3d_gb300 import _lib
+from transposed_convolution_convt3d_gb300 import build as libbuild
+from transposed_convolution_convt3d_gb300.api import Plan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "convt3d.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(convt3d_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in _lib.STATUS:
+        assert lib.convt3d_status_string(code)
+    assert lib.convt3d_version() >= 100
+
+
+def make_desc(**kw):
+    base = dict(N=2, Cin=8, Cout=16, Din=8, Hin=8, Win=8, k=3, stride=1, pad=0, out_pad=0, has_bias=0,
+                epilogue=0, groups=1, eps=1e-5, scale=1.0, precision=0)
+    base.update(kw)
+    return _lib.Desc(*[base[f] for f, _ in _lib.Desc._fields_])
+
+
+def create(lib, **kw):
+    d = make_desc(**kw)
+    h = ctypes.c_void_p()
+    st = lib.convt3d_plan_create(ctypes.byref(d), ctypes.byref(h))
+    return st, h
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=0), 1), (dict(Cin=0), 1), (dict(k=0), 1), (dict(stride=0), 1), (dict(pad=-1), 1),
+    (dict(out_pad=1, stride=1), 1), (dict(epilogue=9), 1), (dict(precision=5), 1),
+    (dict(epilogue=1, groups=3), 1), (dict(epilogue=1, groups=4, eps=0.0), 1),
+    (dict(Din=1, Hin=1, Win=1, k=1, pad=1), 1),
+    (dict(stride=3, k=3), 2), (dict(k=8), 2), (dict(Cout=257), 2), (dict(k=3, pad=3, Din=9, Hin=9, Win=9), 2),
+    (dict(stride=2, k=3, pad=1, Cout=144), 2), (dict(stride=2, k=1), 2),
+])
+def test_plan_validation(lib, kw, status):
+    st, h = create(lib, **kw)
+    assert st == status, lib.convt3d_last_error()
+    assert not h.value
+    assert lib.convt3d_last_error()
+
+
+def test_ffma_accepts_what_tensor_path_rejects(lib):
+    st, h = create(lib, stride=2, k=3, pad=1, Cout=144, precision=1)
+    assert st == 0
+    lib.convt3d_plan_destroy(h)
+
+
+@pytest.mark.parametrize("spec", workloads.ALL, ids=lambda s: s.name)
+@pytest.mark.parametrize("precision", [0, 1])
+def test_plan_facts_for_workloads(lib, spec, precision):
+    p = Plan.from_spec(spec, precision=precision)
+    dims = [oracle.output_size(v, spec.k, spec.stride, spec.pad, spec.out_pad) for v in (spec.D, spec.H, spec.W)]
+    if spec.epilogue == workloads.EPI_SCALE_BATCHNORM_AVGPOOL:
+        assert p.out_shape == (spec.N, spec.Cout, 1, 1, 1)
+    else:
+        assert p.out_shape == (spec.N, spec.Cout, *dims)
+    assert p.workspace_bytes > 0
+    assert p.info["useful_flop"] == spec.useful_flop()
+    assert p.info["gemm_m"] == spec.N * dims[0] * dims[1] * dims[2]
+    assert p.info["num_classes"] == spec.stride ** 3
+    # K summed over parity classes covers every tap exactly once
+    assert p.info["gemm_k_total"] == spec.Cin * spec.k ** 3
+    assert p.info["issued_mma_flop"] >= p.info["useful_flop"] * (3 if precision == 0 else 1) * 0.9
+
+
+def test_parity_classes_tile_every_output_once(lib):
+    # 3-D outputs with odd extents: per-class q-grids must partition the output grid
+    for (D, k, s, p, op) in [(5, 3, 2, 1, 0), (6, 4, 2, 1, 1), (4, 5, 1, 2, 0), (3, 3, 2, 0, 1)]:
+        pl = Plan(1, 4, 16, D, D + 1, D + 2, k, s, p, op, precision=1)
+        Do, Ho, Wo = pl.out_shape[2:]
+        covered = 0
+        for rd in range(s):
+            for rh in range(s):
+                for rw in range(s):
+                    covered += len(range(rd, Do, s)) * len(range(rh, Ho, s)) * len(range(rw, Wo, s))
+        assert covered == Do * Ho * Wo
+        assert pl.info["tiles"] >= -(-Do * Ho * Wo // 64)
+
+
+def test_host_validation_before_any_launch(lib):
+    st, h = create(lib)
+    assert st == 0
+    try:
+        V = ctypes.c_void_p
+        # NULL weight / workspace / x: rejected on the host, nothing is launched
+        assert lib.convt3d_pack_weights(h, None, V(1 << 20), 1 << 30, None) == 1
+        assert lib.convt3d_pack_weights(h, V(1 << 20), None, 1 << 30, None) == 3
+        assert lib.convt3d_pack_weights(h, V(1 << 20), V(1 << 20), 16, None) == 3
+        assert lib.convt3d_forward(h, None, None, None, None, V(1 << 20), V(1 << 20), 1 << 30, None) == 1
+        # misaligned buffers
+        assert lib.convt3d_forward(h, V((1 << 20) + 4), None, None, None, V(1 << 21), V(1 << 22), 1 << 30, None) == 1
+        # forward before pack_weights on this workspace
+        assert lib.convt3d_forward(h, V(1 << 20), None, None, None, V(1 << 21), V(1 << 22), 1 << 30, None) == 7
+        # profile_read without a profiled forward
+        ms = ctypes.c_float()
+        assert lib.convt3d_profile_read(h, ctypes.byref(ms)) == 1
+    finally:
+        lib.convt3d_plan_destroy(h)
+
+
+def test_groupnorm_requires_affine(lib):
+    st, h = create(lib, epilogue=1, groups=4)
+    assert st == 0
+    try:
+        V = ctypes.c_void_p
+        assert lib.convt3d_forward(h, V(1 << 20), None, None, None, V(1 << 21), V(1 << 22), 1 << 30, None) == 1
+    finally:
+        lib.convt3d_plan_destroy(h)

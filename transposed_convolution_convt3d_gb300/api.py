@@ -1,0 +1,121 @@
+"""PyTorch-facing binding of the convt3d C ABI.
+
+Argument marshalling only: tensors are checked, their device pointers and the
+current CUDA stream are handed to libconvt3d, and every step of the
+computation runs in the library's kernels.  PyTorch supplies device memory and
+streams.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (EPI_IDENTITY, EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL,  # noqa: F401
+                   EPI_SOFTMAX_SIGMOID, PREC_3XTF32, PREC_FFMA, Convt3dError)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Plan:
+    """A validated problem description (host-only; creating one needs no GPU)."""
+
+    def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
+                 epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32):
+        self.lib = _lib.load()
+        self.desc = _lib.Desc(N, Cin, Cout, D, H, W, k, stride, pad, out_pad, int(bool(bias)),
+                              int(epilogue), int(groups), float(eps), float(scale), int(precision))
+        h = ctypes.c_void_p()
+        _lib.check(self.lib.convt3d_plan_create(ctypes.byref(self.desc), ctypes.byref(h)), self.lib)
+        self.handle = h
+        shp = (ctypes.c_int64 * 5)()
+        _lib.check(self.lib.convt3d_output_shape(self.handle, shp), self.lib)
+        self.out_shape = tuple(int(v) for v in shp)
+        self.workspace_bytes = int(self.lib.convt3d_workspace_bytes(self.handle))
+        inf = _lib.Info()
+        _lib.check(self.lib.convt3d_plan_info(self.handle, ctypes.byref(inf)), self.lib)
+        self.info = {f: (tuple(getattr(inf, f)) if f == "out_shape" else getattr(inf, f))
+                     for f, _ in _lib.Info._fields_}
+
+    @classmethod
+    def from_spec(cls, spec, precision=PREC_3XTF32):
+        return cls(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
+                   spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, precision)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            self.lib.convt3d_plan_destroy(h)
+            self.handle = None
+
+    # -- device buffers --------------------------------------------------
+    def new_workspace(self, device="cuda"):
+        # 256-byte alignment: the caching allocator hands out 512-byte aligned blocks
+        return torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=device)
+
+    def new_output(self, device="cuda"):
+        return torch.empty(self.out_shape, dtype=torch.float32, device=device)
+
+    @staticmethod
+    def _dev(t, name):
+        if t is None:
+            return None
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
+        return t
+
+    # -- library calls ---------------------------------------------------
+    def pack_weights(self, w, workspace, stream=None):
+        self._dev(w, "w")
+        _lib.check(self.lib.convt3d_pack_weights(self.handle, _ptr(w), _ptr(workspace),
+                                                 workspace.numel(), _stream(stream)), self.lib)
+
+    def forward(self, x, y, workspace, bias=None, gamma=None, beta=None, stream=None):
+        for t, n in ((x, "x"), (y, "y"), (bias, "bias"), (gamma, "gamma"), (beta, "beta")):
+            self._dev(t, n)
+        if tuple(y.shape) != self.out_shape and y.numel() != _numel(self.out_shape):
+            raise ValueError(f"y has shape {tuple(y.shape)}, expected {self.out_shape}")
+        _lib.check(self.lib.convt3d_forward(self.handle, _ptr(x), _ptr(bias), _ptr(gamma), _ptr(beta),
+                                            _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
+                   self.lib)
+        return y
+
+    def check(self, workspace, stream=None):
+        _lib.check(self.lib.convt3d_check(self.handle, _ptr(workspace), _stream(stream)), self.lib)
+
+    def profile_enable(self, on=True):
+        _lib.check(self.lib.convt3d_profile_enable(self.handle, int(bool(on))), self.lib)
+
+    def profile_read(self) -> float:
+        ms = ctypes.c_float()
+        _lib.check(self.lib.convt3d_profile_read(self.handle, ctypes.byref(ms)), self.lib)
+        return float(ms.value)
+
+
+def _numel(shape):
+    n = 1
+    for v in shape:
+        n *= v
+    return n
+
+
+def convt3d(x, w, bias=None, *, stride=1, pad=0, out_pad=0, epilogue=EPI_IDENTITY, groups=1, eps=1e-5,
+            scale=1.0, gamma=None, beta=None, precision=PREC_3XTF32):
+    """One-shot convenience: plan, pack, forward on the current stream; returns y."""
+    N, Cin, D, H, W = x.shape
+    Cout, k = w.shape[1], w.shape[2]
+    plan = Plan(N, Cin, Cout, D, H, W, k, stride, pad, out_pad, bias is not None, epilogue, groups, eps, scale,
+                precision)
+    ws = plan.new_workspace(x.device)
+    y = plan.new_output(x.device)
+    plan.pack_weights(w, ws)
+    plan.forward(x, y, ws, bias, gamma, beta)
+    return y

@@ -1,0 +1,119 @@
+// Internal definitions shared by the host plan and the kernels of libconvt3d.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "convt3d.h"
+
+namespace convt3d {
+
+constexpr int kMaxClasses = 8;   // stride <= 2  ->  at most 2^3 output-parity classes
+constexpr int kMaxGroups = 8;
+constexpr int kMaxTaps = 343;    // k <= 7
+constexpr int kFfmaTileM = 64;   // output positions per FFMA tile
+constexpr int kTcTileM = 128;    // output positions per tensor-core tile (TMEM lanes)
+constexpr int kTcChunk = 32;     // input channels per K step of the tensor-core path (128 B)
+
+// Status word layout at the start of the workspace.
+enum : uint32_t { kErrNone = 0, kErrTimeout = 1, kErrAssert = 2 };
+constexpr size_t kStatusBytes = 256;
+
+// One tap of a parity class: input offset along each dimension
+// (i = q + delta) and the flat index kd*k*k + kh*k + kw into the weight.
+struct TapDesc {
+    int8_t dd, dh, dw, pad_;
+    int16_t widx, pad2_;
+};
+
+// One output-parity class: output positions o = stride*q + r per dimension,
+// q in [0, Q).  Its taps are taps[tap_begin .. tap_begin + ntaps).
+struct ClassDesc {
+    int rd, rh, rw;
+    int Qd, Qh, Qw;
+    int ntaps, tap_begin;
+    int lo_d, lo_h, lo_w;   // smallest delta per dimension
+    int nt_d, nt_h, nt_w;   // taps per dimension
+};
+
+// A unit of GEMM work: one class (FFMA, or stride 1), or the two classes
+// differing only in w-parity (tensor-core path, stride 2), enumerated over a
+// common q-grid of Qd x Qh x Qw positions per sample.
+struct GroupDesc {
+    int ncls;
+    int cls[2];
+    int Qd, Qh, Qw;
+    int vol;                // Qd*Qh*Qw
+    int tiles;              // tiles per sample
+    int tile_prefix;        // tiles of earlier groups within one sample
+    int ksteps;             // K steps per tile (all classes of the group)
+};
+
+struct Geometry {
+    int N, Cin, Cout, Din, Hin, Win, k, stride, pad, out_pad;
+    int Do, Ho, Wo;
+    int nclasses;
+    int ntaps;
+    ClassDesc cls[kMaxClasses];
+    TapDesc taps[kMaxTaps];
+};
+
+// Parameters of the FFMA implicit-GEMM kernel (passed by value).
+struct FfmaParams {
+    const float *x;
+    const float *wpk;       // [ntaps][cin_pad][cout_pad]
+    const float *bias;
+    float *y;
+    double *partials;
+    int N, Cin, cin_pad, Cout, cout_pad, Din, Hin, Win, Do, Ho, Wo, stride;
+    int epilogue, groups;
+    float scale;
+    int ngroups, tiles_per_sample;
+    GroupDesc grp[kMaxGroups];
+    ClassDesc cls[kMaxClasses];
+    TapDesc taps[kMaxTaps];
+};
+
+}  // namespace convt3d
+
+struct convt3d_plan_s {
+    convt3d_desc_t d;
+    convt3d::Geometry g;
+    int tc;                 // 1: tensor-core path, 0: FFMA
+    int cin_pad, cout_pad;
+    int tile_m;
+    int ngroups;
+    convt3d::GroupDesc grp[convt3d::kMaxGroups];
+    int tiles_per_sample;
+    int64_t tiles;
+    // workspace layout (byte offsets, 256-aligned)
+    size_t off_wpk_hi, off_wpk_lo, off_xs_hi, off_xs_lo, off_partials, off_stats, ws_total;
+    size_t wpk_elems, xs_elems, partial_doubles, stat_doubles;
+    // GEMM timing
+    int prof_enabled;
+    int prof_valid;
+    cudaEvent_t ev0, ev1;
+    int ev_created;
+    const void *packed_ws;  // workspace that pack_weights last filled for this plan
+};
+
+// Kernel launchers (defined in the .cu files); each returns cudaGetLastError().
+namespace convt3d {
+cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *hi, float *lo,
+                                int kmajor, cudaStream_t s);
+cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *hi, float *lo,
+                               cudaStream_t s);
+cudaError_t launch_ffma(const convt3d_plan_s &p, const float *x, const float *wpk, const float *bias,
+                        float *y, double *partials, cudaStream_t s);
+cudaError_t launch_tc(const convt3d_plan_s &p, const float *xs_hi, const float *xs_lo,
+                      const float *w_hi, const float *w_lo, const float *bias, float *y,
+                      double *partials, uint32_t *status, cudaStream_t s);
+cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, double *stats,
+                               cudaStream_t s);
+cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, const float *gamma,
+                                const float *beta, float *y, cudaStream_t s);
+cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, double *sums,
+                               const float *gamma, const float *beta, float *y, cudaStream_t s);
+int tc_launches_per_forward(const convt3d_plan_s &p);
+}  // namespace convt3d

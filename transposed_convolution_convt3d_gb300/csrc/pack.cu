@@ -1,0 +1,114 @@
+// Weight re-layout and input staging.
+//
+// The weight of a ConvTranspose3d is [Cin, Cout, k, k, k] (PyTorch layout,
+// as on all three transcript pages); page l2_p49 notes the Cin stride makes
+// per-Cout access strided and re-lays it per output channel.  Here the
+// weight is re-laid per parity class and tap:
+//   tensor-core path: [tap][Cout_pad][Cin_pad] (K-major rows, Cin contiguous),
+//                     split into TF32 hi and lo planes;
+//   FFMA path:        [tap][Cin_pad][Cout_pad] fp32.
+// The tensor-core path also stages x from NCDHW into channels-last
+// [N][D][H][W][Cin_pad] hi/lo planes, the layout its TMA im2col loads read.
+#include "convt3d_internal.h"
+
+namespace convt3d {
+namespace {
+
+// Split v into a TF32-exact head (low 13 mantissa bits cleared) and the
+// exact fp32 remainder: v == hi + lo, |lo| < 2^-10 |v|.
+__device__ __forceinline__ void split_tf32(float v, float &hi, float &lo) {
+    hi = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+    lo = v - hi;
+}
+
+struct TapIndex {
+    int16_t widx[kMaxTaps];
+};
+
+__global__ void pack_weights_kernel(const float *__restrict__ w, float *__restrict__ hi,
+                                    float *__restrict__ lo, int Cin, int Cout, int k3, int ntaps,
+                                    int cin_pad, int cout_pad, int kmajor,
+                                    const __grid_constant__ TapIndex taps) {
+    const int64_t total = (int64_t)ntaps * cin_pad * cout_pad;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int j, ci, co;
+        if (kmajor) {  // [tap][co][ci]
+            ci = (int)(i % cin_pad);
+            co = (int)((i / cin_pad) % cout_pad);
+            j = (int)(i / ((int64_t)cin_pad * cout_pad));
+        } else {       // [tap][ci][co]
+            co = (int)(i % cout_pad);
+            ci = (int)((i / cout_pad) % cin_pad);
+            j = (int)(i / ((int64_t)cin_pad * cout_pad));
+        }
+        float v = 0.0f;
+        if (ci < Cin && co < Cout) v = w[((int64_t)ci * Cout + co) * k3 + taps.widx[j]];
+        if (lo) {
+            float h, l;
+            split_tf32(v, h, l);
+            hi[i] = h;
+            lo[i] = l;
+        } else {
+            hi[i] = v;
+        }
+    }
+}
+
+// NCDHW -> NDHWC(+channel padding) transpose of one sample, 32 positions x
+// 32 channels per block through shared memory; both the global read (along
+// positions) and the write (along channels) are 128-byte rows.
+__global__ void stage_input_kernel(const float *__restrict__ x, float *__restrict__ hi,
+                                   float *__restrict__ lo, int Cin, int cin_pad, int64_t S) {
+    __shared__ float tile[32][33];
+    const int n = blockIdx.z;
+    const int c0 = blockIdx.y * 32;
+    const int64_t s0 = (int64_t)blockIdx.x * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    const float *xn = x + (int64_t)n * Cin * S;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const int c = c0 + ty + j;
+        const int64_t s = s0 + tx;
+        tile[ty + j][tx] = (c < Cin && s < S) ? xn[(int64_t)c * S + s] : 0.0f;
+    }
+    __syncthreads();
+    float *hn = hi + (int64_t)n * S * cin_pad;
+    float *ln = lo + (int64_t)n * S * cin_pad;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const int64_t s = s0 + ty + j;
+        const int c = c0 + tx;
+        if (s < S) {
+            float h, l;
+            split_tf32(tile[tx][ty + j], h, l);
+            hn[s * cin_pad + c] = h;
+            ln[s * cin_pad + c] = l;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *hi, float *lo, int kmajor,
+                                cudaStream_t s) {
+    TapIndex t;
+    for (int j = 0; j < kMaxTaps; ++j) t.widx[j] = j < p.g.ntaps ? p.g.taps[j].widx : 0;
+    const int64_t total = (int64_t)p.g.ntaps * p.cin_pad * p.cout_pad;
+    const int threads = 256;
+    const int blocks = (int)((total + threads - 1) / threads < 4096 ? (total + threads - 1) / threads : 4096);
+    const int k3 = p.g.k * p.g.k * p.g.k;
+    pack_weights_kernel<<<blocks, threads, 0, s>>>(w, hi, lo, p.g.Cin, p.g.Cout, k3, p.g.ntaps, p.cin_pad,
+                                                   p.cout_pad, kmajor, t);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *hi, float *lo, cudaStream_t s) {
+    const int64_t S = (int64_t)p.g.Din * p.g.Hin * p.g.Win;
+    dim3 grid((unsigned)((S + 31) / 32), (unsigned)(p.cin_pad / 32), (unsigned)p.g.N);
+    dim3 block(32, 8);
+    stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S);
+    return cudaGetLastError();
+}
+
+}  // namespace convt3d

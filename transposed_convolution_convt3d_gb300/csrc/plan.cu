@@ -1,0 +1,482 @@
+// Host side of libconvt3d: descriptor validation, the output-parity class
+// decomposition, workspace layout and the C-ABI entry points.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+
+#include "convt3d_internal.h"
+
+using namespace convt3d;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+}
+
+convt3d_status_t fail(convt3d_status_t st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+convt3d_status_t cuda_fail(cudaError_t e, const char *what) {
+    set_error("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    return CONVT3D_ERR_CUDA;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Output extent along one dimension (dilation 1): (in-1)*s - 2p + k + op.
+int64_t out_extent(int64_t in, int k, int s, int p, int op) { return (in - 1) * s - 2 * p + k + op; }
+
+// Output-parity decomposition.  For output index o = s*q + r along one
+// dimension, the taps t that reach it satisfy (r + p - t) = s*delta for an
+// integer delta, and then read input index i = q + delta (the gather form
+// of the index relation od = id*s - p + kd derived on page l2_p49).  For
+// stride 1 there is one class holding all k taps with delta = p - t.
+struct DimTaps {
+    int n;
+    int t[8];
+    int delta[8];
+    int Q;
+};
+
+DimTaps dim_taps(int Dout, int k, int s, int p, int r) {
+    DimTaps d{};
+    for (int t = 0; t < k; ++t) {
+        int num = r + p - t;
+        if (((num % s) + s) % s == 0) {
+            d.t[d.n] = t;
+            d.delta[d.n] = num / s;  // exact division
+            ++d.n;
+        }
+    }
+    d.Q = Dout > r ? (Dout - r + s - 1) / s : 0;
+    return d;
+}
+
+bool build_geometry(const convt3d_desc_t &d, Geometry &g) {
+    memset(&g, 0, sizeof(g));
+    g.N = d.N; g.Cin = d.Cin; g.Cout = d.Cout; g.Din = d.Din; g.Hin = d.Hin; g.Win = d.Win;
+    g.k = d.k; g.stride = d.stride; g.pad = d.pad; g.out_pad = d.out_pad;
+    g.Do = (int)out_extent(d.Din, d.k, d.stride, d.pad, d.out_pad);
+    g.Ho = (int)out_extent(d.Hin, d.k, d.stride, d.pad, d.out_pad);
+    g.Wo = (int)out_extent(d.Win, d.k, d.stride, d.pad, d.out_pad);
+    const int s = d.stride;
+    g.nclasses = s * s * s;
+    int tap = 0;
+    for (int rd = 0; rd < s; ++rd)
+        for (int rh = 0; rh < s; ++rh)
+            for (int rw = 0; rw < s; ++rw) {
+                const int c = (rd * s + rh) * s + rw;
+                DimTaps td = dim_taps(g.Do, d.k, s, d.pad, rd);
+                DimTaps th = dim_taps(g.Ho, d.k, s, d.pad, rh);
+                DimTaps tw = dim_taps(g.Wo, d.k, s, d.pad, rw);
+                ClassDesc &cl = g.cls[c];
+                cl.rd = rd; cl.rh = rh; cl.rw = rw;
+                cl.Qd = td.Q; cl.Qh = th.Q; cl.Qw = tw.Q;
+                cl.nt_d = td.n; cl.nt_h = th.n; cl.nt_w = tw.n;
+                cl.ntaps = td.n * th.n * tw.n;
+                cl.tap_begin = tap;
+                cl.lo_d = cl.lo_h = cl.lo_w = 0;
+                if (td.n) cl.lo_d = *std::min_element(td.delta, td.delta + td.n);
+                if (th.n) cl.lo_h = *std::min_element(th.delta, th.delta + th.n);
+                if (tw.n) cl.lo_w = *std::min_element(tw.delta, tw.delta + tw.n);
+                for (int a = 0; a < td.n; ++a)
+                    for (int b = 0; b < th.n; ++b)
+                        for (int e = 0; e < tw.n; ++e) {
+                            if (tap >= kMaxTaps) return false;
+                            TapDesc &t = g.taps[tap++];
+                            t.dd = (int8_t)td.delta[a];
+                            t.dh = (int8_t)th.delta[b];
+                            t.dw = (int8_t)tw.delta[e];
+                            t.widx = (int16_t)((td.t[a] * d.k + th.t[b]) * d.k + tw.t[e]);
+                        }
+            }
+    g.ntaps = tap;
+    return tap == d.k * d.k * d.k;
+}
+
+// Arrange classes into GEMM groups and order groups heaviest first.
+void build_groups(convt3d_plan_s &p) {
+    const Geometry &g = p.g;
+    const int s = g.stride;
+    const int kchunk = p.tc ? kTcChunk : 8;
+    const int kc = (g.Cin + kchunk - 1) / kchunk;
+    p.ngroups = 0;
+    if (p.tc && s == 2) {
+        for (int rd = 0; rd < 2; ++rd)
+            for (int rh = 0; rh < 2; ++rh) {
+                GroupDesc &G = p.grp[p.ngroups++];
+                G.ncls = 2;
+                G.cls[0] = (rd * 2 + rh) * 2 + 0;
+                G.cls[1] = (rd * 2 + rh) * 2 + 1;
+                const ClassDesc &a = g.cls[G.cls[0]], &b = g.cls[G.cls[1]];
+                G.Qd = a.Qd; G.Qh = a.Qh; G.Qw = std::max(a.Qw, b.Qw);
+                G.ksteps = (a.ntaps + b.ntaps) * kc;
+            }
+    } else {
+        for (int c = 0; c < g.nclasses; ++c) {
+            GroupDesc &G = p.grp[p.ngroups++];
+            G.ncls = 1;
+            G.cls[0] = G.cls[1] = c;
+            const ClassDesc &a = g.cls[c];
+            G.Qd = a.Qd; G.Qh = a.Qh; G.Qw = a.Qw;
+            G.ksteps = a.ntaps * kc;
+        }
+    }
+    std::stable_sort(p.grp, p.grp + p.ngroups,
+                     [](const GroupDesc &a, const GroupDesc &b) { return a.ksteps > b.ksteps; });
+    int prefix = 0;
+    for (int i = 0; i < p.ngroups; ++i) {
+        GroupDesc &G = p.grp[i];
+        G.vol = G.Qd * G.Qh * G.Qw;
+        G.tiles = (G.vol + p.tile_m - 1) / p.tile_m;
+        G.tile_prefix = prefix;
+        prefix += G.tiles;
+    }
+    p.tiles_per_sample = prefix;
+    p.tiles = (int64_t)prefix * g.N;
+}
+
+convt3d_status_t validate(const convt3d_desc_t &d) {
+    if (d.N < 1 || d.Cin < 1 || d.Cout < 1 || d.Din < 1 || d.Hin < 1 || d.Win < 1)
+        return fail(CONVT3D_ERR_INVALID_ARG, "sizes must be >= 1");
+    if (d.k < 1 || d.stride < 1 || d.pad < 0 || d.out_pad < 0)
+        return fail(CONVT3D_ERR_INVALID_ARG, "k, stride >= 1 and pad, out_pad >= 0 required");
+    if (d.out_pad >= d.stride)
+        return fail(CONVT3D_ERR_INVALID_ARG, "out_pad must be smaller than stride");
+    if (d.epilogue < CONVT3D_EPI_IDENTITY || d.epilogue > CONVT3D_EPI_SOFTMAX_SIGMOID)
+        return fail(CONVT3D_ERR_INVALID_ARG, "unknown epilogue %d", d.epilogue);
+    if (d.precision != CONVT3D_PREC_3XTF32 && d.precision != CONVT3D_PREC_FFMA)
+        return fail(CONVT3D_ERR_INVALID_ARG, "unknown precision %d", d.precision);
+    if (d.epilogue == CONVT3D_EPI_RELU_GROUPNORM && (d.groups < 1 || d.Cout % d.groups != 0))
+        return fail(CONVT3D_ERR_INVALID_ARG, "groups must divide Cout");
+    if ((d.epilogue == CONVT3D_EPI_RELU_GROUPNORM || d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL) &&
+        !(d.eps > 0.0f && isfinite(d.eps)))
+        return fail(CONVT3D_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL && !isfinite(d.scale))
+        return fail(CONVT3D_ERR_INVALID_ARG, "scale must be finite");
+    for (int64_t in : {(int64_t)d.Din, (int64_t)d.Hin, (int64_t)d.Win})
+        if (out_extent(in, d.k, d.stride, d.pad, d.out_pad) < 1)
+            return fail(CONVT3D_ERR_INVALID_ARG, "output extent < 1");
+    // Limits of this build (valid operations it does not run).
+    if (d.stride > 2) return fail(CONVT3D_ERR_UNSUPPORTED, "stride > 2");
+    if (d.k > 7) return fail(CONVT3D_ERR_UNSUPPORTED, "k > 7");
+    if (d.pad >= d.k) return fail(CONVT3D_ERR_UNSUPPORTED, "pad >= k");
+    if (d.k < d.stride) return fail(CONVT3D_ERR_UNSUPPORTED, "k < stride (parity classes without taps)");
+    if (d.Cout > 256) return fail(CONVT3D_ERR_UNSUPPORTED, "Cout > 256");
+    const int64_t Do = out_extent(d.Din, d.k, d.stride, d.pad, d.out_pad);
+    const int64_t Ho = out_extent(d.Hin, d.k, d.stride, d.pad, d.out_pad);
+    const int64_t Wo = out_extent(d.Win, d.k, d.stride, d.pad, d.out_pad);
+    const int64_t lim = (int64_t)1 << 31;
+    if ((int64_t)d.N * d.Cout * Do * Ho * Wo >= lim || (int64_t)d.N * d.Cin * d.Din * d.Hin * d.Win >= lim / 2 ||
+        (int64_t)d.N * 256 * d.Din * d.Hin * d.Win >= ((int64_t)1 << 40))
+        return fail(CONVT3D_ERR_UNSUPPORTED, "tensor larger than 2^31 elements");
+    if (d.precision == CONVT3D_PREC_3XTF32) {
+        const int cout_pad = round_up(d.Cout, 16);
+        if (d.stride == 2 && cout_pad > 128)
+            return fail(CONVT3D_ERR_UNSUPPORTED, "3xTF32 with stride 2 needs Cout <= 128");
+    }
+    return CONVT3D_OK;
+}
+
+// The tensor-core path loads activation tiles with TMA im2col, whose
+// bounding-box corners must lie in [-16, 15] for 5-D tensors: per dimension
+// the lower corner is the smallest tap offset and the upper corner makes the
+// box span exactly the class's Q positions.
+bool im2col_corners_ok(const convt3d_plan_s &p) {
+    const Geometry &g = p.g;
+    for (int i = 0; i < p.ngroups; ++i) {
+        const GroupDesc &G = p.grp[i];
+        for (int c = 0; c < G.ncls; ++c) {
+            const ClassDesc &cl = g.cls[G.cls[c]];
+            const int lo[3] = {cl.lo_d, cl.lo_h, cl.lo_w};
+            const int Q[3] = {G.Qd, G.Qh, G.Qw};
+            const int in[3] = {g.Din, g.Hin, g.Win};
+            for (int a = 0; a < 3; ++a) {
+                const int upper = Q[a] - in[a] + lo[a];
+                if (lo[a] < -16 || lo[a] > 15 || upper < -16 || upper > 15) return false;
+            }
+        }
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int convt3d_version(void) { return 100; }
+
+const char *convt3d_last_error(void) { return g_last_error; }
+
+const char *convt3d_status_string(convt3d_status_t st) {
+    switch (st) {
+        case CONVT3D_OK: return "ok";
+        case CONVT3D_ERR_INVALID_ARG: return "invalid argument";
+        case CONVT3D_ERR_UNSUPPORTED: return "unsupported by this build";
+        case CONVT3D_ERR_WORKSPACE: return "workspace missing or too small";
+        case CONVT3D_ERR_CUDA: return "CUDA error";
+        case CONVT3D_ERR_TIMEOUT: return "device-side wait timed out";
+        case CONVT3D_ERR_DEVICE_ASSERT: return "device-side check failed";
+        case CONVT3D_ERR_NOT_PACKED: return "weights not packed into this workspace";
+    }
+    return "unknown status";
+}
+
+convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t *out) {
+    g_last_error[0] = 0;
+    if (!out) return fail(CONVT3D_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!desc) return fail(CONVT3D_ERR_INVALID_ARG, "desc is NULL");
+    convt3d_status_t st = validate(*desc);
+    if (st != CONVT3D_OK) return st;
+    convt3d_plan_s *p = new (std::nothrow) convt3d_plan_s();
+    if (!p) return fail(CONVT3D_ERR_INVALID_ARG, "out of host memory");
+    memset(p, 0, sizeof(*p));
+    p->d = *desc;
+    if (!build_geometry(p->d, p->g)) {
+        delete p;
+        return fail(CONVT3D_ERR_UNSUPPORTED, "tap table overflow");
+    }
+    p->tc = desc->precision == CONVT3D_PREC_3XTF32;
+    p->tile_m = p->tc ? kTcTileM : kFfmaTileM;
+    p->cin_pad = round_up(desc->Cin, p->tc ? kTcChunk : 8);
+    p->cout_pad = round_up(desc->Cout, 16);
+    if (!p->tc)  // the FFMA kernel's register tiles need a power-of-two channel count
+        while (p->cout_pad & (p->cout_pad - 1)) p->cout_pad += 16;
+    build_groups(*p);
+    if (p->tc && !im2col_corners_ok(*p)) {
+        delete p;
+        return fail(CONVT3D_ERR_UNSUPPORTED, "shape outside the TMA im2col corner range");
+    }
+
+    // Workspace layout.
+    size_t off = kStatusBytes;
+    p->wpk_elems = (size_t)p->g.ntaps * p->cin_pad * p->cout_pad;
+    p->off_wpk_hi = off;
+    off = align_up(off + p->wpk_elems * 4, 256);
+    p->off_wpk_lo = off;
+    if (p->tc) off = align_up(off + p->wpk_elems * 4, 256);
+    p->xs_elems = p->tc ? (size_t)desc->N * desc->Din * desc->Hin * desc->Win * p->cin_pad : 0;
+    p->off_xs_hi = off;
+    off = align_up(off + p->xs_elems * 4, 256);
+    p->off_xs_lo = off;
+    off = align_up(off + p->xs_elems * 4, 256);
+    size_t per_tile = 0, stat = 0;
+    if (desc->epilogue == CONVT3D_EPI_RELU_GROUPNORM) {
+        per_tile = 2 * (size_t)desc->groups;
+        stat = (size_t)desc->N * desc->groups * 2;
+    } else if (desc->epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL) {
+        per_tile = 2 * (size_t)desc->Cout;
+        stat = (size_t)desc->N * desc->Cout * 2;
+    }
+    p->partial_doubles = per_tile * (size_t)p->tiles;
+    p->stat_doubles = stat;
+    p->off_partials = off;
+    off = align_up(off + p->partial_doubles * 8, 256);
+    p->off_stats = off;
+    off = align_up(off + p->stat_doubles * 8, 256);
+    p->ws_total = off;
+    *out = p;
+    return CONVT3D_OK;
+}
+
+void convt3d_plan_destroy(convt3d_plan_t p) {
+    if (!p) return;
+    if (p->ev_created) {
+        cudaEventDestroy(p->ev0);
+        cudaEventDestroy(p->ev1);
+    }
+    delete p;
+}
+
+convt3d_status_t convt3d_output_shape(convt3d_plan_t p, int64_t shape[5]) {
+    if (!p || !shape) return fail(CONVT3D_ERR_INVALID_ARG, "NULL argument");
+    const bool pooled = p->d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
+    shape[0] = p->d.N;
+    shape[1] = p->d.Cout;
+    shape[2] = pooled ? 1 : p->g.Do;
+    shape[3] = pooled ? 1 : p->g.Ho;
+    shape[4] = pooled ? 1 : p->g.Wo;
+    return CONVT3D_OK;
+}
+
+size_t convt3d_workspace_bytes(convt3d_plan_t p) { return p ? p->ws_total : 0; }
+
+convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
+    if (!p || !info) return fail(CONVT3D_ERR_INVALID_ARG, "NULL argument");
+    memset(info, 0, sizeof(*info));
+    convt3d_output_shape(p, info->out_shape);
+    const convt3d_desc_t &d = p->d;
+    const Geometry &g = p->g;
+    info->num_classes = g.nclasses;
+    info->gemm_m = (int64_t)d.N * g.Do * g.Ho * g.Wo;
+    info->gemm_n = d.Cout;
+    int64_t ktot = 0;
+    for (int c = 0; c < g.nclasses; ++c) ktot += (int64_t)d.Cin * g.cls[c].ntaps;
+    info->gemm_k_total = ktot;
+    info->tiles = p->tiles;
+    info->tile_m = p->tile_m;
+    const bool gn = d.epilogue == CONVT3D_EPI_RELU_GROUPNORM;
+    const bool bn = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
+    info->launches_per_forward = (p->tc ? 2 : 1) + (gn ? 2 : 0) + (bn ? 2 : 0);
+    info->launches_per_pack = 1;
+    info->useful_flop = 2.0 * d.N * d.Cout * (double)d.Cin * d.k * d.k * d.k * d.Din * d.Hin * d.Win;
+    // Issued: every tile runs all taps of its class(es) over tile_m rows and cout_pad columns;
+    // the tensor-core path issues three products per term.
+    double issued = 0;
+    for (int i = 0; i < p->ngroups; ++i) {
+        const GroupDesc &G = p->grp[i];
+        int taps = 0;
+        for (int c = 0; c < G.ncls; ++c) taps += g.cls[G.cls[c]].ntaps;
+        issued += 2.0 * G.tiles * (double)d.N * p->tile_m * p->cout_pad * (double)p->cin_pad * taps;
+    }
+    info->issued_mma_flop = issued * (p->tc ? 3.0 : 1.0);
+    const double xbytes = 4.0 * d.N * d.Cin * (double)d.Din * d.Hin * d.Win;
+    const double wbytes = 4.0 * d.Cin * d.Cout * (double)d.k * d.k * d.k;
+    const double ybytes = 4.0 * d.N * d.Cout * (double)g.Do * g.Ho * g.Wo;
+    const double out_bytes = bn ? 4.0 * d.N * d.Cout : ybytes;
+    // Main kernel: reads x (tensor-core path: the staged hi+lo copy) and the packed weights once,
+    // writes the output once (BN+pool: nothing but partials).
+    info->gemm_min_bytes = (p->tc ? 2.0 * xbytes : xbytes) + (p->tc ? 2.0 : 1.0) * wbytes + (bn ? 0.0 : ybytes);
+    // Whole forward as the pages define it: x and w in, the output out, plus the second pass
+    // over y that GroupNorm's global statistics force.
+    info->forward_min_bytes = xbytes + wbytes + out_bytes + (gn ? 2.0 * ybytes : 0.0);
+    return CONVT3D_OK;
+}
+
+static convt3d_status_t check_ws(convt3d_plan_t p, void *ws, size_t bytes) {
+    if (!ws) return fail(CONVT3D_ERR_WORKSPACE, "workspace is NULL");
+    if (bytes < p->ws_total)
+        return fail(CONVT3D_ERR_WORKSPACE, "workspace %zu bytes < required %zu", bytes, p->ws_total);
+    if ((uintptr_t)ws % 256) return fail(CONVT3D_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    return CONVT3D_OK;
+}
+
+convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const float *w, void *ws, size_t ws_bytes,
+                                      void *stream) {
+    g_last_error[0] = 0;
+    if (!p || !w) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan or weight");
+    if ((uintptr_t)w % 16) return fail(CONVT3D_ERR_INVALID_ARG, "w must be 16-byte aligned");
+    convt3d_status_t st = check_ws(p, ws, ws_bytes);
+    if (st) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *base = (char *)ws;
+    cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing status word");
+    e = launch_pack_weights(*p, w, (float *)(base + p->off_wpk_hi), p->tc ? (float *)(base + p->off_wpk_lo) : nullptr,
+                            p->tc, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pack_weights launch");
+    p->packed_ws = ws;
+    return CONVT3D_OK;
+}
+
+convt3d_status_t convt3d_forward(convt3d_plan_t p, const float *x, const float *bias, const float *gamma,
+                                 const float *beta, float *y, void *ws, size_t ws_bytes, void *stream) {
+    g_last_error[0] = 0;
+    if (!p || !x || !y) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan, x or y");
+    const convt3d_desc_t &d = p->d;
+    if (d.has_bias && !bias) return fail(CONVT3D_ERR_INVALID_ARG, "has_bias set but bias is NULL");
+    const bool gn = d.epilogue == CONVT3D_EPI_RELU_GROUPNORM;
+    const bool bn = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
+    if ((gn || bn) && (!gamma || !beta)) return fail(CONVT3D_ERR_INVALID_ARG, "gamma and beta are required");
+    for (const void *ptr : {(const void *)x, (const void *)y, (const void *)bias, (const void *)gamma,
+                            (const void *)beta})
+        if ((uintptr_t)ptr % 16) return fail(CONVT3D_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    if ((const void *)x == (const void *)y) return fail(CONVT3D_ERR_INVALID_ARG, "y must not alias x");
+    convt3d_status_t st = check_ws(p, ws, ws_bytes);
+    if (st) return st;
+    if (p->packed_ws != ws) return fail(CONVT3D_ERR_NOT_PACKED, "call convt3d_pack_weights on this workspace first");
+    cudaStream_t s = (cudaStream_t)stream;
+    char *base = (char *)ws;
+    const float *b = d.has_bias ? bias : nullptr;
+    double *partials = (double *)(base + p->off_partials);
+    double *stats = (double *)(base + p->off_stats);
+    cudaError_t e;
+
+    if (p->prof_enabled) {
+        if (!p->ev_created) {
+            if ((e = cudaEventCreate(&p->ev0)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+            if ((e = cudaEventCreate(&p->ev1)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+            p->ev_created = 1;
+        }
+    }
+    if (p->tc) {
+        float *xs_hi = (float *)(base + p->off_xs_hi), *xs_lo = (float *)(base + p->off_xs_lo);
+        e = launch_stage_input(*p, x, xs_hi, xs_lo, s);
+        if (e != cudaSuccess) return cuda_fail(e, "stage_input launch");
+        if (p->prof_enabled && (e = cudaEventRecord(p->ev0, s)) != cudaSuccess) return cuda_fail(e, "event");
+        e = launch_tc(*p, xs_hi, xs_lo, (const float *)(base + p->off_wpk_hi), (const float *)(base + p->off_wpk_lo),
+                      b, y, partials, (uint32_t *)base, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
+    } else {
+        if (p->prof_enabled && (e = cudaEventRecord(p->ev0, s)) != cudaSuccess) return cuda_fail(e, "event");
+        e = launch_ffma(*p, x, (const float *)(base + p->off_wpk_hi), b, y, partials, s);
+        if (e != cudaSuccess) return cuda_fail(e, "FFMA GEMM launch");
+    }
+    if (p->prof_enabled) {
+        if ((e = cudaEventRecord(p->ev1, s)) != cudaSuccess) return cuda_fail(e, "event");
+        p->prof_valid = 1;
+    }
+    if (gn) {
+        e = launch_gn_finalize(*p, partials, stats, s);
+        if (e != cudaSuccess) return cuda_fail(e, "groupnorm finalize launch");
+        e = launch_gn_normalize(*p, stats, gamma, beta, y, s);
+        if (e != cudaSuccess) return cuda_fail(e, "groupnorm normalize launch");
+    } else if (bn) {
+        e = launch_bn_finalize(*p, partials, stats, gamma, beta, y, s);
+        if (e != cudaSuccess) return cuda_fail(e, "batchnorm finalize launch");
+    }
+    return CONVT3D_OK;
+}
+
+convt3d_status_t convt3d_check(convt3d_plan_t p, void *ws, void *stream) {
+    if (!p || !ws) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan or workspace");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t word[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    e = cudaMemcpy(word, ws, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading status word");
+    if (word[0] == kErrNone) return CONVT3D_OK;
+    e = cudaMemset(ws, 0, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing status word");
+    if (word[0] == kErrTimeout)
+        return fail(CONVT3D_ERR_TIMEOUT, "device wait timed out (site %u, block %u)", word[1], word[2]);
+    return fail(CONVT3D_ERR_DEVICE_ASSERT, "device check failed (code %u, site %u)", word[0], word[1]);
+}
+
+convt3d_status_t convt3d_profile_enable(convt3d_plan_t p, int enable) {
+    if (!p) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan");
+    p->prof_enabled = enable ? 1 : 0;
+    p->prof_valid = 0;
+    return CONVT3D_OK;
+}
+
+convt3d_status_t convt3d_profile_read(convt3d_plan_t p, float *ms) {
+    if (!p || !ms) return fail(CONVT3D_ERR_INVALID_ARG, "NULL argument");
+    if (!p->prof_valid) return fail(CONVT3D_ERR_INVALID_ARG, "no profiled forward yet");
+    cudaError_t e = cudaEventSynchronize(p->ev1);
+    if (e != cudaSuccess) return cuda_fail(e, "event synchronize");
+    e = cudaEventElapsedTime(ms, p->ev0, p->ev1);
+    if (e != cudaSuccess) return cuda_fail(e, "event elapsed time");
+    return CONVT3D_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// Statistics finalisation and the GroupNorm normalise pass.
+//
+// The GEMM epilogues leave per-tile partial (sum, sum of squares) in fp64 in
+// the workspace: partials[(n * T + t) * P + j], T tiles per sample, P values
+// per tile.  Reductions here run in a fixed order (no atomics), so results
+// are bitwise reproducible.
+//
+// GroupNorm (page l2_p61): per (n, g) mean and biased variance over
+// Cout/G channels x all positions; GroupNorm's statistics span the whole
+// sample, so a second pass rewrites y in place as (v - mean) * rstd * gamma
+// + beta -- the page's own plan also needs two passes over global memory
+// because a group does not fit in shared memory.
+// BatchNorm + pool (page l2_p77): per-channel batch mean/biased variance of
+// z = scale*(conv + bias) over (n, positions); the pooled output is
+// gamma * (S[n,c]/V - mean) * rstd + beta with S the per-sample spatial sum,
+// the algebra the page derives for folding the average pool into the
+// normalisation.
+#include "convt3d_internal.h"
+
+namespace convt3d {
+namespace {
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One warp per (n, g).
+__global__ void gn_finalize_kernel(const double *__restrict__ partials, double *__restrict__ stats, int N,
+                                   int G, int T, double count, double eps) {
+    const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    if (w >= N * G) return;
+    const int n = w / G, g = w % G;
+    double s1 = 0.0, s2 = 0.0;
+    for (int t = lane; t < T; t += 32) {
+        const double *p = partials + ((int64_t)n * T + t) * 2 * G + 2 * g;
+        s1 += p[0];
+        s2 += p[1];
+    }
+    s1 = warp_sum(s1);
+    s2 = warp_sum(s2);
+    if (lane == 0) {
+        const double mean = s1 / count;
+        double var = s2 / count - mean * mean;
+        var = var > 0.0 ? var : 0.0;
+        stats[2 * w] = mean;
+        stats[2 * w + 1] = 1.0 / sqrt(var + eps);
+    }
+}
+
+// y <- y * a[n,c] + b[n,c] with a = rstd*gamma, b = beta - mean*rstd*gamma.
+// Vectorised over 4 positions when the plane size allows it.
+__global__ void gn_normalize_kernel(float *__restrict__ y, const double *__restrict__ stats,
+                                    const float *__restrict__ gamma, const float *__restrict__ beta, int C,
+                                    int G, int64_t V, int64_t total, int vec) {
+    const int cpg = C / G;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if (vec) {
+        const int64_t V4 = V / 4;
+        const int64_t total4 = total / 4;
+        float4 *y4 = reinterpret_cast<float4 *>(y);
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total4; i += stride) {
+            const int64_t plane = i / V4;
+            const int c = (int)(plane % C);
+            const int n = (int)(plane / C);
+            const int sg = n * G + c / cpg;
+            const double rstd = stats[2 * sg + 1], mean = stats[2 * sg];
+            const float a = (float)(rstd * gamma[c]);
+            const float b = (float)(beta[c] - mean * rstd * gamma[c]);
+            float4 v = y4[i];
+            v.x = fmaf(v.x, a, b);
+            v.y = fmaf(v.y, a, b);
+            v.z = fmaf(v.z, a, b);
+            v.w = fmaf(v.w, a, b);
+            y4[i] = v;
+        }
+    } else {
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += stride) {
+            const int64_t plane = i / V;
+            const int c = (int)(plane % C);
+            const int n = (int)(plane / C);
+            const int sg = n * G + c / cpg;
+            const double rstd = stats[2 * sg + 1], mean = stats[2 * sg];
+            const float a = (float)(rstd * gamma[c]);
+            const float b = (float)(beta[c] - mean * rstd * gamma[c]);
+            y[i] = fmaf(y[i], a, b);
+        }
+    }
+}
+
+// Phase 1: per (n, c) the spatial sum S and the sum of squares over the
+// sample's tiles.  Block = 32 channels x 8 tile lanes of one sample.
+__global__ void bn_reduce_kernel(const double *__restrict__ partials, double *__restrict__ sums, int N, int C,
+                                 int T) {
+    __shared__ double red[2][8][33];
+    const int n = blockIdx.y;
+    const int c = blockIdx.x * 32 + threadIdx.x;
+    const int lane_t = threadIdx.y;
+    double s1 = 0.0, s2 = 0.0;
+    if (c < C) {
+        for (int t = lane_t; t < T; t += 8) {
+            const double *p = partials + ((int64_t)n * T + t) * 2 * C + 2 * c;
+            s1 += p[0];
+            s2 += p[1];
+        }
+    }
+    red[0][lane_t][threadIdx.x] = s1;
+    red[1][lane_t][threadIdx.x] = s2;
+    __syncthreads();
+    if (lane_t == 0 && c < C) {
+        double a = 0.0, b = 0.0;
+        for (int j = 0; j < 8; ++j) {
+            a += red[0][j][threadIdx.x];
+            b += red[1][j][threadIdx.x];
+        }
+        sums[((int64_t)n * C + c) * 2] = a;
+        sums[((int64_t)n * C + c) * 2 + 1] = b;
+    }
+}
+
+// Phase 2: per channel, batch mean and biased variance, then the pooled output.
+__global__ void bn_finalize_kernel(const double *__restrict__ sums, const float *__restrict__ gamma,
+                                   const float *__restrict__ beta, float *__restrict__ y, int N, int C, double V,
+                                   double eps) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    double S = 0.0, Q = 0.0;
+    for (int n = 0; n < N; ++n) {
+        S += sums[((int64_t)n * C + c) * 2];
+        Q += sums[((int64_t)n * C + c) * 2 + 1];
+    }
+    const double cnt = (double)N * V;
+    const double mean = S / cnt;
+    double var = Q / cnt - mean * mean;
+    var = var > 0.0 ? var : 0.0;
+    const double rstd = 1.0 / sqrt(var + eps);
+    for (int n = 0; n < N; ++n) {
+        const double Sn = sums[((int64_t)n * C + c) * 2];
+        y[(int64_t)n * C + c] = (float)((double)gamma[c] * (Sn / V - mean) * rstd + (double)beta[c]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, double *stats, cudaStream_t s) {
+    const int N = p.g.N, G = p.d.groups;
+    const int warps = N * G;
+    const int threads = 256;
+    const int blocks = (warps * 32 + threads - 1) / threads;
+    const double V = (double)p.g.Do * p.g.Ho * p.g.Wo;
+    const double count = V * (p.g.Cout / G);
+    gn_finalize_kernel<<<blocks, threads, 0, s>>>(partials, stats, N, G, p.tiles_per_sample, count, (double)p.d.eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, const float *gamma, const float *beta,
+                                float *y, cudaStream_t s) {
+    const int64_t V = (int64_t)p.g.Do * p.g.Ho * p.g.Wo;
+    const int64_t total = V * p.g.Cout * p.g.N;
+    const int vec = (V % 4 == 0);
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int threads = 512;
+    const int64_t work = vec ? total / 4 : total;
+    int64_t blocks = (int64_t)sms * 4;
+    if (blocks * threads > work) blocks = (work + threads - 1) / threads;
+    if (blocks < 1) blocks = 1;
+    gn_normalize_kernel<<<(unsigned)blocks, threads, 0, s>>>(y, stats, gamma, beta, p.g.Cout, p.d.groups, V, total,
+                                                              vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, double *sums, const float *gamma,
+                               const float *beta, float *y, cudaStream_t s) {
+    const int N = p.g.N, C = p.g.Cout;
+    dim3 grid((C + 31) / 32, N);
+    bn_reduce_kernel<<<grid, dim3(32, 8), 0, s>>>(partials, sums, N, C, p.tiles_per_sample);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const double V = (double)p.g.Do * p.g.Ho * p.g.Wo;
+    bn_finalize_kernel<<<(C + 127) / 128, 128, 0, s>>>(sums, gamma, beta, y, N, C, V, (double)p.d.eps);
+    return cudaGetLastError();
+}
+
+}  // namespace convt3d
