@@ -160,6 +160,24 @@ def committed_traffic(precision, workload):
     return None
 
 
+# ------------------------------------------------------------ replicas ----
+
+def max_over_ranks(value, device=None):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(useful_flop_per_rank, world, slowest_ms_per_step):
+    """Whole-job useful TFLOP/s: every rank processed its own batch in the slowest rank's time."""
+    return useful_flop_per_rank * world / (slowest_ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------ CPU oracle ----
 
 def cpu_oracle_sample(spec, inputs, target_s, max_samples=None):
@@ -283,14 +301,10 @@ def run_gpu(args, spec):
     plan.profile_enable(False)
     plan.check(ws, stream)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     useful = spec.useful_flop()
-    value = useful * world / (ms_per_step * 1e-3) / 1e12
+    value = replica_throughput(useful, world, ms_per_step)
 
     # end to end through the public API from pinned host buffers
     e2e = None
@@ -313,12 +327,8 @@ def run_gpu(args, spec):
             b.synchronize()
             if i > 0:
                 e2e_ms.append(a.elapsed_time(b))
-        e2e_t = sum(e2e_ms) / len(e2e_ms)
-        if world > 1:
-            t = torch.tensor([e2e_t], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_t = float(t.item())
-        e2e = {"value": useful * world / (e2e_t * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_t,
+        e2e_t = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
+        e2e = {"value": replica_throughput(useful, world, e2e_t), "unit": "TFLOP/s", "ms_per_step": e2e_t,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     if rank != 0:

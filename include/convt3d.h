@@ -49,6 +49,9 @@
  *     and reported by convt3d_check.
  *   - y must not alias x.  Results are bitwise reproducible run to run (no
  *     floating-point atomics).
+ *   - A plan caches launch state (encoded TMA descriptors keyed by the
+ *     workspace address); do not call one plan from several host threads at
+ *     once.  Different plans are independent.
  */
 #ifndef CONVT3D_H
 #define CONVT3D_H

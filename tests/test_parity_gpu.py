@@ -56,6 +56,12 @@ SMALL = [
            seed_index=11),
     E.Spec("gn_pad1_bias", N=1, Cin=16, Cout=32, D=6, H=5, W=7, k=4, pad=1, bias=True,
            epilogue=E.EPI_RELU_GROUPNORM, groups=8, seed_index=12),
+    # 32 channels per group: two 16-channel chunks per group
+    E.Spec("gn_cpg32", N=2, Cin=32, Cout=64, D=4, H=5, W=6, k=3, epilogue=E.EPI_RELU_GROUPNORM, groups=2,
+           seed_index=25),
+    # stride-2 GroupNorm (w-parity pairs feed the same groups)
+    E.Spec("gn_s2", N=2, Cin=16, Cout=32, D=3, H=4, W=4, k=4, stride=2, pad=1, bias=True,
+           epilogue=E.EPI_RELU_GROUPNORM, groups=2, seed_index=26),
     # scale + BatchNorm (batch statistics) + pool, k=5
     E.Spec("bn_small", N=3, Cin=20, Cout=32, D=4, H=6, W=5, k=5, bias=True,
            epilogue=E.EPI_SCALE_BATCHNORM_AVGPOOL, scale=2.0, seed_index=13),

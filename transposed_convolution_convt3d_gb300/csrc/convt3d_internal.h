@@ -15,6 +15,7 @@ constexpr int kMaxTaps = 343;    // k <= 7
 constexpr int kFfmaTileM = 64;   // output positions per FFMA tile
 constexpr int kTcTileM = 128;    // output positions per tensor-core tile (TMEM lanes)
 constexpr int kTcChunk = 32;     // input channels per K step of the tensor-core path (128 B)
+constexpr int kTcEpiWarps = 4;   // epilogue warps of the tensor-core kernel; each writes its own partial row
 
 // Status word layout at the start of the workspace.
 enum : uint32_t { kErrNone = 0, kErrTimeout = 1, kErrAssert = 2 };
@@ -87,6 +88,7 @@ struct convt3d_plan_s {
     convt3d::GroupDesc grp[convt3d::kMaxGroups];
     int tiles_per_sample;
     int64_t tiles;
+    int stat_rows_per_tile;  // partial-statistics rows each tile writes (tensor-core: one per epilogue warp)
     // workspace layout (byte offsets, 256-aligned)
     size_t off_wpk_hi, off_wpk_lo, off_xs_hi, off_xs_lo, off_partials, off_stats, ws_total;
     size_t wpk_elems, xs_elems, partial_doubles, stat_doubles;
@@ -96,6 +98,7 @@ struct convt3d_plan_s {
     cudaEvent_t ev0, ev1;
     int ev_created;
     const void *packed_ws;  // workspace that pack_weights last filled for this plan
+    void *tc_cache;         // tensor-core launch state (tc.cu)
 };
 
 // Kernel launchers (defined in the .cu files); each returns cudaGetLastError().
@@ -106,7 +109,7 @@ cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *h
                                cudaStream_t s);
 cudaError_t launch_ffma(const convt3d_plan_s &p, const float *x, const float *wpk, const float *bias,
                         float *y, double *partials, cudaStream_t s);
-cudaError_t launch_tc(const convt3d_plan_s &p, const float *xs_hi, const float *xs_lo,
+cudaError_t launch_tc(convt3d_plan_s &p, const float *xs_hi, const float *xs_lo,
                       const float *w_hi, const float *w_lo, const float *bias, float *y,
                       double *partials, uint32_t *status, cudaStream_t s);
 cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, double *stats,
@@ -115,5 +118,5 @@ cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, co
                                 const float *beta, float *y, cudaStream_t s);
 cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, double *sums,
                                const float *gamma, const float *beta, float *y, cudaStream_t s);
-int tc_launches_per_forward(const convt3d_plan_s &p);
+void tc_cache_free(void *cache);
 }  // namespace convt3d

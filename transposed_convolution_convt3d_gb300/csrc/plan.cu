@@ -286,7 +286,8 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
         per_tile = 2 * (size_t)desc->Cout;
         stat = (size_t)desc->N * desc->Cout * 2;
     }
-    p->partial_doubles = per_tile * (size_t)p->tiles;
+    p->stat_rows_per_tile = p->tc ? kTcEpiWarps : 1;
+    p->partial_doubles = per_tile * (size_t)p->tiles * p->stat_rows_per_tile;
     p->stat_doubles = stat;
     p->off_partials = off;
     off = align_up(off + p->partial_doubles * 8, 256);
@@ -299,6 +300,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
 
 void convt3d_plan_destroy(convt3d_plan_t p) {
     if (!p) return;
+    if (p->tc_cache) tc_cache_free(p->tc_cache);
     if (p->ev_created) {
         cudaEventDestroy(p->ev0);
         cudaEventDestroy(p->ev1);

@@ -1,8 +1,8 @@
 // Statistics finalisation and the GroupNorm normalise pass.
 //
-// The GEMM epilogues leave per-tile partial (sum, sum of squares) in fp64 in
-// the workspace: partials[(n * T + t) * P + j], T tiles per sample, P values
-// per tile.  Reductions here run in a fixed order (no atomics), so results
+// The GEMM epilogues leave partial (sum, sum of squares) in fp64 in the
+// workspace: partials[(n * T + t) * P + j], T partial rows per sample (one per
+// tile, or one per epilogue warp of a tile), P values per row.  Reductions here run in a fixed order (no atomics), so results
 // are bitwise reproducible.
 //
 // GroupNorm (page l2_p61): per (n, g) mean and biased variance over
@@ -51,43 +51,53 @@ __global__ void gn_finalize_kernel(const double *__restrict__ partials, double *
 }
 
 // y <- y * a[n,c] + b[n,c] with a = rstd*gamma, b = beta - mean*rstd*gamma.
-// Vectorised over 4 positions when the plane size allows it.
-__global__ void gn_normalize_kernel(float *__restrict__ y, const double *__restrict__ stats,
-                                    const float *__restrict__ gamma, const float *__restrict__ beta, int C,
-                                    int G, int64_t V, int64_t total, int vec) {
-    const int cpg = C / G;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    if (vec) {
-        const int64_t V4 = V / 4;
-        const int64_t total4 = total / 4;
-        float4 *y4 = reinterpret_cast<float4 *>(y);
-        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total4; i += stride) {
-            const int64_t plane = i / V4;
-            const int c = (int)(plane % C);
-            const int n = (int)(plane / C);
-            const int sg = n * G + c / cpg;
-            const double rstd = stats[2 * sg + 1], mean = stats[2 * sg];
-            const float a = (float)(rstd * gamma[c]);
-            const float b = (float)(beta[c] - mean * rstd * gamma[c]);
-            float4 v = y4[i];
-            v.x = fmaf(v.x, a, b);
-            v.y = fmaf(v.y, a, b);
-            v.z = fmaf(v.z, a, b);
-            v.w = fmaf(v.w, a, b);
-            y4[i] = v;
+// blockIdx.y is the (n, c) plane, blockIdx.x a chunk of it; each thread
+// streams kVec float4s (16-byte loads and stores) when the plane is 16-byte
+// aligned, scalars otherwise.
+constexpr int kNormThreads = 256;
+constexpr int kNormVec = 4;
+
+__global__ void __launch_bounds__(kNormThreads) gn_normalize_kernel(float *__restrict__ y,
+                                                                    const double *__restrict__ stats,
+                                                                    const float *__restrict__ gamma,
+                                                                    const float *__restrict__ beta, int C, int G,
+                                                                    int64_t V, int planes) {
+  for (int plane = blockIdx.y; plane < planes; plane += gridDim.y) {
+    const int c = plane % C, n = plane / C;
+    const int sg = n * G + c / (C / G);
+    const double rstd = stats[2 * sg + 1], mean = stats[2 * sg];
+    const float a = (float)(rstd * gamma[c]);
+    const float b = (float)(beta[c] - mean * rstd * gamma[c]);
+    float *yp = y + (int64_t)plane * V;
+    if ((V & 3) == 0) {
+        float4 *y4 = reinterpret_cast<float4 *>(yp);
+        const int64_t V4 = V >> 2;
+        const int64_t base = (int64_t)blockIdx.x * kNormThreads * kNormVec + threadIdx.x;
+        float4 v[kNormVec];
+#pragma unroll
+        for (int j = 0; j < kNormVec; ++j) {
+            const int64_t i = base + (int64_t)j * kNormThreads;
+            if (i < V4) v[j] = y4[i];
+        }
+#pragma unroll
+        for (int j = 0; j < kNormVec; ++j) {
+            const int64_t i = base + (int64_t)j * kNormThreads;
+            if (i < V4) {
+                v[j].x = fmaf(v[j].x, a, b);
+                v[j].y = fmaf(v[j].y, a, b);
+                v[j].z = fmaf(v[j].z, a, b);
+                v[j].w = fmaf(v[j].w, a, b);
+                y4[i] = v[j];
+            }
         }
     } else {
-        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += stride) {
-            const int64_t plane = i / V;
-            const int c = (int)(plane % C);
-            const int n = (int)(plane / C);
-            const int sg = n * G + c / cpg;
-            const double rstd = stats[2 * sg + 1], mean = stats[2 * sg];
-            const float a = (float)(rstd * gamma[c]);
-            const float b = (float)(beta[c] - mean * rstd * gamma[c]);
-            y[i] = fmaf(y[i], a, b);
+        const int64_t base = (int64_t)blockIdx.x * kNormThreads * kNormVec * 4 + threadIdx.x;
+        for (int j = 0; j < kNormVec * 4; ++j) {
+            const int64_t i = base + (int64_t)j * kNormThreads;
+            if (i < V) yp[i] = fmaf(yp[i], a, b);
         }
     }
+  }
 }
 
 // Phase 1: per (n, c) the spatial sum S and the sum of squares over the
@@ -151,25 +161,18 @@ cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, 
     const int blocks = (warps * 32 + threads - 1) / threads;
     const double V = (double)p.g.Do * p.g.Ho * p.g.Wo;
     const double count = V * (p.g.Cout / G);
-    gn_finalize_kernel<<<blocks, threads, 0, s>>>(partials, stats, N, G, p.tiles_per_sample, count, (double)p.d.eps);
+    gn_finalize_kernel<<<blocks, threads, 0, s>>>(partials, stats, N, G, p.tiles_per_sample * p.stat_rows_per_tile, count,
+                                                  (double)p.d.eps);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, const float *gamma, const float *beta,
                                 float *y, cudaStream_t s) {
     const int64_t V = (int64_t)p.g.Do * p.g.Ho * p.g.Wo;
-    const int64_t total = V * p.g.Cout * p.g.N;
-    const int vec = (V % 4 == 0);
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int threads = 512;
-    const int64_t work = vec ? total / 4 : total;
-    int64_t blocks = (int64_t)sms * 4;
-    if (blocks * threads > work) blocks = (work + threads - 1) / threads;
-    if (blocks < 1) blocks = 1;
-    gn_normalize_kernel<<<(unsigned)blocks, threads, 0, s>>>(y, stats, gamma, beta, p.g.Cout, p.d.groups, V, total,
-                                                              vec);
+    const int64_t per_block = (int64_t)kNormThreads * kNormVec * 4;  // floats per block
+    const int planes = p.g.N * p.g.Cout;
+    dim3 grid((unsigned)((V + per_block - 1) / per_block), (unsigned)(planes < 65535 ? planes : 65535));
+    gn_normalize_kernel<<<grid, kNormThreads, 0, s>>>(y, stats, gamma, beta, p.g.Cout, p.d.groups, V, planes);
     return cudaGetLastError();
 }
 
@@ -177,7 +180,7 @@ cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, 
                                const float *beta, float *y, cudaStream_t s) {
     const int N = p.g.N, C = p.g.Cout;
     dim3 grid((C + 31) / 32, N);
-    bn_reduce_kernel<<<grid, dim3(32, 8), 0, s>>>(partials, sums, N, C, p.tiles_per_sample);
+    bn_reduce_kernel<<<grid, dim3(32, 8), 0, s>>>(partials, sums, N, C, p.tiles_per_sample * p.stat_rows_per_tile);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const double V = (double)p.g.Do * p.g.Ho * p.g.Wo;

@@ -1,9 +1,728 @@
-// Tensor-core (tcgen05, 3xTF32) implicit-GEMM path -- placeholder until the kernel lands.
+// Tensor-core implicit GEMM for the transposed convolution: tcgen05 MMA in
+// split TF32 ("3xTF32": a_hi*b_hi + a_hi*b_lo + a_lo*b_hi, fp32 accumulation
+// in tensor memory), TMA-fed, with the epilogues fused.
+//
+// GEMM view (output-stationary): M = output positions of one parity class,
+// N = Cout, K = Cin x taps of that class.  A 128-row tile is 128 consecutive
+// positions of the class's q-grid within one sample; for each K step
+// (tap, 32 input channels) the TMA im2col unit gathers the 128 x 32 activation
+// slice straight from the channels-last staged input (input index
+// i = q + delta per dimension; out-of-range pixels arrive as zeros), and a
+// tiled TMA load brings the Cout x 32 weight slice.  Both land K-major with the
+// 128-byte swizzle that the tcgen05 shared-memory descriptors describe.
+// For stride 2 the two classes that differ only in w-parity share a CTA tile
+// (two accumulators), so the epilogue writes each output row as contiguous
+// pairs.
+//
+// CTA roles (192 threads, persistent, one CTA per SM):
+//   warp 0      TMA producer (one thread): fills a ring of shared-memory stages
+//   warp 1      MMA issuer (one thread) + tensor-memory allocation
+//   warps 2..5  epilogue: tensor memory -> registers -> fused epilogue -> HBM
+// Accumulators are double-buffered in tensor memory so the epilogue of one
+// tile overlaps the main loop of the next.  Every wait is bounded; a wait that
+// runs out records CONVT3D_ERR_TIMEOUT in the workspace status word, all roles
+// drain and the kernel returns.
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
 #include "convt3d_internal.h"
+#include "ptx.cuh"
+
+// Order of the per-dimension arrays the TMA im2col interfaces take.
+#ifndef CONVT3D_CORNERS_DHW
+#define CONVT3D_CORNERS_DHW 0
+#endif
+#ifndef CONVT3D_OFFSETS_DHW
+#define CONVT3D_OFFSETS_DHW 0
+#endif
 
 namespace convt3d {
-cudaError_t launch_tc(const convt3d_plan_s &, const float *, const float *, const float *, const float *,
-                      const float *, float *, double *, uint32_t *, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = kTcEpiWarps;
+constexpr int kMaxStages = 8;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr uint32_t kABytes = kTcTileM * 128;   // one 128 x 32 fp32 activation plane
+
+struct TcParams {
+    CUtensorMap a_hi[kMaxClasses];
+    CUtensorMap a_lo[kMaxClasses];
+    CUtensorMap b_hi;
+    CUtensorMap b_lo;
+    const float *bias;
+    float *y;
+    double *partials;
+    uint32_t *status;
+    int N, Cout, cout_pad, Do, Ho, Wo, stride, kc;
+    int epilogue, groups;
+    float scale;
+    int ngroups, tiles_per_sample, total_tiles;
+    int stages;
+    uint32_t stage_bytes, b_bytes;
+    uint32_t tmem_cols, acc_stride;
+    GroupDesc grp[kMaxGroups];
+    ClassDesc cls[kMaxClasses];
+    TapDesc taps[kMaxTaps];
+};
+
+struct Tile {
+    int gi, n, t, slot;
+};
+
+__device__ __forceinline__ Tile decode(const TcParams &P, int tile) {
+    Tile r;
+    int rem = tile, gi = 0;
+    while (gi + 1 < P.ngroups && rem >= P.N * P.grp[gi].tiles) {
+        rem -= P.N * P.grp[gi].tiles;
+        ++gi;
+    }
+    r.gi = gi;
+    r.n = rem / P.grp[gi].tiles;
+    r.t = rem % P.grp[gi].tiles;
+    r.slot = r.n * P.tiles_per_sample + P.grp[gi].tile_prefix + r.t;
+    return r;
 }
+
+__device__ __forceinline__ void record_error(uint32_t *status, uint32_t code, uint32_t site) {
+    if (atomicCAS(status, 0u, code) == 0u) {
+        status[1] = site;
+        status[2] = blockIdx.x;
+    }
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Per-channel sums over the 32 lanes for 16 channels held by every lane:
+// five butterfly stages that halve the channel count held per lane; lane l
+// ends with the full sum of channel (l >> 1).
+__device__ __forceinline__ float transpose_reduce16(const float (&v)[16], int lane) {
+    float a[8];
+    {
+        const bool hi = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float send = hi ? v[i] : v[i + 8];
+            const float keep = hi ? v[i + 8] : v[i];
+            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+    }
+    float b[4];
+    {
+        const bool hi = lane & 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float send = hi ? a[i] : a[i + 4];
+            const float keep = hi ? a[i + 4] : a[i];
+            b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+    }
+    float c[2];
+    {
+        const bool hi = lane & 4;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = hi ? b[i] : b[i + 2];
+            const float keep = hi ? b[i + 2] : b[i];
+            c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+    }
+    float d;
+    {
+        const bool hi = lane & 2;
+        const float send = hi ? c[0] : c[1];
+        const float keep = hi ? c[1] : c[0];
+        d = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    return d + __shfl_xor_sync(0xffffffffu, d, 1);
+}
+
+__device__ __forceinline__ float bias_at(const TcParams &P, int c) {
+    return (P.bias && c < P.Cout) ? __ldg(P.bias + c) : 0.f;
+}
+
+// Position of epilogue row m of a tile for one class: output offset within a
+// channel plane, or -1 when the row lies past the q-grid or the output.
+__device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G, const ClassDesc &C, int t, int m) {
+    const int q = t * kTcTileM + m;
+    if (q >= G.vol) return -1;
+    const int qhw = G.Qh * G.Qw;
+    const int od = P.stride * (q / qhw) + C.rd;
+    const int oh = P.stride * ((q / G.Qw) % G.Qh) + C.rh;
+    const int ow = P.stride * (q % G.Qw) + C.rw;
+    if (od >= P.Do || oh >= P.Ho || ow >= P.Wo) return -1;
+    return (od * P.Ho + oh) * P.Wo + ow;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_constant__ TcParams P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    // 1024-byte aligned ring of pipeline stages
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t full0 = ptx::smem_u32(&bars[0]);
+    const uint32_t empty0 = ptx::smem_u32(&bars[kMaxStages]);
+    const uint32_t tfull0 = ptx::smem_u32(&bars[2 * kMaxStages]);
+    const uint32_t tempty0 = ptx::smem_u32(&bars[2 * kMaxStages + 2]);
+    const uint32_t drain = ptx::smem_u32(&bars[2 * kMaxStages + 4]);
+    const uint32_t smem_base = ptx::smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < P.stages; ++s) {
+            ptx::mbar_init(full0 + 8 * s, 1);
+            ptx::mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(tfull0 + 8 * a, 1);
+            ptx::mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
+        }
+        ptx::mbar_init(drain, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), P.tmem_cols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+
+    // ------------------------------------------------------------ producer
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int gi = 0; gi < P.ngroups; ++gi)
+                for (int ci = 0; ci < P.grp[gi].ncls; ++ci) {
+                    ptx::prefetch_tmap(&P.a_hi[P.grp[gi].cls[ci]]);
+                    ptx::prefetch_tmap(&P.a_lo[P.grp[gi].cls[ci]]);
+                }
+            ptx::prefetch_tmap(&P.b_hi);
+            ptx::prefetch_tmap(&P.b_lo);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_phase = 0;  // per-stage bits: armed at least once, last armed parity
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+                const Tile T = decode(P, tile);
+                const GroupDesc &G = P.grp[T.gi];
+                const int q0 = T.t * kTcTileM;
+                const int qd0 = q0 / (G.Qh * G.Qw), qh0 = (q0 / G.Qw) % G.Qh, qw0 = q0 % G.Qw;
+                for (int ci = 0; ok && ci < G.ncls; ++ci) {
+                    const int cls = G.cls[ci];
+                    const ClassDesc &C = P.cls[cls];
+                    const int w0 = qw0 + C.lo_w, h0 = qh0 + C.lo_h, d0 = qd0 + C.lo_d;
+                    for (int j = 0; ok && j < C.ntaps; ++j) {
+                        const TapDesc td = P.taps[C.tap_begin + j];
+                        const uint16_t ow = (uint16_t)(td.dw - C.lo_w);
+                        const uint16_t oh = (uint16_t)(td.dh - C.lo_h);
+                        const uint16_t od = (uint16_t)(td.dd - C.lo_d);
+                        for (int kc = 0; kc < P.kc; ++kc) {
+                            if (!ptx::mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, &abort_flag, kWaitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t fb = full0 + 8 * stage;
+                            const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
+                            ptx::mbar_arrive_expect_tx(fb, 2 * kABytes + 2 * P.b_bytes);
+                            const int c0 = kc * kTcChunk;
+#if CONVT3D_OFFSETS_DHW
+                            ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
+                            ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
+#else
+                            ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
+                            ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
+#endif
+                            ptx::tma_load_3d(sb + 2 * kABytes, &P.b_hi, fb, c0, 0, C.tap_begin + j);
+                            ptx::tma_load_3d(sb + 2 * kABytes + P.b_bytes, &P.b_lo, fb, c0, 0, C.tap_begin + j);
+                            armed |= 1u << stage;
+                            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                            if (++stage == P.stages) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                record_error(P.status, kErrTimeout, 1);
+                abort_flag = 1;
+            }
+            // Drain: every load this thread issued has landed before the CTA may exit.
+            for (int s = 0; s < P.stages; ++s)
+                if (armed & (1u << s)) {
+                    const volatile int never = 0;
+                    ptx::mbar_wait_bounded(full0 + 8 * s, (armed_phase >> s) & 1u, &never, 200000000ull);
+                }
+        }
+    }
+    // ---------------------------------------------------------- MMA issuer
+    else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = ptx::idesc_tf32((uint32_t)P.cout_pad);
+            int stage = 0;
+            uint32_t phase = 0;
+            int iter = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++iter) {
+                const Tile T = decode(P, tile);
+                const GroupDesc &G = P.grp[T.gi];
+                const int acc = iter & 1;
+                const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
+                if (!ptx::mbar_wait_bounded(tempty0 + 8 * acc, aph ^ 1u, &abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                for (int ci = 0; ok && ci < G.ncls; ++ci) {
+                    const ClassDesc &C = P.cls[G.cls[ci]];
+                    const uint32_t d_tmem = tmem_base + (uint32_t)acc * P.acc_stride + (uint32_t)ci * P.cout_pad;
+                    const int nsteps = C.ntaps * P.kc;
+                    for (int s = 0; s < nsteps; ++s) {
+                        if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a_hi = ptx::sdesc_k_sw128(sb + kk * 32);
+                            const uint64_t a_lo = ptx::sdesc_k_sw128(sb + kABytes + kk * 32);
+                            const uint64_t b_hi = ptx::sdesc_k_sw128(sb + 2 * kABytes + kk * 32);
+                            const uint64_t b_lo = ptx::sdesc_k_sw128(sb + 2 * kABytes + P.b_bytes + kk * 32);
+                            ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (s | kk) ? 1u : 0u);
+                            ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+                            ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                        }
+                        ptx::mma_commit(empty0 + 8 * stage);
+                        if (++stage == P.stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                if (ok) ptx::mma_commit(tfull0 + 8 * acc);
+            }
+            if (!ok) {
+                record_error(P.status, kErrTimeout, 2);
+                abort_flag = 1;
+            }
+            // Drain: all issued MMAs complete before tensor memory is released.
+            ptx::mma_commit(drain);
+            const volatile int never = 0;
+            ptx::mbar_wait_bounded(drain, 0, &never, 200000000ull);
+        }
+    }
+    // ------------------------------------------------------------ epilogue
+    else {
+        const int ew = warp - 2;         // 0..3
+        const int quarter = warp & 3;    // tensor-memory lane quarter this warp may access
+        const int m = quarter * 32 + lane;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+        const int C = P.Cout;
+        const int64_t V = (int64_t)P.Do * P.Ho * P.Wo;
+        constexpr bool gn = EPI == CONVT3D_EPI_RELU_GROUPNORM;
+        constexpr bool bn = EPI == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
+        constexpr bool sm = EPI == CONVT3D_EPI_SOFTMAX_SIGMOID;
+        const int nstat = gn ? 2 * P.groups : (bn ? 2 * C : 0);
+        const int cpg = gn ? C / P.groups : 1;
+        int iter = 0;
+        for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++iter) {
+            const Tile T = decode(P, tile);
+            const GroupDesc &G = P.grp[T.gi];
+            const int acc = iter & 1;
+            const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
+            if (!ptx::mbar_wait_bounded(tfull0 + 8 * acc, aph, &abort_flag, kWaitNs)) {
+                if (lane == 0) record_error(P.status, kErrTimeout, 3);
+                abort_flag = 1;
+                break;
+            }
+            ptx::tc_fence_after();
+            __syncwarp();
+
+            int off[2];
+            off[0] = row_offset(P, G, P.cls[G.cls[0]], T.t, m);
+            off[1] = G.ncls > 1 ? row_offset(P, G, P.cls[G.cls[1]], T.t, m) : -1;
+            // Stride-2 pairs write (even, odd) columns of one output row together.
+            const bool pair_store = G.ncls == 2 && (P.Wo % 2 == 0);
+            float *yn = P.y + (int64_t)T.n * C * V;
+            const uint32_t acc_col = (uint32_t)acc * P.acc_stride;
+
+            if (sm) {
+                // softmax over channels then sigmoid, per output position
+                float mx[2] = {-INFINITY, -INFINITY}, inv[2] = {0.f, 0.f};
+                _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                    const uint32_t col = acc_col + (uint32_t)ci * P.cout_pad;
+                    for (int c0 = 0; c0 < C; c0 += 16) {
+                        float v[16];
+                        ptx::tmem_ld16(lane_base + col + c0, v);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < C) mx[ci] = fmaxf(mx[ci], v[i] + bias_at(P, c0 + i));
+                    }
+                    float sum = 0.f;
+                    for (int c0 = 0; c0 < C; c0 += 16) {
+                        float v[16];
+                        ptx::tmem_ld16(lane_base + col + c0, v);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < C) sum += expf(v[i] + bias_at(P, c0 + i) - mx[ci]);
+                    }
+                    inv[ci] = 1.0f / sum;
+                }
+                for (int c0 = 0; c0 < C; c0 += 16) {
+                    float o[2][16];
+                    _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                        float v[16];
+                        ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, v);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float b = bias_at(P, c0 + i);
+                            const float t = expf(v[i] + b - mx[ci]) * inv[ci];
+                            o[ci][i] = 1.0f / (1.0f + expf(-t));
+                        }
+                    }
+                    if (pair_store) {
+                        if (off[0] >= 0 && off[1] >= 0) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (c0 + i < C)
+                                    *reinterpret_cast<float2 *>(yn + (int64_t)(c0 + i) * V + off[0]) =
+                                        make_float2(o[0][i], o[1][i]);
+                        }
+                    } else {
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
+                            if (off[ci] >= 0) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (c0 + i < C) yn[(int64_t)(c0 + i) * V + off[ci]] = o[ci][i];
+                            }
+                    }
+                }
+            } else {
+                // identity / relu+groupnorm store / batchnorm partial sums, 16 channels at a time
+                double *part = P.partials + ((int64_t)T.slot * kEpiWarps + ew) * nstat;
+                const bool gn_inline = gn && (cpg % 16 == 0);  // groups made of whole 16-channel chunks
+                float gs1 = 0.f, gs2 = 0.f;
+                for (int c0 = 0; c0 < C; c0 += 16) {
+                    float v[2][16];
+                    _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
+                        ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, v[ci]);
+                    ptx::tmem_wait_ld();
+                    if (G.ncls == 1) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[1][i] = 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float b = bias_at(P, c0 + i);
+                        v[0][i] += b;
+                        v[1][i] += b;
+                        if (gn) {
+                            v[0][i] = fmaxf(v[0][i], 0.f);
+                            v[1][i] = fmaxf(v[1][i], 0.f);
+                        }
+                    }
+                    if (bn) {
+                        // per-channel sums of z = scale*(conv + bias) over this warp's 32 rows
+                        float sz = 0.f, sz2 = 0.f;
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                            const bool valid = off[ci] >= 0;
+                            float z[16], z2[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                z[i] = valid ? P.scale * v[ci][i] : 0.f;
+                                z2[i] = z[i] * z[i];
+                            }
+                            sz += transpose_reduce16(z, lane);
+                            sz2 += transpose_reduce16(z2, lane);
+                        }
+                        const int c = c0 + (lane >> 1);
+                        if ((lane & 1) == 0 && c < C) {
+                            part[2 * c] = (double)sz;
+                            part[2 * c + 1] = (double)sz2;
+                        }
+                        continue;
+                    }
+                    if (gn_inline) {
+                        const float m0 = off[0] >= 0 ? 1.f : 0.f, m1 = off[1] >= 0 ? 1.f : 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float a = m0 * v[0][i], b = m1 * v[1][i];
+                            gs1 += a + b;
+                            gs2 += a * a + b * b;
+                        }
+                        if ((c0 + 16) % cpg == 0) {  // this chunk closes group g (same for all lanes)
+                            const int g = c0 / cpg;
+                            const double t1 = warp_sum_d((double)gs1);
+                            const double t2 = warp_sum_d((double)gs2);
+                            if (lane == 0) {
+                                part[2 * g] = t1;
+                                part[2 * g + 1] = t2;
+                            }
+                            gs1 = gs2 = 0.f;
+                        }
+                    }
+                    if (pair_store) {
+                        if (off[0] >= 0 && off[1] >= 0) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (c0 + i < C)
+                                    *reinterpret_cast<float2 *>(yn + (int64_t)(c0 + i) * V + off[0]) =
+                                        make_float2(v[0][i], v[1][i]);
+                        }
+                    } else {
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
+                            if (off[ci] >= 0) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (c0 + i < C) yn[(int64_t)(c0 + i) * V + off[ci]] = v[ci][i];
+                            }
+                    }
+                }
+                if (gn && !gn_inline) {
+                    // group statistics of the ReLU output: a second pass over tensor memory
+                    // (all lanes in step; invalid rows contribute nothing)
+                    for (int g = 0; g < P.groups; ++g) {
+                        float s1 = 0.f, s2 = 0.f;
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                            const bool valid = off[ci] >= 0;
+                            const uint32_t col = acc_col + (uint32_t)ci * P.cout_pad;
+                            for (int c0 = (g * cpg) & ~15; c0 < (g + 1) * cpg; c0 += 16) {
+                                float v[16];
+                                ptx::tmem_ld16(lane_base + col + c0, v);
+                                ptx::tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const int c = c0 + i;
+                                    if (c < g * cpg || c >= (g + 1) * cpg) continue;
+                                    const float b = bias_at(P, c);
+                                    const float val = valid ? fmaxf(v[i] + b, 0.f) : 0.f;
+                                    s1 += val;
+                                    s2 += val * val;
+                                }
+                            }
+                        }
+                        const double t1 = warp_sum_d((double)s1);
+                        const double t2 = warp_sum_d((double)s2);
+                        if (lane == 0) {
+                            part[2 * g] = t1;
+                            part[2 * g + 1] = t2;
+                        }
+                    }
+                }
+            }
+            // tensor memory of this accumulator may be overwritten from here on
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(tempty0 + 8 * acc);
+
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, P.tmem_cols);
+    }
+}
+
+// ------------------------------------------------------------------- host
+
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const int *, const int *, cuuint32_t, cuuint32_t,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DriverFns {
+    EncodeIm2colFn im2col = nullptr;
+    EncodeTiledFn tiled = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+
+const DriverFns &driver_fns() {
+    static DriverFns fns = [] {
+        DriverFns f;
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        f.err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q);
+        if (f.err == cudaSuccess && q == cudaDriverEntryPointSuccess) f.im2col = (EncodeIm2colFn)p;
+        p = nullptr;
+        cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e2 == cudaSuccess && q == cudaDriverEntryPointSuccess) f.tiled = (EncodeTiledFn)p;
+        if (f.err == cudaSuccess) f.err = e2;
+        return f;
+    }();
+    return fns;
+}
+
+int round_pow2(int v) {
+    int p = 32;
+    while (p < v) p *= 2;
+    return p;
+}
+
+}  // namespace
+
+// Per-plan state of the tensor-core launch: encoded tensor maps (re-encoded
+// only when the workspace or the staged-input pointers change), tables and
+// launch shape.
+struct TcCache {
+    TcParams P;
+    const void *key[4];
+    void (*kern)(const TcParams);
+    size_t smem;
+    int grid;
+    bool ready;
+};
+
+void tc_cache_free(void *c) { delete static_cast<TcCache *>(c); }
+
+static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, const float *xs_lo,
+                            const float *w_hi, const float *w_lo) {
+    const DriverFns &fn = driver_fns();
+    if (!fn.im2col || !fn.tiled) return fn.err != cudaSuccess ? fn.err : cudaErrorNotSupported;
+    TcParams *P = &tc.P;
+    const Geometry &g = p.g;
+    if (!tc.ready) {
+        memset(P, 0, sizeof(*P));
+        P->N = g.N;
+        P->Cout = g.Cout;
+        P->cout_pad = p.cout_pad;
+        P->Do = g.Do;
+        P->Ho = g.Ho;
+        P->Wo = g.Wo;
+        P->stride = g.stride;
+        P->kc = p.cin_pad / kTcChunk;
+        P->epilogue = p.d.epilogue;
+        P->groups = p.d.groups;
+        P->scale = p.d.scale;
+        P->ngroups = p.ngroups;
+        P->tiles_per_sample = p.tiles_per_sample;
+        P->total_tiles = (int)p.tiles;
+        int ncls_max = 1;
+        for (int i = 0; i < p.ngroups; ++i) {
+            P->grp[i] = p.grp[i];
+            if (p.grp[i].ncls > ncls_max) ncls_max = p.grp[i].ncls;
+        }
+        for (int i = 0; i < kMaxClasses; ++i) P->cls[i] = g.cls[i];
+        for (int i = 0; i < kMaxTaps; ++i) P->taps[i] = g.taps[i];
+        P->acc_stride = (uint32_t)(ncls_max * p.cout_pad);
+        P->tmem_cols = (uint32_t)round_pow2(2 * ncls_max * p.cout_pad);
+        P->b_bytes = (uint32_t)p.cout_pad * 128;
+        P->stage_bytes = 2 * kABytes + 2 * P->b_bytes;
+        const size_t max_dyn = 232448;  // 227 KB opt-in limit per block
+        int stages = (int)((max_dyn - 1024) / P->stage_bytes);
+        if (stages > kMaxStages) stages = kMaxStages;
+        if (stages < 2 || P->tmem_cols > 512) return cudaErrorInvalidConfiguration;
+        P->stages = stages;
+        tc.smem = 1024 + (size_t)stages * P->stage_bytes;
+        switch (p.d.epilogue) {
+            case CONVT3D_EPI_IDENTITY: tc.kern = convt3d_tc_gemm<CONVT3D_EPI_IDENTITY>; break;
+            case CONVT3D_EPI_RELU_GROUPNORM: tc.kern = convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM>; break;
+            case CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL:
+                tc.kern = convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL>;
+                break;
+            case CONVT3D_EPI_SOFTMAX_SIGMOID: tc.kern = convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID>; break;
+            default: return cudaErrorInvalidValue;
+        }
+        cudaError_t e = cudaFuncSetAttribute(tc.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc.smem);
+        if (e != cudaSuccess) return e;
+        int dev = 0, sms = 148;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        tc.grid = (int)(p.tiles < sms ? p.tiles : sms);
+        tc.key[0] = tc.key[1] = tc.key[2] = tc.key[3] = nullptr;
+        tc.ready = true;
+    }
+    if (tc.key[0] == xs_hi && tc.key[1] == xs_lo && tc.key[2] == w_hi && tc.key[3] == w_lo) return cudaSuccess;
+
+    // activation maps: one im2col map per class and plane
+    const cuuint64_t gdim[5] = {(cuuint64_t)p.cin_pad, (cuuint64_t)g.Win, (cuuint64_t)g.Hin, (cuuint64_t)g.Din,
+                                (cuuint64_t)g.N};
+    const cuuint64_t gstr[4] = {(cuuint64_t)p.cin_pad * 4, (cuuint64_t)p.cin_pad * 4 * g.Win,
+                                (cuuint64_t)p.cin_pad * 4 * g.Win * g.Hin,
+                                (cuuint64_t)p.cin_pad * 4 * g.Win * g.Hin * g.Din};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    for (int gi = 0; gi < p.ngroups; ++gi) {
+        const GroupDesc &G = p.grp[gi];
+        for (int ci = 0; ci < G.ncls; ++ci) {
+            const int c = G.cls[ci];
+            const ClassDesc &C = g.cls[c];
+            const int lo_w = C.lo_w, lo_h = C.lo_h, lo_d = C.lo_d;
+            const int up_w = G.Qw - g.Win + lo_w, up_h = G.Qh - g.Hin + lo_h, up_d = G.Qd - g.Din + lo_d;
+#if CONVT3D_CORNERS_DHW
+            const int lower[3] = {lo_d, lo_h, lo_w}, upper[3] = {up_d, up_h, up_w};
+#else
+            const int lower[3] = {lo_w, lo_h, lo_d}, upper[3] = {up_w, up_h, up_d};
+#endif
+            for (int plane = 0; plane < 2; ++plane) {
+                CUresult r = fn.im2col(plane ? &P->a_lo[c] : &P->a_hi[c], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5,
+                                       (void *)(plane ? xs_lo : xs_hi), gdim, gstr, lower, upper, kTcChunk,
+                                       kTcTileM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+            }
+        }
+    }
+    // weight maps: [tap][cout_pad][cin_pad], box 32 x cout_pad x 1
+    const cuuint64_t wdim[3] = {(cuuint64_t)p.cin_pad, (cuuint64_t)p.cout_pad, (cuuint64_t)g.ntaps};
+    const cuuint64_t wstr[2] = {(cuuint64_t)p.cin_pad * 4, (cuuint64_t)p.cin_pad * 4 * p.cout_pad};
+    const cuuint32_t box[3] = {(cuuint32_t)kTcChunk, (cuuint32_t)p.cout_pad, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    for (int plane = 0; plane < 2; ++plane) {
+        CUresult r = fn.tiled(plane ? &P->b_lo : &P->b_hi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                              (void *)(plane ? w_lo : w_hi), wdim, wstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    tc.key[0] = xs_hi;
+    tc.key[1] = xs_lo;
+    tc.key[2] = w_hi;
+    tc.key[3] = w_lo;
+    return cudaSuccess;
+}
+
+cudaError_t launch_tc(convt3d_plan_s &p, const float *xs_hi, const float *xs_lo, const float *w_hi,
+                      const float *w_lo, const float *bias, float *y, double *partials, uint32_t *status,
+                      cudaStream_t s) {
+    static_assert(sizeof(TcParams) < 32000, "kernel parameter block too large");
+    if (!p.tc_cache) {
+        p.tc_cache = new (std::nothrow) TcCache();
+        if (!p.tc_cache) return cudaErrorMemoryAllocation;
+        static_cast<TcCache *>(p.tc_cache)->ready = false;
+    }
+    TcCache &tc = *static_cast<TcCache *>(p.tc_cache);
+    cudaError_t e = tc_setup(p, tc, xs_hi, xs_lo, w_hi, w_lo);
+    if (e != cudaSuccess) return e;
+    tc.P.bias = bias;
+    tc.P.y = y;
+    tc.P.partials = partials;
+    tc.P.status = status;
+    tc.kern<<<tc.grid, kThreads, tc.smem, s>>>(tc.P);
+    return cudaGetLastError();
+}
+
 }  // namespace convt3d
