@@ -168,6 +168,26 @@ convt3d_status_t convt3d_check(convt3d_plan_t plan, void *workspace, void *strea
 convt3d_status_t convt3d_profile_enable(convt3d_plan_t plan, int enable);
 convt3d_status_t convt3d_profile_read(convt3d_plan_t plan, float *gemm_ms);
 
+/* A forward pass for callers that cannot provide a workspace, because they
+ * are not allowed to allocate device memory (a plugin inside a host that owns
+ * every device allocation) or cannot afford cudaMalloc's implicit device-wide
+ * synchronisation.  No counterpart on the pages: this is a library
+ * convenience, not part of the method.
+ *
+ * Packs w and runs the forward (the same kernels as convt3d_pack_weights +
+ * convt3d_forward) using a 32 MiB workspace compiled into the library as a
+ * device array; allocates nothing.  Each GPU that loads the library's device
+ * code holds that array until the process exits.  Returns
+ * CONVT3D_ERR_WORKSPACE, launching nothing, when convt3d_workspace_bytes(plan)
+ * exceeds 32 MiB.  The first call on a device looks up the array's address
+ * with that device current; make that first call outside any stream capture.
+ * All calls share the one array: calls whose GPU work may overlap (other
+ * streams, other threads) race on it and must be serialised by the caller.
+ * Arguments are as for convt3d_pack_weights and convt3d_forward. */
+convt3d_status_t convt3d_forward_static_workspace(convt3d_plan_t plan, const float *w, const float *x,
+                                                  const float *bias, const float *gamma, const float *beta,
+                                                  float *y, void *stream);
+
 /* Static text for a status code. */
 const char *convt3d_status_string(convt3d_status_t status);
 

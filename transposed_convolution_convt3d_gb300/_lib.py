@@ -36,7 +36,7 @@ EXPORTS = [
     "convt3d_plan_create", "convt3d_plan_destroy", "convt3d_output_shape", "convt3d_plan_info",
     "convt3d_workspace_bytes", "convt3d_pack_weights", "convt3d_forward", "convt3d_check",
     "convt3d_profile_enable", "convt3d_profile_read", "convt3d_status_string", "convt3d_last_error",
-    "convt3d_version",
+    "convt3d_version", "convt3d_forward_static_workspace",
 ]
 
 
@@ -109,6 +109,8 @@ def load(path: str | None = None):
         lib.convt3d_last_error.argtypes = []
         lib.convt3d_version.restype = I
         lib.convt3d_version.argtypes = []
+        lib.convt3d_forward_static_workspace.restype = I
+        lib.convt3d_forward_static_workspace.argtypes = [V, V, V, V, V, V, V, V]
         if path is None:
             _lib = lib
         return lib

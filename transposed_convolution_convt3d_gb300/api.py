@@ -88,6 +88,17 @@ class Plan:
                    self.lib)
         return y
 
+    def forward_static_workspace(self, w, x, y, bias=None, gamma=None, beta=None, stream=None):
+        """Pack w and run the forward in the library's built-in 32 MiB device
+        workspace, for callers that may not allocate device memory.  Calls that
+        overlap on the GPU share that workspace and race."""
+        for t, n in ((w, "w"), (x, "x"), (y, "y"), (bias, "bias"), (gamma, "gamma"), (beta, "beta")):
+            self._dev(t, n)
+        _lib.check(self.lib.convt3d_forward_static_workspace(self.handle, _ptr(w), _ptr(x), _ptr(bias),
+                                                             _ptr(gamma), _ptr(beta), _ptr(y), _stream(stream)),
+                   self.lib)
+        return y
+
     def check(self, workspace, stream=None):
         _lib.check(self.lib.convt3d_check(self.handle, _ptr(workspace), _stream(stream)), self.lib)
 

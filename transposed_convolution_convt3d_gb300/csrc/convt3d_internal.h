@@ -119,4 +119,5 @@ cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, co
 cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, double *sums,
                                const float *gamma, const float *beta, float *y, cudaStream_t s);
 void tc_cache_free(void *cache);
+void report_error(const char *fmt, ...);
 }  // namespace convt3d

@@ -219,6 +219,16 @@ bool im2col_corners_ok(const convt3d_plan_s &p) {
 
 }  // namespace
 
+namespace convt3d {
+// Record a failure detail for convt3d_last_error from another translation unit.
+void report_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+}
+}  // namespace convt3d
+
 extern "C" {
 
 int convt3d_version(void) { return 100; }
