@@ -15,7 +15,7 @@ constexpr int kMaxTaps = 343;    // k <= 7
 constexpr int kFfmaTileM = 64;   // output positions per FFMA tile
 constexpr int kTcTileM = 128;    // output positions per tensor-core tile (TMEM lanes)
 constexpr int kTcChunk = 32;     // input channels per K step of the tensor-core path (128 B)
-constexpr int kTcEpiWarps = 4;   // epilogue warps of the tensor-core kernel; each writes its own partial row
+constexpr int kTcStatRows = 4;   // partial-statistics rows per tensor-core tile (one per TMEM lane quarter)
 
 // Status word layout at the start of the workspace.
 enum : uint32_t { kErrNone = 0, kErrTimeout = 1, kErrAssert = 2 };
@@ -51,6 +51,43 @@ struct GroupDesc {
     int ksteps;             // K steps per tile (all classes of the group)
 };
 
+// Ranges of q-grid coordinates that the valid rows of tile t cover
+// (conservative: a dimension is taken whole once the tile wraps in an outer one).
+struct TileSpan {
+    int d0, d1, h0, h1, w0, w1;
+};
+
+__host__ __device__ inline TileSpan tile_span(const GroupDesc &G, int t, int tile_m) {
+    const int q0 = t * tile_m;
+    const int q1 = (q0 + tile_m < G.vol ? q0 + tile_m : G.vol) - 1;
+    const int qhw = G.Qh * G.Qw;
+    TileSpan r;
+    r.d0 = q0 / qhw;
+    r.d1 = q1 / qhw;
+    if (r.d0 == r.d1) {
+        r.h0 = (q0 / G.Qw) % G.Qh;
+        r.h1 = (q1 / G.Qw) % G.Qh;
+    } else {
+        r.h0 = 0;
+        r.h1 = G.Qh - 1;
+    }
+    if (r.d0 == r.d1 && r.h0 == r.h1) {
+        r.w0 = q0 % G.Qw;
+        r.w1 = q1 % G.Qw;
+    } else {
+        r.w0 = 0;
+        r.w1 = G.Qw - 1;
+    }
+    return r;
+}
+
+// A tap contributes to a tile unless its input index (q + delta) falls
+// outside the input for every row of the tile in some dimension.
+__host__ __device__ inline bool tap_live(const TileSpan &r, const TapDesc &td, int Din, int Hin, int Win) {
+    return r.d1 + td.dd >= 0 && r.d0 + td.dd < Din && r.h1 + td.dh >= 0 && r.h0 + td.dh < Hin &&
+           r.w1 + td.dw >= 0 && r.w0 + td.dw < Win;
+}
+
 struct Geometry {
     int N, Cin, Cout, Din, Hin, Win, k, stride, pad, out_pad;
     int Do, Ho, Wo;
@@ -75,6 +112,23 @@ struct FfmaParams {
     ClassDesc cls[kMaxClasses];
     TapDesc taps[kMaxTaps];
 };
+
+// First tap of a class that a tile issues; when no tap is live the first tap
+// still runs (its zero-filled product initialises the accumulator).
+__host__ __device__ inline int first_live_tap(const TapDesc *taps, int Din, int Hin, int Win, const TileSpan &r,
+                                              const ClassDesc &C) {
+    for (int j = 0; j < C.ntaps; ++j)
+        if (tap_live(r, taps[C.tap_begin + j], Din, Hin, Win)) return j;
+    return 0;
+}
+
+// Taps of class C that a tile issues (live taps, and at least one).
+__host__ __device__ inline int issued_taps(const TapDesc *taps, int Din, int Hin, int Win, const TileSpan &r,
+                                           const ClassDesc &C) {
+    int n = 0;
+    for (int j = 0; j < C.ntaps; ++j) n += tap_live(r, taps[C.tap_begin + j], Din, Hin, Win) ? 1 : 0;
+    return n > 0 ? n : 1;
+}
 
 }  // namespace convt3d
 

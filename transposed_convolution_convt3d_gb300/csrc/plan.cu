@@ -296,7 +296,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
         per_tile = 2 * (size_t)desc->Cout;
         stat = (size_t)desc->N * desc->Cout * 2;
     }
-    p->stat_rows_per_tile = p->tc ? kTcEpiWarps : 1;
+    p->stat_rows_per_tile = p->tc ? kTcStatRows : 1;
     p->partial_doubles = per_tile * (size_t)p->tiles * p->stat_rows_per_tile;
     p->stat_doubles = stat;
     p->off_partials = off;
@@ -350,14 +350,20 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
     info->launches_per_forward = (p->tc ? 2 : 1) + (gn ? 2 : 0) + (bn ? 2 : 0);
     info->launches_per_pack = 1;
     info->useful_flop = 2.0 * d.N * d.Cout * (double)d.Cin * d.k * d.k * d.k * d.Din * d.Hin * d.Win;
-    // Issued: every tile runs all taps of its class(es) over tile_m rows and cout_pad columns;
-    // the tensor-core path issues three products per term.
+    // Issued: every tile runs its class(es)' taps over tile_m rows and cout_pad columns -- the
+    // tensor-core path only the taps live for the tile, with three products per term.
     double issued = 0;
     for (int i = 0; i < p->ngroups; ++i) {
         const GroupDesc &G = p->grp[i];
-        int taps = 0;
-        for (int c = 0; c < G.ncls; ++c) taps += g.cls[G.cls[c]].ntaps;
-        issued += 2.0 * G.tiles * (double)d.N * p->tile_m * p->cout_pad * (double)p->cin_pad * taps;
+        double taps = 0;
+        for (int t = 0; t < G.tiles; ++t) {
+            const TileSpan span = tile_span(G, t, p->tile_m);
+            for (int c = 0; c < G.ncls; ++c) {
+                const ClassDesc &C = g.cls[G.cls[c]];
+                taps += p->tc ? issued_taps(g.taps, g.Din, g.Hin, g.Win, span, C) : C.ntaps;
+            }
+        }
+        issued += 2.0 * (double)d.N * p->tile_m * p->cout_pad * (double)p->cin_pad * taps;
     }
     info->issued_mma_flop = issued * (p->tc ? 3.0 : 1.0);
     const double xbytes = 4.0 * d.N * d.Cin * (double)d.Din * d.Hin * d.Win;

@@ -53,14 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed.  Gives up after
 // `limit_ns` nanoseconds, or as soon as *abort becomes non-zero; returns
-// false in both cases.
+// false in both cases.  With sleep_ns > 0 the waiter naps between polls so
+// that it leaves issue slots to the other warps of its sub-partition.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const volatile int *abort,
-                                                  uint64_t limit_ns) {
+                                                  uint64_t limit_ns, uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
+        if (sleep_ns) __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if ((it & 63u) == 0 || sleep_ns) {
             if (*abort) return false;
             if (globaltimer() - t0 > limit_ns) return false;
         }
@@ -150,17 +152,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory matrix descriptor for a K-major operand stored with the
-// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) core groups packed
-// back to back (stride-dimension byte offset 1024).  The leading-dimension
-// offset is unused for swizzled K-major layouts.
-__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor for a K-major operand whose rows (one per
+// M or N index) are `row_bytes` long (128 or 64) and stored with the matching
+// swizzle: 8-row core groups of 8 * row_bytes packed back to back, so the
+// stride-dimension byte offset is 8 * row_bytes.  The leading-dimension offset
+// is unused for swizzled K-major layouts.  Layout codes: 2 = 128-byte swizzle,
+// 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_k_swizzled(uint32_t saddr, uint32_t row_bytes) {
     uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
-    d |= (uint64_t)(16u >> 4) << 16;                  // leading byte offset
-    d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset
-    d |= (uint64_t)1 << 46;                           // descriptor version (tcgen05)
-    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);           // start address
+    d |= (uint64_t)(16u >> 4) << 16;                     // leading byte offset
+    d |= (uint64_t)((8u * row_bytes) >> 4) << 32;        // stride byte offset
+    d |= (uint64_t)1 << 46;                              // descriptor version (tcgen05)
+    d |= (uint64_t)(row_bytes == 128 ? 2 : 4) << 61;     // swizzle mode
     return d;
 }
 

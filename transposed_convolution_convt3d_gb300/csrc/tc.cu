@@ -9,15 +9,18 @@
 // slice straight from the channels-last staged input (input index
 // i = q + delta per dimension; out-of-range pixels arrive as zeros), and a
 // tiled TMA load brings the Cout x 32 weight slice.  Both land K-major with the
-// 128-byte swizzle that the tcgen05 shared-memory descriptors describe.
+// 128-byte (or, for 16-channel steps, 64-byte) swizzle that the tcgen05
+// shared-memory descriptors describe.
 // For stride 2 the two classes that differ only in w-parity share a CTA tile
 // (two accumulators), so the epilogue writes each output row as contiguous
 // pairs.
 //
-// CTA roles (192 threads, persistent, one CTA per SM):
+// CTA roles (persistent, one CTA per SM):
 //   warp 0      TMA producer (one thread): fills a ring of shared-memory stages
 //   warp 1      MMA issuer (one thread) + tensor-memory allocation
-//   warps 2..5  epilogue: tensor memory -> registers -> fused epilogue -> HBM
+//   warps 2..   epilogue, one warp per tensor-memory lane quarter (two for
+//               softmax+sigmoid, splitting the channels): tensor memory ->
+//               registers -> fused epilogue -> HBM
 // Accumulators are double-buffered in tensor memory so the epilogue of one
 // tile overlaps the main loop of the next.  Every wait is bounded; a wait that
 // runs out records CONVT3D_ERR_TIMEOUT in the workspace status word, all roles
@@ -41,11 +44,27 @@
 namespace convt3d {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = kTcEpiWarps;
+// Epilogue warps per CTA: softmax+sigmoid is arithmetic-heavy and gets two warps
+// per tensor-memory lane quarter (each taking half of the channels); the other
+// epilogues use one, which leaves the producer and MMA warps more issue slots.
+template <int EPI>
+struct EpiCfg {
+    static constexpr int warps = EPI == CONVT3D_EPI_SOFTMAX_SIGMOID ? 8 : 4;
+    static constexpr int threads = 64 + 32 * warps;  // producer warp, MMA warp, epilogue warps
+};
+constexpr int kMaxThreads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
 constexpr int kMaxStages = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
-constexpr uint32_t kABytes = kTcTileM * 128;   // one 128 x 32 fp32 activation plane
+// Input channels per K step: 32 (128-byte rows, 128-byte swizzle) or 16
+// (64-byte rows, 64-byte swizzle: half-size stages, twice as many of them).
+#ifndef CONVT3D_TC_KCHUNK
+#define CONVT3D_TC_KCHUNK 32
+#endif
+constexpr int kChunk = CONVT3D_TC_KCHUNK;
+static_assert(kChunk == 16 || kChunk == 32, "K step must be 16 or 32 channels");
+static_assert(kTcChunk % kChunk == 0, "channel padding must be a multiple of the K step");
+constexpr uint32_t kRowBytes = kChunk * 4;
+constexpr uint32_t kABytes = kTcTileM * kRowBytes;  // one 128 x kChunk fp32 activation plane
 
 struct TcParams {
     CUtensorMap a_hi[kMaxClasses];
@@ -57,6 +76,7 @@ struct TcParams {
     double *partials;
     uint32_t *status;
     int N, Cout, cout_pad, Do, Ho, Wo, stride, kc;
+    int Din, Hin, Win;
     int epilogue, groups;
     float scale;
     int ngroups, tiles_per_sample, total_tiles;
@@ -143,8 +163,30 @@ __device__ __forceinline__ float transpose_reduce16(const float (&v)[16], int la
     return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
-__device__ __forceinline__ float bias_at(const TcParams &P, int c) {
-    return (P.bias && c < P.Cout) ? __ldg(P.bias + c) : 0.f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x with the PTX approximate base-2 exponential (ex2.approx.ftz.f32).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// sigmoid(t) = 1/2 + tanh(t/2)/2 for t in [0, 1], with tanh(u) from its
+// Maclaurin series u - u^3/3 + 2u^5/15 - 17u^7/315 + 62u^9/2835
+// - 1382u^11/155925 + 21844u^13/6081075 (coefficients 2^2n (2^2n - 1) B_2n / (2n)!).
+// For u <= 1/2 the series alternates with decreasing terms, so truncation
+// after u^13 errs by less than the next term, 929569/638512875 * 2^-15 < 5e-8.
+__device__ __forceinline__ float sigmoid_unit(float t) {
+    const float u = 0.5f * t, u2 = u * u;
+    float p = 21844.0f / 6081075.0f;
+    p = fmaf(p, u2, -1382.0f / 155925.0f);
+    p = fmaf(p, u2, 62.0f / 2835.0f);
+    p = fmaf(p, u2, -17.0f / 315.0f);
+    p = fmaf(p, u2, 2.0f / 15.0f);
+    p = fmaf(p, u2, -1.0f / 3.0f);
+    p = fmaf(p, u2, 1.0f);
+    return fmaf(0.5f * u, p, 0.5f);
 }
 
 // Position of epilogue row m of a tile for one class: output offset within a
@@ -160,12 +202,19 @@ __device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G,
     return (od * P.Ho + oh) * P.Wo + ow;
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_constant__ TcParams P) {
+// KEEP (softmax only): each epilogue warp keeps its exponentials in registers
+// (Cout <= 32 * warps per lane quarter); otherwise it re-reads tensor memory.
+template <int EPI, bool KEEP>
+__global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const __grid_constant__ TcParams P) {
+    constexpr int kEpiWarps = EpiCfg<EPI>::warps;
+    constexpr int kHalves = kEpiWarps / 4;  // warps per tensor-memory lane quarter
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
+    __shared__ float s_bias[256];                          // bias, zero-padded to 256 channels
+    __shared__ float s_bias_l2e[256];                      // bias * log2(e) (softmax)
+    __shared__ float s_xchg[2 * 2 * 4 * kTcTileM];         // softmax (max, sum) exchange, double-buffered
 
     // 1024-byte aligned ring of pipeline stages
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -190,6 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
         }
         ptx::mbar_init(drain, 1);
         ptx::fence_mbar_init();
+    }
+    for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+        s_bias[c] = (P.bias && c < P.Cout) ? P.bias[c] : 0.f;
+        s_bias_l2e[c] = s_bias[c] * kLog2e;
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), P.tmem_cols);
@@ -219,12 +272,15 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
                 const GroupDesc &G = P.grp[T.gi];
                 const int q0 = T.t * kTcTileM;
                 const int qd0 = q0 / (G.Qh * G.Qw), qh0 = (q0 / G.Qw) % G.Qh, qw0 = q0 % G.Qw;
+                const TileSpan span = tile_span(G, T.t, kTcTileM);
                 for (int ci = 0; ok && ci < G.ncls; ++ci) {
                     const int cls = G.cls[ci];
                     const ClassDesc &C = P.cls[cls];
                     const int w0 = qw0 + C.lo_w, h0 = qh0 + C.lo_h, d0 = qd0 + C.lo_d;
-                    for (int j = 0; ok && j < C.ntaps; ++j) {
+                    const int jfirst = first_live_tap(P.taps, P.Din, P.Hin, P.Win, span, C);
+                    for (int j = jfirst; ok && j < C.ntaps; ++j) {
                         const TapDesc td = P.taps[C.tap_begin + j];
+                        if (j != jfirst && !tap_live(span, td, P.Din, P.Hin, P.Win)) continue;
                         const uint16_t ow = (uint16_t)(td.dw - C.lo_w);
                         const uint16_t oh = (uint16_t)(td.dh - C.lo_h);
                         const uint16_t od = (uint16_t)(td.dd - C.lo_d);
@@ -236,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
                             const uint32_t fb = full0 + 8 * stage;
                             const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
                             ptx::mbar_arrive_expect_tx(fb, 2 * kABytes + 2 * P.b_bytes);
-                            const int c0 = kc * kTcChunk;
+                            const int c0 = kc * kChunk;
 #if CONVT3D_OFFSETS_DHW
                             ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
                             ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
@@ -272,6 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
     else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = ptx::idesc_tf32((uint32_t)P.cout_pad);
+            // A descriptor's start-address field is the byte address >> 4, so the
+            // descriptors of every stage and K slice are one base plus an offset.
+            const uint64_t desc0 = ptx::sdesc_k_swizzled(smem_base, kRowBytes);
+            const uint64_t d_alo = kABytes >> 4, d_bhi = (2 * kABytes) >> 4,
+                           d_blo = (2 * kABytes + P.b_bytes) >> 4;
             int stage = 0;
             uint32_t phase = 0;
             int iter = 0;
@@ -286,31 +347,39 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
                     break;
                 }
                 ptx::tc_fence_after();
+                const TileSpan span = tile_span(G, T.t, kTcTileM);
                 for (int ci = 0; ok && ci < G.ncls; ++ci) {
                     const ClassDesc &C = P.cls[G.cls[ci]];
                     const uint32_t d_tmem = tmem_base + (uint32_t)acc * P.acc_stride + (uint32_t)ci * P.cout_pad;
-                    const int nsteps = C.ntaps * P.kc;
-                    for (int s = 0; s < nsteps; ++s) {
-                        if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
+                    // same tap sequence as the producer: live taps only, the first always
+                    const int jfirst = first_live_tap(P.taps, P.Din, P.Hin, P.Win, span, C);
+                    bool first = true;
+                    for (int j = jfirst; ok && j < C.ntaps; ++j) {
+                        if (j != jfirst && !tap_live(span, P.taps[C.tap_begin + j], P.Din, P.Hin, P.Win)) continue;
+                        for (int kc = 0; kc < P.kc; ++kc) {
+                            if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            const uint64_t ds = desc0 + ((uint64_t)stage * P.stage_bytes >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a_hi = ptx::sdesc_k_sw128(sb + kk * 32);
-                            const uint64_t a_lo = ptx::sdesc_k_sw128(sb + kABytes + kk * 32);
-                            const uint64_t b_hi = ptx::sdesc_k_sw128(sb + 2 * kABytes + kk * 32);
-                            const uint64_t b_lo = ptx::sdesc_k_sw128(sb + 2 * kABytes + P.b_bytes + kk * 32);
-                            ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (s | kk) ? 1u : 0u);
-                            ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
-                            ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
-                        }
-                        ptx::mma_commit(empty0 + 8 * stage);
-                        if (++stage == P.stages) {
-                            stage = 0;
-                            phase ^= 1u;
+                            for (int kk = 0; kk < kChunk / 8; ++kk) {  // 8 TF32 (32 bytes) per MMA
+                                const uint64_t a_hi = ds + (uint64_t)(kk * 2);
+                                const uint64_t a_lo = a_hi + d_alo;
+                                const uint64_t b_hi = a_hi + d_bhi;
+                                const uint64_t b_lo = a_hi + d_blo;
+                                // the class's first product overwrites the accumulator
+                                ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (first && kk == 0) ? 0u : 1u);
+                                ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+                                ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                            }
+                            first = false;
+                            ptx::mma_commit(empty0 + 8 * stage);
+                            if (++stage == P.stages) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
                         }
                     }
                 }
@@ -328,24 +397,33 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
     }
     // ------------------------------------------------------------ epilogue
     else {
-        const int ew = warp - 2;         // 0..3
-        const int quarter = warp & 3;    // tensor-memory lane quarter this warp may access
+        // Two warps per tensor-memory lane quarter; warp `half` of a quarter takes
+        // the 16-channel chunks j with j % 2 == half (groups g % 2 == half when
+        // a group is made of whole chunks).
+        const int ew = warp - 2;          // 0..kEpiWarps-1
+        const int quarter = warp & 3;     // lane quarter this warp may access
+        const int half = ew >> 2;         // which share of the channels (0 when kHalves == 1)
         const int m = quarter * 32 + lane;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         const int C = P.Cout;
+        const int nchunks = (C + 15) / 16;
         const int64_t V = (int64_t)P.Do * P.Ho * P.Wo;
         constexpr bool gn = EPI == CONVT3D_EPI_RELU_GROUPNORM;
         constexpr bool bn = EPI == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
         constexpr bool sm = EPI == CONVT3D_EPI_SOFTMAX_SIGMOID;
         const int nstat = gn ? 2 * P.groups : (bn ? 2 * C : 0);
-        const int cpg = gn ? C / P.groups : 1;
+        const int cpg = gn ? C / P.groups : 16;
+        const bool gn_inline = gn && (cpg % 16 == 0);  // groups made of whole 16-channel chunks
+        auto mine = [&](int j) -> bool {                // does this warp own chunk j?
+            return gn_inline ? ((16 * j) / cpg) % kHalves == half : j % kHalves == half;
+        };
         int iter = 0;
         for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++iter) {
             const Tile T = decode(P, tile);
             const GroupDesc &G = P.grp[T.gi];
             const int acc = iter & 1;
             const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
-            if (!ptx::mbar_wait_bounded(tfull0 + 8 * acc, aph, &abort_flag, kWaitNs)) {
+            if (!ptx::mbar_wait_bounded(tfull0 + 8 * acc, aph, &abort_flag, kWaitNs, 200)) {
                 if (lane == 0) record_error(P.status, kErrTimeout, 3);
                 abort_flag = 1;
                 break;
@@ -360,67 +438,135 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
             const bool pair_store = G.ncls == 2 && (P.Wo % 2 == 0);
             float *yn = P.y + (int64_t)T.n * C * V;
             const uint32_t acc_col = (uint32_t)acc * P.acc_stride;
+            // statistics: one partial row per (tile, lane quarter); the two warps of a
+            // quarter fill disjoint slots of it
+            double *part = P.partials + ((int64_t)T.slot * kTcStatRows + quarter) * nstat;
 
             if (sm) {
-                // softmax over channels then sigmoid, per output position
-                float mx[2] = {-INFINITY, -INFINITY}, inv[2] = {0.f, 0.f};
-                _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
-                    const uint32_t col = acc_col + (uint32_t)ci * P.cout_pad;
-                    for (int c0 = 0; c0 < C; c0 += 16) {
-                        float v[16];
-                        ptx::tmem_ld16(lane_base + col + c0, v);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (c0 + i < C) mx[ci] = fmaxf(mx[ci], v[i] + bias_at(P, c0 + i));
-                    }
-                    float sum = 0.f;
-                    for (int c0 = 0; c0 < C; c0 += 16) {
-                        float v[16];
-                        ptx::tmem_ld16(lane_base + col + c0, v);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (c0 + i < C) sum += expf(v[i] + bias_at(P, c0 + i) - mx[ci]);
-                    }
-                    inv[ci] = 1.0f / sum;
-                }
-                for (int c0 = 0; c0 < C; c0 += 16) {
-                    float o[2][16];
+                // softmax over channels then sigmoid, per output position, in the base-2
+                // domain: u = (conv + bias) * log2(e), softmax weight = 2^(u - max) / sum.
+                // 1) one pass over this warp's chunks: exponentials kept in registers
+                //    (at most two chunks per class, i.e. Cout <= 32 * kHalves), each
+                //    chunk relative to the running maximum when it was read.
+                constexpr int kKeep = 2;
+                float e[KEEP ? kKeep : 1][2][16], mref[KEEP ? kKeep : 1][2];
+                float mx[2] = {-INFINITY, -INFINITY}, sum[2] = {0.f, 0.f};
+                // one chunk: base-2 logits, running max, rescaled running sum; leaves the
+                // exponentials (relative to the chunk's running max `cm`) in ev
+                auto chunk_pass = [&](int j, float (&ev)[2][16], float (&cm_out)[2]) {
+                    const int c0 = 16 * j;
+                    _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
+                        ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, ev[ci]);
+                    ptx::tmem_wait_ld();
                     _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
-                        float v[16];
-                        ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, v);
-                        ptx::tmem_wait_ld();
+                        float cm = mx[ci];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float b = bias_at(P, c0 + i);
-                            const float t = expf(v[i] + b - mx[ci]) * inv[ci];
-                            o[ci][i] = 1.0f / (1.0f + expf(-t));
+                            ev[ci][i] = (c0 + i < C) ? fmaf(ev[ci][i], kLog2e, s_bias_l2e[c0 + i]) : -INFINITY;
+                            cm = fmaxf(cm, ev[ci][i]);
                         }
+                        float cs = mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - cm);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            ev[ci][i] = ex2_approx(ev[ci][i] - cm);
+                            cs += ev[ci][i];
+                        }
+                        mx[ci] = cm;
+                        sum[ci] = cs;
+                        cm_out[ci] = cm;
                     }
+                };
+                if (KEEP) {
+#pragma unroll
+                    for (int jj = 0; jj < (KEEP ? kKeep : 1); ++jj) {
+                        const int j = half + jj * kHalves;
+                        if (j < nchunks) chunk_pass(j, e[jj], mref[jj]);
+                    }
+                } else {
+                    for (int j = half; j < nchunks; j += kHalves) chunk_pass(j, e[0], mref[0]);
+                }
+                // 2) combine with the partner warp of this lane quarter
+                float M[2], inv[2];
+                if (kHalves == 2) {
+                    float *xm = s_xchg + ((iter & 1) * 2 + half) * 4 * kTcTileM;  // [class][max,sum][row]
+                    xm[0 * kTcTileM + m] = mx[0];
+                    xm[1 * kTcTileM + m] = sum[0];
+                    xm[2 * kTcTileM + m] = mx[1];
+                    xm[3 * kTcTileM + m] = sum[1];
+                    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                    const float *xo = s_xchg + ((iter & 1) * 2 + (half ^ 1)) * 4 * kTcTileM;
+#pragma unroll
+                    for (int ci = 0; ci < 2; ++ci) {
+                        const float om = xo[(2 * ci) * kTcTileM + m], os = xo[(2 * ci + 1) * kTcTileM + m];
+                        M[ci] = fmaxf(mx[ci], om);
+                        const float S = (mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - M[ci])) +
+                                        (om == -INFINITY ? 0.f : os * ex2_approx(om - M[ci]));
+                        inv[ci] = __frcp_rn(S);
+                    }
+                } else {
+#pragma unroll
+                    for (int ci = 0; ci < 2; ++ci) {
+                        M[ci] = mx[ci];
+                        inv[ci] = __frcp_rn(sum[ci]);
+                    }
+                }
+                // 3) outputs for this warp's chunks: t = weight in (0, 1], then sigmoid(t)
+                auto store_chunk = [&](int c0, const float (&o)[2][16]) {
                     if (pair_store) {
                         if (off[0] >= 0 && off[1] >= 0) {
+                            float *dst = yn + (int64_t)c0 * V + off[0];
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 if (c0 + i < C)
-                                    *reinterpret_cast<float2 *>(yn + (int64_t)(c0 + i) * V + off[0]) =
-                                        make_float2(o[0][i], o[1][i]);
+                                    *reinterpret_cast<float2 *>(dst + (int64_t)i * V) = make_float2(o[0][i], o[1][i]);
                         }
                     } else {
                         _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
                             if (off[ci] >= 0) {
+                                float *dst = yn + (int64_t)c0 * V + off[ci];
 #pragma unroll
                                 for (int i = 0; i < 16; ++i)
-                                    if (c0 + i < C) yn[(int64_t)(c0 + i) * V + off[ci]] = o[ci][i];
+                                    if (c0 + i < C) dst[(int64_t)i * V] = o[ci][i];
                             }
+                    }
+                };
+                if (KEEP) {
+#pragma unroll
+                    for (int jj = 0; jj < (KEEP ? kKeep : 1); ++jj) {
+                        const int j = half + jj * kHalves;
+                        if (j < nchunks) {
+#pragma unroll
+                            for (int ci = 0; ci < 2; ++ci) {
+                                const float scale = inv[ci] * ex2_approx(mref[jj][ci] - M[ci]);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) e[jj][ci][i] = sigmoid_unit(e[jj][ci][i] * scale);
+                            }
+                            store_chunk(16 * j, e[jj]);
+                        }
+                    }
+                } else {
+                    for (int j = half; j < nchunks; j += kHalves) {
+                        const int c0 = 16 * j;
+                        float o[2][16];
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
+                            ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, o[ci]);
+                        ptx::tmem_wait_ld();
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float u = fmaf(o[ci][i], kLog2e, s_bias_l2e[c0 + i]);
+                                o[ci][i] = sigmoid_unit(ex2_approx(u - M[ci]) * inv[ci]);
+                            }
+                        }
+                        store_chunk(c0, o);
                     }
                 }
             } else {
-                // identity / relu+groupnorm store / batchnorm partial sums, 16 channels at a time
-                double *part = P.partials + ((int64_t)T.slot * kEpiWarps + ew) * nstat;
-                const bool gn_inline = gn && (cpg % 16 == 0);  // groups made of whole 16-channel chunks
-                float gs1 = 0.f, gs2 = 0.f;
-                for (int c0 = 0; c0 < C; c0 += 16) {
+                // identity / relu+groupnorm store / batchnorm partial sums, per owned chunk
+                float gs1 = 0.f, gs2 = 0.f;  // running group sums (groups of whole chunks)
+                for (int j = 0; j < nchunks; ++j) {
+                    if (!mine(j)) continue;
+                    const int c0 = 16 * j;
                     float v[2][16];
                     _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
                         ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, v[ci]);
@@ -431,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
                     }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float b = bias_at(P, c0 + i);
+                        const float b = s_bias[c0 + i];
                         v[0][i] += b;
                         v[1][i] += b;
                         if (gn) {
@@ -497,9 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
                     }
                 }
                 if (gn && !gn_inline) {
-                    // group statistics of the ReLU output: a second pass over tensor memory
-                    // (all lanes in step; invalid rows contribute nothing)
-                    for (int g = 0; g < P.groups; ++g) {
+                    // group statistics of the ReLU output: a second pass over tensor memory,
+                    // groups g % 2 == half (all lanes in step; invalid rows contribute nothing)
+                    for (int g = half; g < P.groups; g += kHalves) {
                         float s1 = 0.f, s2 = 0.f;
                         _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
                             const bool valid = off[ci] >= 0;
@@ -512,8 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
                                 for (int i = 0; i < 16; ++i) {
                                     const int c = c0 + i;
                                     if (c < g * cpg || c >= (g + 1) * cpg) continue;
-                                    const float b = bias_at(P, c);
-                                    const float val = valid ? fmaxf(v[i] + b, 0.f) : 0.f;
+                                    const float val = valid ? fmaxf(v[i] + s_bias[c], 0.f) : 0.f;
                                     s1 += val;
                                     s2 += val * val;
                                 }
@@ -531,7 +676,6 @@ __global__ void __launch_bounds__(kThreads, 1) convt3d_tc_gemm(const __grid_cons
             // tensor memory of this accumulator may be overwritten from here on
             ptx::tc_fence_before();
             ptx::mbar_arrive(tempty0 + 8 * acc);
-
         }
     }
 
@@ -554,6 +698,8 @@ typedef CUresult (*EncodeIm2colFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr CUtensorMapSwizzle kSwizzle = kChunk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 
 struct DriverFns {
     EncodeIm2colFn im2col = nullptr;
@@ -592,6 +738,7 @@ struct TcCache {
     TcParams P;
     const void *key[4];
     void (*kern)(const TcParams);
+    int threads;
     size_t smem;
     int grid;
     bool ready;
@@ -614,7 +761,10 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->Ho = g.Ho;
         P->Wo = g.Wo;
         P->stride = g.stride;
-        P->kc = p.cin_pad / kTcChunk;
+        P->Din = g.Din;
+        P->Hin = g.Hin;
+        P->Win = g.Win;
+        P->kc = p.cin_pad / kChunk;
         P->epilogue = p.d.epilogue;
         P->groups = p.d.groups;
         P->scale = p.d.scale;
@@ -630,24 +780,41 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         for (int i = 0; i < kMaxTaps; ++i) P->taps[i] = g.taps[i];
         P->acc_stride = (uint32_t)(ncls_max * p.cout_pad);
         P->tmem_cols = (uint32_t)round_pow2(2 * ncls_max * p.cout_pad);
-        P->b_bytes = (uint32_t)p.cout_pad * 128;
+        P->b_bytes = (uint32_t)p.cout_pad * kRowBytes;
         P->stage_bytes = 2 * kABytes + 2 * P->b_bytes;
-        const size_t max_dyn = 232448;  // 227 KB opt-in limit per block
+        switch (p.d.epilogue) {
+            case CONVT3D_EPI_IDENTITY:
+                tc.kern = convt3d_tc_gemm<CONVT3D_EPI_IDENTITY, true>;
+                tc.threads = EpiCfg<CONVT3D_EPI_IDENTITY>::threads;
+                break;
+            case CONVT3D_EPI_RELU_GROUPNORM:
+                tc.kern = convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM, true>;
+                tc.threads = EpiCfg<CONVT3D_EPI_RELU_GROUPNORM>::threads;
+                break;
+            case CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL:
+                tc.kern = convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL, true>;
+                tc.threads = EpiCfg<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL>::threads;
+                break;
+            case CONVT3D_EPI_SOFTMAX_SIGMOID:
+                // registers hold the exponentials when each warp owns at most two chunks
+                tc.kern = p.cout_pad <= 32 * EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps / 4 * 2
+                              ? convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, true>
+                              : convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, false>;
+                tc.threads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
+                break;
+            default: return cudaErrorInvalidValue;
+        }
+        // stage ring: as many stages as fit beside the kernel's static shared memory
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, tc.kern);
+        if (e != cudaSuccess) return e;
+        const size_t max_dyn = 232448 - fa.sharedSizeBytes;  // 227 KB opt-in limit per block
         int stages = (int)((max_dyn - 1024) / P->stage_bytes);
         if (stages > kMaxStages) stages = kMaxStages;
         if (stages < 2 || P->tmem_cols > 512) return cudaErrorInvalidConfiguration;
         P->stages = stages;
         tc.smem = 1024 + (size_t)stages * P->stage_bytes;
-        switch (p.d.epilogue) {
-            case CONVT3D_EPI_IDENTITY: tc.kern = convt3d_tc_gemm<CONVT3D_EPI_IDENTITY>; break;
-            case CONVT3D_EPI_RELU_GROUPNORM: tc.kern = convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM>; break;
-            case CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL:
-                tc.kern = convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL>;
-                break;
-            case CONVT3D_EPI_SOFTMAX_SIGMOID: tc.kern = convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID>; break;
-            default: return cudaErrorInvalidValue;
-        }
-        cudaError_t e = cudaFuncSetAttribute(tc.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc.smem);
+        e = cudaFuncSetAttribute(tc.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc.smem);
         if (e != cudaSuccess) return e;
         int dev = 0, sms = 148;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -679,8 +846,8 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
 #endif
             for (int plane = 0; plane < 2; ++plane) {
                 CUresult r = fn.im2col(plane ? &P->a_lo[c] : &P->a_hi[c], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5,
-                                       (void *)(plane ? xs_lo : xs_hi), gdim, gstr, lower, upper, kTcChunk,
-                                       kTcTileM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                       (void *)(plane ? xs_lo : xs_hi), gdim, gstr, lower, upper, kChunk,
+                                       kTcTileM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzle,
                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
                 if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
             }
@@ -689,12 +856,12 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
     // weight maps: [tap][cout_pad][cin_pad], box 32 x cout_pad x 1
     const cuuint64_t wdim[3] = {(cuuint64_t)p.cin_pad, (cuuint64_t)p.cout_pad, (cuuint64_t)g.ntaps};
     const cuuint64_t wstr[2] = {(cuuint64_t)p.cin_pad * 4, (cuuint64_t)p.cin_pad * 4 * p.cout_pad};
-    const cuuint32_t box[3] = {(cuuint32_t)kTcChunk, (cuuint32_t)p.cout_pad, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)kChunk, (cuuint32_t)p.cout_pad, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     for (int plane = 0; plane < 2; ++plane) {
         CUresult r = fn.tiled(plane ? &P->b_lo : &P->b_hi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                               (void *)(plane ? w_lo : w_hi), wdim, wstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              kSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
@@ -721,7 +888,7 @@ cudaError_t launch_tc(convt3d_plan_s &p, const float *xs_hi, const float *xs_lo,
     tc.P.y = y;
     tc.P.partials = partials;
     tc.P.status = status;
-    tc.kern<<<tc.grid, kThreads, tc.smem, s>>>(tc.P);
+    tc.kern<<<tc.grid, tc.threads, tc.smem, s>>>(tc.P);
     return cudaGetLastError();
 }
 
