@@ -127,3 +127,20 @@ def test_full_size_workloads(spec, precision):
         sub = E.sample_slice(inputs, n, n + 1)
         ref = run_oracle(spec.replace(N=1), sub)
         assert_close(got[n:n + 1], ref, f"{spec.name}[n={n}]")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("spec", [SMALL[1], SMALL[7], SMALL[5]], ids=lambda s: s.name)
+def test_host_pipeline_matches_device_path(spec):
+    from transposed_convolution_convt3d_gb300 import HostPipeline
+    spec = spec.replace(N=4) if spec.epilogue != E.EPI_SCALE_BATCHNORM_AVGPOOL else spec
+    inputs = E.make_inputs(spec)
+    ref = run_oracle(spec, inputs)
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in inputs.items()}
+    pipe = HostPipeline(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
+                        spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, chunks=2)
+    y_host = torch.full(pipe.full_shape, float("nan")).pin_memory()
+    for _ in range(2):
+        pipe(host["x"], host["w"], y_host, host["bias"], host["gamma"], host["beta"])
+        torch.cuda.synchronize()
+        assert_close(y_host.numpy(), ref, spec.name)

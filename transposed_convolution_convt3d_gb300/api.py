@@ -130,3 +130,72 @@ def convt3d(x, w, bias=None, *, stride=1, pad=0, out_pad=0, epilogue=EPI_IDENTIT
     plan.pack_weights(w, ws)
     plan.forward(x, y, ws, bias, gamma, beta)
     return y
+
+
+class HostPipeline:
+    """Forward from host memory to host memory with the copies overlapped.
+
+    The batch is split into chunks of samples; chunk i's host->device copy,
+    chunk i-1's computation and chunk i-2's device->host copy run on three
+    streams at once.  Valid for the epilogues whose result for a sample depends
+    on that sample only (identity, ReLU+GroupNorm, softmax+sigmoid); the
+    BatchNorm epilogue's batch statistics need the whole batch, so it runs as
+    one chunk.  Host tensors should be pinned for the copies to be asynchronous.
+    Device buffers, plans and streams are created once, here.
+    """
+
+    def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
+                 epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, chunks=4,
+                 device="cuda"):
+        if epilogue == EPI_SCALE_BATCHNORM_AVGPOOL or N % chunks:
+            chunks = 1
+        self.chunks = chunks
+        self.n_chunk = N // chunks
+        args = (Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale, precision)
+        self.plan = Plan(self.n_chunk, *args)
+        self.full_shape = (N,) + self.plan.out_shape[1:]
+        dev = torch.device(device)
+        self.x = torch.empty((N, Cin, D, H, W), dtype=torch.float32, device=dev)
+        self.y = torch.empty(self.full_shape, dtype=torch.float32, device=dev)
+        self.w = torch.empty((Cin, Cout, k, k, k), dtype=torch.float32, device=dev)
+        self.vec = {name: torch.empty(Cout, dtype=torch.float32, device=dev) for name in ("bias", "gamma", "beta")}
+        self.ws = self.plan.new_workspace(dev)
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    def __call__(self, x_host, w_host, y_host, bias=None, gamma=None, beta=None, stream=None):
+        """Run on pinned host tensors; returns y_host.  The work is ordered after
+        `stream` (default: current stream) and `stream` waits for its end."""
+        caller = stream if stream is not None else torch.cuda.current_stream()
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.wait_stream(caller)
+        nc = self.n_chunk
+        with torch.cuda.stream(self.s_in):
+            self.w.copy_(w_host, non_blocking=True)
+            dv = {}
+            for name, t in (("bias", bias), ("gamma", gamma), ("beta", beta)):
+                if t is not None:
+                    self.vec[name].copy_(t, non_blocking=True)
+                    dv[name] = self.vec[name]
+                else:
+                    dv[name] = None
+        in_done = []
+        for i in range(self.chunks):
+            with torch.cuda.stream(self.s_in):
+                self.x[i * nc:(i + 1) * nc].copy_(x_host[i * nc:(i + 1) * nc], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(self.s_in)
+                in_done.append(ev)
+        for i in range(self.chunks):
+            self.s_comp.wait_event(in_done[i])
+            if i == 0:
+                self.plan.pack_weights(self.w, self.ws, self.s_comp)
+            self.plan.forward(self.x[i * nc:(i + 1) * nc], self.y[i * nc:(i + 1) * nc], self.ws, dv["bias"],
+                              dv["gamma"], dv["beta"], self.s_comp)
+            ev = torch.cuda.Event()
+            ev.record(self.s_comp)
+            self.s_out.wait_event(ev)
+            with torch.cuda.stream(self.s_out):
+                y_host[i * nc:(i + 1) * nc].copy_(self.y[i * nc:(i + 1) * nc], non_blocking=True)
+        caller.wait_stream(self.s_out)
+        caller.wait_stream(self.s_comp)
+        return y_host

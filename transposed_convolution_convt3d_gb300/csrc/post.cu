@@ -26,27 +26,46 @@ __device__ __forceinline__ double warp_sum(double v) {
     return v;
 }
 
-// One warp per (n, g).
-__global__ void gn_finalize_kernel(const double *__restrict__ partials, double *__restrict__ stats, int N,
-                                   int G, int T, double count, double eps) {
-    const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
-    const int lane = threadIdx.x % 32;
-    if (w >= N * G) return;
-    const int n = w / G, g = w % G;
+// One block per (n, g): 256 threads stride over the sample's partial rows,
+// then a fixed-order tree reduction (fp64).
+constexpr int kFinThreads = 256;
+
+__device__ __forceinline__ void block_sum2(double &a, double &b, double (*red)[kFinThreads / 32]) {
+    a = warp_sum(a);
+    b = warp_sum(b);
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (lane == 0) {
+        red[0][w] = a;
+        red[1][w] = b;
+    }
+    __syncthreads();
+    if (w == 0) {
+        a = lane < kFinThreads / 32 ? red[0][lane] : 0.0;
+        b = lane < kFinThreads / 32 ? red[1][lane] : 0.0;
+        a = warp_sum(a);
+        b = warp_sum(b);
+    }
+}
+
+__global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const double *__restrict__ partials,
+                                                                  double *__restrict__ stats, int N, int G, int T,
+                                                                  double count, double eps) {
+    __shared__ double red[2][kFinThreads / 32];
+    const int ng = blockIdx.x;
+    const int n = ng / G, g = ng % G;
     double s1 = 0.0, s2 = 0.0;
-    for (int t = lane; t < T; t += 32) {
+    for (int t = threadIdx.x; t < T; t += kFinThreads) {
         const double *p = partials + ((int64_t)n * T + t) * 2 * G + 2 * g;
         s1 += p[0];
         s2 += p[1];
     }
-    s1 = warp_sum(s1);
-    s2 = warp_sum(s2);
-    if (lane == 0) {
+    block_sum2(s1, s2, red);
+    if (threadIdx.x == 0) {
         const double mean = s1 / count;
         double var = s2 / count - mean * mean;
         var = var > 0.0 ? var : 0.0;
-        stats[2 * w] = mean;
-        stats[2 * w + 1] = 1.0 / sqrt(var + eps);
+        stats[2 * ng] = mean;
+        stats[2 * ng + 1] = 1.0 / sqrt(var + eps);
     }
 }
 
@@ -101,7 +120,7 @@ __global__ void __launch_bounds__(kNormThreads) gn_normalize_kernel(float *__res
 }
 
 // Phase 1: per (n, c) the spatial sum S and the sum of squares over the
-// sample's tiles.  Block = 32 channels x 8 tile lanes of one sample.
+// sample's partial rows.  Block = 32 channels x 8 row lanes of one sample.
 __global__ void bn_reduce_kernel(const double *__restrict__ partials, double *__restrict__ sums, int N, int C,
                                  int T) {
     __shared__ double red[2][8][33];
@@ -156,13 +175,10 @@ __global__ void bn_finalize_kernel(const double *__restrict__ sums, const float 
 
 cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, double *stats, cudaStream_t s) {
     const int N = p.g.N, G = p.d.groups;
-    const int warps = N * G;
-    const int threads = 256;
-    const int blocks = (warps * 32 + threads - 1) / threads;
     const double V = (double)p.g.Do * p.g.Ho * p.g.Wo;
     const double count = V * (p.g.Cout / G);
-    gn_finalize_kernel<<<blocks, threads, 0, s>>>(partials, stats, N, G, p.tiles_per_sample * p.stat_rows_per_tile, count,
-                                                  (double)p.d.eps);
+    gn_finalize_kernel<<<N * G, kFinThreads, 0, s>>>(partials, stats, N, G, p.tiles_per_sample * p.stat_rows_per_tile,
+                                                     count, (double)p.d.eps);
     return cudaGetLastError();
 }
 

@@ -92,17 +92,20 @@ struct Tile {
     int gi, n, t, slot;
 };
 
-__device__ __forceinline__ Tile decode(const TcParams &P, int tile) {
+// Tile index -> (group, sample, tile within the sample's q-grid).  Tiles are
+// ordered group by group (heaviest first), then sample, then tile.  `grp` is
+// the shared-memory copy of the group table.
+__device__ __forceinline__ Tile decode(const TcParams &P, const GroupDesc *grp, int tile) {
     Tile r;
     int rem = tile, gi = 0;
-    while (gi + 1 < P.ngroups && rem >= P.N * P.grp[gi].tiles) {
-        rem -= P.N * P.grp[gi].tiles;
+    while (gi + 1 < P.ngroups && rem >= P.N * grp[gi].tiles) {
+        rem -= P.N * grp[gi].tiles;
         ++gi;
     }
     r.gi = gi;
-    r.n = rem / P.grp[gi].tiles;
-    r.t = rem % P.grp[gi].tiles;
-    r.slot = r.n * P.tiles_per_sample + P.grp[gi].tile_prefix + r.t;
+    r.n = rem / grp[gi].tiles;
+    r.t = rem % grp[gi].tiles;
+    r.slot = r.n * P.tiles_per_sample + grp[gi].tile_prefix + r.t;
     return r;
 }
 
@@ -215,6 +218,11 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     __shared__ float s_bias[256];                          // bias, zero-padded to 256 channels
     __shared__ float s_bias_l2e[256];                      // bias * log2(e) (softmax)
     __shared__ float s_xchg[2 * 2 * 4 * kTcTileM];         // softmax (max, sum) exchange, double-buffered
+    // The group, class and tap tables, copied from the parameter block: the
+    // single-thread producer and MMA loops read them on their critical path.
+    __shared__ GroupDesc s_grp[kMaxGroups];
+    __shared__ ClassDesc s_cls[kMaxClasses];
+    __shared__ TapDesc s_taps[kMaxTaps];
 
     // 1024-byte aligned ring of pipeline stages
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -244,6 +252,9 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         s_bias[c] = (P.bias && c < P.Cout) ? P.bias[c] : 0.f;
         s_bias_l2e[c] = s_bias[c] * kLog2e;
     }
+    for (int i = threadIdx.x; i < kMaxTaps; i += blockDim.x) s_taps[i] = P.taps[i];
+    if (threadIdx.x < kMaxGroups) s_grp[threadIdx.x] = P.grp[threadIdx.x];
+    if (threadIdx.x < kMaxClasses) s_cls[threadIdx.x] = P.cls[threadIdx.x];
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), P.tmem_cols);
         ptx::tmem_relinquish();
@@ -257,9 +268,9 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     if (warp == 0) {
         if (lane == 0) {
             for (int gi = 0; gi < P.ngroups; ++gi)
-                for (int ci = 0; ci < P.grp[gi].ncls; ++ci) {
-                    ptx::prefetch_tmap(&P.a_hi[P.grp[gi].cls[ci]]);
-                    ptx::prefetch_tmap(&P.a_lo[P.grp[gi].cls[ci]]);
+                for (int ci = 0; ci < s_grp[gi].ncls; ++ci) {
+                    ptx::prefetch_tmap(&P.a_hi[s_grp[gi].cls[ci]]);
+                    ptx::prefetch_tmap(&P.a_lo[s_grp[gi].cls[ci]]);
                 }
             ptx::prefetch_tmap(&P.b_hi);
             ptx::prefetch_tmap(&P.b_lo);
@@ -268,18 +279,18 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             uint32_t armed = 0, armed_phase = 0;  // per-stage bits: armed at least once, last armed parity
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
-                const Tile T = decode(P, tile);
-                const GroupDesc &G = P.grp[T.gi];
+                const Tile T = decode(P, s_grp, tile);
+                const GroupDesc &G = s_grp[T.gi];
                 const int q0 = T.t * kTcTileM;
                 const int qd0 = q0 / (G.Qh * G.Qw), qh0 = (q0 / G.Qw) % G.Qh, qw0 = q0 % G.Qw;
                 const TileSpan span = tile_span(G, T.t, kTcTileM);
                 for (int ci = 0; ok && ci < G.ncls; ++ci) {
                     const int cls = G.cls[ci];
-                    const ClassDesc &C = P.cls[cls];
+                    const ClassDesc &C = s_cls[cls];
                     const int w0 = qw0 + C.lo_w, h0 = qh0 + C.lo_h, d0 = qd0 + C.lo_d;
-                    const int jfirst = first_live_tap(P.taps, P.Din, P.Hin, P.Win, span, C);
+                    const int jfirst = first_live_tap(s_taps, P.Din, P.Hin, P.Win, span, C);
                     for (int j = jfirst; ok && j < C.ntaps; ++j) {
-                        const TapDesc td = P.taps[C.tap_begin + j];
+                        const TapDesc td = s_taps[C.tap_begin + j];
                         if (j != jfirst && !tap_live(span, td, P.Din, P.Hin, P.Win)) continue;
                         const uint16_t ow = (uint16_t)(td.dw - C.lo_w);
                         const uint16_t oh = (uint16_t)(td.dh - C.lo_h);
@@ -338,8 +349,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             int iter = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++iter) {
-                const Tile T = decode(P, tile);
-                const GroupDesc &G = P.grp[T.gi];
+                const Tile T = decode(P, s_grp, tile);
+                const GroupDesc &G = s_grp[T.gi];
                 const int acc = iter & 1;
                 const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
                 if (!ptx::mbar_wait_bounded(tempty0 + 8 * acc, aph ^ 1u, &abort_flag, kWaitNs)) {
@@ -349,13 +360,13 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 ptx::tc_fence_after();
                 const TileSpan span = tile_span(G, T.t, kTcTileM);
                 for (int ci = 0; ok && ci < G.ncls; ++ci) {
-                    const ClassDesc &C = P.cls[G.cls[ci]];
+                    const ClassDesc &C = s_cls[G.cls[ci]];
                     const uint32_t d_tmem = tmem_base + (uint32_t)acc * P.acc_stride + (uint32_t)ci * P.cout_pad;
                     // same tap sequence as the producer: live taps only, the first always
-                    const int jfirst = first_live_tap(P.taps, P.Din, P.Hin, P.Win, span, C);
+                    const int jfirst = first_live_tap(s_taps, P.Din, P.Hin, P.Win, span, C);
                     bool first = true;
                     for (int j = jfirst; ok && j < C.ntaps; ++j) {
-                        if (j != jfirst && !tap_live(span, P.taps[C.tap_begin + j], P.Din, P.Hin, P.Win)) continue;
+                        if (j != jfirst && !tap_live(span, s_taps[C.tap_begin + j], P.Din, P.Hin, P.Win)) continue;
                         for (int kc = 0; kc < P.kc; ++kc) {
                             if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
                                 ok = false;
@@ -419,8 +430,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         };
         int iter = 0;
         for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++iter) {
-            const Tile T = decode(P, tile);
-            const GroupDesc &G = P.grp[T.gi];
+            const Tile T = decode(P, s_grp, tile);
+            const GroupDesc &G = s_grp[T.gi];
             const int acc = iter & 1;
             const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
             if (!ptx::mbar_wait_bounded(tfull0 + 8 * acc, aph, &abort_flag, kWaitNs, 200)) {
@@ -432,8 +443,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             __syncwarp();
 
             int off[2];
-            off[0] = row_offset(P, G, P.cls[G.cls[0]], T.t, m);
-            off[1] = G.ncls > 1 ? row_offset(P, G, P.cls[G.cls[1]], T.t, m) : -1;
+            off[0] = row_offset(P, G, s_cls[G.cls[0]], T.t, m);
+            off[1] = G.ncls > 1 ? row_offset(P, G, s_cls[G.cls[1]], T.t, m) : -1;
             // Stride-2 pairs write (even, odd) columns of one output row together.
             const bool pair_store = G.ncls == 2 && (P.Wo % 2 == 0);
             float *yn = P.y + (int64_t)T.n * C * V;
