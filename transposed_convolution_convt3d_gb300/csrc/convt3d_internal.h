@@ -51,41 +51,36 @@ struct GroupDesc {
     int ksteps;             // K steps per tile (all classes of the group)
 };
 
-// Ranges of q-grid coordinates that the valid rows of tile t cover
-// (conservative: a dimension is taken whole once the tile wraps in an outer one).
-struct TileSpan {
-    int d0, d1, h0, h1, w0, w1;
+// Taps a tile issues.  Along d, a class's taps have consecutive decreasing
+// input offsets delta = hi, hi-1, ..., hi-nt_d+1 (taps are enumerated d-major in
+// increasing kernel index, and delta = (r + p - t)/stride), so the d-slices
+// whose input plane q + delta lies inside [0, Din) for some row of the tile form
+// one contiguous range [a0, a1].  The tile issues taps [a0 * nhw, (a1+1) * nhw)
+// of the class (nhw = taps per d-slice), or just tap 0 when no slice is live --
+// that zero-filled product still initialises the accumulator.
+struct TapRange {
+    int begin, end;
 };
 
-__host__ __device__ inline TileSpan tile_span(const GroupDesc &G, int t, int tile_m) {
+__host__ __device__ inline TapRange tile_taps(const GroupDesc &G, const ClassDesc &C, int t, int tile_m, int Din) {
     const int q0 = t * tile_m;
     const int q1 = (q0 + tile_m < G.vol ? q0 + tile_m : G.vol) - 1;
     const int qhw = G.Qh * G.Qw;
-    TileSpan r;
-    r.d0 = q0 / qhw;
-    r.d1 = q1 / qhw;
-    if (r.d0 == r.d1) {
-        r.h0 = (q0 / G.Qw) % G.Qh;
-        r.h1 = (q1 / G.Qw) % G.Qh;
+    const int d0 = q0 / qhw, d1 = q1 / qhw;
+    const int hi = C.lo_d + C.nt_d - 1;  // offset of d-slice 0
+    int a0 = d0 + hi - (Din - 1), a1 = d1 + hi;
+    a0 = a0 > 0 ? a0 : 0;
+    a1 = a1 < C.nt_d - 1 ? a1 : C.nt_d - 1;
+    const int nhw = C.nt_h * C.nt_w;
+    TapRange r;
+    if (a0 > a1 || C.ntaps == 0) {
+        r.begin = 0;
+        r.end = C.ntaps > 0 ? 1 : 0;
     } else {
-        r.h0 = 0;
-        r.h1 = G.Qh - 1;
-    }
-    if (r.d0 == r.d1 && r.h0 == r.h1) {
-        r.w0 = q0 % G.Qw;
-        r.w1 = q1 % G.Qw;
-    } else {
-        r.w0 = 0;
-        r.w1 = G.Qw - 1;
+        r.begin = a0 * nhw;
+        r.end = (a1 + 1) * nhw;
     }
     return r;
-}
-
-// A tap contributes to a tile unless its input index (q + delta) falls
-// outside the input for every row of the tile in some dimension.
-__host__ __device__ inline bool tap_live(const TileSpan &r, const TapDesc &td, int Din, int Hin, int Win) {
-    return r.d1 + td.dd >= 0 && r.d0 + td.dd < Din && r.h1 + td.dh >= 0 && r.h0 + td.dh < Hin &&
-           r.w1 + td.dw >= 0 && r.w0 + td.dw < Win;
 }
 
 struct Geometry {
@@ -112,23 +107,6 @@ struct FfmaParams {
     ClassDesc cls[kMaxClasses];
     TapDesc taps[kMaxTaps];
 };
-
-// First tap of a class that a tile issues; when no tap is live the first tap
-// still runs (its zero-filled product initialises the accumulator).
-__host__ __device__ inline int first_live_tap(const TapDesc *taps, int Din, int Hin, int Win, const TileSpan &r,
-                                              const ClassDesc &C) {
-    for (int j = 0; j < C.ntaps; ++j)
-        if (tap_live(r, taps[C.tap_begin + j], Din, Hin, Win)) return j;
-    return 0;
-}
-
-// Taps of class C that a tile issues (live taps, and at least one).
-__host__ __device__ inline int issued_taps(const TapDesc *taps, int Din, int Hin, int Win, const TileSpan &r,
-                                           const ClassDesc &C) {
-    int n = 0;
-    for (int j = 0; j < C.ntaps; ++j) n += tap_live(r, taps[C.tap_begin + j], Din, Hin, Win) ? 1 : 0;
-    return n > 0 ? n : 1;
-}
 
 }  // namespace convt3d
 

@@ -357,10 +357,14 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
         const GroupDesc &G = p->grp[i];
         double taps = 0;
         for (int t = 0; t < G.tiles; ++t) {
-            const TileSpan span = tile_span(G, t, p->tile_m);
             for (int c = 0; c < G.ncls; ++c) {
                 const ClassDesc &C = g.cls[G.cls[c]];
-                taps += p->tc ? issued_taps(g.taps, g.Din, g.Hin, g.Win, span, C) : C.ntaps;
+                if (p->tc) {
+                    const TapRange r = tile_taps(G, C, t, p->tile_m, g.Din);
+                    taps += r.end - r.begin;
+                } else {
+                    taps += C.ntaps;
+                }
             }
         }
         issued += 2.0 * (double)d.N * p->tile_m * p->cout_pad * (double)p->cin_pad * taps;

@@ -53,7 +53,7 @@ struct EpiCfg {
     static constexpr int threads = 64 + 32 * warps;  // producer warp, MMA warp, epilogue warps
 };
 constexpr int kMaxThreads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 8;  // the MMA issue dispatches stage indices 0..7
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 // Input channels per K step: 32 (128-byte rows, 128-byte swizzle) or 16
 // (64-byte rows, 64-byte swizzle: half-size stages, twice as many of them).
@@ -218,11 +218,9 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     __shared__ float s_bias[256];                          // bias, zero-padded to 256 channels
     __shared__ float s_bias_l2e[256];                      // bias * log2(e) (softmax)
     __shared__ float s_xchg[2 * 2 * 4 * kTcTileM];         // softmax (max, sum) exchange, double-buffered
-    // The group, class and tap tables, copied from the parameter block: the
-    // single-thread producer and MMA loops read them on their critical path.
+    // The group and class tables for the epilogue warps.
     __shared__ GroupDesc s_grp[kMaxGroups];
     __shared__ ClassDesc s_cls[kMaxClasses];
-    __shared__ TapDesc s_taps[kMaxTaps];
 
     // 1024-byte aligned ring of pipeline stages
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -252,7 +250,6 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         s_bias[c] = (P.bias && c < P.Cout) ? P.bias[c] : 0.f;
         s_bias_l2e[c] = s_bias[c] * kLog2e;
     }
-    for (int i = threadIdx.x; i < kMaxTaps; i += blockDim.x) s_taps[i] = P.taps[i];
     if (threadIdx.x < kMaxGroups) s_grp[threadIdx.x] = P.grp[threadIdx.x];
     if (threadIdx.x < kMaxClasses) s_cls[threadIdx.x] = P.cls[threadIdx.x];
     if (warp == 1) {
@@ -265,12 +262,15 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     const uint32_t tmem_base = tmem_slot;
 
     // ------------------------------------------------------------ producer
+    // The producer and MMA loops read only the kernel parameters and loop
+    // counters, so their control flow stays uniform; the MMA issue rate depends
+    // on it.
     if (warp == 0) {
         if (lane == 0) {
             for (int gi = 0; gi < P.ngroups; ++gi)
-                for (int ci = 0; ci < s_grp[gi].ncls; ++ci) {
-                    ptx::prefetch_tmap(&P.a_hi[s_grp[gi].cls[ci]]);
-                    ptx::prefetch_tmap(&P.a_lo[s_grp[gi].cls[ci]]);
+                for (int ci = 0; ci < P.grp[gi].ncls; ++ci) {
+                    ptx::prefetch_tmap(&P.a_hi[P.grp[gi].cls[ci]]);
+                    ptx::prefetch_tmap(&P.a_lo[P.grp[gi].cls[ci]]);
                 }
             ptx::prefetch_tmap(&P.b_hi);
             ptx::prefetch_tmap(&P.b_lo);
@@ -279,19 +279,17 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             uint32_t armed = 0, armed_phase = 0;  // per-stage bits: armed at least once, last armed parity
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
-                const Tile T = decode(P, s_grp, tile);
-                const GroupDesc &G = s_grp[T.gi];
+                const Tile T = decode(P, P.grp, tile);
+                const GroupDesc &G = P.grp[T.gi];
                 const int q0 = T.t * kTcTileM;
                 const int qd0 = q0 / (G.Qh * G.Qw), qh0 = (q0 / G.Qw) % G.Qh, qw0 = q0 % G.Qw;
-                const TileSpan span = tile_span(G, T.t, kTcTileM);
                 for (int ci = 0; ok && ci < G.ncls; ++ci) {
                     const int cls = G.cls[ci];
-                    const ClassDesc &C = s_cls[cls];
+                    const ClassDesc &C = P.cls[cls];
                     const int w0 = qw0 + C.lo_w, h0 = qh0 + C.lo_h, d0 = qd0 + C.lo_d;
-                    const int jfirst = first_live_tap(s_taps, P.Din, P.Hin, P.Win, span, C);
-                    for (int j = jfirst; ok && j < C.ntaps; ++j) {
-                        const TapDesc td = s_taps[C.tap_begin + j];
-                        if (j != jfirst && !tap_live(span, td, P.Din, P.Hin, P.Win)) continue;
+                    const TapRange tr = tile_taps(G, C, T.t, kTcTileM, P.Din);
+                    for (int j = tr.begin; ok && j < tr.end; ++j) {
+                        const TapDesc td = P.taps[C.tap_begin + j];
                         const uint16_t ow = (uint16_t)(td.dw - C.lo_w);
                         const uint16_t oh = (uint16_t)(td.dh - C.lo_h);
                         const uint16_t od = (uint16_t)(td.dd - C.lo_d);
@@ -339,18 +337,13 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = ptx::idesc_tf32((uint32_t)P.cout_pad);
-            // A descriptor's start-address field is the byte address >> 4, so the
-            // descriptors of every stage and K slice are one base plus an offset.
-            const uint64_t desc0 = ptx::sdesc_k_swizzled(smem_base, kRowBytes);
-            const uint64_t d_alo = kABytes >> 4, d_bhi = (2 * kABytes) >> 4,
-                           d_blo = (2 * kABytes + P.b_bytes) >> 4;
             int stage = 0;
             uint32_t phase = 0;
             int iter = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++iter) {
-                const Tile T = decode(P, s_grp, tile);
-                const GroupDesc &G = s_grp[T.gi];
+                const Tile T = decode(P, P.grp, tile);
+                const GroupDesc &G = P.grp[T.gi];
                 const int acc = iter & 1;
                 const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
                 if (!ptx::mbar_wait_bounded(tempty0 + 8 * acc, aph ^ 1u, &abort_flag, kWaitNs)) {
@@ -358,39 +351,34 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     break;
                 }
                 ptx::tc_fence_after();
-                const TileSpan span = tile_span(G, T.t, kTcTileM);
                 for (int ci = 0; ok && ci < G.ncls; ++ci) {
-                    const ClassDesc &C = s_cls[G.cls[ci]];
+                    const ClassDesc &C = P.cls[G.cls[ci]];
                     const uint32_t d_tmem = tmem_base + (uint32_t)acc * P.acc_stride + (uint32_t)ci * P.cout_pad;
-                    // same tap sequence as the producer: live taps only, the first always
-                    const int jfirst = first_live_tap(s_taps, P.Din, P.Hin, P.Win, span, C);
-                    bool first = true;
-                    for (int j = jfirst; ok && j < C.ntaps; ++j) {
-                        if (j != jfirst && !tap_live(span, s_taps[C.tap_begin + j], P.Din, P.Hin, P.Win)) continue;
-                        for (int kc = 0; kc < P.kc; ++kc) {
-                            if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
-                                ok = false;
-                                break;
-                            }
-                            ptx::tc_fence_after();
-                            const uint64_t ds = desc0 + ((uint64_t)stage * P.stage_bytes >> 4);
+                    const TapRange tr = tile_taps(G, C, T.t, kTcTileM, P.Din);  // same taps as the producer
+                    const int nsteps = (tr.end - tr.begin) * P.kc;
+                    for (int s = 0; s < nsteps; ++s) {
+                        if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
 #pragma unroll
-                            for (int kk = 0; kk < kChunk / 8; ++kk) {  // 8 TF32 (32 bytes) per MMA
-                                const uint64_t a_hi = ds + (uint64_t)(kk * 2);
-                                const uint64_t a_lo = a_hi + d_alo;
-                                const uint64_t b_hi = a_hi + d_bhi;
-                                const uint64_t b_lo = a_hi + d_blo;
-                                // the class's first product overwrites the accumulator
-                                ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (first && kk == 0) ? 0u : 1u);
-                                ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
-                                ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
-                            }
-                            first = false;
-                            ptx::mma_commit(empty0 + 8 * stage);
-                            if (++stage == P.stages) {
-                                stage = 0;
-                                phase ^= 1u;
-                            }
+                        for (int kk = 0; kk < kChunk / 8; ++kk) {  // 8 TF32 (32 bytes) per MMA
+                            const uint64_t a_hi = ptx::sdesc_k_swizzled(sb + kk * 32, kRowBytes);
+                            const uint64_t a_lo = ptx::sdesc_k_swizzled(sb + kABytes + kk * 32, kRowBytes);
+                            const uint64_t b_hi = ptx::sdesc_k_swizzled(sb + 2 * kABytes + kk * 32, kRowBytes);
+                            const uint64_t b_lo =
+                                ptx::sdesc_k_swizzled(sb + 2 * kABytes + P.b_bytes + kk * 32, kRowBytes);
+                            // the class's first product overwrites the accumulator
+                            ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (s | kk) ? 1u : 0u);
+                            ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+                            ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                        }
+                        ptx::mma_commit(empty0 + 8 * stage);
+                        if (++stage == P.stages) {
+                            stage = 0;
+                            phase ^= 1u;
                         }
                     }
                 }
