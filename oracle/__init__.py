@@ -11,14 +11,16 @@ Functions whose pins live in ``tests/test_oracle_pins.py``:
   convt3d_scatter  -- pinned by the 1-D worked examples (l2_p61), the stride-2
                       tap table (l2_p49), the stride-1 flipped-kernel identity,
                       the adjoint identity, linearity, the pooled-sum closed form
-  forward          -- epilogues pinned by GN / softmax / BN invariants and the
-                      BN+pool closed form (l2_p77)
+  forward          -- epilogues pinned by GN / softmax / BN invariants, the
+                      BN+pool closed form (l2_p77), and PyTorch CPU fp64
+                      batch_norm in evaluation mode and its running statistics
   count_products   -- pinned by the product count printed on page l2_p49
 """
 from .oracle import (  # noqa: F401
     EPI_IDENTITY,
     EPI_RELU_GROUPNORM,
     EPI_SCALE_BATCHNORM_AVGPOOL,
+    EPI_SCALE_BATCHNORM_EVAL_AVGPOOL,
     EPI_SOFTMAX_SIGMOID,
     build,
     convt3d_scatter,

@@ -3,8 +3,10 @@
  *
  * A plain, slow, obviously-correct CPU statement of what the GPU library
  * computes: a dense 3-D transposed convolution in its scatter (adjoint) form,
- * accumulated in fp64, followed by one of four epilogues evaluated literally
- * in fp64.  Nothing in the product path may link, load or call this file; only
+ * accumulated in fp64, followed by one of five epilogues evaluated literally
+ * in fp64 (identity, ReLU+GroupNorm, scale+BatchNorm with batch statistics
+ * (optionally updating running statistics)+pool, softmax+sigmoid,
+ * scale+BatchNorm in evaluation mode+pool).  Nothing in the product path may link, load or call this file; only
  * the test suite, the smoke check and the benchmark's CPU-baseline arm do.
  * It shares no code, header, table or helper with the CUDA library.
  *
@@ -34,7 +36,8 @@
 #endif
 
 enum { ORACLE_EPI_IDENTITY = 0, ORACLE_EPI_RELU_GROUPNORM = 1,
-       ORACLE_EPI_SCALE_BATCHNORM_AVGPOOL = 2, ORACLE_EPI_SOFTMAX_SIGMOID = 3 };
+       ORACLE_EPI_SCALE_BATCHNORM_AVGPOOL = 2, ORACLE_EPI_SOFTMAX_SIGMOID = 3,
+       ORACLE_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL = 4 };
 
 /* Output extent of a transposed convolution along one dimension (dilation 1):
  * (in - 1) * stride - 2 * pad + k + out_pad.  Page l2_p49 states the general
@@ -219,23 +222,76 @@ static void epi_scale_bn_avgpool(int N, int C, long vol, double scale, double ep
     }
 }
 
+/* Multiply by scale, BatchNorm3d in evaluation mode, AdaptiveAvgPool3d(1)
+ * (page l2_p77's submitted solution assumes evaluation mode): each element is
+ * normalised with the stored running statistics,
+ * (z - running_mean[c]) / sqrt(running_var[c] + eps) * gamma + beta, then the
+ * spatial mean per (n, c).  Written element by element.  out is [N, C]. */
+static void epi_scale_bn_eval_avgpool(int N, int C, long vol, double scale, double eps,
+                                      const float *gamma, const float *beta,
+                                      const float *rmean, const float *rvar,
+                                      const double *Y, double *out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long nc = 0; nc < (long)N * C; ++nc) {
+        const long c = nc % C;
+        const double inv = 1.0 / sqrt((double)rvar[c] + eps);
+        const double ga = gamma ? (double)gamma[c] : 1.0;
+        const double be = beta ? (double)beta[c] : 0.0;
+        const double *row = Y + nc * vol;
+        double acc = 0.0;
+        for (long o = 0; o < vol; ++o) acc += (scale * row[o] - (double)rmean[c]) * inv * ga + be;
+        out[nc] = acc / (double)vol;
+    }
+}
+
+/* BatchNorm3d's running-statistics update in training mode (page l2_p77,
+ * "momentum=0.1"): with the batch mean and the biased batch variance of
+ * z = scale * Y over the n = N * vol elements of each channel,
+ * running_mean <- (1 - m) * running_mean + m * mean and
+ * running_var  <- (1 - m) * running_var  + m * var * n / (n - 1). */
+static void bn_update_running(int N, int C, long vol, double scale, double momentum, const double *Y,
+                              float *rmean, float *rvar) {
+    const double cnt = (double)N * (double)vol;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long c = 0; c < C; ++c) {
+        double sum = 0.0;
+        for (long n = 0; n < N; ++n)
+            for (long o = 0; o < vol; ++o) sum += scale * Y[(n * C + c) * vol + o];
+        const double mean = sum / cnt;
+        double ss = 0.0;
+        for (long n = 0; n < N; ++n)
+            for (long o = 0; o < vol; ++o) {
+                const double d = scale * Y[(n * C + c) * vol + o] - mean;
+                ss += d * d;
+            }
+        const double var_unbiased = cnt > 1.0 ? ss / (cnt - 1.0) : 0.0;
+        rmean[c] = (float)((1.0 - momentum) * (double)rmean[c] + momentum * mean);
+        rvar[c] = (float)((1.0 - momentum) * (double)rvar[c] + momentum * var_unbiased);
+    }
+}
+
 /* Full forward: scatter-form transposed convolution (+bias), then the
  * epilogue, all in fp64; results are rounded once to fp32 (round to nearest
  * even) into y.  If y64 is not NULL the fp64 results are also written there.
- * For the BN+pool epilogue y / y64 hold [N, Cout]; otherwise
- * [N, Cout, Do, Ho, Wo].  Returns 0, -1 on a bad argument, -2 if out of memory. */
+ * For the BN+pool epilogues y / y64 hold [N, Cout]; otherwise
+ * [N, Cout, Do, Ho, Wo].  running_mean / running_var: read by the
+ * evaluation-mode epilogue; updated in place by the batch-statistics epilogue
+ * when both are given (NULL skips the update).  Returns 0, -1 on a bad
+ * argument, -2 if out of memory. */
 int oracle_convt3d_forward(int N, int Cin, int Cout, int Din, int Hin, int Win,
                            int k, int s, int p, int op,
                            const float *x, const float *w, const float *bias,
                            int epilogue, int groups, double eps, double scale,
                            const float *gamma, const float *beta,
+                           float *running_mean, float *running_var, double momentum,
                            float *y, double *y64) {
     const long Do = oracle_output_size(Din, k, s, p, op);
     const long Ho = oracle_output_size(Hin, k, s, p, op);
     const long Wo = oracle_output_size(Win, k, s, p, op);
     if (N <= 0 || Do <= 0 || Ho <= 0 || Wo <= 0) return -1;
     if (epilogue == ORACLE_EPI_RELU_GROUPNORM && (groups <= 0 || Cout % groups)) return -1;
-    if (epilogue < 0 || epilogue > 3) return -1;
+    if (epilogue < 0 || epilogue > 4) return -1;
+    if (epilogue == ORACLE_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL && (!running_mean || !running_var)) return -1;
     const long vol = Do * Ho * Wo;
     const long total = (long)N * Cout * vol;
     double *Y = (double *)malloc(sizeof(double) * (size_t)total);
@@ -243,10 +299,17 @@ int oracle_convt3d_forward(int N, int Cin, int Cout, int Din, int Hin, int Win,
     int rc = oracle_convt3d_scatter(N, Cin, Cout, Din, Hin, Win, k, s, p, op, x, w, bias, Y);
     if (rc) { free(Y); return rc; }
 
-    if (epilogue == ORACLE_EPI_SCALE_BATCHNORM_AVGPOOL) {
+    if (epilogue == ORACLE_EPI_SCALE_BATCHNORM_AVGPOOL || epilogue == ORACLE_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) {
         double *pooled = (double *)malloc(sizeof(double) * (size_t)N * Cout);
         if (!pooled) { free(Y); return -2; }
-        epi_scale_bn_avgpool(N, Cout, vol, scale, eps, gamma, beta, Y, pooled);
+        if (epilogue == ORACLE_EPI_SCALE_BATCHNORM_AVGPOOL) {
+            epi_scale_bn_avgpool(N, Cout, vol, scale, eps, gamma, beta, Y, pooled);
+            if (running_mean && running_var)
+                bn_update_running(N, Cout, vol, scale, momentum, Y, running_mean, running_var);
+        } else {
+            epi_scale_bn_eval_avgpool(N, Cout, vol, scale, eps, gamma, beta, running_mean, running_var, Y,
+                                      pooled);
+        }
         for (long i = 0; i < (long)N * Cout; ++i) {
             y[i] = (float)pooled[i];
             if (y64) y64[i] = pooled[i];

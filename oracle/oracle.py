@@ -17,6 +17,7 @@ EPI_IDENTITY = 0
 EPI_RELU_GROUPNORM = 1
 EPI_SCALE_BATCHNORM_AVGPOOL = 2
 EPI_SOFTMAX_SIGMOID = 3
+EPI_SCALE_BATCHNORM_EVAL_AVGPOOL = 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 # A different source may be named for mutation testing of the pins themselves.
@@ -58,7 +59,7 @@ def _load():
         lib.oracle_count_products.argtypes = [i] * 10 + [P, P]
         lib.oracle_convt3d_forward.restype = i
         lib.oracle_convt3d_forward.argtypes = (
-            [i] * 10 + [P, P, P, i, i, ctypes.c_double, ctypes.c_double, P, P, P, P])
+            [i] * 10 + [P, P, P, i, i, ctypes.c_double, ctypes.c_double, P, P, P, P, ctypes.c_double, P, P])
         _lib = lib
         return lib
 
@@ -115,22 +116,28 @@ def count_products(N, Cin, Cout, Din, Hin, Win, k, stride, pad, out_pad):
 
 
 def forward(x, w, bias=None, *, stride=1, pad=0, out_pad=0, epilogue=EPI_IDENTITY,
-            groups=1, eps=1e-5, scale=1.0, gamma=None, beta=None, want_f64=False):
+            groups=1, eps=1e-5, scale=1.0, gamma=None, beta=None, running_mean=None,
+            running_var=None, momentum=0.1, want_f64=False):
     """Transposed convolution + epilogue, fp64 inside, fp32 result.
 
     Returns y (float32) or (y, y64) when ``want_f64``.  Shapes: [N,Cout,Do,Ho,Wo],
-    or [N,Cout,1,1,1] for the BN+pool epilogue.
+    or [N,Cout,1,1,1] for the BN+pool epilogues.  running_mean / running_var
+    (float32 [Cout]) are read by the evaluation-mode epilogue and updated in
+    place by the batch-statistics one.
     """
     x, w = _f32(x, "x"), _f32(w, "w")
     bias, gamma, beta = _f32(bias, "bias"), _f32(gamma, "gamma"), _f32(beta, "beta")
+    running_mean, running_var = _f32(running_mean, "running_mean"), _f32(running_var, "running_var")
     k = w.shape[2]
     N, Cin, Cout, Din, Hin, Win, Do, Ho, Wo = _shape(x, w, k, stride, pad, out_pad)
-    shape = (N, Cout, 1, 1, 1) if epilogue == EPI_SCALE_BATCHNORM_AVGPOOL else (N, Cout, Do, Ho, Wo)
+    pooled = epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
+    shape = (N, Cout, 1, 1, 1) if pooled else (N, Cout, Do, Ho, Wo)
     y = np.empty(shape, np.float32)
     y64 = np.empty(shape, np.float64) if want_f64 else None
     rc = _load().oracle_convt3d_forward(N, Cin, Cout, Din, Hin, Win, k, stride, pad, out_pad,
                                         _ptr(x), _ptr(w), _ptr(bias), int(epilogue), int(groups),
                                         float(eps), float(scale), _ptr(gamma), _ptr(beta),
+                                        _ptr(running_mean), _ptr(running_var), float(momentum),
                                         _ptr(y), _ptr(y64))
     if rc:
         raise ValueError(f"oracle_convt3d_forward failed ({rc})")

@@ -28,6 +28,10 @@ MUTATIONS = {
     "w_bound_off_by_one": ("if (ow < 0 || ow >= Wo) continue;", "if (ow < 0 || ow > Wo) continue;"),
     "softmax_no_norm": ("const double t = exp(col[(long)c * vol] - m) / S;",
                         "const double t = exp(col[(long)c * vol] - m);"),
+    "running_var_biased": ("const double var_unbiased = cnt > 1.0 ? ss / (cnt - 1.0) : 0.0;",
+                           "const double var_unbiased = cnt > 1.0 ? ss / cnt : 0.0;"),
+    "eval_bn_eps_outside": ("const double inv = 1.0 / sqrt((double)rvar[c] + eps);",
+                            "const double inv = 1.0 / (sqrt((double)rvar[c]) + eps);"),
 }
 
 

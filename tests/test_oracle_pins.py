@@ -385,3 +385,61 @@ def test_rejects_bad_arguments():
         oracle.forward(x, w, epilogue=oracle.EPI_RELU_GROUPNORM, groups=4)  # 6 % 4 != 0
     with pytest.raises(ValueError):
         oracle.forward(x, w, epilogue=7)
+
+
+def test_batchnorm_eval_pool_matches_torch_cpu_fp64():
+    rng = np.random.default_rng(71)
+    N, C = 2, 5
+    x, w, b = rand_case(rng, N, 3, C, 3, 4, 3, 3)
+    gamma = rng.uniform(0.5, 1.5, C).astype(np.float32)
+    beta = rng.uniform(-0.5, 0.5, C).astype(np.float32)
+    rm = rng.uniform(-0.2, 0.2, C).astype(np.float32)
+    rv = rng.uniform(0.5, 2.0, C).astype(np.float32)
+    _, out = oracle.forward(x, w, b, epilogue=oracle.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, scale=2.0, eps=1e-5,
+                            gamma=gamma, beta=beta, running_mean=rm, running_var=rv, want_f64=True)
+    t = F.conv_transpose3d(torch.from_numpy(x).double(), torch.from_numpy(w).double(),
+                           torch.from_numpy(b).double()) * 2.0
+    z = F.batch_norm(t, torch.from_numpy(rm).double(), torch.from_numpy(rv).double(),
+                     torch.from_numpy(gamma).double(), torch.from_numpy(beta).double(), training=False, eps=1e-5)
+    ref = F.adaptive_avg_pool3d(z, 1).numpy()
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def test_batchnorm_running_stats_match_torch_cpu_fp64():
+    rng = np.random.default_rng(73)
+    N, C, m = 3, 4, 0.1
+    x, w, b = rand_case(rng, N, 3, C, 3, 3, 4, 3)
+    gamma = rng.uniform(0.5, 1.5, C).astype(np.float32)
+    beta = rng.uniform(-0.5, 0.5, C).astype(np.float32)
+    rm = rng.uniform(-0.2, 0.2, C).astype(np.float32)
+    rv = rng.uniform(0.5, 2.0, C).astype(np.float32)
+    rm_t, rv_t = torch.from_numpy(rm.copy()).double(), torch.from_numpy(rv.copy()).double()
+    oracle.forward(x, w, b, epilogue=oracle.EPI_SCALE_BATCHNORM_AVGPOOL, scale=2.0, eps=1e-5, gamma=gamma,
+                   beta=beta, running_mean=rm, running_var=rv, momentum=m)
+    t = F.conv_transpose3d(torch.from_numpy(x).double(), torch.from_numpy(w).double(),
+                           torch.from_numpy(b).double()) * 2.0
+    F.batch_norm(t, rm_t, rv_t, torch.from_numpy(gamma).double(), torch.from_numpy(beta).double(),
+                 training=True, momentum=m, eps=1e-5)
+    # stored in fp32 after an fp64 update
+    assert np.max(np.abs(rm - rm_t.numpy())) < 1e-6
+    assert np.max(np.abs(rv - rv_t.numpy())) < 1e-6
+
+
+def test_batchnorm_eval_with_batch_statistics_equals_training_output():
+    # evaluation-mode normalisation with the batch's own mean and biased variance
+    # reproduces the batch-statistics epilogue
+    rng = np.random.default_rng(79)
+    N, C, s = 2, 3, 0.5
+    x, w, b = rand_case(rng, N, 2, C, 3, 3, 3, 3)
+    Y = oracle.convt3d_scatter(x, w, b)
+    z = s * Y
+    mean = z.mean(axis=(0, 2, 3, 4)).astype(np.float32)
+    var = z.var(axis=(0, 2, 3, 4))
+    gamma = rng.uniform(0.5, 1.5, C).astype(np.float32)
+    beta = rng.uniform(-0.5, 0.5, C).astype(np.float32)
+    _, train = oracle.forward(x, w, b, epilogue=oracle.EPI_SCALE_BATCHNORM_AVGPOOL, scale=s, gamma=gamma,
+                              beta=beta, want_f64=True)
+    # the stored statistics are fp32: the bound covers their rounding
+    _, ev = oracle.forward(x, w, b, epilogue=oracle.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, scale=s, gamma=gamma,
+                           beta=beta, running_mean=mean, running_var=var.astype(np.float32), want_f64=True)
+    assert np.max(np.abs(ev - train)) < 1e-5
