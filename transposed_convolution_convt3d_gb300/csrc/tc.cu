@@ -192,6 +192,60 @@ __device__ __forceinline__ float sigmoid_unit(float t) {
     return fmaf(0.5f * u, p, 0.5f);
 }
 
+// Packed two-lane fp32 arithmetic (fma/mul.rn.f32x2): one instruction on a
+// (class 0, class 1) pair of values.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// sigmoid_unit on a pair (same series, packed arithmetic).
+__device__ __forceinline__ float2 sigmoid_unit2(float2 t) {
+    const float2 u = mul2(make_float2(0.5f, 0.5f), t), u2 = mul2(u, u);
+    float2 p = make_float2(21844.0f / 6081075.0f, 21844.0f / 6081075.0f);
+    p = fma2(p, u2, make_float2(-1382.0f / 155925.0f, -1382.0f / 155925.0f));
+    p = fma2(p, u2, make_float2(62.0f / 2835.0f, 62.0f / 2835.0f));
+    p = fma2(p, u2, make_float2(-17.0f / 315.0f, -17.0f / 315.0f));
+    p = fma2(p, u2, make_float2(2.0f / 15.0f, 2.0f / 15.0f));
+    p = fma2(p, u2, make_float2(-1.0f / 3.0f, -1.0f / 3.0f));
+    p = fma2(p, u2, make_float2(1.0f, 1.0f));
+    return fma2(mul2(make_float2(0.5f, 0.5f), u), p, make_float2(0.5f, 0.5f));
+}
+
+// Pairwise reductions of 16 values (4 dependent levels instead of 15).
+__device__ __forceinline__ float tree_max16(const float (&v)[16]) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = fmaxf(v[i], v[i + 8]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = fmaxf(a[i], a[i + 4]);
+    return fmaxf(fmaxf(a[0], a[2]), fmaxf(a[1], a[3]));
+}
+
+__device__ __forceinline__ float tree_sum16(const float (&v)[16]) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = v[i] + v[i + 8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = a[i] + a[i + 4];
+    return (a[0] + a[2]) + (a[1] + a[3]);
+}
+
 // Position of epilogue row m of a tile for one class: output offset within a
 // channel plane, or -1 when the row lies past the q-grid or the output.
 __device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G, const ClassDesc &C, int t, int m) {
@@ -458,20 +512,15 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, ev[ci]);
                     ptx::tmem_wait_ld();
                     _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
-                        float cm = mx[ci];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
+                        for (int i = 0; i < 16; ++i)
                             ev[ci][i] = (c0 + i < C) ? fmaf(ev[ci][i], kLog2e, s_bias_l2e[c0 + i]) : -INFINITY;
-                            cm = fmaxf(cm, ev[ci][i]);
-                        }
-                        float cs = mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - cm);
+                        const float cm = fmaxf(mx[ci], tree_max16(ev[ci]));
+                        const float old = mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - cm);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            ev[ci][i] = ex2_approx(ev[ci][i] - cm);
-                            cs += ev[ci][i];
-                        }
+                        for (int i = 0; i < 16; ++i) ev[ci][i] = ex2_approx(ev[ci][i] - cm);
                         mx[ci] = cm;
-                        sum[ci] = cs;
+                        sum[ci] = old + tree_sum16(ev[ci]);
                         cm_out[ci] = cm;
                     }
                 };
@@ -479,7 +528,30 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
 #pragma unroll
                     for (int jj = 0; jj < (KEEP ? kKeep : 1); ++jj) {
                         const int j = half + jj * kHalves;
-                        if (j < nchunks) chunk_pass(j, e[jj], mref[jj]);
+                        if (j < nchunks) {
+                            const int c0 = 16 * j;
+                            _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
+                                ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, e[jj][ci]);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {  // base-2 logits of both classes at once
+                                const float bl = s_bias_l2e[c0 + i];
+                                const float2 u = fma2(make_float2(e[jj][0][i], e[jj][1][i]),
+                                                      make_float2(kLog2e, kLog2e), make_float2(bl, bl));
+                                const bool in = c0 + i < C;
+                                e[jj][0][i] = in ? u.x : -INFINITY;
+                                e[jj][1][i] = in ? u.y : -INFINITY;
+                            }
+                            _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                                const float cm = fmaxf(mx[ci], tree_max16(e[jj][ci]));
+                                const float old = mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - cm);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) e[jj][ci][i] = ex2_approx(e[jj][ci][i] - cm);
+                                mx[ci] = cm;
+                                sum[ci] = old + tree_sum16(e[jj][ci]);
+                                mref[jj][ci] = cm;
+                            }
+                        }
                     }
                 } else {
                     for (int j = half; j < nchunks; j += kHalves) chunk_pass(j, e[0], mref[0]);
@@ -535,10 +607,14 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         const int j = half + jj * kHalves;
                         if (j < nchunks) {
 #pragma unroll
-                            for (int ci = 0; ci < 2; ++ci) {
-                                const float scale = inv[ci] * ex2_approx(mref[jj][ci] - M[ci]);
+                            // both classes at once: t = weight, then the packed sigmoid
+                            const float2 scale = make_float2(inv[0] * ex2_approx(mref[jj][0] - M[0]),
+                                                             inv[1] * ex2_approx(mref[jj][1] - M[1]));
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) e[jj][ci][i] = sigmoid_unit(e[jj][ci][i] * scale);
+                            for (int i = 0; i < 16; ++i) {
+                                const float2 o = sigmoid_unit2(mul2(make_float2(e[jj][0][i], e[jj][1][i]), scale));
+                                e[jj][0][i] = o.x;
+                                e[jj][1][i] = o.y;
                             }
                             store_chunk(16 * j, e[jj]);
                         }
