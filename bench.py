@@ -181,6 +181,14 @@ def replica_throughput(useful_flop_per_rank, world, slowest_ms_per_step):
 
 # ------------------------------------------------------------ CPU oracle ----
 
+def oracle_running_stats(spec):
+    """The running statistics the evaluation-mode epilogue reads (fresh copies), else nothing."""
+    if spec.epilogue != workloads.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL:
+        return {}
+    rm, rv = workloads.make_running_stats(spec)
+    return {"running_mean": rm.numpy().copy(), "running_var": rv.numpy().copy()}
+
+
 def cpu_oracle_sample(spec, inputs, target_s, max_samples=None):
     """Time the oracle on a bounded sample of the batch: whole samples of the
     per-sample epilogues (for BatchNorm the first n samples form a smaller
@@ -197,7 +205,7 @@ def cpu_oracle_sample(spec, inputs, target_s, max_samples=None):
         t0 = time.perf_counter()
         oracle.forward(f(sub["x"]), f(sub["w"]), f(sub["bias"]), stride=s.stride, pad=s.pad, out_pad=s.out_pad,
                        epilogue=s.epilogue, groups=s.groups, eps=s.eps, scale=s.scale, gamma=f(sub["gamma"]),
-                       beta=f(sub["beta"]))
+                       beta=f(sub["beta"]), **oracle_running_stats(spec))
         elapsed += time.perf_counter() - t0
         done += s.useful_flop()
         n += m
@@ -220,7 +228,7 @@ def run_reference(args, spec):
     def step():
         oracle.forward(f(sub["x"]), f(sub["w"]), f(sub["bias"]), stride=s.stride, pad=s.pad, out_pad=s.out_pad,
                        epilogue=s.epilogue, groups=s.groups, eps=s.eps, scale=s.scale, gamma=f(sub["gamma"]),
-                       beta=f(sub["beta"]))
+                       beta=f(sub["beta"]), **oracle_running_stats(spec))
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -264,17 +272,29 @@ def run_gpu(args, spec):
     y = plan.new_output(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # evaluation-mode BatchNorm runs no GEMM: its kernels are timed as the whole forward
+    eval_bn = spec.epilogue == workloads.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL
+    running = None
+    if eval_bn:
+        running = tuple(t.to(dev) for t in workloads.make_running_stats(spec))
+        plan.set_running_stats(*running)
+
+    fwd_ev = []
 
     def step():
         plan.pack_weights(d["w"], ws, stream)
+        if fwd_ev:
+            fwd_ev[-1][0].record(stream)
         plan.forward(d["x"], y, ws, d["bias"], d["gamma"], d["beta"], stream)
+        if fwd_ev:
+            fwd_ev[-1][1].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
     plan.check(ws, stream)
     torch.cuda.synchronize()
 
-    plan.profile_enable(True)
+    plan.profile_enable(not eval_bn)
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
@@ -291,9 +311,15 @@ def run_gpu(args, spec):
     for i in range(args.steps):
         flush.fill_(float(i))  # evict x, y and the packed weights from L2 between steps
         ev[i][0].record(stream)
+        if eval_bn:
+            fwd_ev.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
         step()
         ev[i][1].record(stream)
-        gemm_ms.append(plan.profile_read())  # synchronises on the GEMM's end event
+        if eval_bn:
+            fwd_ev[-1][1].synchronize()
+            gemm_ms.append(fwd_ev[-1][0].elapsed_time(fwd_ev[-1][1]))
+        else:
+            gemm_ms.append(plan.profile_read())  # synchronises on the GEMM's end event
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -316,6 +342,8 @@ def run_gpu(args, spec):
         pipe = HostPipeline(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
                             spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, prec,
                             chunks=args.e2e_chunks, device=dev)
+        if running is not None:
+            pipe.set_running_stats(*running)
         y_host = torch.empty(pipe.full_shape, dtype=torch.float32).pin_memory()
         h2d = sum(v.numel() * 4 for v in host.values() if v is not None)
         d2h = y_host.numel() * 4
@@ -342,7 +370,13 @@ def run_gpu(args, spec):
 
     pk = peaks()
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
-    if prec == PREC_3XTF32:
+    if eval_bn:
+        # two HBM-bound kernels (box sums over x, contraction with the packed weight)
+        achieved = info["forward_min_bytes"] / (gemm_avg * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": f"{pk['source']} HBM copy bandwidth",
+                "algorithmic_bytes": info["forward_min_bytes"]}
+    elif prec == PREC_3XTF32:
         peak = pk["bf16_tflops"] * TF32_OVER_BF16
         achieved = useful / (gemm_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
@@ -355,7 +389,8 @@ def run_gpu(args, spec):
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 flop x max SM clock",
                 "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak}
-    roof["kernel"] = "convt3d_tc_gemm" if prec == PREC_3XTF32 else "ffma_conv_kernel"
+    roof["kernel"] = ("boxsum_kernel + bn_eval_out_kernel" if eval_bn else
+                      "convt3d_tc_gemm" if prec == PREC_3XTF32 else "ffma_conv_kernel")
     roof["kernel_ms"] = gemm_avg
     roof["kernel_share_of_step"] = gemm_avg / ms_per_step
     roof["traffic"] = committed_traffic(args.precision, spec.name)

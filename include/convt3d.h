@@ -22,6 +22,11 @@
  *                             -> [N, Cout, 1, 1, 1]                       (page l2_p77)
  *   SOFTMAX_SIGMOID           softmax over channels, then elementwise
  *                             sigmoid                                     (page l2_p49)
+ *   SCALE_BATCHNORM_EVAL_AVGPOOL
+ *                             z = scale*Y; BatchNorm3d in evaluation mode
+ *                             (stored running mean/variance); affine; mean
+ *                             over positions -> [N, Cout, 1, 1, 1]        (page l2_p77's
+ *                                                                          submitted solution)
  *
  * Computation: an output-stationary implicit GEMM, M = output positions,
  * N = Cout, K = Cin x taps.  Stride 2 is split into the 8 output-parity
@@ -32,7 +37,7 @@
  * the CUDA cores (kept as an ablation).
  *
  * Conventions for every entry point:
- *   - Layouts: x [N,Cin,Din,Hin,Win], y [N,Cout,Do,Ho,Wo] (BN+pool: [N,Cout]),
+ *   - Layouts: x [N,Cin,Din,Hin,Win], y [N,Cout,Do,Ho,Wo] (BN+pool: [N,Cout,1,1,1]),
  *     w [Cin,Cout,k,k,k] (PyTorch ConvTranspose3d), bias/gamma/beta [Cout];
  *     all fp32, contiguous, device memory, 16-byte aligned.
  *   - Ownership: the caller allocates and owns every device buffer (input,
@@ -67,7 +72,8 @@ typedef enum {
     CONVT3D_EPI_IDENTITY = 0,
     CONVT3D_EPI_RELU_GROUPNORM = 1,
     CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL = 2,
-    CONVT3D_EPI_SOFTMAX_SIGMOID = 3
+    CONVT3D_EPI_SOFTMAX_SIGMOID = 3,
+    CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL = 4
 } convt3d_epilogue_t;
 
 typedef enum {
@@ -106,7 +112,7 @@ typedef struct convt3d_plan_s *convt3d_plan_t;
 
 /* Plan facts, for callers that report or size things. */
 typedef struct {
-    int64_t out_shape[5];        /* y shape ([N,Cout,1,1,1] for BN+pool)                */
+    int64_t out_shape[5];        /* y shape ([N,Cout,1,1,1] for the BN+pool epilogues)  */
     int num_classes;             /* stride^3 output-parity classes                      */
     int64_t gemm_m;              /* output positions (N*Do*Ho*Wo)                        */
     int64_t gemm_n;              /* Cout                                                */
@@ -130,7 +136,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
 /* Release a plan (NULL is ignored). */
 void convt3d_plan_destroy(convt3d_plan_t plan);
 
-/* Output shape: [N,Cout,Do,Ho,Wo], or [N,Cout,1,1,1] for BN+pool. Host only. */
+/* Output shape: [N,Cout,Do,Ho,Wo], or [N,Cout,1,1,1] for the BN+pool epilogues. Host only. */
 convt3d_status_t convt3d_output_shape(convt3d_plan_t plan, int64_t shape[5]);
 
 /* Plan facts (see convt3d_info_t). Host only. */
@@ -157,6 +163,18 @@ convt3d_status_t convt3d_pack_weights(convt3d_plan_t plan, const float *w, void 
 convt3d_status_t convt3d_forward(convt3d_plan_t plan, const float *x, const float *bias,
                                  const float *gamma, const float *beta, float *y,
                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* BatchNorm running statistics, device pointers to Cout floats each (page
+ * l2_p77: nn.BatchNorm3d with momentum 0.1, eps 1e-5).  With
+ * SCALE_BATCHNORM_AVGPOOL, every later forward updates them in place from the
+ * batch statistics: running_mean <- (1 - momentum) * running_mean + momentum *
+ * mean, running_var likewise with the unbiased batch variance (n / (n - 1)
+ * times the biased one, n = N * Do * Ho * Wo).  SCALE_BATCHNORM_EVAL_AVGPOOL
+ * reads them and its forward fails with INVALID_ARG until they are set.  NULL
+ * pointers clear the setting.  The plan keeps the pointers; the caller keeps
+ * the memory valid.  Host only. */
+convt3d_status_t convt3d_set_running_stats(convt3d_plan_t plan, float *running_mean, float *running_var,
+                                           float momentum);
 
 /* Synchronise `stream`, read and clear the workspace status word: returns OK,
  * TIMEOUT (a device-side bounded wait ran out) or DEVICE_ASSERT. */

@@ -63,6 +63,8 @@ def create(lib, **kw):
     (dict(Din=1, Hin=1, Win=1, k=1, pad=1), 1),
     (dict(stride=3, k=3), 2), (dict(k=8), 2), (dict(Cout=257), 2), (dict(k=3, pad=3, Din=9, Hin=9, Win=9), 2),
     (dict(stride=2, k=3, pad=1, Cout=144), 2), (dict(stride=2, k=1), 2),
+    (dict(epilogue=4, eps=-1.0), 1), (dict(epilogue=4, scale=float("inf")), 1),
+    (dict(epilogue=4, Hin=200, Win=200), 2),
 ])
 def test_plan_validation(lib, kw, status):
     st, h = create(lib, **kw)
@@ -82,7 +84,7 @@ def test_ffma_accepts_what_tensor_path_rejects(lib):
 def test_plan_facts_for_workloads(lib, spec, precision):
     p = Plan.from_spec(spec, precision=precision)
     dims = [oracle.output_size(v, spec.k, spec.stride, spec.pad, spec.out_pad) for v in (spec.D, spec.H, spec.W)]
-    if spec.epilogue == workloads.EPI_SCALE_BATCHNORM_AVGPOOL:
+    if spec.epilogue in (workloads.EPI_SCALE_BATCHNORM_AVGPOOL, workloads.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL):
         assert p.out_shape == (spec.N, spec.Cout, 1, 1, 1)
     else:
         assert p.out_shape == (spec.N, spec.Cout, *dims)
@@ -92,7 +94,12 @@ def test_plan_facts_for_workloads(lib, spec, precision):
     assert p.info["num_classes"] == spec.stride ** 3
     # K summed over parity classes covers every tap exactly once
     assert p.info["gemm_k_total"] == spec.Cin * spec.k ** 3
-    assert p.info["issued_mma_flop"] >= p.info["useful_flop"] * (3 if precision == 0 else 1) * 0.9
+    if spec.epilogue == workloads.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL:
+        # no convolution: box sums of x, then one Cin*k^3 contraction per (n, c)
+        assert p.info["issued_mma_flop"] == 2.0 * spec.N * spec.Cout * spec.Cin * spec.k ** 3
+        assert p.info["launches_per_forward"] == 2
+    else:
+        assert p.info["issued_mma_flop"] >= p.info["useful_flop"] * (3 if precision == 0 else 1) * 0.9
 
 
 def test_parity_classes_tile_every_output_once(lib):
@@ -136,5 +143,29 @@ def test_groupnorm_requires_affine(lib):
     try:
         V = ctypes.c_void_p
         assert lib.convt3d_forward(h, V(1 << 20), None, None, None, V(1 << 21), V(1 << 22), 1 << 30, None) == 1
+    finally:
+        lib.convt3d_plan_destroy(h)
+
+
+def test_running_stats_validation_and_eval_requirement(lib):
+    st, h = create(lib, epilogue=4, has_bias=1)
+    assert st == 0
+    try:
+        V = ctypes.c_void_p
+        out = (ctypes.c_int64 * 5)()
+        assert lib.convt3d_output_shape(h, out) == 0
+        assert tuple(out) == (2, 16, 1, 1, 1)
+        fwd = lambda: lib.convt3d_forward(h, V(1 << 20), V(1 << 23), V(1 << 24), V(1 << 25), V(1 << 21),  # noqa: E731
+                                          V(1 << 22), 1 << 30, None)
+        # evaluation mode reads the running statistics: forward refuses until they are set
+        assert fwd() == 1
+        assert lib.convt3d_set_running_stats(h, V(1 << 26), None, 0.1) == 1
+        assert lib.convt3d_set_running_stats(h, V(1 << 26), V(1 << 27), 1.5) == 1
+        assert lib.convt3d_set_running_stats(h, V(1 << 26), V(1 << 27), -0.1) == 1
+        assert lib.convt3d_set_running_stats(h, V((1 << 26) + 2), V(1 << 27), 0.1) == 1
+        assert lib.convt3d_set_running_stats(h, V(1 << 26), V(1 << 27), 0.1) == 0
+        assert fwd() == 7  # past the running-statistics check; stops at the unpacked workspace
+        assert lib.convt3d_set_running_stats(h, None, None, 0.1) == 0
+        assert fwd() == 1
     finally:
         lib.convt3d_plan_destroy(h)

@@ -20,24 +20,41 @@ TOL = 1e-4
 PRECISIONS = [pytest.param(PREC_3XTF32, id="3xtf32"), pytest.param(PREC_FFMA, id="ffma")]
 
 
-def run_gpu(spec, inputs, precision):
+def run_gpu(spec, inputs, precision, running=None, momentum=0.1):
+    """Forward on the GPU.  running: (mean, var) CPU tensors; they are copied to
+    the device, attached to the plan, and their values after the forward are
+    returned beside y."""
     dev = torch.device("cuda")
     plan = Plan.from_spec(spec, precision=precision)
     ws = plan.new_workspace(dev)
     y = plan.new_output(dev)
     y.fill_(float("nan"))
     d = {k: (v.to(dev) if v is not None else None) for k, v in inputs.items()}
+    if running is not None:
+        rm, rv = (t.to(dev).clone() for t in running)
+        plan.set_running_stats(rm, rv, momentum)
     plan.pack_weights(d["w"], ws)
     plan.forward(d["x"], y, ws, d["bias"], d["gamma"], d["beta"])
     plan.check(ws)
+    if running is not None:
+        return y.cpu().numpy(), rm.cpu().numpy(), rv.cpu().numpy()
     return y.cpu().numpy()
 
 
-def run_oracle(spec, inputs):
+def run_oracle(spec, inputs, running=None, momentum=0.1):
+    """The oracle's output; with running=(mean, var) CPU tensors, also the
+    running statistics after the forward (the oracle updates copies)."""
     f = lambda t: None if t is None else t.numpy()  # noqa: E731
-    return oracle.forward(f(inputs["x"]), f(inputs["w"]), f(inputs["bias"]), stride=spec.stride, pad=spec.pad,
-                          out_pad=spec.out_pad, epilogue=spec.epilogue, groups=spec.groups, eps=spec.eps,
-                          scale=spec.scale, gamma=f(inputs["gamma"]), beta=f(inputs["beta"]))
+    rm = rv = None
+    if running is not None:
+        rm, rv = (t.numpy().copy() for t in running)
+    out = oracle.forward(f(inputs["x"]), f(inputs["w"]), f(inputs["bias"]), stride=spec.stride, pad=spec.pad,
+                         out_pad=spec.out_pad, epilogue=spec.epilogue, groups=spec.groups, eps=spec.eps,
+                         scale=spec.scale, gamma=f(inputs["gamma"]), beta=f(inputs["beta"]), running_mean=rm,
+                         running_var=rv, momentum=momentum)
+    if running is not None:
+        return out, rm, rv
+    return out
 
 
 def assert_close(got, ref, what=""):
@@ -144,3 +161,49 @@ def test_host_pipeline_matches_device_path(spec):
         pipe(host["x"], host["w"], y_host, host["bias"], host["gamma"], host["beta"])
         torch.cuda.synchronize()
         assert_close(y_host.numpy(), ref, spec.name)
+
+
+EVAL_CASES = [
+    E.BN.replace(name="bn_eval_full", epilogue=E.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL),
+    E.Spec("bn_eval_s2_p1_op1", N=2, Cin=24, Cout=40, D=5, H=6, W=7, k=3, stride=2, pad=1, out_pad=1, bias=True,
+           epilogue=E.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, scale=0.75, seed_index=30),
+    E.Spec("bn_eval_k4_p2", N=3, Cin=33, Cout=20, D=4, H=5, W=9, k=4, pad=2, bias=False,
+           epilogue=E.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, scale=-1.5, seed_index=31),
+    E.Spec("bn_eval_k7_s2_small", N=1, Cin=5, Cout=7, D=2, H=3, W=2, k=7, stride=2, pad=3, out_pad=1, bias=True,
+           epilogue=E.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, scale=2.0, seed_index=32),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("precision", PRECISIONS)
+@pytest.mark.parametrize("spec", EVAL_CASES, ids=lambda s: s.name)
+def test_batchnorm_eval_mode(spec, precision):
+    """Evaluation-mode BatchNorm+pool (no convolution is run) against the
+    oracle's full convolution followed by the normalisation; the statistics are
+    fixed, so every sample is independent and the full-size case is checked on
+    samples 0 and N-1."""
+    inputs = E.make_inputs(spec)
+    running = E.make_running_stats(spec)
+    got, rm, rv = run_gpu(spec, inputs, precision, running)
+    # evaluation mode leaves the running statistics untouched
+    assert np.array_equal(rm, running[0].numpy()) and np.array_equal(rv, running[1].numpy())
+    samples = range(spec.N) if spec.N <= 3 else (0, spec.N - 1)
+    for n in samples:
+        ref, _, _ = run_oracle(spec.replace(N=1), E.sample_slice(inputs, n, n + 1), running)
+        assert_close(got[n:n + 1], ref, f"{spec.name}[n={n}]")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("precision", PRECISIONS)
+@pytest.mark.parametrize("spec", [SMALL[5], SMALL[6], E.BN], ids=lambda s: s.name)
+def test_batchnorm_running_stats_update(spec, precision):
+    """Training-mode BatchNorm updates the running statistics in place with
+    momentum 0.3 and the unbiased batch variance; output and both statistics
+    match the oracle."""
+    inputs = E.make_inputs(spec)
+    running = E.make_running_stats(spec)
+    got, rm, rv = run_gpu(spec, inputs, precision, running, momentum=0.3)
+    ref, rm_ref, rv_ref = run_oracle(spec, inputs, running, momentum=0.3)
+    assert_close(got, ref, spec.name)
+    assert_close(rm, rm_ref, spec.name + " running_mean")
+    assert_close(rv, rv_ref, spec.name + " running_var")

@@ -16,6 +16,7 @@ EPI_IDENTITY = 0
 EPI_RELU_GROUPNORM = 1
 EPI_SCALE_BATCHNORM_AVGPOOL = 2
 EPI_SOFTMAX_SIGMOID = 3
+EPI_SCALE_BATCHNORM_EVAL_AVGPOOL = 4
 
 PREC_3XTF32 = 0
 PREC_FFMA = 1
@@ -36,7 +37,7 @@ EXPORTS = [
     "convt3d_plan_create", "convt3d_plan_destroy", "convt3d_output_shape", "convt3d_plan_info",
     "convt3d_workspace_bytes", "convt3d_pack_weights", "convt3d_forward", "convt3d_check",
     "convt3d_profile_enable", "convt3d_profile_read", "convt3d_status_string", "convt3d_last_error",
-    "convt3d_version", "convt3d_forward_static_workspace",
+    "convt3d_version", "convt3d_forward_static_workspace", "convt3d_set_running_stats",
 ]
 
 
@@ -111,6 +112,8 @@ def load(path: str | None = None):
         lib.convt3d_version.argtypes = []
         lib.convt3d_forward_static_workspace.restype = I
         lib.convt3d_forward_static_workspace.argtypes = [V, V, V, V, V, V, V, V]
+        lib.convt3d_set_running_stats.restype = I
+        lib.convt3d_set_running_stats.argtypes = [V, V, V, ctypes.c_float]
         if path is None:
             _lib = lib
         return lib

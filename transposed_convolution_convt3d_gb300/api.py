@@ -13,7 +13,8 @@ import torch
 
 from . import _lib
 from ._lib import (EPI_IDENTITY, EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL,  # noqa: F401
-                   EPI_SOFTMAX_SIGMOID, PREC_3XTF32, PREC_FFMA, Convt3dError)
+                   EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, EPI_SOFTMAX_SIGMOID, PREC_3XTF32, PREC_FFMA,
+                   Convt3dError)
 
 
 def _ptr(t):
@@ -99,6 +100,21 @@ class Plan:
                    self.lib)
         return y
 
+    def set_running_stats(self, running_mean, running_var, momentum=0.1):
+        """BatchNorm running statistics (Cout floats each on the device, or both
+        None to clear).  The training-mode BatchNorm epilogue updates them in
+        place on every forward; the evaluation-mode one normalises with them.
+        The plan keeps references so the tensors outlive its use of them."""
+        if (running_mean is None) != (running_var is None):
+            raise ValueError("running_mean and running_var are set together")
+        for t, n in ((running_mean, "running_mean"), (running_var, "running_var")):
+            self._dev(t, n)
+            if t is not None and t.numel() != self.desc.Cout:
+                raise ValueError(f"{n} must hold Cout={self.desc.Cout} values")
+        _lib.check(self.lib.convt3d_set_running_stats(self.handle, _ptr(running_mean), _ptr(running_var),
+                                                      float(momentum)), self.lib)
+        self._running = (running_mean, running_var)
+
     def check(self, workspace, stream=None):
         _lib.check(self.lib.convt3d_check(self.handle, _ptr(workspace), _stream(stream)), self.lib)
 
@@ -139,15 +155,15 @@ class HostPipeline:
     chunk i-1's computation and chunk i-2's device->host copy run on three
     streams at once.  Valid for the epilogues whose result for a sample depends
     on that sample only (identity, ReLU+GroupNorm, softmax+sigmoid); the
-    BatchNorm epilogue's batch statistics need the whole batch, so it runs as
-    one chunk.  Host tensors should be pinned for the copies to be asynchronous.
+    BatchNorm epilogues run as one chunk (the training-mode one's batch
+    statistics need the whole batch).  Host tensors should be pinned for the copies to be asynchronous.
     Device buffers, plans and streams are created once, here.
     """
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, chunks=4,
                  device="cuda"):
-        if epilogue == EPI_SCALE_BATCHNORM_AVGPOOL or N % chunks:
+        if epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) or N % chunks:
             chunks = 1
         self.chunks = chunks
         self.n_chunk = N // chunks
@@ -161,6 +177,10 @@ class HostPipeline:
         self.vec = {name: torch.empty(Cout, dtype=torch.float32, device=dev) for name in ("bias", "gamma", "beta")}
         self.ws = self.plan.new_workspace(dev)
         self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    def set_running_stats(self, running_mean, running_var, momentum=0.1):
+        """Device-resident BatchNorm running statistics, as Plan.set_running_stats."""
+        self.plan.set_running_stats(running_mean, running_var, momentum)
 
     def __call__(self, x_host, w_host, y_host, bias=None, gamma=None, beta=None, stream=None):
         """Run on pinned host tensors; returns y_host.  The work is ordered after

@@ -131,6 +131,10 @@ struct convt3d_plan_s {
     int ev_created;
     const void *packed_ws;  // workspace that pack_weights last filled for this plan
     void *tc_cache;         // tensor-core launch state (tc.cu)
+    float *run_mean;        // BatchNorm running statistics (device, Cout each) or NULL
+    float *run_var;
+    float momentum;
+    size_t off_box;         // evaluation-mode BatchNorm: per-tap input box sums
 };
 
 // Kernel launchers (defined in the .cu files); each returns cudaGetLastError().
@@ -150,6 +154,10 @@ cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, co
                                 const float *beta, float *y, cudaStream_t s);
 cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, double *sums,
                                const float *gamma, const float *beta, float *y, cudaStream_t s);
+cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float *w_a, const float *w_b,
+                           const float *bias, const float *gamma, const float *beta, double *box, float *y,
+                           cudaStream_t s);
+size_t bn_eval_smem_bytes(const convt3d_plan_s &p);
 void tc_cache_free(void *cache);
 void report_error(const char *fmt, ...);
 }  // namespace convt3d

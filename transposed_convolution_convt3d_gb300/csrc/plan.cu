@@ -160,17 +160,17 @@ convt3d_status_t validate(const convt3d_desc_t &d) {
         return fail(CONVT3D_ERR_INVALID_ARG, "k, stride >= 1 and pad, out_pad >= 0 required");
     if (d.out_pad >= d.stride)
         return fail(CONVT3D_ERR_INVALID_ARG, "out_pad must be smaller than stride");
-    if (d.epilogue < CONVT3D_EPI_IDENTITY || d.epilogue > CONVT3D_EPI_SOFTMAX_SIGMOID)
+    if (d.epilogue < CONVT3D_EPI_IDENTITY || d.epilogue > CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
         return fail(CONVT3D_ERR_INVALID_ARG, "unknown epilogue %d", d.epilogue);
     if (d.precision != CONVT3D_PREC_3XTF32 && d.precision != CONVT3D_PREC_FFMA)
         return fail(CONVT3D_ERR_INVALID_ARG, "unknown precision %d", d.precision);
     if (d.epilogue == CONVT3D_EPI_RELU_GROUPNORM && (d.groups < 1 || d.Cout % d.groups != 0))
         return fail(CONVT3D_ERR_INVALID_ARG, "groups must divide Cout");
-    if ((d.epilogue == CONVT3D_EPI_RELU_GROUPNORM || d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL) &&
-        !(d.eps > 0.0f && isfinite(d.eps)))
+    const bool bn_any = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL ||
+                        d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
+    if ((d.epilogue == CONVT3D_EPI_RELU_GROUPNORM || bn_any) && !(d.eps > 0.0f && isfinite(d.eps)))
         return fail(CONVT3D_ERR_INVALID_ARG, "eps must be finite and > 0");
-    if (d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL && !isfinite(d.scale))
-        return fail(CONVT3D_ERR_INVALID_ARG, "scale must be finite");
+    if (bn_any && !isfinite(d.scale)) return fail(CONVT3D_ERR_INVALID_ARG, "scale must be finite");
     for (int64_t in : {(int64_t)d.Din, (int64_t)d.Hin, (int64_t)d.Win})
         if (out_extent(in, d.k, d.stride, d.pad, d.out_pad) < 1)
             return fail(CONVT3D_ERR_INVALID_ARG, "output extent < 1");
@@ -271,10 +271,16 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     if (!p->tc)  // the FFMA kernel's register tiles need a power-of-two channel count
         while (p->cout_pad & (p->cout_pad - 1)) p->cout_pad += 16;
     build_groups(*p);
-    if (p->tc && !im2col_corners_ok(*p)) {
+    const bool eval_bn = desc->epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
+    if (p->tc && !eval_bn && !im2col_corners_ok(*p)) {
         delete p;
         return fail(CONVT3D_ERR_UNSUPPORTED, "shape outside the TMA im2col corner range");
     }
+    if (eval_bn && bn_eval_smem_bytes(*p) > 200 * 1024) {
+        delete p;
+        return fail(CONVT3D_ERR_UNSUPPORTED, "evaluation-mode BatchNorm needs k*H*W + k*k*W <= 25600");
+    }
+    p->momentum = 0.1f;
 
     // Workspace layout.
     size_t off = kStatusBytes;
@@ -283,7 +289,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     off = align_up(off + p->wpk_elems * 4, 256);
     p->off_wpk_lo = off;
     if (p->tc) off = align_up(off + p->wpk_elems * 4, 256);
-    p->xs_elems = p->tc ? (size_t)desc->N * desc->Din * desc->Hin * desc->Win * p->cin_pad : 0;
+    p->xs_elems = (p->tc && !eval_bn) ? (size_t)desc->N * desc->Din * desc->Hin * desc->Win * p->cin_pad : 0;
     p->off_xs_hi = off;
     off = align_up(off + p->xs_elems * 4, 256);
     p->off_xs_lo = off;
@@ -303,6 +309,8 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     off = align_up(off + p->partial_doubles * 8, 256);
     p->off_stats = off;
     off = align_up(off + p->stat_doubles * 8, 256);
+    p->off_box = off;
+    if (eval_bn) off = align_up(off + (size_t)desc->N * desc->Cin * desc->k * desc->k * desc->k * 8, 256);
     p->ws_total = off;
     *out = p;
     return CONVT3D_OK;
@@ -320,7 +328,8 @@ void convt3d_plan_destroy(convt3d_plan_t p) {
 
 convt3d_status_t convt3d_output_shape(convt3d_plan_t p, int64_t shape[5]) {
     if (!p || !shape) return fail(CONVT3D_ERR_INVALID_ARG, "NULL argument");
-    const bool pooled = p->d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
+    const bool pooled = p->d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL ||
+                        p->d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
     shape[0] = p->d.N;
     shape[1] = p->d.Cout;
     shape[2] = pooled ? 1 : p->g.Do;
@@ -347,7 +356,8 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
     info->tile_m = p->tile_m;
     const bool gn = d.epilogue == CONVT3D_EPI_RELU_GROUPNORM;
     const bool bn = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
-    info->launches_per_forward = (p->tc ? 2 : 1) + (gn ? 2 : 0) + (bn ? 2 : 0);
+    const bool ev = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
+    info->launches_per_forward = ev ? 2 : (p->tc ? 2 : 1) + (gn ? 2 : 0) + (bn ? 2 : 0);
     info->launches_per_pack = 1;
     info->useful_flop = 2.0 * d.N * d.Cout * (double)d.Cin * d.k * d.k * d.k * d.Din * d.Hin * d.Win;
     // Issued: every tile runs its class(es)' taps over tile_m rows and cout_pad columns -- the
@@ -373,13 +383,17 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
     const double xbytes = 4.0 * d.N * d.Cin * (double)d.Din * d.Hin * d.Win;
     const double wbytes = 4.0 * d.Cin * d.Cout * (double)d.k * d.k * d.k;
     const double ybytes = 4.0 * d.N * d.Cout * (double)g.Do * g.Ho * g.Wo;
-    const double out_bytes = bn ? 4.0 * d.N * d.Cout : ybytes;
+    const double out_bytes = (bn || ev) ? 4.0 * d.N * d.Cout : ybytes;
     // Main kernel: reads x (tensor-core path: the staged hi+lo copy) and the packed weights once,
     // writes the output once (BN+pool: nothing but partials).
     info->gemm_min_bytes = (p->tc ? 2.0 * xbytes : xbytes) + (p->tc ? 2.0 : 1.0) * wbytes + (bn ? 0.0 : ybytes);
     // Whole forward as the pages define it: x and w in, the output out, plus the second pass
     // over y that GroupNorm's global statistics force.
     info->forward_min_bytes = xbytes + wbytes + out_bytes + (gn ? 2.0 * ybytes : 0.0);
+    if (ev) {  // no convolution runs: box sums over x, then a contraction with w
+        info->issued_mma_flop = 2.0 * d.N * d.Cout * (double)d.Cin * d.k * d.k * d.k;
+        info->gemm_min_bytes = xbytes;
+    }
     return CONVT3D_OK;
 }
 
@@ -417,7 +431,10 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const float *x, const float *
     if (d.has_bias && !bias) return fail(CONVT3D_ERR_INVALID_ARG, "has_bias set but bias is NULL");
     const bool gn = d.epilogue == CONVT3D_EPI_RELU_GROUPNORM;
     const bool bn = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
-    if ((gn || bn) && (!gamma || !beta)) return fail(CONVT3D_ERR_INVALID_ARG, "gamma and beta are required");
+    const bool ev = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
+    if ((gn || bn || ev) && (!gamma || !beta)) return fail(CONVT3D_ERR_INVALID_ARG, "gamma and beta are required");
+    if (ev && (!p->run_mean || !p->run_var))
+        return fail(CONVT3D_ERR_INVALID_ARG, "evaluation-mode BatchNorm needs convt3d_set_running_stats");
     for (const void *ptr : {(const void *)x, (const void *)y, (const void *)bias, (const void *)gamma,
                             (const void *)beta})
         if ((uintptr_t)ptr % 16) return fail(CONVT3D_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
@@ -432,6 +449,14 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const float *x, const float *
     double *stats = (double *)(base + p->off_stats);
     cudaError_t e;
 
+    if (ev) {
+        // no convolution: input box sums and a contraction with the packed weight
+        e = launch_bn_eval(*p, x, (const float *)(base + p->off_wpk_hi),
+                           p->tc ? (const float *)(base + p->off_wpk_lo) : nullptr, b, gamma, beta,
+                           (double *)(base + p->off_box), y, s);
+        if (e != cudaSuccess) return cuda_fail(e, "evaluation-mode batchnorm launch");
+        return CONVT3D_OK;
+    }
     if (p->prof_enabled) {
         if (!p->ev_created) {
             if ((e = cudaEventCreate(&p->ev0)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
@@ -482,6 +507,20 @@ convt3d_status_t convt3d_check(convt3d_plan_t p, void *ws, void *stream) {
     if (word[0] == kErrTimeout)
         return fail(CONVT3D_ERR_TIMEOUT, "device wait timed out (site %u, block %u)", word[1], word[2]);
     return fail(CONVT3D_ERR_DEVICE_ASSERT, "device check failed (code %u, site %u)", word[0], word[1]);
+}
+
+convt3d_status_t convt3d_set_running_stats(convt3d_plan_t p, float *running_mean, float *running_var,
+                                           float momentum) {
+    if (!p) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan");
+    if ((running_mean == nullptr) != (running_var == nullptr))
+        return fail(CONVT3D_ERR_INVALID_ARG, "running_mean and running_var are set together");
+    if (!(momentum >= 0.0f && momentum <= 1.0f)) return fail(CONVT3D_ERR_INVALID_ARG, "momentum must be in [0, 1]");
+    if (((uintptr_t)running_mean | (uintptr_t)running_var) % 4)
+        return fail(CONVT3D_ERR_INVALID_ARG, "running statistics must be 4-byte aligned");
+    p->run_mean = running_mean;
+    p->run_var = running_var;
+    p->momentum = momentum;
+    return CONVT3D_OK;
 }
 
 convt3d_status_t convt3d_profile_enable(convt3d_plan_t p, int enable) {

@@ -149,10 +149,12 @@ __global__ void bn_reduce_kernel(const double *__restrict__ partials, double *__
     }
 }
 
-// Phase 2: per channel, batch mean and biased variance, then the pooled output.
+// Phase 2: per channel, batch mean and biased variance, then the pooled output;
+// optionally the running statistics' update (unbiased variance).
 __global__ void bn_finalize_kernel(const double *__restrict__ sums, const float *__restrict__ gamma,
                                    const float *__restrict__ beta, float *__restrict__ y, int N, int C, double V,
-                                   double eps) {
+                                   double eps, float *__restrict__ rmean, float *__restrict__ rvar,
+                                   double momentum) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= C) return;
     double S = 0.0, Q = 0.0;
@@ -168,6 +170,11 @@ __global__ void bn_finalize_kernel(const double *__restrict__ sums, const float 
     for (int n = 0; n < N; ++n) {
         const double Sn = sums[((int64_t)n * C + c) * 2];
         y[(int64_t)n * C + c] = (float)((double)gamma[c] * (Sn / V - mean) * rstd + (double)beta[c]);
+    }
+    if (rmean && rvar) {
+        const double unbiased = cnt > 1.0 ? var * cnt / (cnt - 1.0) : 0.0;
+        rmean[c] = (float)((1.0 - momentum) * (double)rmean[c] + momentum * mean);
+        rvar[c] = (float)((1.0 - momentum) * (double)rvar[c] + momentum * unbiased);
     }
 }
 
@@ -200,7 +207,8 @@ cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const double V = (double)p.g.Do * p.g.Ho * p.g.Wo;
-    bn_finalize_kernel<<<(C + 127) / 128, 128, 0, s>>>(sums, gamma, beta, y, N, C, V, (double)p.d.eps);
+    bn_finalize_kernel<<<(C + 127) / 128, 128, 0, s>>>(sums, gamma, beta, y, N, C, V, (double)p.d.eps, p.run_mean,
+                                                        p.run_var, (double)p.momentum);
     return cudaGetLastError();
 }
 

@@ -4,12 +4,14 @@ This module holds shapes, distributions and seeds only -- none of the method's
 arithmetic -- so that the CUDA library and the CPU oracle read identical input
 bytes without either importing the other.
 
-The five workloads are the shapes of the three transcript pages (l2_p61
-ReLU+GroupNorm, l2_p77 scale+BatchNorm+pool, l2_p49 stride-2 softmax+sigmoid)
-plus a tiny parity case and a bare stride-2 k=4 identity case.  Values: x ~ N(0,1);
+The workloads are the shapes of the three transcript pages (l2_p61
+ReLU+GroupNorm, l2_p77 scale+BatchNorm+pool, l2_p49 stride-2 softmax+sigmoid),
+a tiny parity case, a bare stride-2 k=4 identity case and the BatchNorm shape
+in evaluation mode.  Values: x ~ N(0,1);
 weight and bias ~ U(-b, b) with b = 1/sqrt(Cout*k^3) (PyTorch's ConvTranspose3d
 default bound); gamma ~ U(0.5, 1.5) and beta ~ U(-0.5, 0.5) where an affine
-normalisation is present.  Drawn on the CPU in fp32 from one
+normalisation is present; BatchNorm running statistics from make_running_stats.
+Drawn on the CPU in fp32 from one
 torch.Generator seeded with 20261202 + workload index, in the order x, w, bias,
 gamma, beta (absent tensors are not drawn).
 """
@@ -24,6 +26,7 @@ EPI_IDENTITY = 0
 EPI_RELU_GROUPNORM = 1
 EPI_SCALE_BATCHNORM_AVGPOOL = 2
 EPI_SOFTMAX_SIGMOID = 3
+EPI_SCALE_BATCHNORM_EVAL_AVGPOOL = 4
 
 SEED_BASE = 20261202
 
@@ -50,7 +53,7 @@ class Spec:
 
     @property
     def affine(self) -> bool:
-        return self.epilogue in (EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL)
+        return self.epilogue in (EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
 
     def useful_flop(self) -> float:
         """2*N*Cout*Cin*k^3*Din*Hin*Win: every product of the definition, no zero taps."""
@@ -72,7 +75,11 @@ SOFTMAX = Spec("softmax_sigmoid_16x32x16x32x32_k3s2", N=16, Cin=32, Cout=64, D=1
 IDENTITY = Spec("identity_8x128x16x32x32_k4s2", N=8, Cin=128, Cout=128, D=16, H=32, W=32, k=4,
                 stride=2, pad=1, out_pad=0, bias=True, epilogue=EPI_IDENTITY, seed_index=4)
 
-ALL = [TINY, GN, BN, SOFTMAX, IDENTITY]
+# The BatchNorm shape with stored running statistics (evaluation mode).
+BN_EVAL = Spec("scale_batchnorm_eval_avgpool_16x64x16x32x32_k5", N=16, Cin=64, Cout=128, D=16, H=32, W=32,
+               k=5, bias=True, epilogue=EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, scale=2.0, seed_index=5)
+
+ALL = [TINY, GN, BN, SOFTMAX, IDENTITY, BN_EVAL]
 BY_NAME = {s.name: s for s in ALL}
 
 
@@ -91,6 +98,16 @@ def make_inputs(spec: Spec, seed: int | None = None) -> dict:
         gamma = torch.empty(spec.Cout, dtype=torch.float32).uniform_(0.5, 1.5, generator=g)
         beta = torch.empty(spec.Cout, dtype=torch.float32).uniform_(-0.5, 0.5, generator=g)
     return {"x": x, "w": w, "bias": bias, "gamma": gamma, "beta": beta}
+
+
+def make_running_stats(spec: Spec, seed: int | None = None):
+    """BatchNorm running mean ~ U(-0.2, 0.2) and running variance ~ U(0.5, 2.0),
+    CPU fp32, Cout each, seeded with 20261202 + 1000 + workload index."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(SEED_BASE + 1000 + spec.seed_index if seed is None else seed)
+    rm = torch.empty(spec.Cout, dtype=torch.float32).uniform_(-0.2, 0.2, generator=g)
+    rv = torch.empty(spec.Cout, dtype=torch.float32).uniform_(0.5, 2.0, generator=g)
+    return rm, rv
 
 
 def sample_slice(inputs: dict, n0: int, n1: int) -> dict:
