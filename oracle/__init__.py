@@ -15,6 +15,12 @@ Functions whose pins live in ``tests/test_oracle_pins.py``:
                       BN+pool closed form (l2_p77), and PyTorch CPU fp64
                       batch_norm in evaluation mode and its running statistics
   count_products   -- pinned by the product count printed on page l2_p49
+  convt3d_scatter_general, output_size_dil
+                   -- per-dimension kernel/stride/padding, dilation and
+                      grouped convolution: pinned by PyTorch CPU fp64
+                      conv_transpose3d, the adjoint identity against an
+                      independently written dilated grouped correlation, and
+                      the block structure of grouped convolution
 """
 from .oracle import (  # noqa: F401
     EPI_IDENTITY,
@@ -24,8 +30,10 @@ from .oracle import (  # noqa: F401
     EPI_SOFTMAX_SIGMOID,
     build,
     convt3d_scatter,
+    convt3d_scatter_general,
     count_products,
     forward,
     num_threads,
     output_size,
+    output_size_dil,
 )

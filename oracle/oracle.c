@@ -17,7 +17,8 @@
  *
  * Layouts (PyTorch conventions used by all three pages):
  *   x    [N, Cin, Din, Hin, Win]          fp32, contiguous (NCDHW)
- *   w    [Cin, Cout, k, k, k]              fp32, contiguous (ConvTranspose3d weight)
+ *   w    [Cin, Cout/G, kd, kh, kw]         fp32, contiguous (ConvTranspose3d weight;
+ *                                          G = convolution groups, 1 on all three pages)
  *   bias [Cout] or NULL
  *   y    [N, Cout, Do, Ho, Wo]             (BN+pool epilogue: [N, Cout])
  *
@@ -47,6 +48,13 @@ long oracle_output_size(long in, long k, long stride, long pad, long out_pad) {
     return (in - 1) * stride - 2 * pad + k + out_pad;
 }
 
+/* The same with dilation (PyTorch's ConvTranspose3d; page l2_p61's shape
+ * analysis writes the dilated form): (in - 1) * stride - 2 * pad
+ * + dilation * (k - 1) + out_pad + 1. */
+long oracle_output_size_dil(long in, long k, long stride, long pad, long out_pad, long dil) {
+    return (in - 1) * stride - 2 * pad + dil * (k - 1) + out_pad + 1;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
@@ -61,48 +69,59 @@ int oracle_num_threads(void) {
  * outside [0,Do)x[0,Ho)x[0,Wo) are dropped (that is how padding crops).  The
  * bias, when given, is added once to every output element.
  *
+ * General form (PyTorch's ConvTranspose3d): per-dimension kernel extent k[],
+ * stride s[], padding p[], output padding op[] and dilation dil[] (index 0 = d,
+ * 1 = h, 2 = w), so tap kd lands at id*s[0] - p[0] + dil[0]*kd; with G groups
+ * the input channels of group g = co / (Cout/G) are ci in [g*Cin/G, (g+1)*Cin/G)
+ * and the weight is [Cin, Cout/G, k[0], k[1], k[2]].
+ *
  * Y receives fp64 results, shape [N, Cout, Do, Ho, Wo].  Parallel over
  * (n, co): each thread owns one output channel volume, so there are no races.
  * Returns 0, or -1 on a bad argument. */
-int oracle_convt3d_scatter(int N, int Cin, int Cout, int Din, int Hin, int Win,
-                           int k, int s, int p, int op,
-                           const float *x, const float *w, const float *bias,
-                           double *Y) {
-    if (N < 0 || Cin <= 0 || Cout <= 0 || k <= 0 || s <= 0 || p < 0 || op < 0) return -1;
-    const long Do = oracle_output_size(Din, k, s, p, op);
-    const long Ho = oracle_output_size(Hin, k, s, p, op);
-    const long Wo = oracle_output_size(Win, k, s, p, op);
+int oracle_convt3d_scatter_general(int N, int Cin, int Cout, int Din, int Hin, int Win,
+                                   const int *kk, const int *ss, const int *pp, const int *opp,
+                                   const int *dil, int G,
+                                   const float *x, const float *w, const float *bias,
+                                   double *Y) {
+    if (N < 0 || Cin <= 0 || Cout <= 0 || G <= 0 || Cin % G || Cout % G) return -1;
+    for (int a = 0; a < 3; ++a)
+        if (kk[a] <= 0 || ss[a] <= 0 || pp[a] < 0 || opp[a] < 0 || dil[a] <= 0) return -1;
+    const long Do = oracle_output_size_dil(Din, kk[0], ss[0], pp[0], opp[0], dil[0]);
+    const long Ho = oracle_output_size_dil(Hin, kk[1], ss[1], pp[1], opp[1], dil[1]);
+    const long Wo = oracle_output_size_dil(Win, kk[2], ss[2], pp[2], opp[2], dil[2]);
     if (Do <= 0 || Ho <= 0 || Wo <= 0) return -1;
     const long in_vol = (long)Din * Hin * Win;
     const long out_vol = Do * Ho * Wo;
-    const long k3 = (long)k * k * k;
+    const long kvol = (long)kk[0] * kk[1] * kk[2];
     const long pairs = (long)N * Cout;
+    const long Cin_g = Cin / G, Cout_g = Cout / G;
 
 #pragma omp parallel for schedule(dynamic, 1)
     for (long pc = 0; pc < pairs; ++pc) {
         const long n = pc / Cout;
         const long co = pc % Cout;
+        const long g = co / Cout_g, col = co % Cout_g;
         double *Yc = Y + (n * Cout + co) * out_vol;
         const double b = bias ? (double)bias[co] : 0.0;
         for (long o = 0; o < out_vol; ++o) Yc[o] = 0.0;
-        for (long ci = 0; ci < Cin; ++ci) {
+        for (long ci = g * Cin_g; ci < (g + 1) * Cin_g; ++ci) {
             const float *xc = x + (n * Cin + ci) * in_vol;
-            const float *wc = w + (ci * Cout + co) * k3;
+            const float *wc = w + (ci * Cout_g + col) * kvol;
             for (long id = 0; id < Din; ++id)
             for (long ih = 0; ih < Hin; ++ih)
             for (long iw = 0; iw < Win; ++iw) {
                 const double xv = (double)xc[(id * Hin + ih) * Win + iw];
-                for (long kd = 0; kd < k; ++kd) {
-                    const long od = id * s - p + kd;
+                for (long kd = 0; kd < kk[0]; ++kd) {
+                    const long od = id * ss[0] - pp[0] + dil[0] * kd;
                     if (od < 0 || od >= Do) continue;
-                    for (long kh = 0; kh < k; ++kh) {
-                        const long oh = ih * s - p + kh;
+                    for (long kh = 0; kh < kk[1]; ++kh) {
+                        const long oh = ih * ss[1] - pp[1] + dil[1] * kh;
                         if (oh < 0 || oh >= Ho) continue;
-                        for (long kw = 0; kw < k; ++kw) {
-                            const long ow = iw * s - p + kw;
+                        for (long kw = 0; kw < kk[2]; ++kw) {
+                            const long ow = iw * ss[2] - pp[2] + dil[2] * kw;
                             if (ow < 0 || ow >= Wo) continue;
                             Yc[(od * Ho + oh) * Wo + ow] +=
-                                xv * (double)wc[(kd * k + kh) * k + kw];
+                                xv * (double)wc[(kd * kk[1] + kh) * kk[2] + kw];
                         }
                     }
                 }
@@ -111,6 +130,16 @@ int oracle_convt3d_scatter(int N, int Cin, int Cout, int Din, int Hin, int Win,
         for (long o = 0; o < out_vol; ++o) Yc[o] += b;
     }
     return 0;
+}
+
+/* The cubic, dense, undilated case (all three pages). */
+int oracle_convt3d_scatter(int N, int Cin, int Cout, int Din, int Hin, int Win,
+                           int k, int s, int p, int op,
+                           const float *x, const float *w, const float *bias,
+                           double *Y) {
+    const int kk[3] = {k, k, k}, ss[3] = {s, s, s}, pp[3] = {p, p, p}, opp[3] = {op, op, op};
+    const int dil[3] = {1, 1, 1};
+    return oracle_convt3d_scatter_general(N, Cin, Cout, Din, Hin, Win, kk, ss, pp, opp, dil, 1, x, w, bias, Y);
 }
 
 /* Products visited by the scatter loop nest, split into those that land in
@@ -276,18 +305,20 @@ static void bn_update_running(int N, int C, long vol, double scale, double momen
  * For the BN+pool epilogues y / y64 hold [N, Cout]; otherwise
  * [N, Cout, Do, Ho, Wo].  running_mean / running_var: read by the
  * evaluation-mode epilogue; updated in place by the batch-statistics epilogue
- * when both are given (NULL skips the update).  Returns 0, -1 on a bad
- * argument, -2 if out of memory. */
-int oracle_convt3d_forward(int N, int Cin, int Cout, int Din, int Hin, int Win,
-                           int k, int s, int p, int op,
-                           const float *x, const float *w, const float *bias,
-                           int epilogue, int groups, double eps, double scale,
-                           const float *gamma, const float *beta,
-                           float *running_mean, float *running_var, double momentum,
-                           float *y, double *y64) {
-    const long Do = oracle_output_size(Din, k, s, p, op);
-    const long Ho = oracle_output_size(Hin, k, s, p, op);
-    const long Wo = oracle_output_size(Win, k, s, p, op);
+ * when both are given (NULL skips the update).  Shape arguments as in
+ * oracle_convt3d_scatter_general.  Returns 0, -1 on a bad argument, -2 if out
+ * of memory. */
+int oracle_convt3d_forward_general(int N, int Cin, int Cout, int Din, int Hin, int Win,
+                                   const int *kk, const int *ss, const int *pp, const int *opp,
+                                   const int *dil, int conv_groups,
+                                   const float *x, const float *w, const float *bias,
+                                   int epilogue, int groups, double eps, double scale,
+                                   const float *gamma, const float *beta,
+                                   float *running_mean, float *running_var, double momentum,
+                                   float *y, double *y64) {
+    const long Do = oracle_output_size_dil(Din, kk[0], ss[0], pp[0], opp[0], dil[0]);
+    const long Ho = oracle_output_size_dil(Hin, kk[1], ss[1], pp[1], opp[1], dil[1]);
+    const long Wo = oracle_output_size_dil(Win, kk[2], ss[2], pp[2], opp[2], dil[2]);
     if (N <= 0 || Do <= 0 || Ho <= 0 || Wo <= 0) return -1;
     if (epilogue == ORACLE_EPI_RELU_GROUPNORM && (groups <= 0 || Cout % groups)) return -1;
     if (epilogue < 0 || epilogue > 4) return -1;
@@ -296,9 +327,9 @@ int oracle_convt3d_forward(int N, int Cin, int Cout, int Din, int Hin, int Win,
     const long total = (long)N * Cout * vol;
     double *Y = (double *)malloc(sizeof(double) * (size_t)total);
     if (!Y) return -2;
-    int rc = oracle_convt3d_scatter(N, Cin, Cout, Din, Hin, Win, k, s, p, op, x, w, bias, Y);
+    int rc = oracle_convt3d_scatter_general(N, Cin, Cout, Din, Hin, Win, kk, ss, pp, opp, dil, conv_groups, x, w,
+                                            bias, Y);
     if (rc) { free(Y); return rc; }
-
     if (epilogue == ORACLE_EPI_SCALE_BATCHNORM_AVGPOOL || epilogue == ORACLE_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) {
         double *pooled = (double *)malloc(sizeof(double) * (size_t)N * Cout);
         if (!pooled) { free(Y); return -2; }
@@ -329,4 +360,19 @@ int oracle_convt3d_forward(int N, int Cin, int Cout, int Din, int Hin, int Win,
     }
     free(Y);
     return 0;
+}
+
+/* The cubic, dense, undilated case (all three pages). */
+int oracle_convt3d_forward(int N, int Cin, int Cout, int Din, int Hin, int Win,
+                           int k, int s, int p, int op,
+                           const float *x, const float *w, const float *bias,
+                           int epilogue, int groups, double eps, double scale,
+                           const float *gamma, const float *beta,
+                           float *running_mean, float *running_var, double momentum,
+                           float *y, double *y64) {
+    const int kk[3] = {k, k, k}, ss[3] = {s, s, s}, pp[3] = {p, p, p}, opp[3] = {op, op, op};
+    const int dil[3] = {1, 1, 1};
+    return oracle_convt3d_forward_general(N, Cin, Cout, Din, Hin, Win, kk, ss, pp, opp, dil, 1, x, w, bias,
+                                          epilogue, groups, eps, scale, gamma, beta, running_mean, running_var,
+                                          momentum, y, y64);
 }

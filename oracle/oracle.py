@@ -60,6 +60,14 @@ def _load():
         lib.oracle_convt3d_forward.restype = i
         lib.oracle_convt3d_forward.argtypes = (
             [i] * 10 + [P, P, P, i, i, ctypes.c_double, ctypes.c_double, P, P, P, P, ctypes.c_double, P, P])
+        lib.oracle_output_size_dil.restype = ctypes.c_long
+        lib.oracle_output_size_dil.argtypes = [ctypes.c_long] * 6
+        lib.oracle_convt3d_scatter_general.restype = i
+        lib.oracle_convt3d_scatter_general.argtypes = [i] * 6 + [P] * 5 + [i] + [P] * 4
+        lib.oracle_convt3d_forward_general.restype = i
+        lib.oracle_convt3d_forward_general.argtypes = (
+            [i] * 6 + [P] * 5 + [i] + [P, P, P, i, i, ctypes.c_double, ctypes.c_double, P, P, P, P,
+                                      ctypes.c_double, P, P])
         _lib = lib
         return lib
 
@@ -115,30 +123,71 @@ def count_products(N, Cin, Cout, Din, Hin, Win, k, stride, pad, out_pad):
     return a.value, b.value
 
 
-def forward(x, w, bias=None, *, stride=1, pad=0, out_pad=0, epilogue=EPI_IDENTITY,
+def _triple(v, name):
+    t = (int(v),) * 3 if np.isscalar(v) else tuple(int(a) for a in v)
+    if len(t) != 3:
+        raise ValueError(f"{name} must be an int or 3 ints (d, h, w)")
+    return t
+
+
+def _ints(t):
+    return (ctypes.c_int * 3)(*t)
+
+
+def output_size_dil(n_in: int, k: int, stride: int, pad: int, out_pad: int, dilation: int) -> int:
+    return int(_load().oracle_output_size_dil(n_in, k, stride, pad, out_pad, dilation))
+
+
+def _general_shape(x, w, stride, pad, out_pad, dilation, conv_groups):
+    N, Cin, Din, Hin, Win = x.shape
+    if w.ndim != 5 or w.shape[0] != Cin:
+        raise ValueError("w must be [Cin, Cout/groups, kd, kh, kw]")
+    kk = tuple(int(a) for a in w.shape[2:])
+    ss, pp, oo, dd = (_triple(v, n) for v, n in ((stride, "stride"), (pad, "pad"), (out_pad, "out_pad"),
+                                                  (dilation, "dilation")))
+    Cout = w.shape[1] * int(conv_groups)
+    outs = tuple(output_size_dil(i, kk[a], ss[a], pp[a], oo[a], dd[a]) for a, i in enumerate((Din, Hin, Win)))
+    return N, Cin, Cout, (Din, Hin, Win), kk, ss, pp, oo, dd, outs
+
+
+def convt3d_scatter_general(x, w, bias=None, *, stride=1, pad=0, out_pad=0, dilation=1, conv_groups=1):
+    """fp64 scatter form with per-dimension shapes, dilation and groups; w is
+    [Cin, Cout/groups, kd, kh, kw].  Returns [N,Cout,Do,Ho,Wo] float64."""
+    x, w, bias = _f32(x, "x"), _f32(w, "w"), _f32(bias, "bias")
+    N, Cin, Cout, ins, kk, ss, pp, oo, dd, outs = _general_shape(x, w, stride, pad, out_pad, dilation, conv_groups)
+    Y = np.empty((N, Cout) + outs, np.float64)
+    rc = _load().oracle_convt3d_scatter_general(N, Cin, Cout, *ins, _ints(kk), _ints(ss), _ints(pp), _ints(oo),
+                                                _ints(dd), int(conv_groups), _ptr(x), _ptr(w), _ptr(bias), _ptr(Y))
+    if rc:
+        raise ValueError(f"oracle_convt3d_scatter_general failed ({rc})")
+    return Y
+
+
+def forward(x, w, bias=None, *, stride=1, pad=0, out_pad=0, dilation=1, conv_groups=1, epilogue=EPI_IDENTITY,
             groups=1, eps=1e-5, scale=1.0, gamma=None, beta=None, running_mean=None,
             running_var=None, momentum=0.1, want_f64=False):
     """Transposed convolution + epilogue, fp64 inside, fp32 result.
 
-    Returns y (float32) or (y, y64) when ``want_f64``.  Shapes: [N,Cout,Do,Ho,Wo],
-    or [N,Cout,1,1,1] for the BN+pool epilogues.  running_mean / running_var
-    (float32 [Cout]) are read by the evaluation-mode epilogue and updated in
-    place by the batch-statistics one.
+    stride / pad / out_pad / dilation: an int or (d, h, w); the kernel extents
+    come from w, [Cin, Cout/conv_groups, kd, kh, kw].  ``groups`` is the
+    GroupNorm group count.  Returns y (float32) or (y, y64) when ``want_f64``.
+    Shapes: [N,Cout,Do,Ho,Wo], or [N,Cout,1,1,1] for the BN+pool epilogues.
+    running_mean / running_var (float32 [Cout]) are read by the evaluation-mode
+    epilogue and updated in place by the batch-statistics one.
     """
     x, w = _f32(x, "x"), _f32(w, "w")
     bias, gamma, beta = _f32(bias, "bias"), _f32(gamma, "gamma"), _f32(beta, "beta")
     running_mean, running_var = _f32(running_mean, "running_mean"), _f32(running_var, "running_var")
-    k = w.shape[2]
-    N, Cin, Cout, Din, Hin, Win, Do, Ho, Wo = _shape(x, w, k, stride, pad, out_pad)
+    N, Cin, Cout, ins, kk, ss, pp, oo, dd, outs = _general_shape(x, w, stride, pad, out_pad, dilation, conv_groups)
     pooled = epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
-    shape = (N, Cout, 1, 1, 1) if pooled else (N, Cout, Do, Ho, Wo)
+    shape = (N, Cout, 1, 1, 1) if pooled else (N, Cout) + outs
     y = np.empty(shape, np.float32)
     y64 = np.empty(shape, np.float64) if want_f64 else None
-    rc = _load().oracle_convt3d_forward(N, Cin, Cout, Din, Hin, Win, k, stride, pad, out_pad,
-                                        _ptr(x), _ptr(w), _ptr(bias), int(epilogue), int(groups),
-                                        float(eps), float(scale), _ptr(gamma), _ptr(beta),
-                                        _ptr(running_mean), _ptr(running_var), float(momentum),
-                                        _ptr(y), _ptr(y64))
+    rc = _load().oracle_convt3d_forward_general(N, Cin, Cout, *ins, _ints(kk), _ints(ss), _ints(pp), _ints(oo),
+                                                _ints(dd), int(conv_groups), _ptr(x), _ptr(w), _ptr(bias),
+                                                int(epilogue), int(groups), float(eps), float(scale), _ptr(gamma),
+                                                _ptr(beta), _ptr(running_mean), _ptr(running_var), float(momentum),
+                                                _ptr(y), _ptr(y64))
     if rc:
-        raise ValueError(f"oracle_convt3d_forward failed ({rc})")
+        raise ValueError(f"oracle_convt3d_forward_general failed ({rc})")
     return (y, y64) if want_f64 else y

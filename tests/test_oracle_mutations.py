@@ -15,9 +15,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 MUTATIONS = {
-    "pad_sign": ("const long od = id * s - p + kd;", "const long od = id * s + p + kd;"),
-    "weight_transposed": ("wc = w + (ci * Cout + co) * k3", "wc = w + (co * Cin + ci) * k3"),
-    "tap_axes_swapped": ("(double)wc[(kd * k + kh) * k + kw]", "(double)wc[(kw * k + kh) * k + kd]"),
+    "pad_sign": ("const long od = id * ss[0] - pp[0] + dil[0] * kd;", "const long od = id * ss[0] + pp[0] + dil[0] * kd;"),
+    "weight_transposed": ("wc = w + (ci * Cout_g + col) * kvol", "wc = w + (col * Cin + ci) * kvol"),
+    "tap_axes_swapped": ("(double)wc[(kd * kk[1] + kh) * kk[2] + kw]", "(double)wc[(kw * kk[1] + kh) * kk[0] + kd]"),
     "gn_unbiased_var": ("const double var = ss / (double)cnt;", "const double var = ss / (double)(cnt - 1);"),
     "bn_var_shifted": ("const double var = ss / cnt;", "const double var = ss / cnt + 1e-3;"),
     "out_size_pad_once": ("return (in - 1) * stride - 2 * pad + k + out_pad;",
@@ -32,6 +32,14 @@ MUTATIONS = {
                            "const double var_unbiased = cnt > 1.0 ? ss / cnt : 0.0;"),
     "eval_bn_eps_outside": ("const double inv = 1.0 / sqrt((double)rvar[c] + eps);",
                             "const double inv = 1.0 / (sqrt((double)rvar[c]) + eps);"),
+    "dilation_dropped_h": ("const long oh = ih * ss[1] - pp[1] + dil[1] * kh;",
+                           "const long oh = ih * ss[1] - pp[1] + kh;"),
+    "stride_axes_mixed": ("const long ow = iw * ss[2] - pp[2] + dil[2] * kw;",
+                          "const long ow = iw * ss[1] - pp[2] + dil[2] * kw;"),
+    "group_channels_from_group0": ("for (long ci = g * Cin_g; ci < (g + 1) * Cin_g; ++ci) {",
+                                   "for (long ci = 0; ci < Cin_g; ++ci) {"),
+    "out_size_dilation_off_by_one": ("return (in - 1) * stride - 2 * pad + dil * (k - 1) + out_pad + 1;",
+                                     "return (in - 1) * stride - 2 * pad + dil * k + out_pad;"),
 }
 
 

@@ -443,3 +443,102 @@ def test_batchnorm_eval_with_batch_statistics_equals_training_output():
     _, ev = oracle.forward(x, w, b, epilogue=oracle.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, scale=s, gamma=gamma,
                            beta=beta, running_mean=mean, running_var=var.astype(np.float32), want_f64=True)
     assert np.max(np.abs(ev - train)) < 1e-5
+
+
+# ------------------------------ general shapes: per-dimension, dilation, groups ----
+
+GENERAL_CASES = [
+    # (kd, kh, kw), stride, pad, out_pad, dilation, conv_groups
+    ((3, 2, 4), (1, 2, 2), (1, 0, 2), (0, 1, 1), (1, 1, 1), 1),
+    ((3, 3, 3), (1, 1, 1), (0, 1, 2), (0, 0, 0), (2, 1, 3), 1),
+    ((2, 3, 3), (2, 1, 2), (0, 1, 1), (1, 0, 0), (1, 2, 2), 1),
+    ((3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), 2),
+    ((1, 3, 2), (1, 2, 1), (0, 1, 0), (0, 1, 0), (1, 1, 1), 4),
+    ((3, 2, 3), (2, 2, 1), (2, 1, 1), (0, 1, 0), (3, 2, 1), 2),
+]
+
+
+def _general_case(rng, N, Cin, Cout, D, H, W, kk, G, bias=True):
+    x = rng.standard_normal((N, Cin, D, H, W)).astype(np.float32)
+    kv = kk[0] * kk[1] * kk[2]
+    w = (rng.uniform(-1, 1, (Cin, Cout // G) + tuple(kk)) / math.sqrt(Cout * kv)).astype(np.float32)
+    b = rng.uniform(-0.3, 0.3, Cout).astype(np.float32) if bias else None
+    return x, w, b
+
+
+@pytest.mark.parametrize("kk,s,p,op,dil,G", GENERAL_CASES)
+def test_general_scatter_matches_torch_cpu_fp64(kk, s, p, op, dil, G):
+    rng = np.random.default_rng(sum(kk) * 7 + sum(s) + 3 * sum(p) + 11 * sum(dil) + G)
+    x, w, b = _general_case(rng, 2, 4, 8, 3, 4, 5, kk, G)
+    Y = oracle.convt3d_scatter_general(x, w, b, stride=s, pad=p, out_pad=op, dilation=dil, conv_groups=G)
+    ref = F.conv_transpose3d(torch.from_numpy(x).double(), torch.from_numpy(w).double(),
+                             torch.from_numpy(b).double(), stride=s, padding=p, output_padding=op,
+                             groups=G, dilation=dil).numpy()
+    assert Y.shape == ref.shape
+    assert np.max(np.abs(Y - ref)) <= 1e-12
+
+
+def _forward_conv_general(y, w, s, p, dil, G, in_shape):
+    """Independent strided, dilated, grouped forward correlation with the same weight:
+    out[n,ci,i] = sum_{co in group(ci), t} w[ci,co',t] * y[n,co,i*s - p + dil*t]."""
+    N = y.shape[0]
+    Cin, Cout_g = w.shape[0], w.shape[1]
+    Cin_g = Cin // G
+    kd, kh, kw = w.shape[2:]
+    out = np.zeros((N, Cin) + tuple(in_shape))
+    Y = y
+    Do, Ho, Wo = Y.shape[2:]
+    w64 = w.astype(np.float64)
+    for ci in range(Cin):
+        g = ci // Cin_g
+        for col in range(Cout_g):
+            co = g * Cout_g + col
+            for a in range(kd):
+                for bb in range(kh):
+                    for c in range(kw):
+                        od = np.arange(in_shape[0]) * s[0] - p[0] + dil[0] * a
+                        oh = np.arange(in_shape[1]) * s[1] - p[1] + dil[1] * bb
+                        ow = np.arange(in_shape[2]) * s[2] - p[2] + dil[2] * c
+                        md, mh, mw = (od >= 0) & (od < Do), (oh >= 0) & (oh < Ho), (ow >= 0) & (ow < Wo)
+                        sub = Y[:, co][:, np.clip(od, 0, Do - 1)][:, :, np.clip(oh, 0, Ho - 1)][:, :, :, np.clip(ow, 0, Wo - 1)]
+                        mask = md[:, None, None] & mh[None, :, None] & mw[None, None, :]
+                        out[:, ci] += w64[ci, col, a, bb, c] * sub * mask
+    return out
+
+
+@pytest.mark.parametrize("kk,s,p,op,dil,G", GENERAL_CASES)
+def test_general_adjoint_identity(kk, s, p, op, dil, G):
+    rng = np.random.default_rng(1000 + sum(kk) + 5 * sum(dil) + G)
+    x, w, _ = _general_case(rng, 1, 4, 4, 3, 3, 4, kk, G, bias=False)
+    Y = oracle.convt3d_scatter_general(x, w, None, stride=s, pad=p, out_pad=op, dilation=dil, conv_groups=G)
+    yr = rng.standard_normal(Y.shape)
+    lhs = float(np.sum(Y * yr))
+    rhs = float(np.sum(x.astype(np.float64) * _forward_conv_general(yr, w, s, p, dil, G, x.shape[2:])))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+def test_groups_are_independent_dense_convolutions():
+    # a grouped transposed convolution is G dense ones on channel slices, concatenated
+    rng = np.random.default_rng(77)
+    G, kk = 3, (3, 2, 3)
+    x, w, b = _general_case(rng, 2, 6, 9, 3, 4, 3, kk, G)
+    Y = oracle.convt3d_scatter_general(x, w, b, stride=(2, 1, 2), pad=(1, 0, 1), out_pad=(1, 0, 0), conv_groups=G)
+    for g in range(G):
+        xs = np.ascontiguousarray(x[:, 2 * g:2 * g + 2])
+        ws = np.ascontiguousarray(w[2 * g:2 * g + 2])
+        Yg = oracle.convt3d_scatter_general(xs, ws, np.ascontiguousarray(b[3 * g:3 * g + 3]), stride=(2, 1, 2),
+                                            pad=(1, 0, 1), out_pad=(1, 0, 0))
+        assert np.array_equal(Y[:, 3 * g:3 * g + 3], Yg)
+
+
+def test_general_forward_epilogues_match_cubic_entry():
+    # the general entry with cubic, dense, undilated arguments is the cubic one
+    rng = np.random.default_rng(91)
+    x, w, b = rand_case(rng, 2, 3, 8, 3, 4, 3, 3)
+    gamma = rng.uniform(0.5, 1.5, 8).astype(np.float32)
+    beta = rng.uniform(-0.5, 0.5, 8).astype(np.float32)
+    a = oracle.forward(x, w, b, stride=2, pad=1, out_pad=1, epilogue=oracle.EPI_RELU_GROUPNORM, groups=2,
+                       gamma=gamma, beta=beta)
+    c = oracle.forward(x, w, b, stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(1, 1, 1), dilation=(1, 1, 1),
+                       conv_groups=1, epilogue=oracle.EPI_RELU_GROUPNORM, groups=2, gamma=gamma, beta=beta)
+    assert np.array_equal(a, c)
