@@ -8,7 +8,7 @@ flushed (a 256 MiB write) before every timed step.  Each step is timed with
 CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--precision 3xtf32|ffma] [--impl gpu|reference]
+                  [--precision 3xtf32|tf32|bf16|ffma] [--impl gpu|reference]
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (the path shards by batch with no collective on the data path);
@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.BY_NAME))
-    ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "ffma"])
+    ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "tf32", "bf16", "ffma"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the CPU baseline sample")
@@ -134,7 +134,7 @@ class ClockSampler:
 # ------------------------------------------------------- traffic from ncu ----
 
 def kernel_source_sha(precision):
-    src = "tc.cu" if precision == "3xtf32" else "ffma.cu"
+    src = "ffma.cu" if precision == "ffma" else "tc.cu"
     path = os.path.join(ROOT, "transposed_convolution_convt3d_gb300", "csrc", src)
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -255,14 +255,15 @@ def run_gpu(args, spec):
     import torch
     import torch.distributed as dist
 
-    from transposed_convolution_convt3d_gb300 import PREC_3XTF32, PREC_FFMA, HostPipeline, Plan
+    from transposed_convolution_convt3d_gb300 import (PREC_3XTF32, PREC_BF16, PREC_FFMA, PREC_TF32, HostPipeline,
+                                                      Plan)
 
     world, rank, local = dist_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    prec = PREC_3XTF32 if args.precision == "3xtf32" else PREC_FFMA
+    prec = {"3xtf32": PREC_3XTF32, "tf32": PREC_TF32, "bf16": PREC_BF16, "ffma": PREC_FFMA}[args.precision]
 
     inputs = workloads.make_inputs(spec)
     d = {k: (v.to(dev) if v is not None else None) for k, v in inputs.items()}
@@ -376,13 +377,16 @@ def run_gpu(args, spec):
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "peak_source": f"{pk['source']} HBM copy bandwidth",
                 "algorithmic_bytes": info["forward_min_bytes"]}
-    elif prec == PREC_3XTF32:
-        peak = pk["bf16_tflops"] * TF32_OVER_BF16
+    elif prec in (PREC_3XTF32, PREC_TF32, PREC_BF16):
+        bf = prec == PREC_BF16
+        peak = pk["bf16_tflops"] * (1.0 if bf else TF32_OVER_BF16)
         achieved = useful / (gemm_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{pk['source']} bf16 burst x nominal TF32/BF16 ratio {TF32_OVER_BF16:.4f}",
-                "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak,
-                "frac_of_3xtf32_peak": achieved / (peak / 3.0)}
+                "peak_source": (f"{pk['source']} bf16 burst" if bf else
+                                f"{pk['source']} bf16 burst x nominal TF32/BF16 ratio {TF32_OVER_BF16:.4f}"),
+                "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak}
+        if prec == PREC_3XTF32:
+            roof["frac_of_3xtf32_peak"] = achieved / (peak / 3.0)
     else:
         peak = SMS * FP32_FMA_PER_CLK_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
         achieved = useful / (gemm_avg * 1e-3) / 1e12
@@ -390,7 +394,7 @@ def run_gpu(args, spec):
                 "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 flop x max SM clock",
                 "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak}
     roof["kernel"] = ("boxsum_kernel + bn_eval_out_kernel" if eval_bn else
-                      "convt3d_tc_gemm" if prec == PREC_3XTF32 else "ffma_conv_kernel")
+                      "ffma_conv_kernel" if prec == PREC_FFMA else "convt3d_tc_gemm")
     roof["kernel_ms"] = gemm_avg
     roof["kernel_share_of_step"] = gemm_avg / ms_per_step
     roof["traffic"] = committed_traffic(args.precision, spec.name)

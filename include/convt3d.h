@@ -11,6 +11,12 @@
  *   where od = id*stride - pad + kd (likewise oh, ow), restricted to
  *   0 <= od < Do, and Do = (Din - 1)*stride - 2*pad + k + out_pad.
  *
+ * General form (PyTorch's ConvTranspose3d; page l2_p61's shape analysis
+ * writes the dilated extent): per-dimension kernel extent, stride, padding
+ * and output padding, dilation (od = id*s - p + dil*kd, Do = (Din - 1)*s - 2p
+ * + dil*(kd - 1) + op + 1) and G convolution groups (output channel co reads
+ * the Cin/G input channels of its group; w is [Cin, Cout/G, kd, kh, kw]).
+ *
  * followed by one epilogue:
  *   IDENTITY                  y = Y                                     (no page; bare op)
  *   RELU_GROUPNORM            v = max(Y,0); GroupNorm(groups) with biased
@@ -29,16 +35,18 @@
  *                                                                          submitted solution)
  *
  * Computation: an output-stationary implicit GEMM, M = output positions,
- * N = Cout, K = Cin x taps.  Stride 2 is split into the 8 output-parity
- * classes, each a dense stride-1 correlation over only the taps that reach
- * it, so no zero-inserted taps are multiplied.  CONVT3D_PREC_3XTF32 runs the
+ * N = Cout, K = Cin x taps.  Stride 2 is split into the output-parity
+ * classes (8 when all three strides are 2), each a dense stride-1
+ * correlation over only the taps that reach it, so no zero-inserted taps are
+ * multiplied.  Grouped convolution runs as the dense GEMM over a packed
+ * weight that is zero outside the diagonal blocks.  CONVT3D_PREC_3XTF32 runs the
  * products on the tcgen05 tensor cores in split TF32 (a_hi*b_hi + a_hi*b_lo +
  * a_lo*b_hi, fp32 accumulation); CONVT3D_PREC_FFMA runs them as fp32 FMAs on
  * the CUDA cores (kept as an ablation).
  *
  * Conventions for every entry point:
  *   - Layouts: x [N,Cin,Din,Hin,Win], y [N,Cout,Do,Ho,Wo] (BN+pool: [N,Cout,1,1,1]),
- *     w [Cin,Cout,k,k,k] (PyTorch ConvTranspose3d), bias/gamma/beta [Cout];
+ *     w [Cin,Cout/G,kd,kh,kw] (PyTorch ConvTranspose3d), bias/gamma/beta [Cout];
  *     all fp32, contiguous, device memory, 16-byte aligned.
  *   - Ownership: the caller allocates and owns every device buffer (input,
  *     output, workspace).  The library never allocates or frees device memory
@@ -77,8 +85,15 @@ typedef enum {
 } convt3d_epilogue_t;
 
 typedef enum {
-    CONVT3D_PREC_3XTF32 = 0, /* tcgen05 tensor cores, split TF32 (default)  */
-    CONVT3D_PREC_FFMA = 1    /* CUDA-core fp32 FMA implicit GEMM (ablation) */
+    CONVT3D_PREC_3XTF32 = 0, /* tcgen05 tensor cores, split TF32 (default)             */
+    CONVT3D_PREC_FFMA = 1,   /* CUDA-core fp32 FMA implicit GEMM (ablation)            */
+    CONVT3D_PREC_TF32 = 2,   /* tcgen05 tensor cores, one TF32 product per term: inputs
+                                rounded to TF32 (nearest), fp32 accumulation; results
+                                within the 1e-2 tier of page l2_p49's harness quote */
+    CONVT3D_PREC_BF16 = 3    /* tcgen05 tensor cores, one BF16 product per term (kind::f16):
+                                inputs rounded to bf16 (nearest even) when staged and
+                                packed, fp32 accumulation and epilogue, fp32 I/O;
+                                same 1e-2 tier                                        */
 } convt3d_precision_t;
 
 typedef enum {
@@ -98,14 +113,24 @@ typedef struct {
     int Din, Hin, Win;    /* input extent (>= 1)                                        */
     int k;                /* cubic kernel size, 1..7                                    */
     int stride;           /* 1 or 2                                                     */
-    int pad;              /* 0 <= pad < k                                               */
-    int out_pad;          /* 0 <= out_pad < stride                                      */
+    int pad;              /* 0 <= pad <= dilation * (k - 1)                             */
+    int out_pad;          /* 0 <= out_pad < max(stride, dilation)                       */
     int has_bias;         /* bias pointer is read iff non-zero                          */
     int epilogue;         /* convt3d_epilogue_t                                         */
     int groups;           /* GroupNorm groups; Cout % groups == 0 (RELU_GROUPNORM only) */
     float eps;            /* GroupNorm / BatchNorm epsilon (> 0)                        */
     float scale;          /* multiplier before BatchNorm (SCALE_BATCHNORM_AVGPOOL)      */
     int precision;        /* convt3d_precision_t                                        */
+    /* General shapes (PyTorch ConvTranspose3d).  A zero-initialised tail gives
+     * the cubic, undilated, dense case described by the fields above.        */
+    int per_dim;          /* non-zero: kdims/strides/pads/out_pads replace k/stride/
+                             pad/out_pad, index 0 = d, 1 = h, 2 = w               */
+    int kdims[3];         /* kernel extent per dimension, 1..7                    */
+    int strides[3];       /* 1 or 2 per dimension                                 */
+    int pads[3];
+    int out_pads[3];
+    int dilation[3];      /* >= 1 per dimension; 0 means 1 (also without per_dim) */
+    int conv_groups;      /* grouped convolution, Cin % G == Cout % G == 0; 0 = 1 */
 } convt3d_desc_t;
 
 typedef struct convt3d_plan_s *convt3d_plan_t;
@@ -113,7 +138,7 @@ typedef struct convt3d_plan_s *convt3d_plan_t;
 /* Plan facts, for callers that report or size things. */
 typedef struct {
     int64_t out_shape[5];        /* y shape ([N,Cout,1,1,1] for the BN+pool epilogues)  */
-    int num_classes;             /* stride^3 output-parity classes                      */
+    int num_classes;             /* output-parity classes (product of the strides)       */
     int64_t gemm_m;              /* output positions (N*Do*Ho*Wo)                        */
     int64_t gemm_n;              /* Cout                                                */
     int64_t gemm_k_total;        /* sum over classes of Cin * taps(class)                */
@@ -121,7 +146,7 @@ typedef struct {
     int tile_m;                  /* output positions per tile                            */
     int launches_per_forward;    /* kernels convt3d_forward launches                     */
     int launches_per_pack;       /* kernels convt3d_pack_weights launches                */
-    double useful_flop;          /* 2*N*Cout*Cin*k^3*Din*Hin*Win                         */
+    double useful_flop;          /* 2*N*Cout*(Cin/G)*kd*kh*kw*Din*Hin*Win                */
     double issued_mma_flop;      /* tensor/FMA flop the main kernel issues per forward   */
     double gemm_min_bytes;       /* algorithmic HBM bytes of the main kernel             */
     double forward_min_bytes;    /* algorithmic HBM bytes of the whole forward           */
@@ -147,7 +172,8 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t plan, convt3d_info_t *info);
  * status word).  0 on a NULL plan.  Host only. */
 size_t convt3d_workspace_bytes(convt3d_plan_t plan);
 
-/* Re-lay the weight w [Cin,Cout,k,k,k] into the workspace: per parity class
+/* Re-lay the weight w [Cin,Cout/G,kd,kh,kw] (G = conv_groups; [Cin,Cout,k,k,k]
+ * in the cubic dense case) into the workspace: per parity class
  * and tap, Cout rows by Cin columns, split into TF32 hi and lo planes
  * (3XTF32) or kept fp32 (FFMA).  Call whenever w changes; forward reads only
  * the packed copy.  Also clears the workspace status word.  Asynchronous on

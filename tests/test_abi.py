@@ -44,7 +44,8 @@ def test_status_strings(lib):
 
 def make_desc(**kw):
     base = dict(N=2, Cin=8, Cout=16, Din=8, Hin=8, Win=8, k=3, stride=1, pad=0, out_pad=0, has_bias=0,
-                epilogue=0, groups=1, eps=1e-5, scale=1.0, precision=0)
+                epilogue=0, groups=1, eps=1e-5, scale=1.0, precision=0, per_dim=0, kdims=(0, 0, 0),
+                strides=(0, 0, 0), pads=(0, 0, 0), out_pads=(0, 0, 0), dilation=(0, 0, 0), conv_groups=0)
     base.update(kw)
     return _lib.Desc(*[base[f] for f, _ in _lib.Desc._fields_])
 
@@ -65,6 +66,13 @@ def create(lib, **kw):
     (dict(stride=2, k=3, pad=1, Cout=144), 2), (dict(stride=2, k=1), 2),
     (dict(epilogue=4, eps=-1.0), 1), (dict(epilogue=4, scale=float("inf")), 1),
     (dict(epilogue=4, Hin=200, Win=200), 2),
+    # general shapes
+    (dict(dilation=(-1, 1, 1)), 1), (dict(conv_groups=-2), 1), (dict(conv_groups=3), 1),
+    (dict(per_dim=1, kdims=(3, 0, 3), strides=(1, 1, 1)), 1),
+    (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 2, 1), out_pads=(0, 2, 0)), 1),
+    (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 1, 3)), 2), (dict(per_dim=1, kdims=(3, 8, 3), strides=(1, 1, 1)), 2),
+    (dict(stride=2, dilation=(2, 2, 2)), 2), (dict(dilation=(16, 1, 1)), 2),
+    (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 1, 2), pads=(0, 0, 0), Cout=144), 2),
 ])
 def test_plan_validation(lib, kw, status):
     st, h = create(lib, **kw)
@@ -77,6 +85,38 @@ def test_ffma_accepts_what_tensor_path_rejects(lib):
     st, h = create(lib, stride=2, k=3, pad=1, Cout=144, precision=1)
     assert st == 0
     lib.convt3d_plan_destroy(h)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(per_dim=1, kdims=(3, 2, 4), strides=(1, 2, 2), pads=(1, 0, 2), out_pads=(0, 1, 1)),
+    dict(dilation=(2, 1, 3), pad=1),
+    dict(conv_groups=4, Cin=8, Cout=16),
+    dict(per_dim=1, kdims=(2, 3, 3), strides=(2, 1, 2), pads=(0, 1, 1), out_pads=(1, 0, 0), dilation=(1, 2, 3)),
+])
+@pytest.mark.parametrize("precision", [0, 1])
+def test_general_shapes_plan_facts(lib, kw, precision):
+    st, h = create(lib, precision=precision, **kw)
+    assert st == 0, lib.convt3d_last_error()
+    try:
+        d = make_desc(precision=precision, **kw)
+        kk = tuple(d.kdims) if d.per_dim else (d.k,) * 3
+        ss = tuple(d.strides) if d.per_dim else (d.stride,) * 3
+        pp = tuple(d.pads) if d.per_dim else (d.pad,) * 3
+        oo = tuple(d.out_pads) if d.per_dim else (d.out_pad,) * 3
+        dd = tuple(v or 1 for v in d.dilation)
+        G = d.conv_groups or 1
+        outs = [oracle.output_size_dil(n, kk[a], ss[a], pp[a], oo[a], dd[a])
+                for a, n in enumerate((d.Din, d.Hin, d.Win))]
+        shp = (ctypes.c_int64 * 5)()
+        assert lib.convt3d_output_shape(h, shp) == 0
+        assert tuple(shp) == (d.N, d.Cout, *outs)
+        inf = _lib.Info()
+        assert lib.convt3d_plan_info(h, ctypes.byref(inf)) == 0
+        assert inf.num_classes == ss[0] * ss[1] * ss[2]
+        assert inf.gemm_k_total == d.Cin * kk[0] * kk[1] * kk[2]  # every tap once over the classes
+        assert inf.useful_flop == 2.0 * d.N * d.Cout * (d.Cin // G) * kk[0] * kk[1] * kk[2] * d.Din * d.Hin * d.Win
+    finally:
+        lib.convt3d_plan_destroy(h)
 
 
 @pytest.mark.parametrize("spec", workloads.ALL, ids=lambda s: s.name)

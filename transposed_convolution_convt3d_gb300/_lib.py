@@ -20,6 +20,8 @@ EPI_SCALE_BATCHNORM_EVAL_AVGPOOL = 4
 
 PREC_3XTF32 = 0
 PREC_FFMA = 1
+PREC_TF32 = 2
+PREC_BF16 = 3
 
 STATUS = {
     0: "CONVT3D_OK",
@@ -48,6 +50,9 @@ class Desc(ctypes.Structure):
         ("k", ctypes.c_int), ("stride", ctypes.c_int), ("pad", ctypes.c_int), ("out_pad", ctypes.c_int),
         ("has_bias", ctypes.c_int), ("epilogue", ctypes.c_int), ("groups", ctypes.c_int),
         ("eps", ctypes.c_float), ("scale", ctypes.c_float), ("precision", ctypes.c_int),
+        ("per_dim", ctypes.c_int), ("kdims", ctypes.c_int * 3), ("strides", ctypes.c_int * 3),
+        ("pads", ctypes.c_int * 3), ("out_pads", ctypes.c_int * 3), ("dilation", ctypes.c_int * 3),
+        ("conv_groups", ctypes.c_int),
     ]
 
 

@@ -14,7 +14,7 @@ import torch
 from . import _lib
 from ._lib import (EPI_IDENTITY, EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL,  # noqa: F401
                    EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, EPI_SOFTMAX_SIGMOID, PREC_3XTF32, PREC_FFMA,
-                   Convt3dError)
+                   PREC_TF32, PREC_BF16, Convt3dError)
 
 
 def _ptr(t):
@@ -26,14 +26,39 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _triple(v):
+    if isinstance(v, (tuple, list)):
+        if len(v) != 3:
+            raise ValueError("expected an int or 3 ints (d, h, w)")
+        return tuple(int(a) for a in v)
+    return (int(v),) * 3
+
+
+def make_desc(N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False, epilogue=EPI_IDENTITY,
+              groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1, conv_groups=1):
+    """A convt3d_desc_t.  k, stride, pad, out_pad and dilation are an int or
+    (d, h, w); conv_groups is the convolution's group count (weight
+    [Cin, Cout/conv_groups, kd, kh, kw]); groups is GroupNorm's."""
+    kk, ss, pp, oo, dd = (_triple(v) for v in (k, stride, pad, out_pad, dilation))
+    per_dim = any(len(set(t)) > 1 for t in (kk, ss, pp, oo))
+    d = _lib.Desc(N, Cin, Cout, D, H, W, kk[0], ss[0], pp[0], oo[0], int(bool(bias)), int(epilogue), int(groups),
+                  float(eps), float(scale), int(precision))
+    d.per_dim = int(per_dim)
+    for a in range(3):
+        d.kdims[a], d.strides[a], d.pads[a], d.out_pads[a], d.dilation[a] = kk[a], ss[a], pp[a], oo[a], dd[a]
+    d.conv_groups = int(conv_groups)
+    return d
+
+
 class Plan:
     """A validated problem description (host-only; creating one needs no GPU)."""
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
-                 epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32):
+                 epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1,
+                 conv_groups=1):
         self.lib = _lib.load()
-        self.desc = _lib.Desc(N, Cin, Cout, D, H, W, k, stride, pad, out_pad, int(bool(bias)),
-                              int(epilogue), int(groups), float(eps), float(scale), int(precision))
+        self.desc = make_desc(N, Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale,
+                              precision, dilation, conv_groups)
         h = ctypes.c_void_p()
         _lib.check(self.lib.convt3d_plan_create(ctypes.byref(self.desc), ctypes.byref(h)), self.lib)
         self.handle = h
@@ -49,7 +74,8 @@ class Plan:
     @classmethod
     def from_spec(cls, spec, precision=PREC_3XTF32):
         return cls(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
-                   spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, precision)
+                   spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, precision,
+                   spec.dilation, spec.conv_groups)
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -134,13 +160,14 @@ def _numel(shape):
     return n
 
 
-def convt3d(x, w, bias=None, *, stride=1, pad=0, out_pad=0, epilogue=EPI_IDENTITY, groups=1, eps=1e-5,
-            scale=1.0, gamma=None, beta=None, precision=PREC_3XTF32):
-    """One-shot convenience: plan, pack, forward on the current stream; returns y."""
+def convt3d(x, w, bias=None, *, stride=1, pad=0, out_pad=0, dilation=1, conv_groups=1, epilogue=EPI_IDENTITY,
+            groups=1, eps=1e-5, scale=1.0, gamma=None, beta=None, precision=PREC_3XTF32):
+    """One-shot convenience: plan, pack, forward on the current stream; returns y.
+    w is [Cin, Cout/conv_groups, kd, kh, kw]."""
     N, Cin, D, H, W = x.shape
-    Cout, k = w.shape[1], w.shape[2]
+    Cout, k = w.shape[1] * conv_groups, tuple(w.shape[2:])
     plan = Plan(N, Cin, Cout, D, H, W, k, stride, pad, out_pad, bias is not None, epilogue, groups, eps, scale,
-                precision)
+                precision, dilation, conv_groups)
     ws = plan.new_workspace(x.device)
     y = plan.new_output(x.device)
     plan.pack_weights(w, ws)
@@ -162,18 +189,19 @@ class HostPipeline:
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, chunks=4,
-                 device="cuda"):
+                 device="cuda", dilation=1, conv_groups=1):
         if epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) or N % chunks:
             chunks = 1
         self.chunks = chunks
         self.n_chunk = N // chunks
-        args = (Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale, precision)
+        args = (Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale, precision,
+                dilation, conv_groups)
         self.plan = Plan(self.n_chunk, *args)
         self.full_shape = (N,) + self.plan.out_shape[1:]
         dev = torch.device(device)
         self.x = torch.empty((N, Cin, D, H, W), dtype=torch.float32, device=dev)
         self.y = torch.empty(self.full_shape, dtype=torch.float32, device=dev)
-        self.w = torch.empty((Cin, Cout, k, k, k), dtype=torch.float32, device=dev)
+        self.w = torch.empty((Cin, Cout // conv_groups) + _triple(k), dtype=torch.float32, device=dev)
         self.vec = {name: torch.empty(Cout, dtype=torch.float32, device=dev) for name in ("bias", "gamma", "beta")}
         self.ws = self.plan.new_workspace(dev)
         self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(dev) for _ in range(3))

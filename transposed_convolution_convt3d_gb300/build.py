@@ -32,6 +32,8 @@ def nvcc() -> str:
 def _flags(verbose: bool):
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                 "--expt-relaxed-constexpr"]
+    # extra compile-time settings, e.g. CONVT3D_NVCC_FLAGS="-DCONVT3D_SOFTMAX_EPI_WARPS=16"
+    f += os.environ.get("CONVT3D_NVCC_FLAGS", "").split()
     if verbose:
         f += ["-Xptxas", "-v"]
     return f
@@ -41,8 +43,16 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
+STAMP = LIB + ".flags"
+
+
 def _stale(force: bool) -> bool:
     if force or not os.path.exists(LIB):
+        return True
+    try:
+        if open(STAMP).read() != " ".join(_flags(False)):
+            return True
+    except OSError:
         return True
     t = os.path.getmtime(LIB)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
@@ -79,6 +89,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("link failed: " + " ".join(link))
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(" ".join(_flags(False)))
     return LIB
 
 

@@ -8,13 +8,16 @@
 //   S[n,c] = sum_{ci, tap} w[ci, c, tap] * B[n, ci, tap],
 // where B is the sum of x[n, ci] over the input box whose scatter through that
 // tap lands inside the output (ConvTranspose3d scatters input i through tap t
-// to o = stride*i - pad + t per dimension).  The box is a product of one
+// to o = stride*i - pad + dilation*t per dimension).  Grouped convolution needs
+// nothing more: the packed weight is zero between channels of different groups.  The box is a product of one
 // interval per dimension, so B is three passes of 1-D interval sums:
 //   boxsum_kernel    one block per (n, ci): x once along d into k accumulators
 //                    per (h, w) column, then intervals along h, then along w;
-//   bn_eval_out_kernel  one block per (n, c): the Cin*k^3 contraction with the
-//                    packed weight, fp64 accumulation, then the formula above.
+//   bn_eval_out_kernel  one block per (c, 16 samples): the Cin*k^3 contraction
+//                    with the packed weight, then the formula above in fp64.
 // The work is O(N*Cin*D*H*W*k + N*Cout*Cin*k^3), a read of x and of the weight.
+#include <cuda_bf16.h>
+
 #include "convt3d_internal.h"
 
 namespace convt3d {
@@ -24,15 +27,15 @@ constexpr int kMaxK = 7;
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
-// Inputs i whose output s*i - p + t lies in [0, out - 1], clamped to [0, in - 1].
+// Inputs i whose output s*i - p + dil*t lies in [0, out - 1], clamped to [0, in - 1].
 struct Interval {
     int lo, hi;
 };
 
-__device__ __forceinline__ Interval tap_interval(int t, int s, int p, int in, int out) {
+__device__ __forceinline__ Interval tap_interval(int t, int s, int p, int dil, int in, int out) {
     Interval r;
-    r.lo = -floor_div(-(p - t), s);           // ceil((p - t) / s)
-    r.hi = floor_div(out - 1 + p - t, s);
+    r.lo = -floor_div(-(p - dil * t), s);           // ceil((p - dil*t) / s)
+    r.hi = floor_div(out - 1 + p - dil * t, s);
     r.lo = r.lo > 0 ? r.lo : 0;
     r.hi = r.hi < in - 1 ? r.hi : in - 1;
     return r;
@@ -40,53 +43,80 @@ __device__ __forceinline__ Interval tap_interval(int t, int s, int p, int in, in
 
 struct BoxParams {
     const float *x;
-    double *box;  // [N][k^3][Cin]
-    int Cin, D, H, W, k, s, p, Do, Ho, Wo;
+    float *box;  // [N][kd*kh*kw][Cin]
+    int Cin, D, H, W, Do, Ho, Wo;
+    int kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw;  // kernel, stride, pad, dilation per dimension
 };
 
+// One block per (n, ci).  fp32 sums: at most D*H*W terms of the input each,
+// far inside the tolerance the contraction's result is held to.
 __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
-    extern __shared__ double sm[];
-    const int k = P.k, H = P.H, W = P.W, HW = H * W;
-    double *a1 = sm;                 // [k][H][W]: sums along d
-    double *a2 = sm + (size_t)k * HW;  // [k][k][W]: then along h
+    extern __shared__ float sm[];
+    const int H = P.H, W = P.W, HW = H * W;
+    float *a1 = sm;                        // [kd][H][W]: sums along d
+    float *a2 = sm + (size_t)P.kd * HW;    // [kd][kh][W]: then along h
     const int n = blockIdx.x / P.Cin, ci = blockIdx.x % P.Cin;
     const float *xp = P.x + (size_t)blockIdx.x * P.D * HW;
 
     int dlo[kMaxK], dhi[kMaxK];
 #pragma unroll
     for (int t = 0; t < kMaxK; ++t) {
-        const Interval iv = t < k ? tap_interval(t, P.s, P.p, P.D, P.Do) : Interval{1, 0};
+        const Interval iv = t < P.kd ? tap_interval(t, P.sd, P.pd, P.dd, P.D, P.Do) : Interval{1, 0};
         dlo[t] = iv.lo;
         dhi[t] = iv.hi;
     }
-    for (int col = threadIdx.x; col < HW; col += blockDim.x) {
-        double acc[kMaxK];
+    if (HW % 4 == 0) {
+        // 128-bit loads: the slab of (n, ci) starts on a 16-byte boundary when H*W % 4 == 0
+        for (int c4 = threadIdx.x; c4 < HW / 4; c4 += blockDim.x) {
+            float4 acc[kMaxK];
 #pragma unroll
-        for (int t = 0; t < kMaxK; ++t) acc[t] = 0.0;
-        for (int d = 0; d < P.D; ++d) {
-            const double v = (double)__ldg(xp + (size_t)d * HW + col);
+            for (int t = 0; t < kMaxK; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int d = 0; d < P.D; ++d) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(xp + (size_t)d * HW) + c4);
+#pragma unroll
+                for (int t = 0; t < kMaxK; ++t)
+                    if (d >= dlo[t] && d <= dhi[t]) {
+                        acc[t].x += v.x;
+                        acc[t].y += v.y;
+                        acc[t].z += v.z;
+                        acc[t].w += v.w;
+                    }
+            }
 #pragma unroll
             for (int t = 0; t < kMaxK; ++t)
-                if (d >= dlo[t] && d <= dhi[t]) acc[t] += v;
+                if (t < P.kd) reinterpret_cast<float4 *>(a1 + (size_t)t * HW)[c4] = acc[t];
         }
+    } else {
+        for (int col = threadIdx.x; col < HW; col += blockDim.x) {
+            float acc[kMaxK];
 #pragma unroll
-        for (int t = 0; t < kMaxK; ++t)
-            if (t < k) a1[(size_t)t * HW + col] = acc[t];
+            for (int t = 0; t < kMaxK; ++t) acc[t] = 0.f;
+            for (int d = 0; d < P.D; ++d) {
+                const float v = __ldg(xp + (size_t)d * HW + col);
+#pragma unroll
+                for (int t = 0; t < kMaxK; ++t)
+                    if (d >= dlo[t] && d <= dhi[t]) acc[t] += v;
+            }
+#pragma unroll
+            for (int t = 0; t < kMaxK; ++t)
+                if (t < P.kd) a1[(size_t)t * HW + col] = acc[t];
+        }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < k * k * W; i += blockDim.x) {
-        const int w = i % W, th = (i / W) % k, td = i / (W * k);
-        const Interval iv = tap_interval(th, P.s, P.p, H, P.Ho);
-        double acc = 0.0;
+    for (int i = threadIdx.x; i < P.kd * P.kh * W; i += blockDim.x) {
+        const int w = i % W, th = (i / W) % P.kh, td = i / (W * P.kh);
+        const Interval iv = tap_interval(th, P.sh, P.ph, P.dh, H, P.Ho);
+        float acc = 0.f;
         for (int h = iv.lo; h <= iv.hi; ++h) acc += a1[(size_t)td * HW + h * W + w];
         a2[i] = acc;
     }
     __syncthreads();
-    const int k3 = k * k * k;
+    const int k3 = P.kd * P.kh * P.kw;
     for (int i = threadIdx.x; i < k3; i += blockDim.x) {
-        const int tw = i % k, tdh = i / k;  // i = (td*k + th)*k + tw
-        const Interval iv = tap_interval(tw, P.s, P.p, W, P.Wo);
-        double acc = 0.0;
+        const int tw = i % P.kw, tdh = i / P.kw;  // i = (td*kh + th)*kw + tw
+        const Interval iv = tap_interval(tw, P.sw, P.pw, P.dw, W, P.Wo);
+        float acc = 0.f;
         for (int w = iv.lo; w <= iv.hi; ++w) acc += a2[(size_t)tdh * W + w];
         P.box[((size_t)n * k3 + i) * P.Cin + ci] = acc;
     }
@@ -96,43 +126,66 @@ struct TapTable {
     int16_t widx[kMaxTaps];
 };
 
+constexpr int kOutSamples = 16;  // samples per contraction block
+
 struct OutParams {
-    const double *box;
+    const float *box;
     const float *w_a, *w_b;  // tensor-core layout: TF32 hi/lo planes [tap][cout_pad][cin_pad]; FFMA: [tap][cin_pad][cout_pad]
     const float *bias, *gamma, *beta, *rmean, *rvar;
     float *y;
-    int Cin, Cout, cin_pad, cout_pad, ntaps, k3, kmajor;
+    int N, Cin, Cout, cin_pad, cout_pad, ntaps, k3, kmajor, wbf16;
     double inv_vol, scale, eps;
 };
 
-__global__ void __launch_bounds__(256) bn_eval_out_kernel(const OutParams P,
+// One block of 512 threads per (c, group of 16 samples): each weight element
+// is read once per block and multiplied into the 16 samples' box sums;
+// per-thread fp32 partial sums, then a block reduction.
+constexpr int kOutThreads = 512;
+
+__global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParams P,
                                                           const __grid_constant__ TapTable taps) {
-    const int n = blockIdx.x / P.Cout, c = blockIdx.x % P.Cout;
-    const double *bx = P.box + (size_t)n * P.k3 * P.Cin;
+    const int c = blockIdx.x, n0 = blockIdx.y * kOutSamples;
+    const int nn = P.N - n0 < kOutSamples ? P.N - n0 : kOutSamples;
+    const size_t nstride = (size_t)P.k3 * P.Cin;
+    const float *bx = P.box + (size_t)n0 * nstride;
     const int total = P.ntaps * P.Cin;
-    double acc = 0.0;
+    float acc[kOutSamples];
+#pragma unroll
+    for (int q = 0; q < kOutSamples; ++q) acc[q] = 0.f;
     for (int i = threadIdx.x; i < total; i += blockDim.x) {
-        const int j = i / P.Cin, ci = i % P.Cin;
+        const int j = i / P.Cin, ci = i - j * P.Cin;
         float wv;
         if (P.kmajor) {
             const size_t o = ((size_t)j * P.cout_pad + c) * P.cin_pad + ci;
-            wv = P.w_a[o] + P.w_b[o];  // hi + lo: the fp32 weight, exactly
+            if (P.wbf16)
+                wv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_a)[o]);
+            else  // hi + lo: the fp32 weight, exactly (or its TF32 rounding)
+                wv = P.w_b ? P.w_a[o] + P.w_b[o] : P.w_a[o];
         } else {
             wv = P.w_a[((size_t)j * P.cin_pad + ci) * P.cout_pad + c];
         }
-        acc += (double)wv * bx[(size_t)taps.widx[j] * P.Cin + ci];
-    }
+        const float *b = bx + (size_t)taps.widx[j] * P.Cin + ci;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    __shared__ double red[8];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+        for (int q = 0; q < kOutSamples; ++q)
+            if (q < nn) acc[q] = fmaf(wv, b[q * nstride], acc[q]);
+    }
+    __shared__ float red[kOutSamples][kOutThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int q = 0; q < kOutSamples; ++q) {
+        float v = acc[q];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[q][warp] = v;
+    }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < nn) {
+        const int q = threadIdx.x;
         double S = 0.0;
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) S += red[i];
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) S += (double)red[q][i];
         const double mean_y = S * P.inv_vol + (P.bias ? (double)P.bias[c] : 0.0);
         const double rstd = 1.0 / sqrt((double)P.rvar[c] + P.eps);
-        P.y[(size_t)n * P.Cout + c] =
+        P.y[(size_t)(n0 + q) * P.Cout + c] =
             (float)((double)P.gamma[c] * (P.scale * mean_y - (double)P.rmean[c]) * rstd + (double)P.beta[c]);
     }
 }
@@ -140,15 +193,17 @@ __global__ void __launch_bounds__(256) bn_eval_out_kernel(const OutParams P,
 }  // namespace
 
 size_t bn_eval_smem_bytes(const convt3d_plan_s &p) {
-    const size_t k = p.g.k;
-    return (k * p.g.Hin * p.g.Win + k * k * p.g.Win) * sizeof(double);
+    const size_t kd = p.g.kk[0], kh = p.g.kk[1];
+    return (kd * p.g.Hin * p.g.Win + kd * kh * p.g.Win) * sizeof(float);
 }
 
 cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float *w_a, const float *w_b,
-                           const float *bias, const float *gamma, const float *beta, double *box, float *y,
+                           const float *bias, const float *gamma, const float *beta, float *box, float *y,
                            cudaStream_t s) {
     const Geometry &g = p.g;
-    BoxParams bp{x, box, g.Cin, g.Din, g.Hin, g.Win, g.k, g.stride, g.pad, g.Do, g.Ho, g.Wo};
+    BoxParams bp{x,        box,      g.Cin,    g.Din,    g.Hin,    g.Win,    g.Do,     g.Ho,     g.Wo,
+                 g.kk[0],  g.kk[1],  g.kk[2],  g.ss[0],  g.ss[1],  g.ss[2],  g.pp[0],  g.pp[1],  g.pp[2],
+                 g.dil[0], g.dil[1], g.dil[2]};
     const size_t smem = bn_eval_smem_bytes(p);
     cudaError_t e = cudaFuncSetAttribute(boxsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -168,17 +223,20 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
     op.rmean = p.run_mean;
     op.rvar = p.run_var;
     op.y = y;
+    op.N = g.N;
     op.Cin = g.Cin;
     op.Cout = g.Cout;
     op.cin_pad = p.cin_pad;
     op.cout_pad = p.cout_pad;
     op.ntaps = g.ntaps;
-    op.k3 = g.k * g.k * g.k;
+    op.k3 = g.kvol;
     op.kmajor = p.tc;
+    op.wbf16 = p.bf16;
     op.inv_vol = 1.0 / ((double)g.Do * g.Ho * g.Wo);
     op.scale = (double)p.d.scale;
     op.eps = (double)p.d.eps;
-    bn_eval_out_kernel<<<(unsigned)(g.N * g.Cout), 256, 0, s>>>(op, t);
+    dim3 grid((unsigned)g.Cout, (unsigned)((g.N + kOutSamples - 1) / kOutSamples));
+    bn_eval_out_kernel<<<grid, kOutThreads, 0, s>>>(op, t);
     return cudaGetLastError();
 }
 

@@ -14,7 +14,8 @@ constexpr int kMaxGroups = 8;
 constexpr int kMaxTaps = 343;    // k <= 7
 constexpr int kFfmaTileM = 64;   // output positions per FFMA tile
 constexpr int kTcTileM = 128;    // output positions per tensor-core tile (TMEM lanes)
-constexpr int kTcChunk = 32;     // input channels per K step of the tensor-core path (128 B)
+constexpr int kTcChunk = 32;     // fp32 input channels per K step of the tensor-core path (128 B)
+constexpr int kTcRowBytes = 128; // bytes of one operand row per K step (the 128-byte swizzle span)
 constexpr int kTcStatRows = 4;   // partial-statistics rows per tensor-core tile (one per TMEM lane quarter)
 
 // Status word layout at the start of the workspace.
@@ -36,6 +37,7 @@ struct ClassDesc {
     int ntaps, tap_begin;
     int lo_d, lo_h, lo_w;   // smallest delta per dimension
     int nt_d, nt_h, nt_w;   // taps per dimension
+    int step_d;             // delta decrease between consecutive d-slices (the d dilation)
 };
 
 // A unit of GEMM work: one class (FFMA, or stride 1), or the two classes
@@ -51,13 +53,15 @@ struct GroupDesc {
     int ksteps;             // K steps per tile (all classes of the group)
 };
 
-// Taps a tile issues.  Along d, a class's taps have consecutive decreasing
-// input offsets delta = hi, hi-1, ..., hi-nt_d+1 (taps are enumerated d-major in
-// increasing kernel index, and delta = (r + p - t)/stride), so the d-slices
-// whose input plane q + delta lies inside [0, Din) for some row of the tile form
-// one contiguous range [a0, a1].  The tile issues taps [a0 * nhw, (a1+1) * nhw)
-// of the class (nhw = taps per d-slice), or just tap 0 when no slice is live --
-// that zero-filled product still initialises the accumulator.
+// Taps a tile issues.  Along d, a class's taps have decreasing input offsets
+// delta = hi, hi - step, ..., hi - (nt_d-1)*step (taps are enumerated d-major in
+// increasing kernel index, delta = (r + p - dil*t)/stride, and consecutive taps
+// of a class are stride/gcd(stride, dil) apart, so step is the dilation for the
+// supported shapes), so the d-slices whose input plane q + delta lies inside
+// [0, Din) for some row of the tile form one contiguous range [a0, a1].  The
+// tile issues taps [a0 * nhw, (a1+1) * nhw) of the class (nhw = taps per
+// d-slice), or just tap 0 when no slice is live -- that zero-filled product
+// still initialises the accumulator.
 struct TapRange {
     int begin, end;
 };
@@ -67,8 +71,14 @@ __host__ __device__ inline TapRange tile_taps(const GroupDesc &G, const ClassDes
     const int q1 = (q0 + tile_m < G.vol ? q0 + tile_m : G.vol) - 1;
     const int qhw = G.Qh * G.Qw;
     const int d0 = q0 / qhw, d1 = q1 / qhw;
-    const int hi = C.lo_d + C.nt_d - 1;  // offset of d-slice 0
+    const int step = C.step_d;
+    const int hi = C.lo_d + (C.nt_d - 1) * step;  // offset of d-slice 0
+    // live slices a: hi + d0 - (Din - 1) <= a * step <= hi + d1
     int a0 = d0 + hi - (Din - 1), a1 = d1 + hi;
+    if (step != 1) {
+        a0 = a0 > 0 ? (a0 + step - 1) / step : 0;
+        a1 = a1 >= 0 ? a1 / step : -1;
+    }
     a0 = a0 > 0 ? a0 : 0;
     a1 = a1 < C.nt_d - 1 ? a1 : C.nt_d - 1;
     const int nhw = C.nt_h * C.nt_w;
@@ -84,7 +94,10 @@ __host__ __device__ inline TapRange tile_taps(const GroupDesc &G, const ClassDes
 }
 
 struct Geometry {
-    int N, Cin, Cout, Din, Hin, Win, k, stride, pad, out_pad;
+    int N, Cin, Cout, Din, Hin, Win;
+    int kk[3], ss[3], pp[3], op[3], dil[3];  // per dimension (d, h, w): kernel, stride, pad, out pad, dilation
+    int kvol;                                // kk[0] * kk[1] * kk[2]
+    int G;                                   // convolution groups
     int Do, Ho, Wo;
     int nclasses;
     int ntaps;
@@ -99,7 +112,7 @@ struct FfmaParams {
     const float *bias;
     float *y;
     double *partials;
-    int N, Cin, cin_pad, Cout, cout_pad, Din, Hin, Win, Do, Ho, Wo, stride;
+    int N, Cin, cin_pad, Cout, cout_pad, Din, Hin, Win, Do, Ho, Wo, sd, sh, sw;
     int epilogue, groups;
     float scale;
     int ngroups, tiles_per_sample;
@@ -114,6 +127,10 @@ struct convt3d_plan_s {
     convt3d_desc_t d;
     convt3d::Geometry g;
     int tc;                 // 1: tensor-core path, 0: FFMA
+    int planes;             // tensor-core operand planes: 2 = split TF32 (hi, lo), 1 = TF32 or BF16
+    int bf16;               // tensor-core operands in bf16 (kind::f16 MMA)
+    int chunk;              // input channels per K step (one 128-byte operand row)
+    int elem_bytes;         // bytes per staged / packed operand element
     int cin_pad, cout_pad;
     int tile_m;
     int ngroups;
@@ -155,7 +172,7 @@ cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, co
 cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, double *sums,
                                const float *gamma, const float *beta, float *y, cudaStream_t s);
 cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float *w_a, const float *w_b,
-                           const float *bias, const float *gamma, const float *beta, double *box, float *y,
+                           const float *bias, const float *gamma, const float *beta, float *box, float *y,
                            cudaStream_t s);
 size_t bn_eval_smem_bytes(const convt3d_plan_s &p);
 void tc_cache_free(void *cache);

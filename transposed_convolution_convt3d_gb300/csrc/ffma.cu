@@ -165,9 +165,9 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
         const int q = ti.t * kBM + tid;
         int off = -1;
         if (q < vol) {
-            const int od = P.stride * (q / Qhw) + cl.rd;
-            const int oh = P.stride * ((q / cl.Qw) % cl.Qh) + cl.rh;
-            const int ow = P.stride * (q % cl.Qw) + cl.rw;
+            const int od = P.sd * (q / Qhw) + cl.rd;
+            const int oh = P.sh * ((q / cl.Qw) % cl.Qh) + cl.rh;
+            const int ow = P.sw * (q % cl.Qw) + cl.rw;
             if (od < P.Do && oh < P.Ho && ow < P.Wo) off = (od * P.Ho + oh) * P.Wo + ow;
         }
         rowoff[tid] = off;
@@ -268,7 +268,9 @@ cudaError_t launch_ffma(const convt3d_plan_s &p, const float *x, const float *wp
     P.x = x; P.wpk = wpk; P.bias = bias; P.y = y; P.partials = partials;
     P.N = p.g.N; P.Cin = p.g.Cin; P.cin_pad = p.cin_pad; P.Cout = p.g.Cout; P.cout_pad = p.cout_pad;
     P.Din = p.g.Din; P.Hin = p.g.Hin; P.Win = p.g.Win; P.Do = p.g.Do; P.Ho = p.g.Ho; P.Wo = p.g.Wo;
-    P.stride = p.g.stride;
+    P.sd = p.g.ss[0];
+    P.sh = p.g.ss[1];
+    P.sw = p.g.ss[2];
     P.epilogue = p.d.epilogue;
     P.groups = p.d.groups;
     P.scale = p.d.scale;

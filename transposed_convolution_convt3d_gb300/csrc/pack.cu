@@ -1,14 +1,17 @@
 // Weight re-layout and input staging.
 //
-// The weight of a ConvTranspose3d is [Cin, Cout, k, k, k] (PyTorch layout,
-// as on all three transcript pages); page l2_p49 notes the Cin stride makes
+// The weight of a ConvTranspose3d is [Cin, Cout/G, kd, kh, kw] (PyTorch layout,
+// as on all three transcript pages, where G = 1); page l2_p49 notes the Cin stride makes
 // per-Cout access strided and re-lays it per output channel.  Here the
 // weight is re-laid per parity class and tap:
 //   tensor-core path: [tap][Cout_pad][Cin_pad] (K-major rows, Cin contiguous),
 //                     split into TF32 hi and lo planes;
 //   FFMA path:        [tap][Cin_pad][Cout_pad] fp32.
 // The tensor-core path also stages x from NCDHW into channels-last
-// [N][D][H][W][Cin_pad] hi/lo planes, the layout its TMA im2col loads read.
+// [N][D][H][W][Cin_pad] hi/lo planes (one TF32-rounded or bf16 plane for the
+// single-product precisions), the layout its TMA im2col loads read.
+#include <cuda_bf16.h>
+
 #include "convt3d_internal.h"
 
 namespace convt3d {
@@ -21,13 +24,24 @@ __device__ __forceinline__ void split_tf32(float v, float &hi, float &lo) {
     lo = v - hi;
 }
 
+// Round v to the nearest TF32 value (ties away from zero): the PTX
+// conversion cvt.rna.tf32.f32, whose result keeps 10 explicit mantissa bits.
+__device__ __forceinline__ float round_tf32(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
+
 struct TapIndex {
     int16_t widx[kMaxTaps];
 };
 
+// Grouped convolution (G > 1): w is [Cin, Cout/G, taps]; the packed copy is the
+// dense [Cout][Cin] matrix per tap with zeros where ci and co lie in different
+// groups, so the GEMM needs no knowledge of groups.
 __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restrict__ hi,
                                     float *__restrict__ lo, int Cin, int Cout, int k3, int ntaps,
-                                    int cin_pad, int cout_pad, int kmajor,
+                                    int cin_pad, int cout_pad, int kmajor, int mode, int cin_g, int cout_g,
                                     const __grid_constant__ TapIndex taps) {
     const int64_t total = (int64_t)ntaps * cin_pad * cout_pad;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -43,14 +57,17 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
             j = (int)(i / ((int64_t)cin_pad * cout_pad));
         }
         float v = 0.0f;
-        if (ci < Cin && co < Cout) v = w[((int64_t)ci * Cout + co) * k3 + taps.widx[j]];
+        if (ci < Cin && co < Cout && ci / cin_g == co / cout_g)
+            v = w[((int64_t)ci * cout_g + co % cout_g) * k3 + taps.widx[j]];
         if (lo) {
             float h, l;
             split_tf32(v, h, l);
             hi[i] = h;
             lo[i] = l;
+        } else if (mode == 2) {  // bf16 operands: the plane holds 2-byte elements
+            reinterpret_cast<__nv_bfloat16 *>(hi)[i] = __float2bfloat16_rn(v);
         } else {
-            hi[i] = v;
+            hi[i] = mode == 1 ? round_tf32(v) : v;  // TF32-rounded, or fp32 for the FFMA path
         }
     }
 }
@@ -59,7 +76,7 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
 // 32 channels per block through shared memory; both the global read (along
 // positions) and the write (along channels) are 128-byte rows.
 __global__ void stage_input_kernel(const float *__restrict__ x, float *__restrict__ hi,
-                                   float *__restrict__ lo, int Cin, int cin_pad, int64_t S) {
+                                   float *__restrict__ lo, int Cin, int cin_pad, int64_t S, int bf16) {
     __shared__ float tile[32][33];
     const int n = blockIdx.z;
     const int c0 = blockIdx.y * 32;
@@ -74,16 +91,23 @@ __global__ void stage_input_kernel(const float *__restrict__ x, float *__restric
     }
     __syncthreads();
     float *hn = hi + (int64_t)n * S * cin_pad;
-    float *ln = lo + (int64_t)n * S * cin_pad;
+    float *ln = lo ? lo + (int64_t)n * S * cin_pad : nullptr;
 #pragma unroll
     for (int j = 0; j < 32; j += 8) {
         const int64_t s = s0 + ty + j;
         const int c = c0 + tx;
         if (s < S) {
-            float h, l;
-            split_tf32(tile[tx][ty + j], h, l);
-            hn[s * cin_pad + c] = h;
-            ln[s * cin_pad + c] = l;
+            if (ln) {
+                float h, l;
+                split_tf32(tile[tx][ty + j], h, l);
+                hn[s * cin_pad + c] = h;
+                ln[s * cin_pad + c] = l;
+            } else if (bf16) {  // single bf16 plane (2-byte elements)
+                reinterpret_cast<__nv_bfloat16 *>(hi)[((int64_t)n * S + s) * cin_pad + c] =
+                    __float2bfloat16_rn(tile[tx][ty + j]);
+            } else {  // single TF32 plane
+                hn[s * cin_pad + c] = round_tf32(tile[tx][ty + j]);
+            }
         }
     }
 }
@@ -97,9 +121,9 @@ cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *
     const int64_t total = (int64_t)p.g.ntaps * p.cin_pad * p.cout_pad;
     const int threads = 256;
     const int blocks = (int)((total + threads - 1) / threads < 4096 ? (total + threads - 1) / threads : 4096);
-    const int k3 = p.g.k * p.g.k * p.g.k;
-    pack_weights_kernel<<<blocks, threads, 0, s>>>(w, hi, lo, p.g.Cin, p.g.Cout, k3, p.g.ntaps, p.cin_pad,
-                                                   p.cout_pad, kmajor, t);
+    pack_weights_kernel<<<blocks, threads, 0, s>>>(w, hi, lo, p.g.Cin, p.g.Cout, p.g.kvol, p.g.ntaps, p.cin_pad,
+                                                   p.cout_pad, kmajor, p.bf16 ? 2 : (p.planes == 1 ? 1 : 0),
+                                                   p.g.Cin / p.g.G, p.g.Cout / p.g.G, t);
     return cudaGetLastError();
 }
 
@@ -107,7 +131,7 @@ cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *h
     const int64_t S = (int64_t)p.g.Din * p.g.Hin * p.g.Win;
     dim3 grid((unsigned)((S + 31) / 32), (unsigned)(p.cin_pad / 32), (unsigned)p.g.N);
     dim3 block(32, 8);
-    stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S);
+    stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S, p.bf16);
     return cudaGetLastError();
 }
 

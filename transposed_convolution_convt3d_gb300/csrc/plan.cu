@@ -40,14 +40,36 @@ convt3d_status_t cuda_fail(cudaError_t e, const char *what) {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Output extent along one dimension (dilation 1): (in-1)*s - 2p + k + op.
-int64_t out_extent(int64_t in, int k, int s, int p, int op) { return (in - 1) * s - 2 * p + k + op; }
+// Output extent along one dimension: (in-1)*s - 2p + dil*(k-1) + op + 1.
+int64_t out_extent(int64_t in, int k, int s, int p, int op, int dil) {
+    return (in - 1) * s - 2 * p + (int64_t)dil * (k - 1) + op + 1;
+}
+
+// The per-dimension shape a descriptor describes (index 0 = d, 1 = h, 2 = w).
+struct Shape {
+    int kk[3], ss[3], pp[3], op[3], dil[3];
+    int G;
+};
+
+Shape shape_of(const convt3d_desc_t &d) {
+    Shape s;
+    for (int a = 0; a < 3; ++a) {
+        s.kk[a] = d.per_dim ? d.kdims[a] : d.k;
+        s.ss[a] = d.per_dim ? d.strides[a] : d.stride;
+        s.pp[a] = d.per_dim ? d.pads[a] : d.pad;
+        s.op[a] = d.per_dim ? d.out_pads[a] : d.out_pad;
+        s.dil[a] = d.dilation[a] == 0 ? 1 : d.dilation[a];
+    }
+    s.G = d.conv_groups == 0 ? 1 : d.conv_groups;
+    return s;
+}
 
 // Output-parity decomposition.  For output index o = s*q + r along one
-// dimension, the taps t that reach it satisfy (r + p - t) = s*delta for an
+// dimension, the taps t that reach it satisfy (r + p - dil*t) = s*delta for an
 // integer delta, and then read input index i = q + delta (the gather form
-// of the index relation od = id*s - p + kd derived on page l2_p49).  For
-// stride 1 there is one class holding all k taps with delta = p - t.
+// of the index relation od = id*s - p + kd derived on page l2_p49, with the
+// dilated tap position dil*kd).  For stride 1 there is one class holding all
+// k taps with delta = p - dil*t.
 struct DimTaps {
     int n;
     int t[8];
@@ -55,10 +77,10 @@ struct DimTaps {
     int Q;
 };
 
-DimTaps dim_taps(int Dout, int k, int s, int p, int r) {
+DimTaps dim_taps(int Dout, int k, int s, int p, int dil, int r) {
     DimTaps d{};
     for (int t = 0; t < k; ++t) {
-        int num = r + p - t;
+        int num = r + p - dil * t;
         if (((num % s) + s) % s == 0) {
             d.t[d.n] = t;
             d.delta[d.n] = num / s;  // exact division
@@ -71,27 +93,33 @@ DimTaps dim_taps(int Dout, int k, int s, int p, int r) {
 
 bool build_geometry(const convt3d_desc_t &d, Geometry &g) {
     memset(&g, 0, sizeof(g));
+    const Shape sh = shape_of(d);
     g.N = d.N; g.Cin = d.Cin; g.Cout = d.Cout; g.Din = d.Din; g.Hin = d.Hin; g.Win = d.Win;
-    g.k = d.k; g.stride = d.stride; g.pad = d.pad; g.out_pad = d.out_pad;
-    g.Do = (int)out_extent(d.Din, d.k, d.stride, d.pad, d.out_pad);
-    g.Ho = (int)out_extent(d.Hin, d.k, d.stride, d.pad, d.out_pad);
-    g.Wo = (int)out_extent(d.Win, d.k, d.stride, d.pad, d.out_pad);
-    const int s = d.stride;
-    g.nclasses = s * s * s;
+    for (int a = 0; a < 3; ++a) {
+        g.kk[a] = sh.kk[a]; g.ss[a] = sh.ss[a]; g.pp[a] = sh.pp[a]; g.op[a] = sh.op[a]; g.dil[a] = sh.dil[a];
+    }
+    g.kvol = g.kk[0] * g.kk[1] * g.kk[2];
+    g.G = sh.G;
+    const int in[3] = {d.Din, d.Hin, d.Win};
+    int out[3];
+    for (int a = 0; a < 3; ++a) out[a] = (int)out_extent(in[a], g.kk[a], g.ss[a], g.pp[a], g.op[a], g.dil[a]);
+    g.Do = out[0]; g.Ho = out[1]; g.Wo = out[2];
+    g.nclasses = g.ss[0] * g.ss[1] * g.ss[2];
     int tap = 0;
-    for (int rd = 0; rd < s; ++rd)
-        for (int rh = 0; rh < s; ++rh)
-            for (int rw = 0; rw < s; ++rw) {
-                const int c = (rd * s + rh) * s + rw;
-                DimTaps td = dim_taps(g.Do, d.k, s, d.pad, rd);
-                DimTaps th = dim_taps(g.Ho, d.k, s, d.pad, rh);
-                DimTaps tw = dim_taps(g.Wo, d.k, s, d.pad, rw);
+    for (int rd = 0; rd < g.ss[0]; ++rd)
+        for (int rh = 0; rh < g.ss[1]; ++rh)
+            for (int rw = 0; rw < g.ss[2]; ++rw) {
+                const int c = (rd * g.ss[1] + rh) * g.ss[2] + rw;
+                DimTaps td = dim_taps(g.Do, g.kk[0], g.ss[0], g.pp[0], g.dil[0], rd);
+                DimTaps th = dim_taps(g.Ho, g.kk[1], g.ss[1], g.pp[1], g.dil[1], rh);
+                DimTaps tw = dim_taps(g.Wo, g.kk[2], g.ss[2], g.pp[2], g.dil[2], rw);
                 ClassDesc &cl = g.cls[c];
                 cl.rd = rd; cl.rh = rh; cl.rw = rw;
                 cl.Qd = td.Q; cl.Qh = th.Q; cl.Qw = tw.Q;
                 cl.nt_d = td.n; cl.nt_h = th.n; cl.nt_w = tw.n;
                 cl.ntaps = td.n * th.n * tw.n;
                 cl.tap_begin = tap;
+                cl.step_d = g.dil[0];
                 cl.lo_d = cl.lo_h = cl.lo_w = 0;
                 if (td.n) cl.lo_d = *std::min_element(td.delta, td.delta + td.n);
                 if (th.n) cl.lo_h = *std::min_element(th.delta, th.delta + th.n);
@@ -104,27 +132,26 @@ bool build_geometry(const convt3d_desc_t &d, Geometry &g) {
                             t.dd = (int8_t)td.delta[a];
                             t.dh = (int8_t)th.delta[b];
                             t.dw = (int8_t)tw.delta[e];
-                            t.widx = (int16_t)((td.t[a] * d.k + th.t[b]) * d.k + tw.t[e]);
+                            t.widx = (int16_t)((td.t[a] * g.kk[1] + th.t[b]) * g.kk[2] + tw.t[e]);
                         }
             }
     g.ntaps = tap;
-    return tap == d.k * d.k * d.k;
+    return tap == g.kvol;
 }
 
 // Arrange classes into GEMM groups and order groups heaviest first.
 void build_groups(convt3d_plan_s &p) {
     const Geometry &g = p.g;
-    const int s = g.stride;
-    const int kchunk = p.tc ? kTcChunk : 8;
+    const int kchunk = p.chunk;
     const int kc = (g.Cin + kchunk - 1) / kchunk;
     p.ngroups = 0;
-    if (p.tc && s == 2) {
-        for (int rd = 0; rd < 2; ++rd)
-            for (int rh = 0; rh < 2; ++rh) {
+    if (p.tc && g.ss[2] == 2) {  // the two w-parity classes of each (rd, rh) share a tile
+        for (int rd = 0; rd < g.ss[0]; ++rd)
+            for (int rh = 0; rh < g.ss[1]; ++rh) {
                 GroupDesc &G = p.grp[p.ngroups++];
                 G.ncls = 2;
-                G.cls[0] = (rd * 2 + rh) * 2 + 0;
-                G.cls[1] = (rd * 2 + rh) * 2 + 1;
+                G.cls[0] = (rd * g.ss[1] + rh) * 2 + 0;
+                G.cls[1] = (rd * g.ss[1] + rh) * 2 + 1;
                 const ClassDesc &a = g.cls[G.cls[0]], &b = g.cls[G.cls[1]];
                 G.Qd = a.Qd; G.Qh = a.Qh; G.Qw = std::max(a.Qw, b.Qw);
                 G.ksteps = (a.ntaps + b.ntaps) * kc;
@@ -156,13 +183,24 @@ void build_groups(convt3d_plan_s &p) {
 convt3d_status_t validate(const convt3d_desc_t &d) {
     if (d.N < 1 || d.Cin < 1 || d.Cout < 1 || d.Din < 1 || d.Hin < 1 || d.Win < 1)
         return fail(CONVT3D_ERR_INVALID_ARG, "sizes must be >= 1");
-    if (d.k < 1 || d.stride < 1 || d.pad < 0 || d.out_pad < 0)
-        return fail(CONVT3D_ERR_INVALID_ARG, "k, stride >= 1 and pad, out_pad >= 0 required");
-    if (d.out_pad >= d.stride)
-        return fail(CONVT3D_ERR_INVALID_ARG, "out_pad must be smaller than stride");
+    for (int a = 0; a < 3; ++a)
+        if (d.dilation[a] < 0) return fail(CONVT3D_ERR_INVALID_ARG, "dilation must be >= 1 (0 means 1)");
+    if (d.conv_groups < 0) return fail(CONVT3D_ERR_INVALID_ARG, "conv_groups must be >= 1 (0 means 1)");
+    const Shape sh = shape_of(d);
+    const int in[3] = {d.Din, d.Hin, d.Win};
+    int64_t out[3];
+    for (int a = 0; a < 3; ++a) {
+        if (sh.kk[a] < 1 || sh.ss[a] < 1 || sh.pp[a] < 0 || sh.op[a] < 0)
+            return fail(CONVT3D_ERR_INVALID_ARG, "k, stride >= 1 and pad, out_pad >= 0 required");
+        if (sh.op[a] >= std::max(sh.ss[a], sh.dil[a]))
+            return fail(CONVT3D_ERR_INVALID_ARG, "out_pad must be smaller than stride or dilation");
+        out[a] = out_extent(in[a], sh.kk[a], sh.ss[a], sh.pp[a], sh.op[a], sh.dil[a]);
+        if (out[a] < 1) return fail(CONVT3D_ERR_INVALID_ARG, "output extent < 1");
+    }
+    if (d.Cin % sh.G || d.Cout % sh.G) return fail(CONVT3D_ERR_INVALID_ARG, "conv_groups must divide Cin and Cout");
     if (d.epilogue < CONVT3D_EPI_IDENTITY || d.epilogue > CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
         return fail(CONVT3D_ERR_INVALID_ARG, "unknown epilogue %d", d.epilogue);
-    if (d.precision != CONVT3D_PREC_3XTF32 && d.precision != CONVT3D_PREC_FFMA)
+    if (d.precision < CONVT3D_PREC_3XTF32 || d.precision > CONVT3D_PREC_BF16)
         return fail(CONVT3D_ERR_INVALID_ARG, "unknown precision %d", d.precision);
     if (d.epilogue == CONVT3D_EPI_RELU_GROUPNORM && (d.groups < 1 || d.Cout % d.groups != 0))
         return fail(CONVT3D_ERR_INVALID_ARG, "groups must divide Cout");
@@ -171,26 +209,24 @@ convt3d_status_t validate(const convt3d_desc_t &d) {
     if ((d.epilogue == CONVT3D_EPI_RELU_GROUPNORM || bn_any) && !(d.eps > 0.0f && isfinite(d.eps)))
         return fail(CONVT3D_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (bn_any && !isfinite(d.scale)) return fail(CONVT3D_ERR_INVALID_ARG, "scale must be finite");
-    for (int64_t in : {(int64_t)d.Din, (int64_t)d.Hin, (int64_t)d.Win})
-        if (out_extent(in, d.k, d.stride, d.pad, d.out_pad) < 1)
-            return fail(CONVT3D_ERR_INVALID_ARG, "output extent < 1");
     // Limits of this build (valid operations it does not run).
-    if (d.stride > 2) return fail(CONVT3D_ERR_UNSUPPORTED, "stride > 2");
-    if (d.k > 7) return fail(CONVT3D_ERR_UNSUPPORTED, "k > 7");
-    if (d.pad >= d.k) return fail(CONVT3D_ERR_UNSUPPORTED, "pad >= k");
-    if (d.k < d.stride) return fail(CONVT3D_ERR_UNSUPPORTED, "k < stride (parity classes without taps)");
+    for (int a = 0; a < 3; ++a) {
+        if (sh.ss[a] > 2) return fail(CONVT3D_ERR_UNSUPPORTED, "stride > 2");
+        if (sh.kk[a] > 7) return fail(CONVT3D_ERR_UNSUPPORTED, "k > 7");
+        if (sh.dil[a] * (sh.kk[a] - 1) > 30) return fail(CONVT3D_ERR_UNSUPPORTED, "dilation * (k - 1) > 30");
+        if (sh.pp[a] > sh.dil[a] * (sh.kk[a] - 1)) return fail(CONVT3D_ERR_UNSUPPORTED, "pad > dilation * (k - 1)");
+        if (sh.ss[a] == 2 && (sh.kk[a] < 2 || sh.dil[a] % 2 == 0))
+            return fail(CONVT3D_ERR_UNSUPPORTED, "stride 2 needs k >= 2 and an odd dilation (parity classes without taps)");
+    }
     if (d.Cout > 256) return fail(CONVT3D_ERR_UNSUPPORTED, "Cout > 256");
-    const int64_t Do = out_extent(d.Din, d.k, d.stride, d.pad, d.out_pad);
-    const int64_t Ho = out_extent(d.Hin, d.k, d.stride, d.pad, d.out_pad);
-    const int64_t Wo = out_extent(d.Win, d.k, d.stride, d.pad, d.out_pad);
     const int64_t lim = (int64_t)1 << 31;
-    if ((int64_t)d.N * d.Cout * Do * Ho * Wo >= lim || (int64_t)d.N * d.Cin * d.Din * d.Hin * d.Win >= lim / 2 ||
+    if ((int64_t)d.N * d.Cout * out[0] * out[1] * out[2] >= lim || (int64_t)d.N * d.Cin * d.Din * d.Hin * d.Win >= lim / 2 ||
         (int64_t)d.N * 256 * d.Din * d.Hin * d.Win >= ((int64_t)1 << 40))
         return fail(CONVT3D_ERR_UNSUPPORTED, "tensor larger than 2^31 elements");
-    if (d.precision == CONVT3D_PREC_3XTF32) {
+    if (d.precision != CONVT3D_PREC_FFMA) {
         const int cout_pad = round_up(d.Cout, 16);
-        if (d.stride == 2 && cout_pad > 128)
-            return fail(CONVT3D_ERR_UNSUPPORTED, "3xTF32 with stride 2 needs Cout <= 128");
+        if (sh.ss[2] == 2 && cout_pad > 128)
+            return fail(CONVT3D_ERR_UNSUPPORTED, "3xTF32 with stride 2 along w needs Cout <= 128");
     }
     return CONVT3D_OK;
 }
@@ -208,9 +244,11 @@ bool im2col_corners_ok(const convt3d_plan_s &p) {
             const int lo[3] = {cl.lo_d, cl.lo_h, cl.lo_w};
             const int Q[3] = {G.Qd, G.Qh, G.Qw};
             const int in[3] = {g.Din, g.Hin, g.Win};
+            const int span[3] = {(cl.nt_d - 1) * g.dil[0], (cl.nt_h - 1) * g.dil[1], (cl.nt_w - 1) * g.dil[2]};
             for (int a = 0; a < 3; ++a) {
                 const int upper = Q[a] - in[a] + lo[a];
                 if (lo[a] < -16 || lo[a] > 15 || upper < -16 || upper > 15) return false;
+                if (span[a] > 15) return false;  // per-load im2col offsets (delta - lo) kept within 0..15
             }
         }
     }
@@ -264,9 +302,13 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
         delete p;
         return fail(CONVT3D_ERR_UNSUPPORTED, "tap table overflow");
     }
-    p->tc = desc->precision == CONVT3D_PREC_3XTF32;
+    p->tc = desc->precision != CONVT3D_PREC_FFMA;
+    p->planes = desc->precision == CONVT3D_PREC_3XTF32 ? 2 : (p->tc ? 1 : 0);
+    p->bf16 = desc->precision == CONVT3D_PREC_BF16;
+    p->elem_bytes = p->bf16 ? 2 : 4;
+    p->chunk = p->tc ? kTcRowBytes / p->elem_bytes : 8;
     p->tile_m = p->tc ? kTcTileM : kFfmaTileM;
-    p->cin_pad = round_up(desc->Cin, p->tc ? kTcChunk : 8);
+    p->cin_pad = round_up(desc->Cin, p->chunk);
     p->cout_pad = round_up(desc->Cout, 16);
     if (!p->tc)  // the FFMA kernel's register tiles need a power-of-two channel count
         while (p->cout_pad & (p->cout_pad - 1)) p->cout_pad += 16;
@@ -278,7 +320,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     }
     if (eval_bn && bn_eval_smem_bytes(*p) > 200 * 1024) {
         delete p;
-        return fail(CONVT3D_ERR_UNSUPPORTED, "evaluation-mode BatchNorm needs k*H*W + k*k*W <= 25600");
+        return fail(CONVT3D_ERR_UNSUPPORTED, "evaluation-mode BatchNorm needs kd*H*W + kd*kh*W <= 51200");
     }
     p->momentum = 0.1f;
 
@@ -286,14 +328,14 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     size_t off = kStatusBytes;
     p->wpk_elems = (size_t)p->g.ntaps * p->cin_pad * p->cout_pad;
     p->off_wpk_hi = off;
-    off = align_up(off + p->wpk_elems * 4, 256);
+    off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
     p->off_wpk_lo = off;
-    if (p->tc) off = align_up(off + p->wpk_elems * 4, 256);
+    if (p->planes == 2) off = align_up(off + p->wpk_elems * 4, 256);
     p->xs_elems = (p->tc && !eval_bn) ? (size_t)desc->N * desc->Din * desc->Hin * desc->Win * p->cin_pad : 0;
     p->off_xs_hi = off;
-    off = align_up(off + p->xs_elems * 4, 256);
+    off = align_up(off + p->xs_elems * p->elem_bytes, 256);
     p->off_xs_lo = off;
-    off = align_up(off + p->xs_elems * 4, 256);
+    if (p->planes == 2) off = align_up(off + p->xs_elems * 4, 256);
     size_t per_tile = 0, stat = 0;
     if (desc->epilogue == CONVT3D_EPI_RELU_GROUPNORM) {
         per_tile = 2 * (size_t)desc->groups;
@@ -310,7 +352,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     p->off_stats = off;
     off = align_up(off + p->stat_doubles * 8, 256);
     p->off_box = off;
-    if (eval_bn) off = align_up(off + (size_t)desc->N * desc->Cin * desc->k * desc->k * desc->k * 8, 256);
+    if (eval_bn) off = align_up(off + (size_t)desc->N * desc->Cin * p->g.kvol * 4, 256);
     p->ws_total = off;
     *out = p;
     return CONVT3D_OK;
@@ -359,7 +401,7 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
     const bool ev = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
     info->launches_per_forward = ev ? 2 : (p->tc ? 2 : 1) + (gn ? 2 : 0) + (bn ? 2 : 0);
     info->launches_per_pack = 1;
-    info->useful_flop = 2.0 * d.N * d.Cout * (double)d.Cin * d.k * d.k * d.k * d.Din * d.Hin * d.Win;
+    info->useful_flop = 2.0 * d.N * d.Cout * (double)(d.Cin / g.G) * g.kvol * d.Din * d.Hin * d.Win;
     // Issued: every tile runs its class(es)' taps over tile_m rows and cout_pad columns -- the
     // tensor-core path only the taps live for the tile, with three products per term.
     double issued = 0;
@@ -379,19 +421,20 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
         }
         issued += 2.0 * (double)d.N * p->tile_m * p->cout_pad * (double)p->cin_pad * taps;
     }
-    info->issued_mma_flop = issued * (p->tc ? 3.0 : 1.0);
+    info->issued_mma_flop = issued * (p->planes == 2 ? 3.0 : 1.0);
     const double xbytes = 4.0 * d.N * d.Cin * (double)d.Din * d.Hin * d.Win;
-    const double wbytes = 4.0 * d.Cin * d.Cout * (double)d.k * d.k * d.k;
+    const double wbytes = 4.0 * d.Cin * (d.Cout / g.G) * (double)g.kvol;
     const double ybytes = 4.0 * d.N * d.Cout * (double)g.Do * g.Ho * g.Wo;
     const double out_bytes = (bn || ev) ? 4.0 * d.N * d.Cout : ybytes;
     // Main kernel: reads x (tensor-core path: the staged hi+lo copy) and the packed weights once,
     // writes the output once (BN+pool: nothing but partials).
-    info->gemm_min_bytes = (p->tc ? 2.0 * xbytes : xbytes) + (p->tc ? 2.0 : 1.0) * wbytes + (bn ? 0.0 : ybytes);
+    const double planes = p->planes == 2 ? 2.0 : (p->bf16 ? 0.5 : 1.0);  // staged operand bytes / fp32 bytes
+    info->gemm_min_bytes = planes * xbytes + planes * wbytes + (bn ? 0.0 : ybytes);
     // Whole forward as the pages define it: x and w in, the output out, plus the second pass
     // over y that GroupNorm's global statistics force.
     info->forward_min_bytes = xbytes + wbytes + out_bytes + (gn ? 2.0 * ybytes : 0.0);
     if (ev) {  // no convolution runs: box sums over x, then a contraction with w
-        info->issued_mma_flop = 2.0 * d.N * d.Cout * (double)d.Cin * d.k * d.k * d.k;
+        info->issued_mma_flop = 2.0 * d.N * d.Cout * (double)d.Cin * g.kvol;
         info->gemm_min_bytes = xbytes;
     }
     return CONVT3D_OK;
@@ -416,8 +459,8 @@ convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const float *w, void *ws
     char *base = (char *)ws;
     cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing status word");
-    e = launch_pack_weights(*p, w, (float *)(base + p->off_wpk_hi), p->tc ? (float *)(base + p->off_wpk_lo) : nullptr,
-                            p->tc, s);
+    e = launch_pack_weights(*p, w, (float *)(base + p->off_wpk_hi),
+                            p->planes == 2 ? (float *)(base + p->off_wpk_lo) : nullptr, p->tc, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack_weights launch");
     p->packed_ws = ws;
     return CONVT3D_OK;
@@ -452,8 +495,8 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const float *x, const float *
     if (ev) {
         // no convolution: input box sums and a contraction with the packed weight
         e = launch_bn_eval(*p, x, (const float *)(base + p->off_wpk_hi),
-                           p->tc ? (const float *)(base + p->off_wpk_lo) : nullptr, b, gamma, beta,
-                           (double *)(base + p->off_box), y, s);
+                           p->planes == 2 ? (const float *)(base + p->off_wpk_lo) : nullptr, b, gamma, beta,
+                           (float *)(base + p->off_box), y, s);
         if (e != cudaSuccess) return cuda_fail(e, "evaluation-mode batchnorm launch");
         return CONVT3D_OK;
     }
@@ -465,12 +508,13 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const float *x, const float *
         }
     }
     if (p->tc) {
-        float *xs_hi = (float *)(base + p->off_xs_hi), *xs_lo = (float *)(base + p->off_xs_lo);
+        const bool two = p->planes == 2;
+        float *xs_hi = (float *)(base + p->off_xs_hi), *xs_lo = two ? (float *)(base + p->off_xs_lo) : nullptr;
         e = launch_stage_input(*p, x, xs_hi, xs_lo, s);
         if (e != cudaSuccess) return cuda_fail(e, "stage_input launch");
         if (p->prof_enabled && (e = cudaEventRecord(p->ev0, s)) != cudaSuccess) return cuda_fail(e, "event");
-        e = launch_tc(*p, xs_hi, xs_lo, (const float *)(base + p->off_wpk_hi), (const float *)(base + p->off_wpk_lo),
-                      b, y, partials, (uint32_t *)base, s);
+        e = launch_tc(*p, xs_hi, xs_lo, (const float *)(base + p->off_wpk_hi),
+                      two ? (const float *)(base + p->off_wpk_lo) : nullptr, b, y, partials, (uint32_t *)base, s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
     } else {
         if (p->prof_enabled && (e = cudaEventRecord(p->ev0, s)) != cudaSuccess) return cuda_fail(e, "event");

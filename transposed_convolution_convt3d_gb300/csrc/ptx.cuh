@@ -84,6 +84,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// 5-D tiled load (c, w, h, d, n): coordinates may be negative or past the
+// extent (those elements arrive as zeros); c must be 16-byte aligned.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, uint32_t bar, int c, int w, int h,
+                                            int d, int n) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(d), "r"(n)
+        : "memory");
+}
+
 // 5-D im2col load: starting pixel (w, h, d, n), channel offset c, filter
 // offsets (ow, oh, od); the tensor map fixes the pixel count and channels.
 __device__ __forceinline__ void tma_load_im2col_5d(uint32_t dst, const void *tmap, uint32_t bar, int c, int w,
@@ -130,6 +141,17 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (here both operands bf16), one CTA.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -172,6 +194,12 @@ __device__ __forceinline__ uint64_t sdesc_k_swizzled(uint32_t saddr, uint32_t ro
 // K-major, M = 128, N = n.
 __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t n) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, BF16 A and B (format
+// code 1 in both operand fields), both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 }  // namespace ptx

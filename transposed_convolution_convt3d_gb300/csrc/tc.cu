@@ -1,6 +1,8 @@
 // Tensor-core implicit GEMM for the transposed convolution: tcgen05 MMA in
 // split TF32 ("3xTF32": a_hi*b_hi + a_hi*b_lo + a_lo*b_hi, fp32 accumulation
-// in tensor memory), TMA-fed, with the epilogues fused.
+// in tensor memory), single TF32 (one product of TF32-rounded operands) or
+// BF16 (kind::f16, one product of bf16 operands, 64 channels per 128-byte
+// row), TMA-fed, with the epilogues fused.
 //
 // GEMM view (output-stationary): M = output positions of one parity class,
 // N = Cout, K = Cin x taps of that class.  A 128-row tile is 128 consecutive
@@ -11,9 +13,9 @@
 // tiled TMA load brings the Cout x 32 weight slice.  Both land K-major with the
 // 128-byte (or, for 16-channel steps, 64-byte) swizzle that the tcgen05
 // shared-memory descriptors describe.
-// For stride 2 the two classes that differ only in w-parity share a CTA tile
-// (two accumulators), so the epilogue writes each output row as contiguous
-// pairs.
+// With stride 2 along w the two classes that differ only in w-parity share a CTA tile
+// (two accumulators), so the identity and ReLU epilogues write each output
+// row as contiguous pairs.
 //
 // CTA roles (persistent, one CTA per SM):
 //   warp 0      TMA producer (one thread): fills a ring of shared-memory stages
@@ -41,6 +43,11 @@
 #define CONVT3D_OFFSETS_DHW 0
 #endif
 
+// Epilogue warps of the softmax kernel: 4, 8 or 16 (1, 2 or 4 per lane quarter).
+#ifndef CONVT3D_SOFTMAX_EPI_WARPS
+#define CONVT3D_SOFTMAX_EPI_WARPS 8
+#endif
+
 namespace convt3d {
 namespace {
 
@@ -49,10 +56,22 @@ namespace {
 // epilogues use one, which leaves the producer and MMA warps more issue slots.
 template <int EPI>
 struct EpiCfg {
-    static constexpr int warps = EPI == CONVT3D_EPI_SOFTMAX_SIGMOID ? 8 : 4;
+    static constexpr int warps = EPI == CONVT3D_EPI_SOFTMAX_SIGMOID ? CONVT3D_SOFTMAX_EPI_WARPS : 4;
     static constexpr int threads = 64 + 32 * warps;  // producer warp, MMA warp, epilogue warps
 };
-constexpr int kMaxThreads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
+
+// Softmax: 16-channel chunks per epilogue warp whose exponentials stay in
+// registers between the sum and the output pass (the register budget per
+// thread halves when the warp count doubles).
+constexpr int kSoftmaxKeepChunks = CONVT3D_SOFTMAX_EPI_WARPS >= 16 ? 1 : 2;
+
+// Shared-memory floats of the softmax (max, sum) exchange between the warps of a
+// lane quarter: 2 buffers x warps per quarter x (2 classes x 2 values) x 128 rows.
+template <int EPI>
+constexpr int sm_exchange_floats() {
+    return EPI == CONVT3D_EPI_SOFTMAX_SIGMOID && EpiCfg<EPI>::warps > 4 ? 2 * (EpiCfg<EPI>::warps / 4) * 4 * kTcTileM
+                                                                      : 1;
+}
 constexpr int kMaxStages = 8;  // the MMA issue dispatches stage indices 0..7
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 // Input channels per K step: 32 (128-byte rows, 128-byte swizzle) or 16
@@ -75,13 +94,16 @@ struct TcParams {
     float *y;
     double *partials;
     uint32_t *status;
-    int N, Cout, cout_pad, Do, Ho, Wo, stride, kc;
+    int N, Cout, cout_pad, Do, Ho, Wo, sd, sh, sw, kc;
     int Din, Hin, Win;
     int epilogue, groups;
     float scale;
     int ngroups, tiles_per_sample, total_tiles;
     int stages;
     uint32_t stage_bytes, b_bytes;
+    int planes;  // 2: split TF32 (A and B hi/lo), 1: single TF32 or BF16
+    int bf16;    // operands in bf16 (kind::f16 MMA)
+    int chunk;   // input channels per K step (one 128-byte row)
     uint32_t tmem_cols, acc_stride;
     GroupDesc grp[kMaxGroups];
     ClassDesc cls[kMaxClasses];
@@ -93,19 +115,20 @@ struct Tile {
 };
 
 // Tile index -> (group, sample, tile within the sample's q-grid).  Tiles are
-// ordered group by group (heaviest first), then sample, then tile.  `grp` is
+// ordered sample by sample, then group by group (heaviest first), then tile:
+// the parity groups of a stride-2 problem all read the same input planes, and
+// finishing one sample's groups together keeps those planes in L2 between
+// them (group-major order re-read the whole input once per group).  `grp` is
 // the shared-memory copy of the group table.
 __device__ __forceinline__ Tile decode(const TcParams &P, const GroupDesc *grp, int tile) {
     Tile r;
-    int rem = tile, gi = 0;
-    while (gi + 1 < P.ngroups && rem >= P.N * grp[gi].tiles) {
-        rem -= P.N * grp[gi].tiles;
-        ++gi;
-    }
+    r.n = tile / P.tiles_per_sample;
+    const int rem = tile - r.n * P.tiles_per_sample;
+    int gi = 0;
+    while (gi + 1 < P.ngroups && rem >= grp[gi + 1].tile_prefix) ++gi;
     r.gi = gi;
-    r.n = rem / grp[gi].tiles;
-    r.t = rem % grp[gi].tiles;
-    r.slot = r.n * P.tiles_per_sample + grp[gi].tile_prefix + r.t;
+    r.t = rem - grp[gi].tile_prefix;
+    r.slot = tile;
     return r;
 }
 
@@ -175,56 +198,54 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// sigmoid(t) = 1/2 + tanh(t/2)/2 for t in [0, 1], with tanh(u) from its
-// Maclaurin series u - u^3/3 + 2u^5/15 - 17u^7/315 + 62u^9/2835
-// - 1382u^11/155925 + 21844u^13/6081075 (coefficients 2^2n (2^2n - 1) B_2n / (2n)!).
-// For u <= 1/2 the series alternates with decreasing terms, so truncation
-// after u^13 errs by less than the next term, 929569/638512875 * 2^-15 < 5e-8.
-__device__ __forceinline__ float sigmoid_unit(float t) {
-    const float u = 0.5f * t, u2 = u * u;
-    float p = 21844.0f / 6081075.0f;
-    p = fmaf(p, u2, -1382.0f / 155925.0f);
-    p = fmaf(p, u2, 62.0f / 2835.0f);
-    p = fmaf(p, u2, -17.0f / 315.0f);
-    p = fmaf(p, u2, 2.0f / 15.0f);
-    p = fmaf(p, u2, -1.0f / 3.0f);
-    p = fmaf(p, u2, 1.0f);
-    return fmaf(0.5f * u, p, 0.5f);
-}
-
-// Packed two-lane fp32 arithmetic (fma/mul.rn.f32x2): one instruction on a
-// (class 0, class 1) pair of values.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+// Packed two-lane fp32 arithmetic (add/mul/fma.rn.f32x2): one instruction on a
+// pair of values held as one 64-bit register pair.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
     return d;
 }
 
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+__device__ __forceinline__ void unpack2(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
 
-// sigmoid_unit on a pair (same series, packed arithmetic).
-__device__ __forceinline__ float2 sigmoid_unit2(float2 t) {
-    const float2 u = mul2(make_float2(0.5f, 0.5f), t), u2 = mul2(u, u);
-    float2 p = make_float2(21844.0f / 6081075.0f, 21844.0f / 6081075.0f);
-    p = fma2(p, u2, make_float2(-1382.0f / 155925.0f, -1382.0f / 155925.0f));
-    p = fma2(p, u2, make_float2(62.0f / 2835.0f, 62.0f / 2835.0f));
-    p = fma2(p, u2, make_float2(-17.0f / 315.0f, -17.0f / 315.0f));
-    p = fma2(p, u2, make_float2(2.0f / 15.0f, 2.0f / 15.0f));
-    p = fma2(p, u2, make_float2(-1.0f / 3.0f, -1.0f / 3.0f));
-    p = fma2(p, u2, make_float2(1.0f, 1.0f));
-    return fma2(mul2(make_float2(0.5f, 0.5f), u), p, make_float2(0.5f, 0.5f));
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// sigmoid(t) for t in [0, 1] as 1/2 + t * (s0 + s1 t^2 + s2 t^4 + s3 t^6): the
+// odd part of sigmoid about 0 fitted by a linear program minimising the largest
+// error over 20,001 points of [0, 1] (max error 5.6e-8; 1.2e-7 with the fp32
+// Horner evaluation below).
+constexpr float kSig0 = 0.24999944865703583f;
+constexpr float kSig1 = -0.020825687795877457f;
+constexpr float kSig2 = 0.0020543981809169054f;
+constexpr float kSig3 = -0.0001696429681032896f;
+
+// Coefficients that evaluate sigmoid(f * e) from e directly:
+// 1/2 + e * (s0 f + s1 f^3 e^2 + s2 f^5 e^4 + s3 f^7 e^6), packed as pairs.
+__device__ __forceinline__ void sigmoid_coefficients(float f, uint64_t (&A)[4]) {
+    const float f2 = f * f;
+    const float a0 = kSig0 * f, a1 = kSig1 * f * f2, a2 = kSig2 * f * f2 * f2, a3 = kSig3 * f * f2 * f2 * f2;
+    A[0] = pack2(a0, a0);
+    A[1] = pack2(a1, a1);
+    A[2] = pack2(a2, a2);
+    A[3] = pack2(a3, a3);
 }
 
 // Pairwise reductions of 16 values (4 dependent levels instead of 15).
@@ -252,17 +273,23 @@ __device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G,
     const int q = t * kTcTileM + m;
     if (q >= G.vol) return -1;
     const int qhw = G.Qh * G.Qw;
-    const int od = P.stride * (q / qhw) + C.rd;
-    const int oh = P.stride * ((q / G.Qw) % G.Qh) + C.rh;
-    const int ow = P.stride * (q % G.Qw) + C.rw;
+    const int od = P.sd * (q / qhw) + C.rd;
+    const int oh = P.sh * ((q / G.Qw) % G.Qh) + C.rh;
+    const int ow = P.sw * (q % G.Qw) + C.rw;
     if (od >= P.Do || oh >= P.Ho || ow >= P.Wo) return -1;
     return (od * P.Ho + oh) * P.Wo + ow;
 }
 
 // KEEP (softmax only): each epilogue warp keeps its exponentials in registers
 // (Cout <= 32 * warps per lane quarter); otherwise it re-reads tensor memory.
-template <int EPI, bool KEEP>
+// OPS: operand format, fixed at compile time so that the producer and MMA
+// loops stay branch-free: 0 = split TF32 (hi and lo planes), 1 = TF32, 2 = BF16.
+// BOX: every tile of every group is a whole box of the q-grid (one d-plane,
+// 128 / Qw full rows of Qw positions), so the activation slice of a tap is one
+// tiled TMA box at the tap's input offset rather than an im2col gather.
+template <int EPI, bool KEEP, int OPS, bool BOX>
 __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const __grid_constant__ TcParams P) {
+    constexpr int kPlanes = OPS == 0 ? 2 : 1;
     constexpr int kEpiWarps = EpiCfg<EPI>::warps;
     constexpr int kHalves = kEpiWarps / 4;  // warps per tensor-memory lane quarter
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -270,8 +297,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
     __shared__ float s_bias[256];                          // bias, zero-padded to 256 channels
-    __shared__ float s_bias_l2e[256];                      // bias * log2(e) (softmax)
-    __shared__ float s_xchg[2 * 2 * 4 * kTcTileM];         // softmax (max, sum) exchange, double-buffered
+    __shared__ __align__(16) float s_bias_l2e[256];        // bias * log2(e) (softmax)
+    __shared__ float s_xchg[sm_exchange_floats<EPI>()];   // softmax (max, sum) exchange, double-buffered
     // The group and class tables for the epilogue warps.
     __shared__ GroupDesc s_grp[kMaxGroups];
     __shared__ ClassDesc s_cls[kMaxClasses];
@@ -324,10 +351,10 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             for (int gi = 0; gi < P.ngroups; ++gi)
                 for (int ci = 0; ci < P.grp[gi].ncls; ++ci) {
                     ptx::prefetch_tmap(&P.a_hi[P.grp[gi].cls[ci]]);
-                    ptx::prefetch_tmap(&P.a_lo[P.grp[gi].cls[ci]]);
+                    if (kPlanes == 2) ptx::prefetch_tmap(&P.a_lo[P.grp[gi].cls[ci]]);
                 }
             ptx::prefetch_tmap(&P.b_hi);
-            ptx::prefetch_tmap(&P.b_lo);
+            if (kPlanes == 2) ptx::prefetch_tmap(&P.b_lo);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_phase = 0;  // per-stage bits: armed at least once, last armed parity
@@ -354,17 +381,30 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                             }
                             const uint32_t fb = full0 + 8 * stage;
                             const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
-                            ptx::mbar_arrive_expect_tx(fb, 2 * kABytes + 2 * P.b_bytes);
-                            const int c0 = kc * kChunk;
+                            // stage layout: A_hi [A_lo] B_hi [B_lo]
+                            ptx::mbar_arrive_expect_tx(fb, P.stage_bytes);
+                            const int c0 = kc * P.chunk;
+                            const uint32_t sbb = sb + (uint32_t)kPlanes * kABytes;
+                            if constexpr (BOX) {
+                                const int bw = qw0 + td.dw, bh = qh0 + td.dh, bd = qd0 + td.dd;
+                                ptx::tma_load_5d(sb, &P.a_hi[cls], fb, c0, bw, bh, bd, T.n);
+                                if (kPlanes == 2) ptx::tma_load_5d(sb + kABytes, &P.a_lo[cls], fb, c0, bw, bh, bd, T.n);
+                            } else {
 #if CONVT3D_OFFSETS_DHW
-                            ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
-                            ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
+                                ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
+                                if (kPlanes == 2)
+                                    ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, od, oh,
+                                                            ow);
 #else
-                            ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
-                            ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
+                                ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
+                                if (kPlanes == 2)
+                                    ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, ow, oh,
+                                                            od);
 #endif
-                            ptx::tma_load_3d(sb + 2 * kABytes, &P.b_hi, fb, c0, 0, C.tap_begin + j);
-                            ptx::tma_load_3d(sb + 2 * kABytes + P.b_bytes, &P.b_lo, fb, c0, 0, C.tap_begin + j);
+                            }
+                            ptx::tma_load_3d(sbb, &P.b_hi, fb, c0, 0, C.tap_begin + j);
+                            if (kPlanes == 2)
+                                ptx::tma_load_3d(sbb + P.b_bytes, &P.b_lo, fb, c0, 0, C.tap_begin + j);
                             armed |= 1u << stage;
                             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                             if (++stage == P.stages) {
@@ -390,7 +430,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     // ---------------------------------------------------------- MMA issuer
     else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_tf32((uint32_t)P.cout_pad);
+            const uint32_t idesc =
+                OPS == 2 ? ptx::idesc_bf16((uint32_t)P.cout_pad) : ptx::idesc_tf32((uint32_t)P.cout_pad);
             int stage = 0;
             uint32_t phase = 0;
             int iter = 0;
@@ -417,17 +458,33 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         }
                         ptx::tc_fence_after();
                         const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
+                        if constexpr (OPS == 0) {
 #pragma unroll
-                        for (int kk = 0; kk < kChunk / 8; ++kk) {  // 8 TF32 (32 bytes) per MMA
-                            const uint64_t a_hi = ptx::sdesc_k_swizzled(sb + kk * 32, kRowBytes);
-                            const uint64_t a_lo = ptx::sdesc_k_swizzled(sb + kABytes + kk * 32, kRowBytes);
-                            const uint64_t b_hi = ptx::sdesc_k_swizzled(sb + 2 * kABytes + kk * 32, kRowBytes);
-                            const uint64_t b_lo =
-                                ptx::sdesc_k_swizzled(sb + 2 * kABytes + P.b_bytes + kk * 32, kRowBytes);
-                            // the class's first product overwrites the accumulator
-                            ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (s | kk) ? 1u : 0u);
-                            ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
-                            ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                            for (int kk = 0; kk < kChunk / 8; ++kk) {  // 8 TF32 (32 bytes) per MMA
+                                const uint64_t a_hi = ptx::sdesc_k_swizzled(sb + kk * 32, kRowBytes);
+                                const uint64_t a_lo = ptx::sdesc_k_swizzled(sb + kABytes + kk * 32, kRowBytes);
+                                const uint64_t b_hi = ptx::sdesc_k_swizzled(sb + 2 * kABytes + kk * 32, kRowBytes);
+                                const uint64_t b_lo =
+                                    ptx::sdesc_k_swizzled(sb + 2 * kABytes + P.b_bytes + kk * 32, kRowBytes);
+                                // the class's first product overwrites the accumulator
+                                ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (s | kk) ? 1u : 0u);
+                                ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+                                ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                            }
+                        } else if constexpr (OPS == 2) {
+#pragma unroll
+                            for (int kk = 0; kk < kChunk / 8; ++kk) {  // 16 bf16 (32 bytes) per MMA
+                                const uint64_t a = ptx::sdesc_k_swizzled(sb + kk * 32, kRowBytes);
+                                const uint64_t b = ptx::sdesc_k_swizzled(sb + kABytes + kk * 32, kRowBytes);
+                                ptx::mma_bf16(d_tmem, a, b, idesc, (s | kk) ? 1u : 0u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < kChunk / 8; ++kk) {
+                                const uint64_t a = ptx::sdesc_k_swizzled(sb + kk * 32, kRowBytes);
+                                const uint64_t b = ptx::sdesc_k_swizzled(sb + kABytes + kk * 32, kRowBytes);
+                                ptx::mma_tf32(d_tmem, a, b, idesc, (s | kk) ? 1u : 0u);
+                            }
                         }
                         ptx::mma_commit(empty0 + 8 * stage);
                         if (++stage == P.stages) {
@@ -497,143 +554,172 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
 
             if (sm) {
                 // softmax over channels then sigmoid, per output position, in the base-2
-                // domain: u = (conv + bias) * log2(e), softmax weight = 2^(u - max) / sum.
-                // 1) one pass over this warp's chunks: exponentials kept in registers
-                //    (at most two chunks per class, i.e. Cout <= 32 * kHalves), each
-                //    chunk relative to the running maximum when it was read.
-                constexpr int kKeep = 2;
-                float e[KEEP ? kKeep : 1][2][16], mref[KEEP ? kKeep : 1][2];
-                float mx[2] = {-INFINITY, -INFINITY}, sum[2] = {0.f, 0.f};
-                // one chunk: base-2 logits, running max, rescaled running sum; leaves the
-                // exponentials (relative to the chunk's running max `cm`) in ev
-                auto chunk_pass = [&](int j, float (&ev)[2][16], float (&cm_out)[2]) {
-                    const int c0 = 16 * j;
-                    _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
-                        ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, ev[ci]);
-                    ptx::tmem_wait_ld();
-                    _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                // domain: u = (conv + bias) * log2(e), softmax weight = 2^(u - M) / S.
+                // Channel pairs (c, c+1) of one class travel together through packed
+                // f32x2 arithmetic; the max and the exponentials are per element.
+                const uint64_t l2e2 = pack2(kLog2e, kLog2e);
+                // base-2 logits of one chunk of one class as 8 channel pairs (channels
+                // past Cout get -inf, whose exponential is 0)
+                auto logits = [&](int c0, const float (&raw)[16], uint64_t (&u)[8]) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            ev[ci][i] = (c0 + i < C) ? fmaf(ev[ci][i], kLog2e, s_bias_l2e[c0 + i]) : -INFINITY;
-                        const float cm = fmaxf(mx[ci], tree_max16(ev[ci]));
-                        const float old = mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - cm);
+                    for (int k = 0; k < 8; ++k)
+                        u[k] = ffma2(pack2(raw[2 * k], raw[2 * k + 1]), l2e2,
+                                     *reinterpret_cast<const uint64_t *>(&s_bias_l2e[c0 + 2 * k]));
+                    if (c0 + 16 > C) {  // ragged last chunk (warp-uniform branch)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) ev[ci][i] = ex2_approx(ev[ci][i] - cm);
-                        mx[ci] = cm;
-                        sum[ci] = old + tree_sum16(ev[ci]);
-                        cm_out[ci] = cm;
+                        for (int k = 0; k < 8; ++k) {
+                            float a, b;
+                            unpack2(u[k], a, b);
+                            u[k] = pack2(c0 + 2 * k < C ? a : -INFINITY, c0 + 2 * k + 1 < C ? b : -INFINITY);
+                        }
                     }
                 };
+                auto max8 = [](const uint64_t (&u)[8]) {
+                    float a[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) unpack2(u[k], a[2 * k], a[2 * k + 1]);
+                    return tree_max16(a);
+                };
+                // u <- 2^(u - mx) in place; returns the sum of the 16 exponentials
+                auto exp8 = [](uint64_t (&u)[8], float mx) {
+                    const uint64_t neg = pack2(-mx, -mx);
+                    uint64_t acc[4];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        float a, b;
+                        unpack2(fadd2(u[k], neg), a, b);
+                        u[k] = pack2(ex2_approx(a), ex2_approx(b));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[k] = fadd2(u[k], u[k + 4]);
+                    acc[0] = fadd2(fadd2(acc[0], acc[2]), fadd2(acc[1], acc[3]));
+                    float a, b;
+                    unpack2(acc[0], a, b);
+                    return a + b;
+                };
+                // sigmoid(f * e) for 8 pairs, with the polynomial's coefficients
+                // pre-multiplied by powers of f (see sigmoid_coefficients), then the stores
+                auto finish = [&](int c0, int ci, uint64_t (&e)[8], const uint64_t (&A)[4]) {
+                    const uint64_t half2 = pack2(0.5f, 0.5f);
+                    float o[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint64_t x2 = fmul2(e[k], e[k]);
+                        uint64_t q = ffma2(A[3], x2, A[2]);
+                        q = ffma2(q, x2, A[1]);
+                        q = ffma2(q, x2, A[0]);
+                        unpack2(ffma2(e[k], q, half2), o[2 * k], o[2 * k + 1]);
+                    }
+                    if (off[ci] >= 0) {
+                        float *dst = yn + (int64_t)c0 * V + off[ci];
+                        if (c0 + 16 <= C) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) dst[(int64_t)i * V] = o[i];
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (c0 + i < C) dst[(int64_t)i * V] = o[i];
+                        }
+                    }
+                };
+                // 1) this warp's chunks: maximum and sum of exponentials per class
+                constexpr int kKeep = kSoftmaxKeepChunks;
+                uint64_t e[KEEP ? kKeep : 1][2][8];
+                float mx[2] = {-INFINITY, -INFINITY}, sum[2] = {0.f, 0.f};
                 if (KEEP) {
+                    _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                        float raw[kKeep][16];
 #pragma unroll
-                    for (int jj = 0; jj < (KEEP ? kKeep : 1); ++jj) {
-                        const int j = half + jj * kHalves;
-                        if (j < nchunks) {
-                            const int c0 = 16 * j;
-                            _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
-                                ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, e[jj][ci]);
-                            ptx::tmem_wait_ld();
+                        for (int jj = 0; jj < kKeep; ++jj) {
+                            const int j = half + jj * kHalves;
+                            if (j < nchunks)
+                                ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + 16 * j, raw[jj]);
+                        }
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {  // base-2 logits of both classes at once
-                                const float bl = s_bias_l2e[c0 + i];
-                                const float2 u = fma2(make_float2(e[jj][0][i], e[jj][1][i]),
-                                                      make_float2(kLog2e, kLog2e), make_float2(bl, bl));
-                                const bool in = c0 + i < C;
-                                e[jj][0][i] = in ? u.x : -INFINITY;
-                                e[jj][1][i] = in ? u.y : -INFINITY;
+                        for (int jj = 0; jj < kKeep; ++jj) {
+                            const int j = half + jj * kHalves;
+                            if (j < nchunks) {
+                                logits(16 * j, raw[jj], e[jj][ci]);
+                                mx[ci] = fmaxf(mx[ci], max8(e[jj][ci]));
                             }
-                            _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
-                                const float cm = fmaxf(mx[ci], tree_max16(e[jj][ci]));
-                                const float old = mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - cm);
+                        }
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) e[jj][ci][i] = ex2_approx(e[jj][ci][i] - cm);
-                                mx[ci] = cm;
-                                sum[ci] = old + tree_sum16(e[jj][ci]);
-                                mref[jj][ci] = cm;
-                            }
+                        for (int jj = 0; jj < kKeep; ++jj) {
+                            const int j = half + jj * kHalves;
+                            if (j < nchunks) sum[ci] += exp8(e[jj][ci], mx[ci]);
                         }
                     }
                 } else {
-                    for (int j = half; j < nchunks; j += kHalves) chunk_pass(j, e[0], mref[0]);
+                    // online: rescale the running sum whenever the maximum grows
+                    for (int j = half; j < nchunks; j += kHalves) {
+                        float raw[2][16];
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
+                            ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + 16 * j, raw[ci]);
+                        ptx::tmem_wait_ld();
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                            logits(16 * j, raw[ci], e[0][ci]);
+                            const float cm = fmaxf(mx[ci], max8(e[0][ci]));
+                            const float old = mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - cm);
+                            mx[ci] = cm;
+                            sum[ci] = old + exp8(e[0][ci], cm);
+                        }
+                    }
                 }
-                // 2) combine with the partner warp of this lane quarter
-                float M[2], inv[2];
-                if (kHalves == 2) {
-                    float *xm = s_xchg + ((iter & 1) * 2 + half) * 4 * kTcTileM;  // [class][max,sum][row]
+                // 2) combine with the partner warp of this lane quarter: global maximum M
+                //    and sum S; this warp's exponentials (relative to mx) scale by f
+                float f[2], M[2];
+                if (kHalves > 1) {
+                    float *xm = s_xchg + ((iter & 1) * kHalves + half) * 4 * kTcTileM;  // [class][max,sum][row]
                     xm[0 * kTcTileM + m] = mx[0];
                     xm[1 * kTcTileM + m] = sum[0];
                     xm[2 * kTcTileM + m] = mx[1];
                     xm[3 * kTcTileM + m] = sum[1];
-                    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-                    const float *xo = s_xchg + ((iter & 1) * 2 + (half ^ 1)) * 4 * kTcTileM;
+                    asm volatile("bar.sync %0, %1;" ::"r"(1 + quarter), "r"(32 * kHalves) : "memory");
+                    const float *xb = s_xchg + (iter & 1) * kHalves * 4 * kTcTileM;
 #pragma unroll
                     for (int ci = 0; ci < 2; ++ci) {
-                        const float om = xo[(2 * ci) * kTcTileM + m], os = xo[(2 * ci + 1) * kTcTileM + m];
-                        M[ci] = fmaxf(mx[ci], om);
-                        const float S = (mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - M[ci])) +
-                                        (om == -INFINITY ? 0.f : os * ex2_approx(om - M[ci]));
-                        inv[ci] = __frcp_rn(S);
+                        M[ci] = mx[ci];
+#pragma unroll
+                        for (int h = 0; h < kHalves; ++h)
+                            M[ci] = fmaxf(M[ci], xb[(h * 4 + 2 * ci) * kTcTileM + m]);
+                        float S = 0.f;
+#pragma unroll
+                        for (int h = 0; h < kHalves; ++h) {
+                            const float om = xb[(h * 4 + 2 * ci) * kTcTileM + m];
+                            const float os = xb[(h * 4 + 2 * ci + 1) * kTcTileM + m];
+                            S += om == -INFINITY ? 0.f : os * ex2_approx(om - M[ci]);
+                        }
+                        const float inv = __frcp_rn(S);
+                        const float mine_scale = mx[ci] == -INFINITY ? 0.f : ex2_approx(mx[ci] - M[ci]);
+                        f[ci] = KEEP ? mine_scale * inv : inv;
                     }
                 } else {
 #pragma unroll
                     for (int ci = 0; ci < 2; ++ci) {
                         M[ci] = mx[ci];
-                        inv[ci] = __frcp_rn(sum[ci]);
+                        f[ci] = __frcp_rn(sum[ci]);
                     }
                 }
-                // 3) outputs for this warp's chunks: t = weight in (0, 1], then sigmoid(t)
-                auto store_chunk = [&](int c0, const float (&o)[2][16]) {
-                    if (pair_store) {
-                        if (off[0] >= 0 && off[1] >= 0) {
-                            float *dst = yn + (int64_t)c0 * V + off[0];
+                // 3) outputs: weight t = f * e in (0, 1], then sigmoid(t)
+                _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                    uint64_t A[4];
+                    sigmoid_coefficients(f[ci], A);
+                    if (KEEP) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (c0 + i < C)
-                                    *reinterpret_cast<float2 *>(dst + (int64_t)i * V) = make_float2(o[0][i], o[1][i]);
+                        for (int jj = 0; jj < kKeep; ++jj) {
+                            const int j = half + jj * kHalves;
+                            if (j < nchunks) finish(16 * j, ci, e[jj][ci], A);
                         }
                     } else {
-                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
-                            if (off[ci] >= 0) {
-                                float *dst = yn + (int64_t)c0 * V + off[ci];
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    if (c0 + i < C) dst[(int64_t)i * V] = o[ci][i];
-                            }
-                    }
-                };
-                if (KEEP) {
-#pragma unroll
-                    for (int jj = 0; jj < (KEEP ? kKeep : 1); ++jj) {
-                        const int j = half + jj * kHalves;
-                        if (j < nchunks) {
-#pragma unroll
-                            // both classes at once: t = weight, then the packed sigmoid
-                            const float2 scale = make_float2(inv[0] * ex2_approx(mref[jj][0] - M[0]),
-                                                             inv[1] * ex2_approx(mref[jj][1] - M[1]));
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float2 o = sigmoid_unit2(mul2(make_float2(e[jj][0][i], e[jj][1][i]), scale));
-                                e[jj][0][i] = o.x;
-                                e[jj][1][i] = o.y;
-                            }
-                            store_chunk(16 * j, e[jj]);
+                        for (int j = half; j < nchunks; j += kHalves) {
+                            float raw[16];
+                            ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + 16 * j, raw);
+                            ptx::tmem_wait_ld();
+                            logits(16 * j, raw, e[0][ci]);
+                            exp8(e[0][ci], M[ci]);
+                            finish(16 * j, ci, e[0][ci], A);
                         }
-                    }
-                } else {
-                    for (int j = half; j < nchunks; j += kHalves) {
-                        const int c0 = 16 * j;
-                        float o[2][16];
-                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
-                            ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, o[ci]);
-                        ptx::tmem_wait_ld();
-                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float u = fmaf(o[ci][i], kLog2e, s_bias_l2e[c0 + i]);
-                                o[ci][i] = sigmoid_unit(ex2_approx(u - M[ci]) * inv[ci]);
-                            }
-                        }
-                        store_chunk(c0, o);
                     }
                 }
             } else {
@@ -816,10 +902,47 @@ struct TcCache {
     int threads;
     size_t smem;
     int grid;
+    bool box;  // activation slices loaded as tiled boxes (see box_tiles)
     bool ready;
 };
 
 void tc_cache_free(void *c) { delete static_cast<TcCache *>(c); }
+
+// The kernel instance for the plan's epilogue, operand format OPS and (for
+// softmax) register-kept exponentials; threads receives its block size.
+template <int OPS, bool BOX>
+static void (*select_kernel(const convt3d_plan_s &p, int &threads))(const TcParams) {
+    switch (p.d.epilogue) {
+        case CONVT3D_EPI_IDENTITY:
+            threads = EpiCfg<CONVT3D_EPI_IDENTITY>::threads;
+            return convt3d_tc_gemm<CONVT3D_EPI_IDENTITY, true, OPS, BOX>;
+        case CONVT3D_EPI_RELU_GROUPNORM:
+            threads = EpiCfg<CONVT3D_EPI_RELU_GROUPNORM>::threads;
+            return convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM, true, OPS, BOX>;
+        case CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL:
+            threads = EpiCfg<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL>::threads;
+            return convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL, true, OPS, BOX>;
+        case CONVT3D_EPI_SOFTMAX_SIGMOID:
+            threads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
+            // registers hold the exponentials when each warp owns at most
+            // kSoftmaxKeepChunks 16-channel chunks
+            return p.cout_pad <= 16 * kSoftmaxKeepChunks * (EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps / 4)
+                       ? convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, true, OPS, BOX>
+                       : convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, false, OPS, BOX>;
+    }
+    return nullptr;
+}
+
+// Tiles are whole boxes of every group's q-grid: Qw a power of two up to 128
+// and each d-plane of Qh * Qw positions a multiple of the 128-row tile.
+static bool box_tiles(const convt3d_plan_s &p) {
+    for (int i = 0; i < p.ngroups; ++i) {
+        const GroupDesc &G = p.grp[i];
+        if (G.vol == 0) continue;
+        if (G.Qw > kTcTileM || (G.Qw & (G.Qw - 1)) || (G.Qh * G.Qw) % kTcTileM) return false;
+    }
+    return true;
+}
 
 static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, const float *xs_lo,
                             const float *w_hi, const float *w_lo) {
@@ -835,11 +958,15 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->Do = g.Do;
         P->Ho = g.Ho;
         P->Wo = g.Wo;
-        P->stride = g.stride;
+        P->sd = g.ss[0];
+        P->sh = g.ss[1];
+        P->sw = g.ss[2];
         P->Din = g.Din;
         P->Hin = g.Hin;
         P->Win = g.Win;
-        P->kc = p.cin_pad / kChunk;
+        P->chunk = kRowBytes / p.elem_bytes;
+        P->kc = p.cin_pad / P->chunk;
+        P->bf16 = p.bf16;
         P->epilogue = p.d.epilogue;
         P->groups = p.d.groups;
         P->scale = p.d.scale;
@@ -856,29 +983,18 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->acc_stride = (uint32_t)(ncls_max * p.cout_pad);
         P->tmem_cols = (uint32_t)round_pow2(2 * ncls_max * p.cout_pad);
         P->b_bytes = (uint32_t)p.cout_pad * kRowBytes;
-        P->stage_bytes = 2 * kABytes + 2 * P->b_bytes;
-        switch (p.d.epilogue) {
-            case CONVT3D_EPI_IDENTITY:
-                tc.kern = convt3d_tc_gemm<CONVT3D_EPI_IDENTITY, true>;
-                tc.threads = EpiCfg<CONVT3D_EPI_IDENTITY>::threads;
-                break;
-            case CONVT3D_EPI_RELU_GROUPNORM:
-                tc.kern = convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM, true>;
-                tc.threads = EpiCfg<CONVT3D_EPI_RELU_GROUPNORM>::threads;
-                break;
-            case CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL:
-                tc.kern = convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL, true>;
-                tc.threads = EpiCfg<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL>::threads;
-                break;
-            case CONVT3D_EPI_SOFTMAX_SIGMOID:
-                // registers hold the exponentials when each warp owns at most two chunks
-                tc.kern = p.cout_pad <= 32 * EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps / 4 * 2
-                              ? convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, true>
-                              : convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, false>;
-                tc.threads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
-                break;
-            default: return cudaErrorInvalidValue;
-        }
+        P->planes = p.planes;
+        P->stage_bytes = (uint32_t)p.planes * (kABytes + P->b_bytes);
+        tc.box = box_tiles(p);
+        const int ops = p.planes == 2 ? 0 : (p.bf16 ? 2 : 1);
+        if (tc.box)
+            tc.kern = ops == 0 ? select_kernel<0, true>(p, tc.threads)
+                               : (ops == 1 ? select_kernel<1, true>(p, tc.threads) : select_kernel<2, true>(p, tc.threads));
+        else
+            tc.kern = ops == 0 ? select_kernel<0, false>(p, tc.threads)
+                               : (ops == 1 ? select_kernel<1, false>(p, tc.threads)
+                                           : select_kernel<2, false>(p, tc.threads));
+        if (!tc.kern) return cudaErrorInvalidValue;
         // stage ring: as many stages as fit beside the kernel's static shared memory
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, tc.kern);
@@ -901,13 +1017,30 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
     if (tc.key[0] == xs_hi && tc.key[1] == xs_lo && tc.key[2] == w_hi && tc.key[3] == w_lo) return cudaSuccess;
 
     // activation maps: one im2col map per class and plane
+    const cuuint64_t eb = (cuuint64_t)p.elem_bytes;
+    const CUtensorMapDataType dt = p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const cuuint64_t gdim[5] = {(cuuint64_t)p.cin_pad, (cuuint64_t)g.Win, (cuuint64_t)g.Hin, (cuuint64_t)g.Din,
                                 (cuuint64_t)g.N};
-    const cuuint64_t gstr[4] = {(cuuint64_t)p.cin_pad * 4, (cuuint64_t)p.cin_pad * 4 * g.Win,
-                                (cuuint64_t)p.cin_pad * 4 * g.Win * g.Hin,
-                                (cuuint64_t)p.cin_pad * 4 * g.Win * g.Hin * g.Din};
+    const cuuint64_t gstr[4] = {(cuuint64_t)p.cin_pad * eb, (cuuint64_t)p.cin_pad * eb * g.Win,
+                                (cuuint64_t)p.cin_pad * eb * g.Win * g.Hin,
+                                (cuuint64_t)p.cin_pad * eb * g.Win * g.Hin * g.Din};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    for (int gi = 0; gi < p.ngroups; ++gi) {
+    if (tc.box) {
+        // one tiled map per plane, box {chunk, Qw, 128 / Qw, 1, 1}, copied into every class slot
+        int qw = 1;
+        for (int gi = 0; gi < p.ngroups; ++gi)
+            if (p.grp[gi].vol) qw = p.grp[gi].Qw;
+        const cuuint32_t abox[5] = {(cuuint32_t)P->chunk, (cuuint32_t)qw, (cuuint32_t)(kTcTileM / qw), 1, 1};
+        for (int plane = 0; plane < p.planes; ++plane) {
+            CUtensorMap m;
+            CUresult r = fn.tiled(&m, dt, 5, (void *)(plane ? xs_lo : xs_hi), gdim, gstr, abox, estr,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+            for (int c = 0; c < kMaxClasses; ++c) (plane ? P->a_lo[c] : P->a_hi[c]) = m;
+        }
+    }
+    for (int gi = 0; gi < p.ngroups && !tc.box; ++gi) {
         const GroupDesc &G = p.grp[gi];
         for (int ci = 0; ci < G.ncls; ++ci) {
             const int c = G.cls[ci];
@@ -919,9 +1052,9 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
 #else
             const int lower[3] = {lo_w, lo_h, lo_d}, upper[3] = {up_w, up_h, up_d};
 #endif
-            for (int plane = 0; plane < 2; ++plane) {
-                CUresult r = fn.im2col(plane ? &P->a_lo[c] : &P->a_hi[c], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5,
-                                       (void *)(plane ? xs_lo : xs_hi), gdim, gstr, lower, upper, kChunk,
+            for (int plane = 0; plane < p.planes; ++plane) {
+                CUresult r = fn.im2col(plane ? &P->a_lo[c] : &P->a_hi[c], dt, 5,
+                                       (void *)(plane ? xs_lo : xs_hi), gdim, gstr, lower, upper, P->chunk,
                                        kTcTileM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzle,
                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
                 if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -930,11 +1063,11 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
     }
     // weight maps: [tap][cout_pad][cin_pad], box 32 x cout_pad x 1
     const cuuint64_t wdim[3] = {(cuuint64_t)p.cin_pad, (cuuint64_t)p.cout_pad, (cuuint64_t)g.ntaps};
-    const cuuint64_t wstr[2] = {(cuuint64_t)p.cin_pad * 4, (cuuint64_t)p.cin_pad * 4 * p.cout_pad};
-    const cuuint32_t box[3] = {(cuuint32_t)kChunk, (cuuint32_t)p.cout_pad, 1};
+    const cuuint64_t wstr[2] = {(cuuint64_t)p.cin_pad * eb, (cuuint64_t)p.cin_pad * eb * p.cout_pad};
+    const cuuint32_t box[3] = {(cuuint32_t)P->chunk, (cuuint32_t)p.cout_pad, 1};
     const cuuint32_t es[3] = {1, 1, 1};
-    for (int plane = 0; plane < 2; ++plane) {
-        CUresult r = fn.tiled(plane ? &P->b_lo : &P->b_hi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+    for (int plane = 0; plane < p.planes; ++plane) {
+        CUresult r = fn.tiled(plane ? &P->b_lo : &P->b_hi, dt, 3,
                               (void *)(plane ? w_lo : w_hi), wdim, wstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               kSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -8,8 +8,8 @@ The workloads are the shapes of the three transcript pages (l2_p61
 ReLU+GroupNorm, l2_p77 scale+BatchNorm+pool, l2_p49 stride-2 softmax+sigmoid),
 a tiny parity case, a bare stride-2 k=4 identity case and the BatchNorm shape
 in evaluation mode.  Values: x ~ N(0,1);
-weight and bias ~ U(-b, b) with b = 1/sqrt(Cout*k^3) (PyTorch's ConvTranspose3d
-default bound); gamma ~ U(0.5, 1.5) and beta ~ U(-0.5, 0.5) where an affine
+weight and bias ~ U(-b, b) with b = 1/sqrt(Cout/G * kd*kh*kw) (PyTorch's
+ConvTranspose3d default bound; G = convolution groups); gamma ~ U(0.5, 1.5) and beta ~ U(-0.5, 0.5) where an affine
 normalisation is present; BatchNorm running statistics from make_running_stats.
 Drawn on the CPU in fp32 from one
 torch.Generator seeded with 20261202 + workload index, in the order x, w, bias,
@@ -50,14 +50,25 @@ class Spec:
     eps: float = 1e-5
     scale: float = 1.0
     seed_index: int = 0
+    dilation: object = 1     # int or (d, h, w); k, stride, pad, out_pad likewise
+    conv_groups: int = 1
+
+    @property
+    def kdims(self):
+        return tuple(self.k) if isinstance(self.k, (tuple, list)) else (self.k,) * 3
+
+    @property
+    def kvol(self):
+        a, b, c = self.kdims
+        return a * b * c
 
     @property
     def affine(self) -> bool:
         return self.epilogue in (EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
 
     def useful_flop(self) -> float:
-        """2*N*Cout*Cin*k^3*Din*Hin*Win: every product of the definition, no zero taps."""
-        return 2.0 * self.N * self.Cout * self.Cin * self.k ** 3 * self.D * self.H * self.W
+        """2*N*Cout*(Cin/G)*kd*kh*kw*Din*Hin*Win: every product of the definition, no zero taps."""
+        return 2.0 * self.N * self.Cout * (self.Cin // self.conv_groups) * self.kvol * self.D * self.H * self.W
 
     def replace(self, **kw) -> "Spec":
         return dataclasses.replace(self, **kw)
@@ -87,9 +98,9 @@ def make_inputs(spec: Spec, seed: int | None = None) -> dict:
     """CPU fp32 tensors x, w, bias, gamma, beta (None where absent)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(SEED_BASE + spec.seed_index if seed is None else seed)
-    bound = 1.0 / math.sqrt(spec.Cout * spec.k ** 3)
+    bound = 1.0 / math.sqrt(spec.Cout // spec.conv_groups * spec.kvol)
     x = torch.randn((spec.N, spec.Cin, spec.D, spec.H, spec.W), generator=g, dtype=torch.float32)
-    w = torch.empty((spec.Cin, spec.Cout, spec.k, spec.k, spec.k), dtype=torch.float32)
+    w = torch.empty((spec.Cin, spec.Cout // spec.conv_groups) + spec.kdims, dtype=torch.float32)
     w.uniform_(-bound, bound, generator=g)
     bias = gamma = beta = None
     if spec.bias:
