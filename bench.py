@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the CPU baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-chunks", type=int, default=4, help="sample chunks the end-to-end pipeline overlaps")
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="streams per copy direction in the end-to-end pipeline")
     return ap.parse_args()
 
 
@@ -342,7 +344,7 @@ def run_gpu(args, spec):
         host = {k: (v.pin_memory() if v is not None else None) for k, v in inputs.items()}
         pipe = HostPipeline(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
                             spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, prec,
-                            chunks=args.e2e_chunks, device=dev)
+                            chunks=args.e2e_chunks, device=dev, copy_streams=args.e2e_copy_streams)
         if running is not None:
             pipe.set_running_stats(*running)
         y_host = torch.empty(pipe.full_shape, dtype=torch.float32).pin_memory()
@@ -362,7 +364,8 @@ def run_gpu(args, spec):
         e2e_t = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
         e2e = {"value": replica_throughput(useful, world, e2e_t), "unit": "TFLOP/s", "ms_per_step": e2e_t,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "path": f"HostPipeline, {e2e_chunks} chunk(s) of samples, pinned host buffers"}
+               "path": f"HostPipeline, {e2e_chunks} chunk(s) of samples, {args.e2e_copy_streams} copy stream(s) "
+                       "per direction, pinned host buffers"}
 
     if rank != 0:
         if world > 1:

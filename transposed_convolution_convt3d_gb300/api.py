@@ -179,8 +179,8 @@ class HostPipeline:
     """Forward from host memory to host memory with the copies overlapped.
 
     The batch is split into chunks of samples; chunk i's host->device copy,
-    chunk i-1's computation and chunk i-2's device->host copy run on three
-    streams at once.  Valid for the epilogues whose result for a sample depends
+    chunk i-1's computation and chunk i-2's device->host copy run at once, each
+    copy split over `copy_streams` streams per direction.  Valid for the epilogues whose result for a sample depends
     on that sample only (identity, ReLU+GroupNorm, softmax+sigmoid); the
     BatchNorm epilogues run as one chunk (the training-mode one's batch
     statistics need the whole batch).  Host tensors should be pinned for the copies to be asynchronous.
@@ -189,7 +189,7 @@ class HostPipeline:
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, chunks=4,
-                 device="cuda", dilation=1, conv_groups=1):
+                 device="cuda", dilation=1, conv_groups=1, copy_streams=1):
         if epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) or N % chunks:
             chunks = 1
         self.chunks = chunks
@@ -204,7 +204,12 @@ class HostPipeline:
         self.w = torch.empty((Cin, Cout // conv_groups) + _triple(k), dtype=torch.float32, device=dev)
         self.vec = {name: torch.empty(Cout, dtype=torch.float32, device=dev) for name in ("bias", "gamma", "beta")}
         self.ws = self.plan.new_workspace(dev)
-        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        # each chunk's copies are split over `copy_streams` streams per direction, so
+        # that several copy engines move it at once
+        self.copy_streams = max(1, int(copy_streams))
+        self.s_in = [torch.cuda.Stream(dev) for _ in range(self.copy_streams)]
+        self.s_out = [torch.cuda.Stream(dev) for _ in range(self.copy_streams)]
+        self.s_comp = torch.cuda.Stream(dev)
 
     def set_running_stats(self, running_mean, running_var, momentum=0.1):
         """Device-resident BatchNorm running statistics, as Plan.set_running_stats."""
@@ -214,10 +219,18 @@ class HostPipeline:
         """Run on pinned host tensors; returns y_host.  The work is ordered after
         `stream` (default: current stream) and `stream` waits for its end."""
         caller = stream if stream is not None else torch.cuda.current_stream()
-        for s in (self.s_in, self.s_comp, self.s_out):
+        for s in self.s_in + self.s_out + [self.s_comp]:
             s.wait_stream(caller)
-        nc = self.n_chunk
-        with torch.cuda.stream(self.s_in):
+        nc, k = self.n_chunk, self.copy_streams
+
+        def pieces(dst, src):  # the same k contiguous slices of two equally shaped tensors
+            d, s_ = dst.view(-1), src.reshape(-1)
+            n = d.numel()
+            for j in range(k):
+                a, b = n * j // k, n * (j + 1) // k
+                yield j, d[a:b], s_[a:b]
+
+        with torch.cuda.stream(self.s_in[0]):
             self.w.copy_(w_host, non_blocking=True)
             dv = {}
             for name, t in (("bias", bias), ("gamma", gamma), ("beta", beta)):
@@ -228,22 +241,27 @@ class HostPipeline:
                     dv[name] = None
         in_done = []
         for i in range(self.chunks):
-            with torch.cuda.stream(self.s_in):
-                self.x[i * nc:(i + 1) * nc].copy_(x_host[i * nc:(i + 1) * nc], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(self.s_in)
-                in_done.append(ev)
+            evs = []
+            for j, d, s_ in pieces(self.x[i * nc:(i + 1) * nc], x_host[i * nc:(i + 1) * nc]):
+                with torch.cuda.stream(self.s_in[j]):
+                    d.copy_(s_, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(self.s_in[j])
+                    evs.append(ev)
+            in_done.append(evs)
         for i in range(self.chunks):
-            self.s_comp.wait_event(in_done[i])
+            for ev in in_done[i]:
+                self.s_comp.wait_event(ev)
             if i == 0:
                 self.plan.pack_weights(self.w, self.ws, self.s_comp)
             self.plan.forward(self.x[i * nc:(i + 1) * nc], self.y[i * nc:(i + 1) * nc], self.ws, dv["bias"],
                               dv["gamma"], dv["beta"], self.s_comp)
             ev = torch.cuda.Event()
             ev.record(self.s_comp)
-            self.s_out.wait_event(ev)
-            with torch.cuda.stream(self.s_out):
-                y_host[i * nc:(i + 1) * nc].copy_(self.y[i * nc:(i + 1) * nc], non_blocking=True)
-        caller.wait_stream(self.s_out)
-        caller.wait_stream(self.s_comp)
+            for j, d, s_ in pieces(y_host[i * nc:(i + 1) * nc], self.y[i * nc:(i + 1) * nc]):
+                self.s_out[j].wait_event(ev)
+                with torch.cuda.stream(self.s_out[j]):
+                    d.copy_(s_, non_blocking=True)
+        for s in self.s_out + [self.s_comp]:
+            caller.wait_stream(s)
         return y_host

@@ -40,6 +40,34 @@ struct ClassDesc {
     int step_d;             // delta decrease between consecutive d-slices (the d dilation)
 };
 
+// Unsigned division by an invariant divisor d >= 1 as a multiply-high, a
+// subtract and two shifts, exact for every 32-bit dividend (Granlund and
+// Montgomery, "Division by Invariant Integers using Multiplication", 1994,
+// their unsigned algorithm with l = ceil(log2 d)).
+struct FastDiv {
+    uint32_t m;
+    uint16_t s1, s2;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    int l = 0;
+    while (l < 32 && (1ull << l) < d) ++l;
+    FastDiv f;
+    f.m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+    f.s1 = (uint16_t)(l < 1 ? l : 1);
+    f.s2 = (uint16_t)(l > 1 ? l - 1 : 0);
+    return f;
+}
+
+__host__ __device__ __forceinline__ uint32_t fastdiv(uint32_t n, FastDiv f) {
+#ifdef __CUDA_ARCH__
+    const uint32_t t = __umulhi(f.m, n);
+#else
+    const uint32_t t = (uint32_t)(((uint64_t)f.m * n) >> 32);
+#endif
+    return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 // A unit of GEMM work: one class (FFMA, or stride 1), or the two classes
 // differing only in w-parity (tensor-core path, stride 2), enumerated over a
 // common q-grid of Qd x Qh x Qw positions per sample.
@@ -51,6 +79,14 @@ struct GroupDesc {
     int tiles;              // tiles per sample
     int tile_prefix;        // tiles of earlier groups within one sample
     int ksteps;             // K steps per tile (all classes of the group)
+    FastDiv div_qw, div_qhw;  // division by Qw and by Qh * Qw (q-grid position of a row)
+    // Merged w-taps of a w-parity pair (tensor-core path): for each distinct w
+    // offset, which classes have it (bit c) and the tap's index among class c's
+    // w-taps; entries that both classes have come first.
+    int nm;
+    int8_t mdw[8];
+    uint8_t mmask[8];
+    int8_t me[8][2];
 };
 
 // Taps a tile issues.  Along d, a class's taps have decreasing input offsets
@@ -128,6 +164,7 @@ struct convt3d_plan_s {
     convt3d::Geometry g;
     int tc;                 // 1: tensor-core path, 0: FFMA
     int planes;             // tensor-core operand planes: 2 = split TF32 (hi, lo), 1 = TF32 or BF16
+    int merged;             // w-parity pairs share activation loads and MMAs (see GroupDesc::nm)
     int bf16;               // tensor-core operands in bf16 (kind::f16 MMA)
     int chunk;              // input channels per K step (one 128-byte operand row)
     int elem_bytes;         // bytes per staged / packed operand element

@@ -166,6 +166,32 @@ void build_groups(convt3d_plan_s &p) {
             G.ksteps = a.ntaps * kc;
         }
     }
+    // Merged w-taps of each pair: the distinct w offsets of the two classes,
+    // shared ones first.  A K step of a shared offset loads the activation
+    // slice once and feeds both classes with one MMA of N = 2 * Cout_pad.
+    for (int i = 0; i < p.ngroups; ++i) {
+        GroupDesc &G = p.grp[i];
+        G.nm = 0;
+        if (G.ncls != 2) continue;
+        const ClassDesc &c0 = g.cls[G.cls[0]], &c1 = g.cls[G.cls[1]];
+        int dw[2][8], n[2] = {c0.nt_w, c1.nt_w};
+        for (int e = 0; e < n[0]; ++e) dw[0][e] = g.taps[c0.tap_begin + e].dw;
+        for (int e = 0; e < n[1]; ++e) dw[1][e] = g.taps[c1.tap_begin + e].dw;
+        for (int pass = 0; pass < 2; ++pass)  // pass 0: shared offsets, pass 1: the rest
+            for (int c = 0; c < 2; ++c)
+                for (int e = 0; e < n[c]; ++e) {
+                    int other = -1;
+                    for (int f = 0; f < n[1 - c]; ++f)
+                        if (dw[1 - c][f] == dw[c][e]) other = f;
+                    const bool shared = other >= 0;
+                    if ((pass == 0) != shared || (shared && c == 1)) continue;
+                    const int m = G.nm++;
+                    G.mdw[m] = (int8_t)dw[c][e];
+                    G.mmask[m] = (uint8_t)(shared ? 3 : 1 << c);
+                    G.me[m][c] = (int8_t)e;
+                    G.me[m][1 - c] = (int8_t)other;
+                }
+    }
     std::stable_sort(p.grp, p.grp + p.ngroups,
                      [](const GroupDesc &a, const GroupDesc &b) { return a.ksteps > b.ksteps; });
     int prefix = 0;
@@ -173,6 +199,8 @@ void build_groups(convt3d_plan_s &p) {
         GroupDesc &G = p.grp[i];
         G.vol = G.Qd * G.Qh * G.Qw;
         G.tiles = (G.vol + p.tile_m - 1) / p.tile_m;
+        G.div_qw = make_fastdiv((uint32_t)std::max(G.Qw, 1));
+        G.div_qhw = make_fastdiv((uint32_t)std::max(G.Qh * G.Qw, 1));
         G.tile_prefix = prefix;
         prefix += G.tiles;
     }
@@ -313,6 +341,9 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     if (!p->tc)  // the FFMA kernel's register tiles need a power-of-two channel count
         while (p->cout_pad & (p->cout_pad - 1)) p->cout_pad += 16;
     build_groups(*p);
+    // Pairs merge where the combined MMA fits (N = 2 * Cout_pad <= 128): there the
+    // instruction count, not the tensor pipe, bounds the main loop.
+    p->merged = p->tc && p->g.ss[2] == 2 && p->cout_pad <= 64;
     const bool eval_bn = desc->epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
     if (p->tc && !eval_bn && !im2col_corners_ok(*p)) {
         delete p;

@@ -52,19 +52,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Gives up after
-// `limit_ns` nanoseconds, or as soon as *abort becomes non-zero; returns
+// about `limit_ns` nanoseconds, or as soon as *abort becomes non-zero; returns
 // false in both cases.  With sleep_ns > 0 the waiter naps between polls so
-// that it leaves issue slots to the other warps of its sub-partition.
+// that it leaves issue slots to the other warps of its sub-partition.  The
+// clock is read only on every 64th failed poll (every poll when napping) and
+// the limit counts from the first such read, so a wait that completes within
+// a few polls -- the common case inside a pipeline -- never touches the
+// global timer.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const volatile int *abort,
                                                   uint64_t limit_ns, uint32_t sleep_ns = 0) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (sleep_ns) __nanosleep(sleep_ns);
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 || sleep_ns) {
+        if (sleep_ns) __nanosleep(sleep_ns);
+        if ((it & 63u) == 63u || sleep_ns) {
             if (*abort) return false;
-            if (globaltimer() - t0 > limit_ns) return false;
+            const uint64_t now = globaltimer();
+            if (t0 == 0)
+                t0 = now;
+            else if (now - t0 > limit_ns)
+                return false;
         }
     }
 }
@@ -81,17 +88,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-// 5-D tiled load (c, w, h, d, n): coordinates may be negative or past the
-// extent (those elements arrive as zeros); c must be 16-byte aligned.
-__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, uint32_t bar, int c, int w, int h,
-                                            int d, int n) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(d), "r"(n)
         : "memory");
 }
 

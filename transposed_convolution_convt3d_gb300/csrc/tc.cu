@@ -272,24 +272,30 @@ __device__ __forceinline__ float tree_sum16(const float (&v)[16]) {
 __device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G, const ClassDesc &C, int t, int m) {
     const int q = t * kTcTileM + m;
     if (q >= G.vol) return -1;
-    const int qhw = G.Qh * G.Qw;
-    const int od = P.sd * (q / qhw) + C.rd;
-    const int oh = P.sh * ((q / G.Qw) % G.Qh) + C.rh;
-    const int ow = P.sw * (q % G.Qw) + C.rw;
+    const int qd = (int)fastdiv((uint32_t)q, G.div_qhw);
+    const int r = q - qd * (G.Qh * G.Qw);
+    const int qh = (int)fastdiv((uint32_t)r, G.div_qw);
+    const int od = P.sd * qd + C.rd;
+    const int oh = P.sh * qh + C.rh;
+    const int ow = P.sw * (r - qh * G.Qw) + C.rw;
     if (od >= P.Do || oh >= P.Ho || ow >= P.Wo) return -1;
     return (od * P.Ho + oh) * P.Wo + ow;
 }
 
-// KEEP (softmax only): each epilogue warp keeps its exponentials in registers
-// (Cout <= 32 * warps per lane quarter); otherwise it re-reads tensor memory.
+// KEEP (softmax only): 1 = each epilogue warp keeps its exponentials in
+// registers (Cout <= 16 * kSoftmaxKeepChunks * warps per lane quarter); 2 = as
+// 1, for w-parity pairs with each warp owning one class's channels (8 warps);
+// 0 = the exponentials are recomputed from tensor memory.
 // OPS: operand format, fixed at compile time so that the producer and MMA
 // loops stay branch-free: 0 = split TF32 (hi and lo planes), 1 = TF32, 2 = BF16.
-// BOX: every tile of every group is a whole box of the q-grid (one d-plane,
-// 128 / Qw full rows of Qw positions), so the activation slice of a tap is one
-// tiled TMA box at the tap's input offset rather than an im2col gather.
-template <int EPI, bool KEEP, int OPS, bool BOX>
+// MERGED: every group is a w-parity pair walked by merged w-taps (GroupDesc::nm):
+// a K step whose w offset both classes have loads the activation slice once,
+// the two classes' weight slices side by side, and issues one MMA of
+// N = 2 * Cout_pad into both accumulators (they are adjacent in tensor memory).
+template <int EPI, int KEEP, int OPS, bool MERGED>
 __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const __grid_constant__ TcParams P) {
     constexpr int kPlanes = OPS == 0 ? 2 : 1;
+    constexpr int kBSlots = MERGED ? 2 : 1;  // weight slices per plane in a stage
     constexpr int kEpiWarps = EpiCfg<EPI>::warps;
     constexpr int kHalves = kEpiWarps / 4;  // warps per tensor-memory lane quarter
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -359,59 +365,78 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             uint32_t phase = 0;
             uint32_t armed = 0, armed_phase = 0;  // per-stage bits: armed at least once, last armed parity
             bool ok = true;
+            // One K step per input-channel chunk of one tap: the activation slice of
+            // class `cls` at tap `td`, the weight slice of tap tb0 and, merged, of tap tb1.
+            auto issue_tap = [&](const Tile &T, int cls, const ClassDesc &C, int qd0, int qh0, int qw0,
+                                 const TapDesc td, int tb0, int tb1) {
+                const int w0 = qw0 + C.lo_w, h0 = qh0 + C.lo_h, d0 = qd0 + C.lo_d;
+                const uint16_t ow = (uint16_t)(td.dw - C.lo_w);
+                const uint16_t oh = (uint16_t)(td.dh - C.lo_h);
+                const uint16_t od = (uint16_t)(td.dd - C.lo_d);
+                const uint32_t nb = tb1 >= 0 ? 2u : 1u;
+                for (int kc = 0; kc < P.kc; ++kc) {
+                    if (!ptx::mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, &abort_flag, kWaitNs)) {
+                        ok = false;
+                        return;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
+                    // stage layout: A_hi [A_lo] B_hi(slot 0 [, slot 1]) [B_lo(slot 0 [, slot 1])]
+                    ptx::mbar_arrive_expect_tx(fb, (uint32_t)kPlanes * (kABytes + nb * P.b_bytes));
+                    const int c0 = kc * P.chunk;
+                    const uint32_t sbb = sb + (uint32_t)kPlanes * kABytes;
+#if CONVT3D_OFFSETS_DHW
+                    ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
+                    if (kPlanes == 2)
+                        ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
+#else
+                    ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
+                    if (kPlanes == 2)
+                        ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
+#endif
+                    ptx::tma_load_3d(sbb, &P.b_hi, fb, c0, 0, tb0);
+                    if (MERGED && tb1 >= 0) ptx::tma_load_3d(sbb + P.b_bytes, &P.b_hi, fb, c0, 0, tb1);
+                    if (kPlanes == 2) {
+                        const uint32_t lo = sbb + (uint32_t)kBSlots * P.b_bytes;
+                        ptx::tma_load_3d(lo, &P.b_lo, fb, c0, 0, tb0);
+                        if (MERGED && tb1 >= 0) ptx::tma_load_3d(lo + P.b_bytes, &P.b_lo, fb, c0, 0, tb1);
+                    }
+                    armed |= 1u << stage;
+                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == P.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            };
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
                 const Tile T = decode(P, P.grp, tile);
                 const GroupDesc &G = P.grp[T.gi];
                 const int q0 = T.t * kTcTileM;
                 const int qd0 = q0 / (G.Qh * G.Qw), qh0 = (q0 / G.Qw) % G.Qh, qw0 = q0 % G.Qw;
-                for (int ci = 0; ok && ci < G.ncls; ++ci) {
-                    const int cls = G.cls[ci];
-                    const ClassDesc &C = P.cls[cls];
-                    const int w0 = qw0 + C.lo_w, h0 = qh0 + C.lo_h, d0 = qd0 + C.lo_d;
-                    const TapRange tr = tile_taps(G, C, T.t, kTcTileM, P.Din);
-                    for (int j = tr.begin; ok && j < tr.end; ++j) {
-                        const TapDesc td = P.taps[C.tap_begin + j];
-                        const uint16_t ow = (uint16_t)(td.dw - C.lo_w);
-                        const uint16_t oh = (uint16_t)(td.dh - C.lo_h);
-                        const uint16_t od = (uint16_t)(td.dd - C.lo_d);
-                        for (int kc = 0; kc < P.kc; ++kc) {
-                            if (!ptx::mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, &abort_flag, kWaitNs)) {
-                                ok = false;
-                                break;
+                if constexpr (MERGED) {
+                    const ClassDesc &C0 = P.cls[G.cls[0]], &C1 = P.cls[G.cls[1]];
+                    const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);  // d-slices: same for both
+                    const int nhw0 = C0.nt_h * C0.nt_w;
+                    const int a_begin = tr.begin / nhw0, a_end = (tr.end + nhw0 - 1) / nhw0;
+                    for (int a = a_begin; ok && a < a_end; ++a)
+                        for (int b = 0; ok && b < C0.nt_h; ++b)
+                            for (int m = 0; ok && m < G.nm; ++m) {
+                                const int mask = G.mmask[m];
+                                const int t0 = C0.tap_begin + (a * C0.nt_h + b) * C0.nt_w + G.me[m][0];
+                                const int t1 = C1.tap_begin + (a * C1.nt_h + b) * C1.nt_w + G.me[m][1];
+                                if (mask & 1)
+                                    issue_tap(T, G.cls[0], C0, qd0, qh0, qw0, P.taps[t0], t0, mask == 3 ? t1 : -1);
+                                else
+                                    issue_tap(T, G.cls[1], C1, qd0, qh0, qw0, P.taps[t1], t1, -1);
                             }
-                            const uint32_t fb = full0 + 8 * stage;
-                            const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
-                            // stage layout: A_hi [A_lo] B_hi [B_lo]
-                            ptx::mbar_arrive_expect_tx(fb, P.stage_bytes);
-                            const int c0 = kc * P.chunk;
-                            const uint32_t sbb = sb + (uint32_t)kPlanes * kABytes;
-                            if constexpr (BOX) {
-                                const int bw = qw0 + td.dw, bh = qh0 + td.dh, bd = qd0 + td.dd;
-                                ptx::tma_load_5d(sb, &P.a_hi[cls], fb, c0, bw, bh, bd, T.n);
-                                if (kPlanes == 2) ptx::tma_load_5d(sb + kABytes, &P.a_lo[cls], fb, c0, bw, bh, bd, T.n);
-                            } else {
-#if CONVT3D_OFFSETS_DHW
-                                ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, od, oh, ow);
-                                if (kPlanes == 2)
-                                    ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, od, oh,
-                                                            ow);
-#else
-                                ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
-                                if (kPlanes == 2)
-                                    ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, ow, oh,
-                                                            od);
-#endif
-                            }
-                            ptx::tma_load_3d(sbb, &P.b_hi, fb, c0, 0, C.tap_begin + j);
-                            if (kPlanes == 2)
-                                ptx::tma_load_3d(sbb + P.b_bytes, &P.b_lo, fb, c0, 0, C.tap_begin + j);
-                            armed |= 1u << stage;
-                            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-                            if (++stage == P.stages) {
-                                stage = 0;
-                                phase ^= 1u;
-                            }
-                        }
+                } else {
+                    for (int ci = 0; ok && ci < G.ncls; ++ci) {
+                        const int cls = G.cls[ci];
+                        const ClassDesc &C = P.cls[cls];
+                        const TapRange tr = tile_taps(G, C, T.t, kTcTileM, P.Din);
+                        for (int j = tr.begin; ok && j < tr.end; ++j)
+                            issue_tap(T, cls, C, qd0, qh0, qw0, P.taps[C.tap_begin + j], C.tap_begin + j, -1);
                     }
                 }
             }
@@ -432,10 +457,59 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         if (lane == 0) {
             const uint32_t idesc =
                 OPS == 2 ? ptx::idesc_bf16((uint32_t)P.cout_pad) : ptx::idesc_tf32((uint32_t)P.cout_pad);
+            // merged steps of both classes: N = 2 * Cout_pad
+            const uint32_t idesc2 =
+                OPS == 2 ? ptx::idesc_bf16(2u * (uint32_t)P.cout_pad) : ptx::idesc_tf32(2u * (uint32_t)P.cout_pad);
+            constexpr uint64_t kA16 = kABytes >> 4;                  // one activation plane, 16-byte units
+            const uint64_t b16 = (uint64_t)(P.b_bytes >> 4);         // one weight slice
+            const uint64_t blo16 = (uint64_t)kBSlots * b16;          // B_lo after the B_hi slots
             int stage = 0;
             uint32_t phase = 0;
             int iter = 0;
             bool ok = true;
+            // The K steps of one tap; `init`: the first product overwrites the accumulator(s).
+            auto mma_tap = [&](uint32_t d_tmem, uint32_t id, bool init) {
+                for (int kc = 0; kc < P.kc; ++kc) {
+                    if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
+                        ok = false;
+                        return;
+                    }
+                    ptx::tc_fence_after();
+                    // One descriptor per stage; the others differ only in the start-address
+                    // field (16-byte units), which never carries out of its 14 bits here.
+                    const uint64_t d0 = ptx::sdesc_k_swizzled(smem_base + (uint32_t)stage * P.stage_bytes, kRowBytes);
+                    const uint32_t first = (init && kc == 0) ? 0u : 1u;
+                    if constexpr (OPS == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < kChunk / 8; ++kk) {  // 8 TF32 (32 bytes) per MMA
+                            const uint64_t a_hi = d0 + 2 * kk;
+                            const uint64_t a_lo = a_hi + kA16;
+                            const uint64_t b_hi = a_hi + 2 * kA16;
+                            const uint64_t b_lo = b_hi + blo16;
+                            ptx::mma_tf32(d_tmem, a_hi, b_hi, id, kk ? 1u : first);
+                            ptx::mma_tf32(d_tmem, a_hi, b_lo, id, 1u);
+                            ptx::mma_tf32(d_tmem, a_lo, b_hi, id, 1u);
+                        }
+                    } else if constexpr (OPS == 2) {
+#pragma unroll
+                        for (int kk = 0; kk < kChunk / 8; ++kk) {  // 16 bf16 (32 bytes) per MMA
+                            const uint64_t a = d0 + 2 * kk;
+                            ptx::mma_bf16(d_tmem, a, a + kA16, id, kk ? 1u : first);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kChunk / 8; ++kk) {
+                            const uint64_t a = d0 + 2 * kk;
+                            ptx::mma_tf32(d_tmem, a, a + kA16, id, kk ? 1u : first);
+                        }
+                    }
+                    ptx::mma_commit(empty0 + 8 * stage);
+                    if (++stage == P.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            };
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++iter) {
                 const Tile T = decode(P, P.grp, tile);
                 const GroupDesc &G = P.grp[T.gi];
@@ -446,50 +520,68 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     break;
                 }
                 ptx::tc_fence_after();
-                for (int ci = 0; ok && ci < G.ncls; ++ci) {
-                    const ClassDesc &C = P.cls[G.cls[ci]];
-                    const uint32_t d_tmem = tmem_base + (uint32_t)acc * P.acc_stride + (uint32_t)ci * P.cout_pad;
-                    const TapRange tr = tile_taps(G, C, T.t, kTcTileM, P.Din);  // same taps as the producer
-                    const int nsteps = (tr.end - tr.begin) * P.kc;
-                    for (int s = 0; s < nsteps; ++s) {
-                        if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
-                        if constexpr (OPS == 0) {
-#pragma unroll
-                            for (int kk = 0; kk < kChunk / 8; ++kk) {  // 8 TF32 (32 bytes) per MMA
-                                const uint64_t a_hi = ptx::sdesc_k_swizzled(sb + kk * 32, kRowBytes);
-                                const uint64_t a_lo = ptx::sdesc_k_swizzled(sb + kABytes + kk * 32, kRowBytes);
-                                const uint64_t b_hi = ptx::sdesc_k_swizzled(sb + 2 * kABytes + kk * 32, kRowBytes);
-                                const uint64_t b_lo =
-                                    ptx::sdesc_k_swizzled(sb + 2 * kABytes + P.b_bytes + kk * 32, kRowBytes);
-                                // the class's first product overwrites the accumulator
-                                ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (s | kk) ? 1u : 0u);
-                                ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
-                                ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                const uint32_t acc_base = tmem_base + (uint32_t)acc * P.acc_stride;
+                if constexpr (MERGED) {
+                    // same walk as the producer; shared offsets come first, so a merged step
+                    // never meets one accumulator initialised and the other not
+                    const ClassDesc &C0 = P.cls[G.cls[0]];
+                    const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);
+                    const int nhw0 = C0.nt_h * C0.nt_w;
+                    const int a_begin = tr.begin / nhw0, a_end = (tr.end + nhw0 - 1) / nhw0;
+                    uint32_t ini = 0;  // bit c: class c's accumulator holds a product
+                    for (int a = a_begin; ok && a < a_end; ++a)
+                        for (int b = 0; ok && b < C0.nt_h; ++b)
+                            for (int m = 0; ok && m < G.nm; ++m) {
+                                const uint32_t mask = G.mmask[m];
+                                const uint32_t d_tmem = acc_base + (mask == 2u ? (uint32_t)P.cout_pad : 0u);
+                                mma_tap(d_tmem, mask == 3u ? idesc2 : idesc, (ini & mask) == 0u);
+                                ini |= mask;
                             }
-                        } else if constexpr (OPS == 2) {
-#pragma unroll
-                            for (int kk = 0; kk < kChunk / 8; ++kk) {  // 16 bf16 (32 bytes) per MMA
-                                const uint64_t a = ptx::sdesc_k_swizzled(sb + kk * 32, kRowBytes);
-                                const uint64_t b = ptx::sdesc_k_swizzled(sb + kABytes + kk * 32, kRowBytes);
-                                ptx::mma_bf16(d_tmem, a, b, idesc, (s | kk) ? 1u : 0u);
+                } else {
+                    // flat step loop per class (the issue rate of the MMA-bound shapes depends on it)
+                    for (int ci = 0; ok && ci < G.ncls; ++ci) {
+                        const ClassDesc &C = P.cls[G.cls[ci]];
+                        const uint32_t d_tmem = acc_base + (uint32_t)ci * P.cout_pad;
+                        const TapRange tr = tile_taps(G, C, T.t, kTcTileM, P.Din);  // same taps as the producer
+                        const int nsteps = (tr.end - tr.begin) * P.kc;
+                        for (int s = 0; s < nsteps; ++s) {
+                            if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
+                                ok = false;
+                                break;
                             }
-                        } else {
+                            ptx::tc_fence_after();
+                            const uint64_t d0 =
+                                ptx::sdesc_k_swizzled(smem_base + (uint32_t)stage * P.stage_bytes, kRowBytes);
+                            if constexpr (OPS == 0) {
 #pragma unroll
-                            for (int kk = 0; kk < kChunk / 8; ++kk) {
-                                const uint64_t a = ptx::sdesc_k_swizzled(sb + kk * 32, kRowBytes);
-                                const uint64_t b = ptx::sdesc_k_swizzled(sb + kABytes + kk * 32, kRowBytes);
-                                ptx::mma_tf32(d_tmem, a, b, idesc, (s | kk) ? 1u : 0u);
+                                for (int kk = 0; kk < kChunk / 8; ++kk) {
+                                    const uint64_t a_hi = d0 + 2 * kk;
+                                    const uint64_t a_lo = a_hi + kA16;
+                                    const uint64_t b_hi = a_hi + 2 * kA16;
+                                    const uint64_t b_lo = b_hi + b16;
+                                    // the class's first product overwrites the accumulator
+                                    ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, (s | kk) ? 1u : 0u);
+                                    ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+                                    ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                                }
+                            } else if constexpr (OPS == 2) {
+#pragma unroll
+                                for (int kk = 0; kk < kChunk / 8; ++kk) {
+                                    const uint64_t a = d0 + 2 * kk;
+                                    ptx::mma_bf16(d_tmem, a, a + kA16, idesc, (s | kk) ? 1u : 0u);
+                                }
+                            } else {
+#pragma unroll
+                                for (int kk = 0; kk < kChunk / 8; ++kk) {
+                                    const uint64_t a = d0 + 2 * kk;
+                                    ptx::mma_tf32(d_tmem, a, a + kA16, idesc, (s | kk) ? 1u : 0u);
+                                }
                             }
-                        }
-                        ptx::mma_commit(empty0 + 8 * stage);
-                        if (++stage == P.stages) {
-                            stage = 0;
-                            phase ^= 1u;
+                            ptx::mma_commit(empty0 + 8 * stage);
+                            if (++stage == P.stages) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
                         }
                     }
                 }
@@ -622,6 +714,40 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         }
                     }
                 };
+                if constexpr (KEEP == 2) {
+                    // w-parity pair: warp `half` of the lane quarter owns class `half`
+                    // with all its channels, so each row's softmax stays inside one
+                    // thread (no exchange between the warps)
+                    const int ci = half;
+                    constexpr int kAll = 2 * kSoftmaxKeepChunks;  // 16-channel chunks per class
+                    uint64_t e[kAll][8];
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int j0 = 0; j0 < kAll; j0 += 2) {
+                        float raw[2][16];
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj)
+                            if (j0 + jj < nchunks)
+                                ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + 16 * (j0 + jj),
+                                               raw[jj]);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj)
+                            if (j0 + jj < nchunks) {
+                                logits(16 * (j0 + jj), raw[jj], e[j0 + jj]);
+                                mx = fmaxf(mx, max8(e[j0 + jj]));
+                            }
+                    }
+                    float sum = 0.f;
+#pragma unroll
+                    for (int j = 0; j < kAll; ++j)
+                        if (j < nchunks) sum += exp8(e[j], mx);
+                    uint64_t A[4];
+                    sigmoid_coefficients(__frcp_rn(sum), A);
+#pragma unroll
+                    for (int j = 0; j < kAll; ++j)
+                        if (j < nchunks) finish(16 * j, ci, e[j], A);
+                } else {
                 // 1) this warp's chunks: maximum and sum of exponentials per class
                 constexpr int kKeep = kSoftmaxKeepChunks;
                 uint64_t e[KEEP ? kKeep : 1][2][8];
@@ -721,6 +847,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                             finish(16 * j, ci, e[0][ci], A);
                         }
                     }
+                }
                 }
             } else {
                 // identity / relu+groupnorm store / batchnorm partial sums, per owned chunk
@@ -902,7 +1029,6 @@ struct TcCache {
     int threads;
     size_t smem;
     int grid;
-    bool box;  // activation slices loaded as tiled boxes (see box_tiles)
     bool ready;
 };
 
@@ -910,38 +1036,30 @@ void tc_cache_free(void *c) { delete static_cast<TcCache *>(c); }
 
 // The kernel instance for the plan's epilogue, operand format OPS and (for
 // softmax) register-kept exponentials; threads receives its block size.
-template <int OPS, bool BOX>
+template <int OPS, bool MERGED>
 static void (*select_kernel(const convt3d_plan_s &p, int &threads))(const TcParams) {
     switch (p.d.epilogue) {
         case CONVT3D_EPI_IDENTITY:
             threads = EpiCfg<CONVT3D_EPI_IDENTITY>::threads;
-            return convt3d_tc_gemm<CONVT3D_EPI_IDENTITY, true, OPS, BOX>;
+            return convt3d_tc_gemm<CONVT3D_EPI_IDENTITY, 1, OPS, MERGED>;
         case CONVT3D_EPI_RELU_GROUPNORM:
             threads = EpiCfg<CONVT3D_EPI_RELU_GROUPNORM>::threads;
-            return convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM, true, OPS, BOX>;
+            return convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM, 1, OPS, MERGED>;
         case CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL:
             threads = EpiCfg<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL>::threads;
-            return convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL, true, OPS, BOX>;
+            return convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL, 1, OPS, MERGED>;
         case CONVT3D_EPI_SOFTMAX_SIGMOID:
             threads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
             // registers hold the exponentials when each warp owns at most
             // kSoftmaxKeepChunks 16-channel chunks
+            if (EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps == 8 && p.g.ss[2] == 2 &&
+                p.cout_pad <= 16 * 2 * kSoftmaxKeepChunks)
+                return convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2, OPS, MERGED>;
             return p.cout_pad <= 16 * kSoftmaxKeepChunks * (EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps / 4)
-                       ? convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, true, OPS, BOX>
-                       : convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, false, OPS, BOX>;
+                       ? convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 1, OPS, MERGED>
+                       : convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 0, OPS, MERGED>;
     }
     return nullptr;
-}
-
-// Tiles are whole boxes of every group's q-grid: Qw a power of two up to 128
-// and each d-plane of Qh * Qw positions a multiple of the 128-row tile.
-static bool box_tiles(const convt3d_plan_s &p) {
-    for (int i = 0; i < p.ngroups; ++i) {
-        const GroupDesc &G = p.grp[i];
-        if (G.vol == 0) continue;
-        if (G.Qw > kTcTileM || (G.Qw & (G.Qw - 1)) || (G.Qh * G.Qw) % kTcTileM) return false;
-    }
-    return true;
 }
 
 static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, const float *xs_lo,
@@ -984,10 +1102,9 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->tmem_cols = (uint32_t)round_pow2(2 * ncls_max * p.cout_pad);
         P->b_bytes = (uint32_t)p.cout_pad * kRowBytes;
         P->planes = p.planes;
-        P->stage_bytes = (uint32_t)p.planes * (kABytes + P->b_bytes);
-        tc.box = box_tiles(p);
+        P->stage_bytes = (uint32_t)p.planes * (kABytes + (p.merged ? 2u : 1u) * P->b_bytes);
         const int ops = p.planes == 2 ? 0 : (p.bf16 ? 2 : 1);
-        if (tc.box)
+        if (p.merged)
             tc.kern = ops == 0 ? select_kernel<0, true>(p, tc.threads)
                                : (ops == 1 ? select_kernel<1, true>(p, tc.threads) : select_kernel<2, true>(p, tc.threads));
         else
@@ -1025,22 +1142,7 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
                                 (cuuint64_t)p.cin_pad * eb * g.Win * g.Hin,
                                 (cuuint64_t)p.cin_pad * eb * g.Win * g.Hin * g.Din};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    if (tc.box) {
-        // one tiled map per plane, box {chunk, Qw, 128 / Qw, 1, 1}, copied into every class slot
-        int qw = 1;
-        for (int gi = 0; gi < p.ngroups; ++gi)
-            if (p.grp[gi].vol) qw = p.grp[gi].Qw;
-        const cuuint32_t abox[5] = {(cuuint32_t)P->chunk, (cuuint32_t)qw, (cuuint32_t)(kTcTileM / qw), 1, 1};
-        for (int plane = 0; plane < p.planes; ++plane) {
-            CUtensorMap m;
-            CUresult r = fn.tiled(&m, dt, 5, (void *)(plane ? xs_lo : xs_hi), gdim, gstr, abox, estr,
-                                  CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-            for (int c = 0; c < kMaxClasses; ++c) (plane ? P->a_lo[c] : P->a_hi[c]) = m;
-        }
-    }
-    for (int gi = 0; gi < p.ngroups && !tc.box; ++gi) {
+    for (int gi = 0; gi < p.ngroups; ++gi) {
         const GroupDesc &G = p.grp[gi];
         for (int ci = 0; ci < G.ncls; ++ci) {
             const int c = G.cls[ci];
