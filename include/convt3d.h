@@ -46,6 +46,7 @@
  *
  * Conventions for every entry point:
  *   - Layouts: x [N,Cin,Din,Hin,Win], y [N,Cout,Do,Ho,Wo] (BN+pool: [N,Cout,1,1,1]),
+ *     or channels-last x [N,Din,Hin,Win,Cin], y [N,Do,Ho,Wo,Cout] (desc.channels_last),
  *     w [Cin,Cout/G,kd,kh,kw] (PyTorch ConvTranspose3d), bias/gamma/beta [Cout];
  *     all fp32, contiguous, device memory, 16-byte aligned.
  *   - Ownership: the caller allocates and owns every device buffer (input,
@@ -131,6 +132,9 @@ typedef struct {
     int out_pads[3];
     int dilation[3];      /* >= 1 per dimension; 0 means 1 (also without per_dim) */
     int conv_groups;      /* grouped convolution, Cin % G == Cout % G == 0; 0 = 1 */
+    int channels_last;    /* non-zero: x is [N,Din,Hin,Win,Cin] and y [N,Do,Ho,Wo,Cout]
+                             in memory (NDHWC); shapes are still reported as
+                             [N,Cout,Do,Ho,Wo]; the pooled BN output is unchanged */
 } convt3d_desc_t;
 
 typedef struct convt3d_plan_s *convt3d_plan_t;

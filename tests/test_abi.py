@@ -45,7 +45,8 @@ def test_status_strings(lib):
 def make_desc(**kw):
     base = dict(N=2, Cin=8, Cout=16, Din=8, Hin=8, Win=8, k=3, stride=1, pad=0, out_pad=0, has_bias=0,
                 epilogue=0, groups=1, eps=1e-5, scale=1.0, precision=0, per_dim=0, kdims=(0, 0, 0),
-                strides=(0, 0, 0), pads=(0, 0, 0), out_pads=(0, 0, 0), dilation=(0, 0, 0), conv_groups=0)
+                strides=(0, 0, 0), pads=(0, 0, 0), out_pads=(0, 0, 0), dilation=(0, 0, 0), conv_groups=0,
+                channels_last=0)
     base.update(kw)
     return _lib.Desc(*[base[f] for f, _ in _lib.Desc._fields_])
 

@@ -30,12 +30,17 @@ def run_gpu(spec, inputs, precision, running=None, momentum=0.1):
     y = plan.new_output(dev)
     y.fill_(float("nan"))
     d = {k: (v.to(dev) if v is not None else None) for k, v in inputs.items()}
+    if spec.channels_last:  # same values, NDHWC memory order
+        d["x"] = d["x"].permute(0, 2, 3, 4, 1).contiguous()
     if running is not None:
         rm, rv = (t.to(dev).clone() for t in running)
         plan.set_running_stats(rm, rv, momentum)
     plan.pack_weights(d["w"], ws)
     plan.forward(d["x"], y, ws, d["bias"], d["gamma"], d["beta"])
     plan.check(ws)
+    if spec.channels_last and y.dim() == 5 and tuple(y.shape) != plan.out_shape:
+        y = y.permute(0, 4, 1, 2, 3)  # back to NCDHW for the comparison
+    y = y.contiguous()
     if running is not None:
         return y.cpu().numpy(), rm.cpu().numpy(), rv.cpu().numpy()
     return y.cpu().numpy()
@@ -327,3 +332,37 @@ def test_low_precision_full_size_workloads(spec, precision):
     n = spec.N - 1
     ref = run_oracle(spec.replace(N=1), E.sample_slice(rin, n, n + 1))
     assert_close(got[n:n + 1], ref, f"{spec.name}[n={n}]")
+
+
+# Channels-last x and y (NDHWC), every epilogue, both precisions and the
+# evaluation-mode BatchNorm; ragged channel counts take the scalar store path.
+CHANNELS_LAST = [
+    SMALL[1].replace(name="cl_gn_ragged", channels_last=True),
+    SMALL[2].replace(name="cl_gn_pad1_bias", channels_last=True),
+    SMALL[5].replace(name="cl_bn_small", channels_last=True),
+    SMALL[7].replace(name="cl_softmax_s2", channels_last=True),
+    SMALL[8].replace(name="cl_softmax_s2_odd", channels_last=True),
+    E.Spec("cl_identity_s2_k4_c36", N=2, Cin=36, Cout=36, D=3, H=5, W=6, k=4, stride=2, pad=1, bias=True,
+           channels_last=True, seed_index=50),
+    GENERAL[0].replace(name="cl_gen_kdims_strides", channels_last=True),
+    GENERAL[3].replace(name="cl_gen_mixed_softmax", channels_last=True),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("precision", PRECISIONS)
+@pytest.mark.parametrize("spec", CHANNELS_LAST, ids=lambda s: s.name)
+def test_channels_last(spec, precision):
+    inputs = E.make_inputs(spec)
+    assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("precision", PRECISIONS)
+def test_channels_last_eval_batchnorm(precision):
+    spec = EVAL_CASES[1].replace(name="cl_bn_eval", channels_last=True)
+    inputs = E.make_inputs(spec)
+    running = E.make_running_stats(spec)
+    got, _, _ = run_gpu(spec, inputs, precision, running)
+    ref, _, _ = run_oracle(spec, inputs, running)
+    assert_close(got, ref, spec.name)

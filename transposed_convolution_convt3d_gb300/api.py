@@ -35,10 +35,12 @@ def _triple(v):
 
 
 def make_desc(N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False, epilogue=EPI_IDENTITY,
-              groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1, conv_groups=1):
+              groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1, conv_groups=1,
+              channels_last=False):
     """A convt3d_desc_t.  k, stride, pad, out_pad and dilation are an int or
     (d, h, w); conv_groups is the convolution's group count (weight
-    [Cin, Cout/conv_groups, kd, kh, kw]); groups is GroupNorm's."""
+    [Cin, Cout/conv_groups, kd, kh, kw]); groups is GroupNorm's; channels_last
+    selects NDHWC x and y."""
     kk, ss, pp, oo, dd = (_triple(v) for v in (k, stride, pad, out_pad, dilation))
     per_dim = any(len(set(t)) > 1 for t in (kk, ss, pp, oo))
     d = _lib.Desc(N, Cin, Cout, D, H, W, kk[0], ss[0], pp[0], oo[0], int(bool(bias)), int(epilogue), int(groups),
@@ -47,6 +49,7 @@ def make_desc(N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False, 
     for a in range(3):
         d.kdims[a], d.strides[a], d.pads[a], d.out_pads[a], d.dilation[a] = kk[a], ss[a], pp[a], oo[a], dd[a]
     d.conv_groups = int(conv_groups)
+    d.channels_last = int(bool(channels_last))
     return d
 
 
@@ -55,16 +58,20 @@ class Plan:
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1,
-                 conv_groups=1):
+                 conv_groups=1, channels_last=False):
         self.lib = _lib.load()
+        self.channels_last = bool(channels_last)
         self.desc = make_desc(N, Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale,
-                              precision, dilation, conv_groups)
+                              precision, dilation, conv_groups, channels_last)
         h = ctypes.c_void_p()
         _lib.check(self.lib.convt3d_plan_create(ctypes.byref(self.desc), ctypes.byref(h)), self.lib)
         self.handle = h
         shp = (ctypes.c_int64 * 5)()
         _lib.check(self.lib.convt3d_output_shape(self.handle, shp), self.lib)
-        self.out_shape = tuple(int(v) for v in shp)
+        self.out_shape = tuple(int(v) for v in shp)  # logical [N, Cout, Do, Ho, Wo]
+        # memory shape of y: NDHWC when channels_last (the pooled [N, Cout, 1, 1, 1] is the same either way)
+        n_, c_, d_, h_, w_ = self.out_shape
+        self.out_alloc_shape = (n_, d_, h_, w_, c_) if self.channels_last else self.out_shape
         self.workspace_bytes = int(self.lib.convt3d_workspace_bytes(self.handle))
         inf = _lib.Info()
         _lib.check(self.lib.convt3d_plan_info(self.handle, ctypes.byref(inf)), self.lib)
@@ -75,7 +82,7 @@ class Plan:
     def from_spec(cls, spec, precision=PREC_3XTF32):
         return cls(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
                    spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, precision,
-                   spec.dilation, spec.conv_groups)
+                   spec.dilation, spec.conv_groups, spec.channels_last)
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -89,7 +96,7 @@ class Plan:
         return torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=device)
 
     def new_output(self, device="cuda"):
-        return torch.empty(self.out_shape, dtype=torch.float32, device=device)
+        return torch.empty(self.out_alloc_shape, dtype=torch.float32, device=device)
 
     @staticmethod
     def _dev(t, name):
@@ -108,8 +115,8 @@ class Plan:
     def forward(self, x, y, workspace, bias=None, gamma=None, beta=None, stream=None):
         for t, n in ((x, "x"), (y, "y"), (bias, "bias"), (gamma, "gamma"), (beta, "beta")):
             self._dev(t, n)
-        if tuple(y.shape) != self.out_shape and y.numel() != _numel(self.out_shape):
-            raise ValueError(f"y has shape {tuple(y.shape)}, expected {self.out_shape}")
+        if tuple(y.shape) not in (self.out_shape, self.out_alloc_shape) and y.numel() != _numel(self.out_shape):
+            raise ValueError(f"y has shape {tuple(y.shape)}, expected {self.out_alloc_shape}")
         _lib.check(self.lib.convt3d_forward(self.handle, _ptr(x), _ptr(bias), _ptr(gamma), _ptr(beta),
                                             _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
                    self.lib)
@@ -189,17 +196,18 @@ class HostPipeline:
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, chunks=4,
-                 device="cuda", dilation=1, conv_groups=1, copy_streams=1):
+                 device="cuda", dilation=1, conv_groups=1, copy_streams=1, channels_last=False):
         if epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) or N % chunks:
             chunks = 1
         self.chunks = chunks
         self.n_chunk = N // chunks
         args = (Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale, precision,
-                dilation, conv_groups)
+                dilation, conv_groups, channels_last)
         self.plan = Plan(self.n_chunk, *args)
-        self.full_shape = (N,) + self.plan.out_shape[1:]
+        self.full_shape = (N,) + self.plan.out_alloc_shape[1:]
         dev = torch.device(device)
-        self.x = torch.empty((N, Cin, D, H, W), dtype=torch.float32, device=dev)
+        self.x = torch.empty((N, D, H, W, Cin) if channels_last else (N, Cin, D, H, W), dtype=torch.float32,
+                             device=dev)
         self.y = torch.empty(self.full_shape, dtype=torch.float32, device=dev)
         self.w = torch.empty((Cin, Cout // conv_groups) + _triple(k), dtype=torch.float32, device=dev)
         self.vec = {name: torch.empty(Cout, dtype=torch.float32, device=dev) for name in ("bias", "gamma", "beta")}

@@ -45,6 +45,7 @@ struct BoxParams {
     const float *x;
     float *box;  // [N][kd*kh*kw][Cin]
     int Cin, D, H, W, Do, Ho, Wo;
+    int cl;      // channels-last x
     int kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw;  // kernel, stride, pad, dilation per dimension
 };
 
@@ -56,7 +57,9 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
     float *a1 = sm;                        // [kd][H][W]: sums along d
     float *a2 = sm + (size_t)P.kd * HW;    // [kd][kh][W]: then along h
     const int n = blockIdx.x / P.Cin, ci = blockIdx.x % P.Cin;
-    const float *xp = P.x + (size_t)blockIdx.x * P.D * HW;
+    // element (d, col) of this (n, ci) slab: NCDHW contiguous, or channels-last with stride Cin
+    const float *xp = P.cl ? P.x + (size_t)n * P.D * HW * P.Cin + ci : P.x + (size_t)blockIdx.x * P.D * HW;
+    const size_t es = P.cl ? (size_t)P.Cin : 1;
 
     int dlo[kMaxK], dhi[kMaxK];
 #pragma unroll
@@ -65,7 +68,7 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
         dlo[t] = iv.lo;
         dhi[t] = iv.hi;
     }
-    if (HW % 4 == 0) {
+    if (HW % 4 == 0 && !P.cl) {
         // 128-bit loads: the slab of (n, ci) starts on a 16-byte boundary when H*W % 4 == 0
         for (int c4 = threadIdx.x; c4 < HW / 4; c4 += blockDim.x) {
             float4 acc[kMaxK];
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
 #pragma unroll
             for (int t = 0; t < kMaxK; ++t) acc[t] = 0.f;
             for (int d = 0; d < P.D; ++d) {
-                const float v = __ldg(xp + (size_t)d * HW + col);
+                const float v = __ldg(xp + ((size_t)d * HW + col) * es);
 #pragma unroll
                 for (int t = 0; t < kMaxK; ++t)
                     if (d >= dlo[t] && d <= dhi[t]) acc[t] += v;
@@ -202,8 +205,8 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
                            cudaStream_t s) {
     const Geometry &g = p.g;
     BoxParams bp{x,        box,      g.Cin,    g.Din,    g.Hin,    g.Win,    g.Do,     g.Ho,     g.Wo,
-                 g.kk[0],  g.kk[1],  g.kk[2],  g.ss[0],  g.ss[1],  g.ss[2],  g.pp[0],  g.pp[1],  g.pp[2],
-                 g.dil[0], g.dil[1], g.dil[2]};
+                 p.cl,     g.kk[0],  g.kk[1],  g.kk[2],  g.ss[0],  g.ss[1],  g.ss[2],  g.pp[0],  g.pp[1],
+                 g.pp[2],  g.dil[0], g.dil[1], g.dil[2]};
     const size_t smem = bn_eval_smem_bytes(p);
     cudaError_t e = cudaFuncSetAttribute(boxsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -149,6 +149,7 @@ struct FfmaParams {
     float *y;
     double *partials;
     int N, Cin, cin_pad, Cout, cout_pad, Din, Hin, Win, Do, Ho, Wo, sd, sh, sw;
+    int64_t xcs, xps, ycs, yps;  // element strides of a channel and of a position within a sample (x, y)
     int epilogue, groups;
     float scale;
     int ngroups, tiles_per_sample;
@@ -164,6 +165,7 @@ struct convt3d_plan_s {
     convt3d::Geometry g;
     int tc;                 // 1: tensor-core path, 0: FFMA
     int planes;             // tensor-core operand planes: 2 = split TF32 (hi, lo), 1 = TF32 or BF16
+    int cl;                 // channels-last x and y (NDHWC)
     int merged;             // w-parity pairs share activation loads and MMAs (see GroupDesc::nm)
     int bf16;               // tensor-core operands in bf16 (kind::f16 MMA)
     int chunk;              // input channels per K step (one 128-byte operand row)

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
         const int ci = ci0 + lk;
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-            areg[r] = (sp[r] >= 0 && ci < P.Cin) ? __ldg(xn + (int64_t)ci * Sin + sp[r]) : 0.0f;
+            areg[r] = (sp[r] >= 0 && ci < P.Cin) ? __ldg(xn + (int64_t)ci * P.xcs + sp[r] * P.xps) : 0.0f;
         const float4 *wsrc = reinterpret_cast<const float4 *>(
             P.wpk + ((int64_t)(cl.tap_begin + j) * P.cin_pad + ci0) * cpad);
 #pragma unroll
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
     for (int idx = tid; idx < kBM * C; idx += kThreads) {
         const int m = idx % kBM, c = idx / kBM;
         const int off = rowoff[m];
-        if (off >= 0) yn[(int64_t)c * Sout + off] = E[m * es + c];
+        if (off >= 0) yn[(int64_t)c * P.ycs + off * P.yps] = E[m * es + c];
     }
 }
 
@@ -271,6 +271,11 @@ cudaError_t launch_ffma(const convt3d_plan_s &p, const float *x, const float *wp
     P.sd = p.g.ss[0];
     P.sh = p.g.ss[1];
     P.sw = p.g.ss[2];
+    const int64_t Sin = (int64_t)p.g.Din * p.g.Hin * p.g.Win, Sout = (int64_t)p.g.Do * p.g.Ho * p.g.Wo;
+    P.xcs = p.cl ? 1 : Sin;
+    P.xps = p.cl ? p.g.Cin : 1;
+    P.ycs = p.cl ? 1 : Sout;
+    P.yps = p.cl ? p.g.Cout : 1;
     P.epilogue = p.d.epilogue;
     P.groups = p.d.groups;
     P.scale = p.d.scale;

@@ -7,7 +7,7 @@
 //   tensor-core path: [tap][Cout_pad][Cin_pad] (K-major rows, Cin contiguous),
 //                     split into TF32 hi and lo planes;
 //   FFMA path:        [tap][Cin_pad][Cout_pad] fp32.
-// The tensor-core path also stages x from NCDHW into channels-last
+// The tensor-core path also stages x (NCDHW, or already channels-last) into channels-last
 // [N][D][H][W][Cin_pad] hi/lo planes (one TF32-rounded or bf16 plane for the
 // single-product precisions), the layout its TMA im2col loads read.
 #include <cuda_bf16.h>
@@ -112,6 +112,28 @@ __global__ void stage_input_kernel(const float *__restrict__ x, float *__restric
     }
 }
 
+// Channels-last input [N][D][H][W][Cin] -> the same rows padded to cin_pad
+// channels (hi/lo planes, or one TF32 / bf16 plane): no transpose, 8 rows x
+// 32 channels per block, coalesced on both sides.
+__global__ void stage_input_cl_kernel(const float *__restrict__ x, float *__restrict__ hi, float *__restrict__ lo,
+                                      int Cin, int cin_pad, int64_t rows, int bf16) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + threadIdx.y;
+    const int c = blockIdx.y * 32 + threadIdx.x;
+    if (r >= rows) return;
+    const float v = c < Cin ? __ldg(x + r * Cin + c) : 0.0f;
+    const int64_t o = r * cin_pad + c;
+    if (lo) {
+        float h, l;
+        split_tf32(v, h, l);
+        hi[o] = h;
+        lo[o] = l;
+    } else if (bf16) {
+        reinterpret_cast<__nv_bfloat16 *>(hi)[o] = __float2bfloat16_rn(v);
+    } else {
+        hi[o] = round_tf32(v);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *hi, float *lo, int kmajor,
@@ -129,6 +151,12 @@ cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *
 
 cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *hi, float *lo, cudaStream_t s) {
     const int64_t S = (int64_t)p.g.Din * p.g.Hin * p.g.Win;
+    if (p.cl) {
+        const int64_t rows = S * p.g.N;
+        dim3 grid((unsigned)((rows + 7) / 8), (unsigned)(p.cin_pad / 32));
+        stage_input_cl_kernel<<<grid, dim3(32, 8), 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, rows, p.bf16);
+        return cudaGetLastError();
+    }
     dim3 grid((unsigned)((S + 31) / 32), (unsigned)(p.cin_pad / 32), (unsigned)p.g.N);
     dim3 block(32, 8);
     stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S, p.bf16);

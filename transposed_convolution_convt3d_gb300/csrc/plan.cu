@@ -332,6 +332,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     }
     p->tc = desc->precision != CONVT3D_PREC_FFMA;
     p->planes = desc->precision == CONVT3D_PREC_3XTF32 ? 2 : (p->tc ? 1 : 0);
+    p->cl = desc->channels_last != 0;
     p->bf16 = desc->precision == CONVT3D_PREC_BF16;
     p->elem_bytes = p->bf16 ? 2 : 4;
     p->chunk = p->tc ? kTcRowBytes / p->elem_bytes : 8;

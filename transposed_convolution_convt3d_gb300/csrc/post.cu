@@ -178,6 +178,44 @@ __global__ void bn_finalize_kernel(const double *__restrict__ sums, const float 
     }
 }
 
+// Channels-last variant: the per-channel scale and shift of one sample sit in
+// shared memory; each thread rescales 4 consecutive elements of the sample's
+// [V][C] block (128-bit when C % 4 == 0).  grid: (blocks over V*C, N).
+__global__ void __launch_bounds__(kNormThreads) gn_normalize_cl_kernel(float *__restrict__ y,
+                                                                       const double *__restrict__ stats,
+                                                                       const float *__restrict__ gamma,
+                                                                       const float *__restrict__ beta, int C, int G,
+                                                                       int64_t V) {
+    __shared__ float sa[256], sb[256];
+    const int n = blockIdx.y;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        const int sg = n * G + c / (C / G);
+        const double rstd = stats[2 * sg + 1], mean = stats[2 * sg];
+        sa[c] = (float)(rstd * gamma[c]);
+        sb[c] = (float)(beta[c] - mean * rstd * gamma[c]);
+    }
+    __syncthreads();
+    float *yn = y + (int64_t)n * V * C;
+    const int64_t total = V * C;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x * 4;
+    for (int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; e < total; e += stride) {
+        if ((C & 3) == 0) {  // e % 4 == 0, so the 4 elements share a row and start 16-byte aligned
+            const int c = (int)(e % C);
+            float4 v = *reinterpret_cast<float4 *>(yn + e);
+            v.x = fmaf(v.x, sa[c], sb[c]);
+            v.y = fmaf(v.y, sa[c + 1], sb[c + 1]);
+            v.z = fmaf(v.z, sa[c + 2], sb[c + 2]);
+            v.w = fmaf(v.w, sa[c + 3], sb[c + 3]);
+            *reinterpret_cast<float4 *>(yn + e) = v;
+        } else {
+            for (int64_t i = e; i < e + 4 && i < total; ++i) {
+                const int c = (int)(i % C);
+                yn[i] = fmaf(yn[i], sa[c], sb[c]);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, double *stats, cudaStream_t s) {
@@ -192,6 +230,13 @@ cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, 
 cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, const float *gamma, const float *beta,
                                 float *y, cudaStream_t s) {
     const int64_t V = (int64_t)p.g.Do * p.g.Ho * p.g.Wo;
+    if (p.cl) {
+        const int64_t per_sample = V * p.g.Cout;
+        const int64_t want = (per_sample / 4 + kNormThreads - 1) / kNormThreads;
+        dim3 grid((unsigned)(want < 4096 ? (want > 0 ? want : 1) : 4096), (unsigned)p.g.N);
+        gn_normalize_cl_kernel<<<grid, kNormThreads, 0, s>>>(y, stats, gamma, beta, p.g.Cout, p.d.groups, V);
+        return cudaGetLastError();
+    }
     const int64_t per_block = (int64_t)kNormThreads * kNormVec * 4;  // floats per block
     const int planes = p.g.N * p.g.Cout;
     dim3 grid((unsigned)((V + per_block - 1) / per_block), (unsigned)(planes < 65535 ? planes : 65535));

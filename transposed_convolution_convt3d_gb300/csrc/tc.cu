@@ -102,6 +102,7 @@ struct TcParams {
     int stages;
     uint32_t stage_bytes, b_bytes;
     int planes;  // 2: split TF32 (A and B hi/lo), 1: single TF32 or BF16
+    int cl;      // channels-last output
     int bf16;    // operands in bf16 (kind::f16 MMA)
     int chunk;   // input channels per K step (one 128-byte row)
     uint32_t tmem_cols, acc_stride;
@@ -639,6 +640,33 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             // Stride-2 pairs write (even, odd) columns of one output row together.
             const bool pair_store = G.ncls == 2 && (P.Wo % 2 == 0);
             float *yn = P.y + (int64_t)T.n * C * V;
+            // 16 channels c0.. of output position `off` of this sample: NCDHW (one
+            // store per channel plane) or channels-last (contiguous, 16-byte stores
+            // when every row starts 16-byte aligned)
+            auto store_row16 = [&](float *yb, int off, int c0, const float (&o)[16]) {
+                if (P.cl) {
+                    float *dst = yb + (int64_t)off * C + c0;
+                    if (c0 + 16 <= C && (C & 3) == 0) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < C) dst[i] = o[i];
+                    }
+                } else {
+                    float *dst = yb + (int64_t)c0 * V + off;
+                    if (c0 + 16 <= C) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) dst[(int64_t)i * V] = o[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < C) dst[(int64_t)i * V] = o[i];
+                    }
+                }
+            };
             const uint32_t acc_col = (uint32_t)acc * P.acc_stride;
             // statistics: one partial row per (tile, lane quarter); the two warps of a
             // quarter fill disjoint slots of it
@@ -702,17 +730,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         q = ffma2(q, x2, A[0]);
                         unpack2(ffma2(e[k], q, half2), o[2 * k], o[2 * k + 1]);
                     }
-                    if (off[ci] >= 0) {
-                        float *dst = yn + (int64_t)c0 * V + off[ci];
-                        if (c0 + 16 <= C) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) dst[(int64_t)i * V] = o[i];
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (c0 + i < C) dst[(int64_t)i * V] = o[i];
-                        }
-                    }
+                    if (off[ci] >= 0) store_row16(yn, off[ci], c0, o);
                 };
                 if constexpr (KEEP == 2) {
                     // w-parity pair: warp `half` of the lane quarter owns class `half`
@@ -913,7 +931,10 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                             gs1 = gs2 = 0.f;
                         }
                     }
-                    if (pair_store) {
+                    if (P.cl) {
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
+                            if (off[ci] >= 0) store_row16(yn, off[ci], c0, v[ci]);
+                    } else if (pair_store) {
                         if (off[0] >= 0 && off[1] >= 0) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
@@ -1102,6 +1123,7 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->tmem_cols = (uint32_t)round_pow2(2 * ncls_max * p.cout_pad);
         P->b_bytes = (uint32_t)p.cout_pad * kRowBytes;
         P->planes = p.planes;
+        P->cl = p.cl;
         P->stage_bytes = (uint32_t)p.planes * (kABytes + (p.merged ? 2u : 1u) * P->b_bytes);
         const int ops = p.planes == 2 ? 0 : (p.bf16 ? 2 : 1);
         if (p.merged)

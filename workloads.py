@@ -52,6 +52,7 @@ class Spec:
     seed_index: int = 0
     dilation: object = 1     # int or (d, h, w); k, stride, pad, out_pad likewise
     conv_groups: int = 1
+    channels_last: bool = False  # x and y in NDHWC memory order (make_inputs still returns NCDHW x)
 
     @property
     def kdims(self):
