@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the CPU baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-chunks", type=int, default=4, help="sample chunks the end-to-end pipeline overlaps")
+    ap.add_argument("--io-bf16", action="store_true",
+                    help="x, w and y as bf16 tensors (requires --precision bf16)")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="streams per copy direction in the end-to-end pipeline")
     return ap.parse_args()
@@ -196,7 +198,7 @@ def cpu_oracle_sample(spec, inputs, target_s, max_samples=None):
     per-sample epilogues (for BatchNorm the first n samples form a smaller
     batch).  Returns (useful TFLOP/s, seconds, samples, cores)."""
     import oracle
-    f = lambda t: None if t is None else t.numpy()  # noqa: E731
+    f = lambda t: None if t is None else t.float().numpy()  # noqa: E731
     done, elapsed, n = 0, 0.0, 0
     limit = spec.N if max_samples is None else min(spec.N, max_samples)
     step = 1
@@ -267,7 +269,11 @@ def run_gpu(args, spec):
     dev = torch.device("cuda", local)
     prec = {"3xtf32": PREC_3XTF32, "tf32": PREC_TF32, "bf16": PREC_BF16, "ffma": PREC_FFMA}[args.precision]
 
+    if args.io_bf16:
+        spec = spec.replace(io_bf16=True)
     inputs = workloads.make_inputs(spec)
+    if args.io_bf16:
+        inputs["x"], inputs["w"] = inputs["x"].to(torch.bfloat16), inputs["w"].to(torch.bfloat16)
     d = {k: (v.to(dev) if v is not None else None) for k, v in inputs.items()}
     plan = Plan.from_spec(spec, precision=prec)
     info = plan.info
@@ -344,12 +350,13 @@ def run_gpu(args, spec):
         host = {k: (v.pin_memory() if v is not None else None) for k, v in inputs.items()}
         pipe = HostPipeline(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
                             spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, prec,
-                            chunks=args.e2e_chunks, device=dev, copy_streams=args.e2e_copy_streams)
+                            chunks=args.e2e_chunks, device=dev, copy_streams=args.e2e_copy_streams,
+                            io_bf16=args.io_bf16)
         if running is not None:
             pipe.set_running_stats(*running)
-        y_host = torch.empty(pipe.full_shape, dtype=torch.float32).pin_memory()
-        h2d = sum(v.numel() * 4 for v in host.values() if v is not None)
-        d2h = y_host.numel() * 4
+        y_host = torch.empty(pipe.full_shape, dtype=pipe.plan.io_dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = y_host.numel() * y_host.element_size()
         e2e_ms = []
         for i in range(args.e2e_steps + 1):
             flush.fill_(float(i))
@@ -414,7 +421,7 @@ def run_gpu(args, spec):
         "metric": "useful_tflops", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": spec.name, "precision": args.precision, "x": [spec.N, spec.Cin, spec.D, spec.H, spec.W],
+        "config": {"workload": spec.name, "precision": args.precision, "io": "bf16" if args.io_bf16 else "f32", "x": [spec.N, spec.Cin, spec.D, spec.H, spec.W],
                    "w": [spec.Cin, spec.Cout, spec.k, spec.k, spec.k], "stride": spec.stride, "pad": spec.pad,
                    "out_pad": spec.out_pad, "out": list(plan.out_shape), "epilogue": spec.epilogue,
                    "step": "pack_weights + forward (all kernels)", "l2": "flushed (256 MiB write) before each step",

@@ -48,7 +48,8 @@
  *   - Layouts: x [N,Cin,Din,Hin,Win], y [N,Cout,Do,Ho,Wo] (BN+pool: [N,Cout,1,1,1]),
  *     or channels-last x [N,Din,Hin,Win,Cin], y [N,Do,Ho,Wo,Cout] (desc.channels_last),
  *     w [Cin,Cout/G,kd,kh,kw] (PyTorch ConvTranspose3d), bias/gamma/beta [Cout];
- *     all fp32, contiguous, device memory, 16-byte aligned.
+ *     fp32 (x, w and y bf16 with desc.io_bf16), contiguous, device memory,
+ *     16-byte aligned.
  *   - Ownership: the caller allocates and owns every device buffer (input,
  *     output, workspace).  The library never allocates or frees device memory
  *     and never synchronises a stream except in convt3d_check and
@@ -135,6 +136,9 @@ typedef struct {
     int channels_last;    /* non-zero: x is [N,Din,Hin,Win,Cin] and y [N,Do,Ho,Wo,Cout]
                              in memory (NDHWC); shapes are still reported as
                              [N,Cout,Do,Ho,Wo]; the pooled BN output is unchanged */
+    int io_bf16;          /* non-zero: x, w and y are bf16 (2-byte) arrays; bias,
+                             gamma, beta and the running statistics stay fp32;
+                             requires precision CONVT3D_PREC_BF16                   */
 } convt3d_desc_t;
 
 typedef struct convt3d_plan_s *convt3d_plan_t;
@@ -182,7 +186,7 @@ size_t convt3d_workspace_bytes(convt3d_plan_t plan);
  * (3XTF32) or kept fp32 (FFMA).  Call whenever w changes; forward reads only
  * the packed copy.  Also clears the workspace status word.  Asynchronous on
  * `stream`. */
-convt3d_status_t convt3d_pack_weights(convt3d_plan_t plan, const float *w, void *workspace,
+convt3d_status_t convt3d_pack_weights(convt3d_plan_t plan, const void *w, void *workspace,
                                       size_t workspace_bytes, void *stream);
 
 /* One forward pass: y = epilogue(convT(x, w) + bias).  bias may be NULL when
@@ -190,8 +194,8 @@ convt3d_status_t convt3d_pack_weights(convt3d_plan_t plan, const float *w, void 
  * SCALE_BATCHNORM_AVGPOOL and ignored otherwise.  Uses the weights packed by
  * the last convt3d_pack_weights on the same workspace.  Asynchronous on
  * `stream`; y is complete when the stream reaches this point. */
-convt3d_status_t convt3d_forward(convt3d_plan_t plan, const float *x, const float *bias,
-                                 const float *gamma, const float *beta, float *y,
+convt3d_status_t convt3d_forward(convt3d_plan_t plan, const void *x, const float *bias,
+                                 const float *gamma, const float *beta, void *y,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* BatchNorm running statistics, device pointers to Cout floats each (page
@@ -232,9 +236,9 @@ convt3d_status_t convt3d_profile_read(convt3d_plan_t plan, float *gemm_ms);
  * All calls share the one array: calls whose GPU work may overlap (other
  * streams, other threads) race on it and must be serialised by the caller.
  * Arguments are as for convt3d_pack_weights and convt3d_forward. */
-convt3d_status_t convt3d_forward_static_workspace(convt3d_plan_t plan, const float *w, const float *x,
+convt3d_status_t convt3d_forward_static_workspace(convt3d_plan_t plan, const void *w, const void *x,
                                                   const float *bias, const float *gamma, const float *beta,
-                                                  float *y, void *stream);
+                                                  void *y, void *stream);
 
 /* Static text for a status code. */
 const char *convt3d_status_string(convt3d_status_t status);

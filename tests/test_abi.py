@@ -46,7 +46,7 @@ def make_desc(**kw):
     base = dict(N=2, Cin=8, Cout=16, Din=8, Hin=8, Win=8, k=3, stride=1, pad=0, out_pad=0, has_bias=0,
                 epilogue=0, groups=1, eps=1e-5, scale=1.0, precision=0, per_dim=0, kdims=(0, 0, 0),
                 strides=(0, 0, 0), pads=(0, 0, 0), out_pads=(0, 0, 0), dilation=(0, 0, 0), conv_groups=0,
-                channels_last=0)
+                channels_last=0, io_bf16=0)
     base.update(kw)
     return _lib.Desc(*[base[f] for f, _ in _lib.Desc._fields_])
 
@@ -74,6 +74,7 @@ def create(lib, **kw):
     (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 1, 3)), 2), (dict(per_dim=1, kdims=(3, 8, 3), strides=(1, 1, 1)), 2),
     (dict(stride=2, dilation=(2, 2, 2)), 2), (dict(dilation=(16, 1, 1)), 2),
     (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 1, 2), pads=(0, 0, 0), Cout=144), 2),
+    (dict(io_bf16=1), 2), (dict(io_bf16=1, precision=2), 2), (dict(io_bf16=1, precision=1), 2),
 ])
 def test_plan_validation(lib, kw, status):
     st, h = create(lib, **kw)

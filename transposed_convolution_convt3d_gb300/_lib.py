@@ -52,7 +52,7 @@ class Desc(ctypes.Structure):
         ("eps", ctypes.c_float), ("scale", ctypes.c_float), ("precision", ctypes.c_int),
         ("per_dim", ctypes.c_int), ("kdims", ctypes.c_int * 3), ("strides", ctypes.c_int * 3),
         ("pads", ctypes.c_int * 3), ("out_pads", ctypes.c_int * 3), ("dilation", ctypes.c_int * 3),
-        ("conv_groups", ctypes.c_int), ("channels_last", ctypes.c_int),
+        ("conv_groups", ctypes.c_int), ("channels_last", ctypes.c_int), ("io_bf16", ctypes.c_int),
     ]
 
 

@@ -36,7 +36,7 @@ def _triple(v):
 
 def make_desc(N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False, epilogue=EPI_IDENTITY,
               groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1, conv_groups=1,
-              channels_last=False):
+              channels_last=False, io_bf16=False):
     """A convt3d_desc_t.  k, stride, pad, out_pad and dilation are an int or
     (d, h, w); conv_groups is the convolution's group count (weight
     [Cin, Cout/conv_groups, kd, kh, kw]); groups is GroupNorm's; channels_last
@@ -50,6 +50,7 @@ def make_desc(N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False, 
         d.kdims[a], d.strides[a], d.pads[a], d.out_pads[a], d.dilation[a] = kk[a], ss[a], pp[a], oo[a], dd[a]
     d.conv_groups = int(conv_groups)
     d.channels_last = int(bool(channels_last))
+    d.io_bf16 = int(bool(io_bf16))
     return d
 
 
@@ -58,11 +59,12 @@ class Plan:
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1,
-                 conv_groups=1, channels_last=False):
+                 conv_groups=1, channels_last=False, io_bf16=False):
         self.lib = _lib.load()
         self.channels_last = bool(channels_last)
+        self.io_dtype = torch.bfloat16 if io_bf16 else torch.float32  # x, w and y
         self.desc = make_desc(N, Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale,
-                              precision, dilation, conv_groups, channels_last)
+                              precision, dilation, conv_groups, channels_last, io_bf16)
         h = ctypes.c_void_p()
         _lib.check(self.lib.convt3d_plan_create(ctypes.byref(self.desc), ctypes.byref(h)), self.lib)
         self.handle = h
@@ -82,7 +84,7 @@ class Plan:
     def from_spec(cls, spec, precision=PREC_3XTF32):
         return cls(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
                    spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, precision,
-                   spec.dilation, spec.conv_groups, spec.channels_last)
+                   spec.dilation, spec.conv_groups, spec.channels_last, spec.io_bf16)
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -96,24 +98,26 @@ class Plan:
         return torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=device)
 
     def new_output(self, device="cuda"):
-        return torch.empty(self.out_alloc_shape, dtype=torch.float32, device=device)
+        return torch.empty(self.out_alloc_shape, dtype=self.io_dtype, device=device)
 
     @staticmethod
-    def _dev(t, name):
+    def _dev(t, name, dtype=torch.float32):
         if t is None:
             return None
-        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
-            raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
+        if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous {dtype} CUDA tensor")
         return t
 
     # -- library calls ---------------------------------------------------
     def pack_weights(self, w, workspace, stream=None):
-        self._dev(w, "w")
+        self._dev(w, "w", self.io_dtype)
         _lib.check(self.lib.convt3d_pack_weights(self.handle, _ptr(w), _ptr(workspace),
                                                  workspace.numel(), _stream(stream)), self.lib)
 
     def forward(self, x, y, workspace, bias=None, gamma=None, beta=None, stream=None):
-        for t, n in ((x, "x"), (y, "y"), (bias, "bias"), (gamma, "gamma"), (beta, "beta")):
+        self._dev(x, "x", self.io_dtype)
+        self._dev(y, "y", self.io_dtype)
+        for t, n in ((bias, "bias"), (gamma, "gamma"), (beta, "beta")):
             self._dev(t, n)
         if tuple(y.shape) not in (self.out_shape, self.out_alloc_shape) and y.numel() != _numel(self.out_shape):
             raise ValueError(f"y has shape {tuple(y.shape)}, expected {self.out_alloc_shape}")
@@ -126,7 +130,9 @@ class Plan:
         """Pack w and run the forward in the library's built-in 32 MiB device
         workspace, for callers that may not allocate device memory.  Calls that
         overlap on the GPU share that workspace and race."""
-        for t, n in ((w, "w"), (x, "x"), (y, "y"), (bias, "bias"), (gamma, "gamma"), (beta, "beta")):
+        for t, n in ((w, "w"), (x, "x"), (y, "y")):
+            self._dev(t, n, self.io_dtype)
+        for t, n in ((bias, "bias"), (gamma, "gamma"), (beta, "beta")):
             self._dev(t, n)
         _lib.check(self.lib.convt3d_forward_static_workspace(self.handle, _ptr(w), _ptr(x), _ptr(bias),
                                                              _ptr(gamma), _ptr(beta), _ptr(y), _stream(stream)),
@@ -196,20 +202,20 @@ class HostPipeline:
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, chunks=4,
-                 device="cuda", dilation=1, conv_groups=1, copy_streams=1, channels_last=False):
+                 device="cuda", dilation=1, conv_groups=1, copy_streams=1, channels_last=False, io_bf16=False):
         if epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) or N % chunks:
             chunks = 1
         self.chunks = chunks
         self.n_chunk = N // chunks
         args = (Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale, precision,
-                dilation, conv_groups, channels_last)
+                dilation, conv_groups, channels_last, io_bf16)
         self.plan = Plan(self.n_chunk, *args)
+        dt = self.plan.io_dtype
         self.full_shape = (N,) + self.plan.out_alloc_shape[1:]
         dev = torch.device(device)
-        self.x = torch.empty((N, D, H, W, Cin) if channels_last else (N, Cin, D, H, W), dtype=torch.float32,
-                             device=dev)
-        self.y = torch.empty(self.full_shape, dtype=torch.float32, device=dev)
-        self.w = torch.empty((Cin, Cout // conv_groups) + _triple(k), dtype=torch.float32, device=dev)
+        self.x = torch.empty((N, D, H, W, Cin) if channels_last else (N, Cin, D, H, W), dtype=dt, device=dev)
+        self.y = torch.empty(self.full_shape, dtype=dt, device=dev)
+        self.w = torch.empty((Cin, Cout // conv_groups) + _triple(k), dtype=dt, device=dev)
         self.vec = {name: torch.empty(Cout, dtype=torch.float32, device=dev) for name in ("bias", "gamma", "beta")}
         self.ws = self.plan.new_workspace(dev)
         # each chunk's copies are split over `copy_streams` streams per direction, so

@@ -46,6 +46,7 @@ struct BoxParams {
     float *box;  // [N][kd*kh*kw][Cin]
     int Cin, D, H, W, Do, Ho, Wo;
     int cl;      // channels-last x
+    int x16;     // x is a bf16 array
     int kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw;  // kernel, stride, pad, dilation per dimension
 };
 
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
         dlo[t] = iv.lo;
         dhi[t] = iv.hi;
     }
-    if (HW % 4 == 0 && !P.cl) {
+    if (HW % 4 == 0 && !P.cl && !P.x16) {
         // 128-bit loads: the slab of (n, ci) starts on a 16-byte boundary when H*W % 4 == 0
         for (int c4 = threadIdx.x; c4 < HW / 4; c4 += blockDim.x) {
             float4 acc[kMaxK];
@@ -96,7 +97,9 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
 #pragma unroll
             for (int t = 0; t < kMaxK; ++t) acc[t] = 0.f;
             for (int d = 0; d < P.D; ++d) {
-                const float v = __ldg(xp + ((size_t)d * HW + col) * es);
+                const size_t xi = ((size_t)d * HW + col) * es;
+                const float v = P.x16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.x)[(xp - P.x) + xi])
+                                      : __ldg(xp + xi);
 #pragma unroll
                 for (int t = 0; t < kMaxK; ++t)
                     if (d >= dlo[t] && d <= dhi[t]) acc[t] += v;
@@ -136,7 +139,7 @@ struct OutParams {
     const float *w_a, *w_b;  // tensor-core layout: TF32 hi/lo planes [tap][cout_pad][cin_pad]; FFMA: [tap][cin_pad][cout_pad]
     const float *bias, *gamma, *beta, *rmean, *rvar;
     float *y;
-    int N, Cin, Cout, cin_pad, cout_pad, ntaps, k3, kmajor, wbf16;
+    int N, Cin, Cout, cin_pad, cout_pad, ntaps, k3, kmajor, wbf16, y16;
     double inv_vol, scale, eps;
 };
 
@@ -188,8 +191,12 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
         for (int i = 0; i < (int)(blockDim.x >> 5); ++i) S += (double)red[q][i];
         const double mean_y = S * P.inv_vol + (P.bias ? (double)P.bias[c] : 0.0);
         const double rstd = 1.0 / sqrt((double)P.rvar[c] + P.eps);
-        P.y[(size_t)(n0 + q) * P.Cout + c] =
+        const float out =
             (float)((double)P.gamma[c] * (P.scale * mean_y - (double)P.rmean[c]) * rstd + (double)P.beta[c]);
+        if (P.y16)
+            reinterpret_cast<__nv_bfloat16 *>(P.y)[(size_t)(n0 + q) * P.Cout + c] = __float2bfloat16_rn(out);
+        else
+            P.y[(size_t)(n0 + q) * P.Cout + c] = out;
     }
 }
 
@@ -205,8 +212,8 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
                            cudaStream_t s) {
     const Geometry &g = p.g;
     BoxParams bp{x,        box,      g.Cin,    g.Din,    g.Hin,    g.Win,    g.Do,     g.Ho,     g.Wo,
-                 p.cl,     g.kk[0],  g.kk[1],  g.kk[2],  g.ss[0],  g.ss[1],  g.ss[2],  g.pp[0],  g.pp[1],
-                 g.pp[2],  g.dil[0], g.dil[1], g.dil[2]};
+                 p.cl,     p.io16,   g.kk[0],  g.kk[1],  g.kk[2],  g.ss[0],  g.ss[1],  g.ss[2],  g.pp[0],
+                 g.pp[1],  g.pp[2],  g.dil[0], g.dil[1], g.dil[2]};
     const size_t smem = bn_eval_smem_bytes(p);
     cudaError_t e = cudaFuncSetAttribute(boxsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -235,6 +242,7 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
     op.k3 = g.kvol;
     op.kmajor = p.tc;
     op.wbf16 = p.bf16;
+    op.y16 = p.io16;
     op.inv_vol = 1.0 / ((double)g.Do * g.Ho * g.Wo);
     op.scale = (double)p.d.scale;
     op.eps = (double)p.d.eps;

@@ -166,6 +166,7 @@ struct convt3d_plan_s {
     int tc;                 // 1: tensor-core path, 0: FFMA
     int planes;             // tensor-core operand planes: 2 = split TF32 (hi, lo), 1 = TF32 or BF16
     int cl;                 // channels-last x and y (NDHWC)
+    int io16;               // x, w and y are bf16 arrays (the float pointers below alias them)
     int merged;             // w-parity pairs share activation loads and MMAs (see GroupDesc::nm)
     int bf16;               // tensor-core operands in bf16 (kind::f16 MMA)
     int chunk;              // input channels per K step (one 128-byte operand row)

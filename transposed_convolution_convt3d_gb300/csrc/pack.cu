@@ -42,7 +42,7 @@ struct TapIndex {
 __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restrict__ hi,
                                     float *__restrict__ lo, int Cin, int Cout, int k3, int ntaps,
                                     int cin_pad, int cout_pad, int kmajor, int mode, int cin_g, int cout_g,
-                                    const __grid_constant__ TapIndex taps) {
+                                    int w16, const __grid_constant__ TapIndex taps) {
     const int64_t total = (int64_t)ntaps * cin_pad * cout_pad;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -57,8 +57,10 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
             j = (int)(i / ((int64_t)cin_pad * cout_pad));
         }
         float v = 0.0f;
-        if (ci < Cin && co < Cout && ci / cin_g == co / cout_g)
-            v = w[((int64_t)ci * cout_g + co % cout_g) * k3 + taps.widx[j]];
+        if (ci < Cin && co < Cout && ci / cin_g == co / cout_g) {
+            const int64_t src = ((int64_t)ci * cout_g + co % cout_g) * k3 + taps.widx[j];
+            v = w16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(w)[src]) : w[src];
+        }
         if (lo) {
             float h, l;
             split_tf32(v, h, l);
@@ -76,18 +78,21 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
 // 32 channels per block through shared memory; both the global read (along
 // positions) and the write (along channels) are 128-byte rows.
 __global__ void stage_input_kernel(const float *__restrict__ x, float *__restrict__ hi,
-                                   float *__restrict__ lo, int Cin, int cin_pad, int64_t S, int bf16) {
+                                   float *__restrict__ lo, int Cin, int cin_pad, int64_t S, int bf16, int x16) {
     __shared__ float tile[32][33];
     const int n = blockIdx.z;
     const int c0 = blockIdx.y * 32;
     const int64_t s0 = (int64_t)blockIdx.x * 32;
     const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-    const float *xn = x + (int64_t)n * Cin * S;
+    const int64_t xb = (int64_t)n * Cin * S;
 #pragma unroll
     for (int j = 0; j < 32; j += 8) {
         const int c = c0 + ty + j;
         const int64_t s = s0 + tx;
-        tile[ty + j][tx] = (c < Cin && s < S) ? xn[(int64_t)c * S + s] : 0.0f;
+        const int64_t i = xb + (int64_t)c * S + s;
+        tile[ty + j][tx] = (c < Cin && s < S)
+                               ? (x16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[i]) : x[i])
+                               : 0.0f;
     }
     __syncthreads();
     float *hn = hi + (int64_t)n * S * cin_pad;
@@ -116,11 +121,13 @@ __global__ void stage_input_kernel(const float *__restrict__ x, float *__restric
 // channels (hi/lo planes, or one TF32 / bf16 plane): no transpose, 8 rows x
 // 32 channels per block, coalesced on both sides.
 __global__ void stage_input_cl_kernel(const float *__restrict__ x, float *__restrict__ hi, float *__restrict__ lo,
-                                      int Cin, int cin_pad, int64_t rows, int bf16) {
+                                      int Cin, int cin_pad, int64_t rows, int bf16, int x16) {
     const int64_t r = (int64_t)blockIdx.x * 8 + threadIdx.y;
     const int c = blockIdx.y * 32 + threadIdx.x;
     if (r >= rows) return;
-    const float v = c < Cin ? __ldg(x + r * Cin + c) : 0.0f;
+    const float v = c >= Cin ? 0.0f
+                    : (x16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[r * Cin + c])
+                           : __ldg(x + r * Cin + c));
     const int64_t o = r * cin_pad + c;
     if (lo) {
         float h, l;
@@ -145,7 +152,7 @@ cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *
     const int blocks = (int)((total + threads - 1) / threads < 4096 ? (total + threads - 1) / threads : 4096);
     pack_weights_kernel<<<blocks, threads, 0, s>>>(w, hi, lo, p.g.Cin, p.g.Cout, p.g.kvol, p.g.ntaps, p.cin_pad,
                                                    p.cout_pad, kmajor, p.bf16 ? 2 : (p.planes == 1 ? 1 : 0),
-                                                   p.g.Cin / p.g.G, p.g.Cout / p.g.G, t);
+                                                   p.g.Cin / p.g.G, p.g.Cout / p.g.G, p.io16, t);
     return cudaGetLastError();
 }
 
@@ -154,12 +161,12 @@ cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *h
     if (p.cl) {
         const int64_t rows = S * p.g.N;
         dim3 grid((unsigned)((rows + 7) / 8), (unsigned)(p.cin_pad / 32));
-        stage_input_cl_kernel<<<grid, dim3(32, 8), 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, rows, p.bf16);
+        stage_input_cl_kernel<<<grid, dim3(32, 8), 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, rows, p.bf16, p.io16);
         return cudaGetLastError();
     }
     dim3 grid((unsigned)((S + 31) / 32), (unsigned)(p.cin_pad / 32), (unsigned)p.g.N);
     dim3 block(32, 8);
-    stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S, p.bf16);
+    stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S, p.bf16, p.io16);
     return cudaGetLastError();
 }
 

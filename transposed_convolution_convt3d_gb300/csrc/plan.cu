@@ -238,6 +238,8 @@ convt3d_status_t validate(const convt3d_desc_t &d) {
         return fail(CONVT3D_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (bn_any && !isfinite(d.scale)) return fail(CONVT3D_ERR_INVALID_ARG, "scale must be finite");
     // Limits of this build (valid operations it does not run).
+    if (d.io_bf16 && d.precision != CONVT3D_PREC_BF16)
+        return fail(CONVT3D_ERR_UNSUPPORTED, "bf16 tensors need precision CONVT3D_PREC_BF16");
     for (int a = 0; a < 3; ++a) {
         if (sh.ss[a] > 2) return fail(CONVT3D_ERR_UNSUPPORTED, "stride > 2");
         if (sh.kk[a] > 7) return fail(CONVT3D_ERR_UNSUPPORTED, "k > 7");
@@ -333,6 +335,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     p->tc = desc->precision != CONVT3D_PREC_FFMA;
     p->planes = desc->precision == CONVT3D_PREC_3XTF32 ? 2 : (p->tc ? 1 : 0);
     p->cl = desc->channels_last != 0;
+    p->io16 = desc->io_bf16 != 0;
     p->bf16 = desc->precision == CONVT3D_PREC_BF16;
     p->elem_bytes = p->bf16 ? 2 : 4;
     p->chunk = p->tc ? kTcRowBytes / p->elem_bytes : 8;
@@ -480,9 +483,10 @@ static convt3d_status_t check_ws(convt3d_plan_t p, void *ws, size_t bytes) {
     return CONVT3D_OK;
 }
 
-convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const float *w, void *ws, size_t ws_bytes,
+convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const void *wv, void *ws, size_t ws_bytes,
                                       void *stream) {
     g_last_error[0] = 0;
+    const float *w = static_cast<const float *>(wv);  // bf16 data when io_bf16: the kernels reinterpret it
     if (!p || !w) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan or weight");
     if ((uintptr_t)w % 16) return fail(CONVT3D_ERR_INVALID_ARG, "w must be 16-byte aligned");
     convt3d_status_t st = check_ws(p, ws, ws_bytes);
@@ -498,9 +502,12 @@ convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const float *w, void *ws
     return CONVT3D_OK;
 }
 
-convt3d_status_t convt3d_forward(convt3d_plan_t p, const float *x, const float *bias, const float *gamma,
-                                 const float *beta, float *y, void *ws, size_t ws_bytes, void *stream) {
+convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *bias, const float *gamma,
+                                 const float *beta, void *yv, void *ws, size_t ws_bytes, void *stream) {
     g_last_error[0] = 0;
+    // bf16 data when io_bf16: the kernels reinterpret these pointers
+    const float *x = static_cast<const float *>(xv);
+    float *y = static_cast<float *>(yv);
     if (!p || !x || !y) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan, x or y");
     const convt3d_desc_t &d = p->d;
     if (d.has_bias && !bias) return fail(CONVT3D_ERR_INVALID_ARG, "has_bias set but bias is NULL");

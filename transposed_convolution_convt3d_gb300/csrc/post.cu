@@ -15,6 +15,8 @@
 // gamma * (S[n,c]/V - mean) * rstd + beta with S the per-sample spatial sum,
 // the algebra the page derives for folding the average pool into the
 // normalisation.
+#include <cuda_bf16.h>
+
 #include "convt3d_internal.h"
 
 namespace convt3d {
@@ -154,7 +156,7 @@ __global__ void bn_reduce_kernel(const double *__restrict__ partials, double *__
 __global__ void bn_finalize_kernel(const double *__restrict__ sums, const float *__restrict__ gamma,
                                    const float *__restrict__ beta, float *__restrict__ y, int N, int C, double V,
                                    double eps, float *__restrict__ rmean, float *__restrict__ rvar,
-                                   double momentum) {
+                                   double momentum, int y16) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= C) return;
     double S = 0.0, Q = 0.0;
@@ -169,7 +171,11 @@ __global__ void bn_finalize_kernel(const double *__restrict__ sums, const float 
     const double rstd = 1.0 / sqrt(var + eps);
     for (int n = 0; n < N; ++n) {
         const double Sn = sums[((int64_t)n * C + c) * 2];
-        y[(int64_t)n * C + c] = (float)((double)gamma[c] * (Sn / V - mean) * rstd + (double)beta[c]);
+        const float out = (float)((double)gamma[c] * (Sn / V - mean) * rstd + (double)beta[c]);
+        if (y16)
+            reinterpret_cast<__nv_bfloat16 *>(y)[(int64_t)n * C + c] = __float2bfloat16_rn(out);
+        else
+            y[(int64_t)n * C + c] = out;
     }
     if (rmean && rvar) {
         const double unbiased = cnt > 1.0 ? var * cnt / (cnt - 1.0) : 0.0;
@@ -216,6 +222,74 @@ __global__ void __launch_bounds__(kNormThreads) gn_normalize_cl_kernel(float *__
     }
 }
 
+// bf16 output, NCDHW: one (n, c) plane per blockIdx.y, pairs of elements
+// (4-byte bf16x2 loads and stores) along the plane; an odd plane length leaves
+// one last element for the x = 0 block.
+__global__ void __launch_bounds__(kNormThreads) gn_normalize_bf16_kernel(__nv_bfloat16 *__restrict__ y,
+                                                                         const double *__restrict__ stats,
+                                                                         const float *__restrict__ gamma,
+                                                                         const float *__restrict__ beta, int C, int G,
+                                                                         int64_t V, int planes) {
+    for (int plane = blockIdx.y; plane < planes; plane += gridDim.y) {
+        const int c = plane % C, n = plane / C;
+        const int sg = n * G + c / (C / G);
+        const double rstd = stats[2 * sg + 1], mean = stats[2 * sg];
+        const float a = (float)(rstd * gamma[c]);
+        const float b = (float)(beta[c] - mean * rstd * gamma[c]);
+        __nv_bfloat16 *yp = y + (int64_t)plane * V;
+        const bool even_base = ((int64_t)plane * V) % 2 == 0;  // 4-byte alignment of the pairs
+        const int64_t first = even_base ? 0 : 1;
+        if (!even_base && blockIdx.x == 0 && threadIdx.x == 0)
+            yp[0] = __float2bfloat16_rn(fmaf(__bfloat162float(yp[0]), a, b));
+        const int64_t npairs = (V - first) / 2;
+        __nv_bfloat162 *y2 = reinterpret_cast<__nv_bfloat162 *>(yp + first);
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < npairs;
+             i += (int64_t)gridDim.x * blockDim.x) {
+            const float2 v = __bfloat1622float2(y2[i]);
+            y2[i] = __floats2bfloat162_rn(fmaf(v.x, a, b), fmaf(v.y, a, b));
+        }
+        const int64_t last = first + 2 * npairs;
+        if (last < V && blockIdx.x == 0 && threadIdx.x == 0)
+            yp[last] = __float2bfloat16_rn(fmaf(__bfloat162float(yp[last]), a, b));
+    }
+}
+
+// bf16 output, channels-last: per-channel scale and shift of one sample in
+// shared memory; each thread rescales element pairs (c, c+1) of the sample's
+// [V][C] block, channel by invariant-divisor division (C even), else singly.
+__global__ void __launch_bounds__(kNormThreads) gn_normalize_bf16_cl_kernel(__nv_bfloat16 *__restrict__ y,
+                                                                            const double *__restrict__ stats,
+                                                                            const float *__restrict__ gamma,
+                                                                            const float *__restrict__ beta, int C,
+                                                                            int G, int64_t V, FastDiv divc) {
+    __shared__ float sa[256], sb[256];
+    const int n = blockIdx.y;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        const int sg = n * G + c / (C / G);
+        const double rstd = stats[2 * sg + 1], mean = stats[2 * sg];
+        sa[c] = (float)(rstd * gamma[c]);
+        sb[c] = (float)(beta[c] - mean * rstd * gamma[c]);
+    }
+    __syncthreads();
+    __nv_bfloat16 *yn = y + (int64_t)n * V * C;
+    const uint32_t total = (uint32_t)(V * C);  // < 2^31 elements per sample
+    const uint32_t stride = gridDim.x * blockDim.x;
+    if ((C & 1) == 0) {
+        __nv_bfloat162 *y2 = reinterpret_cast<__nv_bfloat162 *>(yn);
+        for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total / 2; i += stride) {
+            const uint32_t e = 2 * i;
+            const int c = (int)(e - fastdiv(e, divc) * (uint32_t)C);
+            const float2 v = __bfloat1622float2(y2[i]);
+            y2[i] = __floats2bfloat162_rn(fmaf(v.x, sa[c], sb[c]), fmaf(v.y, sa[c + 1], sb[c + 1]));
+        }
+    } else {
+        for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
+            const int c = (int)(e - fastdiv(e, divc) * (uint32_t)C);
+            yn[e] = __float2bfloat16_rn(fmaf(__bfloat162float(yn[e]), sa[c], sb[c]));
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, double *stats, cudaStream_t s) {
@@ -230,6 +304,22 @@ cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, 
 cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, const float *gamma, const float *beta,
                                 float *y, cudaStream_t s) {
     const int64_t V = (int64_t)p.g.Do * p.g.Ho * p.g.Wo;
+    if (p.io16) {
+        __nv_bfloat16 *yh = reinterpret_cast<__nv_bfloat16 *>(y);
+        if (p.cl) {
+            const int64_t want = (V * p.g.Cout / 2 + 8 * kNormThreads - 1) / (8 * kNormThreads);
+            dim3 grid((unsigned)(want < 4096 ? (want > 0 ? want : 1) : 4096), (unsigned)p.g.N);
+            gn_normalize_bf16_cl_kernel<<<grid, kNormThreads, 0, s>>>(yh, stats, gamma, beta, p.g.Cout, p.d.groups, V,
+                                                                       make_fastdiv((uint32_t)p.g.Cout));
+        } else {
+            const int planes = p.g.N * p.g.Cout;
+            const int64_t want = (V / 2 + 8 * kNormThreads - 1) / (8 * kNormThreads);  // ~8 pairs per thread
+            dim3 grid((unsigned)(want < 1024 ? (want > 0 ? want : 1) : 1024), (unsigned)(planes < 65535 ? planes : 65535));
+            gn_normalize_bf16_kernel<<<grid, kNormThreads, 0, s>>>(yh, stats, gamma, beta, p.g.Cout, p.d.groups, V,
+                                                                    planes);
+        }
+        return cudaGetLastError();
+    }
     if (p.cl) {
         const int64_t per_sample = V * p.g.Cout;
         const int64_t want = (per_sample / 4 + kNormThreads - 1) / kNormThreads;
@@ -253,7 +343,7 @@ cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, 
     if (e != cudaSuccess) return e;
     const double V = (double)p.g.Do * p.g.Ho * p.g.Wo;
     bn_finalize_kernel<<<(C + 127) / 128, 128, 0, s>>>(sums, gamma, beta, y, N, C, V, (double)p.d.eps, p.run_mean,
-                                                        p.run_var, (double)p.momentum);
+                                                        p.run_var, (double)p.momentum, p.io16);
     return cudaGetLastError();
 }
 

@@ -29,9 +29,9 @@ void *g_device_ptr[kMaxDevices];  // device address of g_static_workspace, per d
 
 }  // namespace
 
-extern "C" convt3d_status_t convt3d_forward_static_workspace(convt3d_plan_t plan, const float *w, const float *x,
+extern "C" convt3d_status_t convt3d_forward_static_workspace(convt3d_plan_t plan, const void *w, const void *x,
                                                              const float *bias, const float *gamma,
-                                                             const float *beta, float *y, void *stream) {
+                                                             const float *beta, void *y, void *stream) {
     if (!plan || !w || !x || !y) {
         convt3d::report_error("NULL plan, w, x or y");
         return CONVT3D_ERR_INVALID_ARG;

@@ -32,6 +32,8 @@
 
 #include <new>
 
+#include <cuda_bf16.h>
+
 #include "convt3d_internal.h"
 #include "ptx.cuh"
 
@@ -103,6 +105,7 @@ struct TcParams {
     uint32_t stage_bytes, b_bytes;
     int planes;  // 2: split TF32 (A and B hi/lo), 1: single TF32 or BF16
     int cl;      // channels-last output
+    int io16;    // y is a bf16 array
     int bf16;    // operands in bf16 (kind::f16 MMA)
     int chunk;   // input channels per K step (one 128-byte row)
     uint32_t tmem_cols, acc_stride;
@@ -643,7 +646,46 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             // 16 channels c0.. of output position `off` of this sample: NCDHW (one
             // store per channel plane) or channels-last (contiguous, 16-byte stores
             // when every row starts 16-byte aligned)
+            const bool plain_out = !P.io16 && !P.cl;  // NCDHW fp32, the common case, tested first
             auto store_row16 = [&](float *yb, int off, int c0, const float (&o)[16]) {
+                if (plain_out) {
+                    float *dst = yb + (int64_t)c0 * V + off;
+                    if (c0 + 16 <= C) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) dst[(int64_t)i * V] = o[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < C) dst[(int64_t)i * V] = o[i];
+                    }
+                    return;
+                }
+                if (P.io16) {  // bf16 output: same element positions, 2-byte values
+                    __nv_bfloat16 *yh = reinterpret_cast<__nv_bfloat16 *>(P.y) + (int64_t)T.n * C * V;
+                    if (P.cl) {
+                        __nv_bfloat16 *dst = yh + (int64_t)off * C + c0;
+                        if (c0 + 16 <= C && (C & 7) == 0) {  // two 16-byte stores of 8 bf16
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+                                w[i] = *reinterpret_cast<const uint32_t *>(&h);
+                            }
+                            reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                            reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (c0 + i < C) dst[i] = __float2bfloat16_rn(o[i]);
+                        }
+                    } else {
+                        __nv_bfloat16 *dst = yh + (int64_t)c0 * V + off;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < C) dst[(int64_t)i * V] = __float2bfloat16_rn(o[i]);
+                    }
+                    return;
+                }
                 if (P.cl) {
                     float *dst = yb + (int64_t)off * C + c0;
                     if (c0 + 16 <= C && (C & 3) == 0) {
@@ -931,7 +973,16 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                             gs1 = gs2 = 0.f;
                         }
                     }
-                    if (P.cl) {
+                    if (P.io16 && !P.cl && pair_store) {  // bf16 NCDHW: (even, odd) outputs as one bf16x2
+                        if (off[0] >= 0 && off[1] >= 0) {
+                            __nv_bfloat16 *yh = reinterpret_cast<__nv_bfloat16 *>(P.y) + (int64_t)T.n * C * V;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (c0 + i < C)
+                                    *reinterpret_cast<__nv_bfloat162 *>(yh + (int64_t)(c0 + i) * V + off[0]) =
+                                        __floats2bfloat162_rn(v[0][i], v[1][i]);
+                        }
+                    } else if (P.cl || P.io16) {
                         _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
                             if (off[ci] >= 0) store_row16(yn, off[ci], c0, v[ci]);
                     } else if (pair_store) {
@@ -1124,6 +1175,7 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->b_bytes = (uint32_t)p.cout_pad * kRowBytes;
         P->planes = p.planes;
         P->cl = p.cl;
+        P->io16 = p.io16;
         P->stage_bytes = (uint32_t)p.planes * (kABytes + (p.merged ? 2u : 1u) * P->b_bytes);
         const int ops = p.planes == 2 ? 0 : (p.bf16 ? 2 : 1);
         if (p.merged)

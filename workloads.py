@@ -53,6 +53,7 @@ class Spec:
     dilation: object = 1     # int or (d, h, w); k, stride, pad, out_pad likewise
     conv_groups: int = 1
     channels_last: bool = False  # x and y in NDHWC memory order (make_inputs still returns NCDHW x)
+    io_bf16: bool = False        # x, w and y as bf16 tensors (make_inputs still returns fp32 values)
 
     @property
     def kdims(self):
