@@ -138,10 +138,13 @@ class ClockSampler:
 # ------------------------------------------------------- traffic from ncu ----
 
 def kernel_source_sha(precision):
-    src = "ffma.cu" if precision == "ffma" else "tc.cu"
-    path = os.path.join(ROOT, "transposed_convolution_convt3d_gb300", "csrc", src)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Fingerprint of the main kernel's sources: its .cu file plus the shared headers."""
+    csrc = os.path.join(ROOT, "transposed_convolution_convt3d_gb300", "csrc")
+    h = hashlib.sha256()
+    for src in ("ffma.cu" if precision == "ffma" else "tc.cu", "ptx.cuh", "convt3d_internal.h"):
+        with open(os.path.join(csrc, src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def committed_traffic(precision, workload):

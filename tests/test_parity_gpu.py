@@ -424,3 +424,30 @@ def test_long_reduction(cin, precision):
                   epilogue=E.EPI_RELU_GROUPNORM, groups=8, seed_index=63)
     inputs = E.make_inputs(spec)
     assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name, 1e-3)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("layout", ["cl", "io16", "cl_io16"])
+def test_host_pipeline_layouts(layout):
+    """HostPipeline from pinned host tensors with channels-last and/or bf16 x/w/y."""
+    from transposed_convolution_convt3d_gb300 import HostPipeline
+    cl, io16 = "cl" in layout, "io16" in layout
+    spec = SMALL[7].replace(N=4, channels_last=cl, io_bf16=io16)
+    prec = PREC_BF16 if io16 else PREC_3XTF32
+    inputs = E.make_inputs(spec)
+    ref = run_oracle(spec, rounded_inputs(inputs, PREC_BF16) if io16 else inputs)
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in inputs.items()}
+    if cl:
+        host["x"] = host["x"].permute(0, 2, 3, 4, 1).contiguous().pin_memory()
+    if io16:
+        host["x"], host["w"] = host["x"].to(torch.bfloat16).pin_memory(), host["w"].to(torch.bfloat16).pin_memory()
+    pipe = HostPipeline(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
+                        spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, prec, chunks=2,
+                        channels_last=cl, io_bf16=io16)
+    y_host = torch.full(pipe.full_shape, float("nan"), dtype=pipe.plan.io_dtype).pin_memory()
+    pipe(host["x"], host["w"], y_host, host["bias"], host["gamma"], host["beta"])
+    torch.cuda.synchronize()
+    got = y_host.float()
+    if cl:
+        got = got.permute(0, 4, 1, 2, 3)
+    assert_close(got.contiguous().numpy(), ref, spec.name, TOL_LOW_VS_FP32 if io16 else TOL)

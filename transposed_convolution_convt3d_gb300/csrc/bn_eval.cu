@@ -12,7 +12,8 @@
 // nothing more: the packed weight is zero between channels of different groups.  The box is a product of one
 // interval per dimension, so B is three passes of 1-D interval sums:
 //   boxsum_kernel    one block per (n, ci): x once along d into k accumulators
-//                    per (h, w) column, then intervals along h, then along w;
+//                    per (h, w) column, then intervals along h (prefix sums,
+//                    one difference per interval), then along w;
 //   bn_eval_out_kernel  one block per (c, 16 samples): the Cin*k^3 contraction
 //                    with the packed weight, then the formula above in fp64.
 // The work is O(N*Cin*D*H*W*k + N*Cout*Cin*k^3), a read of x and of the weight.
@@ -43,8 +44,8 @@ __device__ __forceinline__ Interval tap_interval(int t, int s, int p, int dil, i
 
 struct BoxParams {
     const float *x;
-    float *box;  // [N][kd*kh*kw][Cin]
-    int Cin, D, H, W, Do, Ho, Wo;
+    float *box;  // [kd*kh*kw][Cin][N]: the samples of one (tap, ci) side by side
+    int N, Cin, D, H, W, Do, Ho, Wo;
     int cl;      // channels-last x
     int x16;     // x is a bf16 array
     int kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw;  // kernel, stride, pad, dilation per dimension
@@ -110,12 +111,21 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
         }
     }
     __syncthreads();
+    // along h: inclusive prefix sums of each (td, w) column, then one difference per interval
+    for (int col = threadIdx.x; col < P.kd * W; col += blockDim.x) {
+        float *c = a1 + (size_t)(col / W) * HW + col % W;
+        float run = 0.f;
+        for (int h = 0; h < H; ++h) {
+            run += c[(size_t)h * W];
+            c[(size_t)h * W] = run;
+        }
+    }
+    __syncthreads();
     for (int i = threadIdx.x; i < P.kd * P.kh * W; i += blockDim.x) {
         const int w = i % W, th = (i / W) % P.kh, td = i / (W * P.kh);
         const Interval iv = tap_interval(th, P.sh, P.ph, P.dh, H, P.Ho);
-        float acc = 0.f;
-        for (int h = iv.lo; h <= iv.hi; ++h) acc += a1[(size_t)td * HW + h * W + w];
-        a2[i] = acc;
+        const float *c = a1 + (size_t)td * HW + w;
+        a2[i] = iv.hi < iv.lo ? 0.f : c[(size_t)iv.hi * W] - (iv.lo > 0 ? c[(size_t)(iv.lo - 1) * W] : 0.f);
     }
     __syncthreads();
     const int k3 = P.kd * P.kh * P.kw;
@@ -124,7 +134,7 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
         const Interval iv = tap_interval(tw, P.sw, P.pw, P.dw, W, P.Wo);
         float acc = 0.f;
         for (int w = iv.lo; w <= iv.hi; ++w) acc += a2[(size_t)tdh * W + w];
-        P.box[((size_t)n * k3 + i) * P.Cin + ci] = acc;
+        P.box[((size_t)i * P.Cin + ci) * P.N + n] = acc;
     }
 }
 
@@ -152,12 +162,13 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
                                                           const __grid_constant__ TapTable taps) {
     const int c = blockIdx.x, n0 = blockIdx.y * kOutSamples;
     const int nn = P.N - n0 < kOutSamples ? P.N - n0 : kOutSamples;
-    const size_t nstride = (size_t)P.k3 * P.Cin;
-    const float *bx = P.box + (size_t)n0 * nstride;
+    // 16 samples' box sums of one (tap, ci) are consecutive: four 16-byte loads
+    const bool vec = nn == kOutSamples && P.N % 4 == 0;
     const int total = P.ntaps * P.Cin;
     float acc[kOutSamples];
 #pragma unroll
     for (int q = 0; q < kOutSamples; ++q) acc[q] = 0.f;
+#pragma unroll 4
     for (int i = threadIdx.x; i < total; i += blockDim.x) {
         const int j = i / P.Cin, ci = i - j * P.Cin;
         float wv;
@@ -170,10 +181,21 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
         } else {
             wv = P.w_a[((size_t)j * P.cin_pad + ci) * P.cout_pad + c];
         }
-        const float *b = bx + (size_t)taps.widx[j] * P.Cin + ci;
+        const float *b = P.box + ((size_t)taps.widx[j] * P.Cin + ci) * P.N + n0;
+        if (vec) {
 #pragma unroll
-        for (int q = 0; q < kOutSamples; ++q)
-            if (q < nn) acc[q] = fmaf(wv, b[q * nstride], acc[q]);
+            for (int q4 = 0; q4 < kOutSamples / 4; ++q4) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(b) + q4);
+                acc[4 * q4] = fmaf(wv, v.x, acc[4 * q4]);
+                acc[4 * q4 + 1] = fmaf(wv, v.y, acc[4 * q4 + 1]);
+                acc[4 * q4 + 2] = fmaf(wv, v.z, acc[4 * q4 + 2]);
+                acc[4 * q4 + 3] = fmaf(wv, v.w, acc[4 * q4 + 3]);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < kOutSamples; ++q)
+                if (q < nn) acc[q] = fmaf(wv, b[q], acc[q]);
+        }
     }
     __shared__ float red[kOutSamples][kOutThreads / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,7 +233,7 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
                            const float *bias, const float *gamma, const float *beta, float *box, float *y,
                            cudaStream_t s) {
     const Geometry &g = p.g;
-    BoxParams bp{x,        box,      g.Cin,    g.Din,    g.Hin,    g.Win,    g.Do,     g.Ho,     g.Wo,
+    BoxParams bp{x,        box,      g.N,      g.Cin,    g.Din,    g.Hin,    g.Win,    g.Do,     g.Ho,     g.Wo,
                  p.cl,     p.io16,   g.kk[0],  g.kk[1],  g.kk[2],  g.ss[0],  g.ss[1],  g.ss[2],  g.pp[0],
                  g.pp[1],  g.pp[2],  g.dil[0], g.dil[1], g.dil[2]};
     const size_t smem = bn_eval_smem_bytes(p);

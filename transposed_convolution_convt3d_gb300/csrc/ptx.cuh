@@ -51,6 +51,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but an incomplete phase suspends the thread in hardware
+// for up to `hint_ns` nanoseconds (it resumes as soon as the phase completes),
+// so a waiting thread issues no polling instructions meanwhile.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Longest hardware suspension of one poll: short against the wait limits
+// (seconds), long against the pipeline's phases (microseconds).
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Wait until the phase with the given parity has completed.  Gives up after
 // about `limit_ns` nanoseconds, or as soon as *abort becomes non-zero; returns
 // false in both cases.  With sleep_ns > 0 the waiter naps between polls so
@@ -63,7 +82,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns, uint32_t sleep_ns = 0) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
         if (sleep_ns) __nanosleep(sleep_ns);
         if ((it & 63u) == 63u || sleep_ns) {
             if (*abort) return false;
