@@ -761,7 +761,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 };
                 // sigmoid(f * e) for 8 pairs, with the polynomial's coefficients
                 // pre-multiplied by powers of f (see sigmoid_coefficients), then the stores
-                auto finish = [&](int c0, int ci, uint64_t (&e)[8], const uint64_t (&A)[4]) {
+                auto finish = [&](int c0, int row_off, uint64_t (&e)[8], const uint64_t (&A)[4]) {
                     const uint64_t half2 = pack2(0.5f, 0.5f);
                     float o[16];
 #pragma unroll
@@ -772,14 +772,16 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         q = ffma2(q, x2, A[0]);
                         unpack2(ffma2(e[k], q, half2), o[2 * k], o[2 * k + 1]);
                     }
-                    if (off[ci] >= 0) store_row16(yn, off[ci], c0, o);
+                    if (row_off >= 0) store_row16(yn, row_off, c0, o);
                 };
                 if constexpr (KEEP == 2) {
                     // w-parity pair: warp `half` of the lane quarter owns class `half`
                     // with all its channels, so each row's softmax stays inside one
                     // thread (no exchange between the warps)
                     const int ci = half;
+                    const int row_off = half ? off[1] : off[0];  // a select, not an indexed array
                     constexpr int kAll = 2 * kSoftmaxKeepChunks;  // 16-channel chunks per class
+                    const uint32_t col0 = lane_base + acc_col + (uint32_t)ci * P.cout_pad;
                     uint64_t e[kAll][8];
                     float mx = -INFINITY;
 #pragma unroll
@@ -787,9 +789,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         float raw[2][16];
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj)
-                            if (j0 + jj < nchunks)
-                                ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + 16 * (j0 + jj),
-                                               raw[jj]);
+                            if (j0 + jj < nchunks) ptx::tmem_ld16(col0 + 16 * (j0 + jj), raw[jj]);
                         ptx::tmem_wait_ld();
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj)
@@ -806,7 +806,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     sigmoid_coefficients(__frcp_rn(sum), A);
 #pragma unroll
                     for (int j = 0; j < kAll; ++j)
-                        if (j < nchunks) finish(16 * j, ci, e[j], A);
+                        if (j < nchunks) finish(16 * j, row_off, e[j], A);
                 } else {
                 // 1) this warp's chunks: maximum and sum of exponentials per class
                 constexpr int kKeep = kSoftmaxKeepChunks;
@@ -895,7 +895,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
 #pragma unroll
                         for (int jj = 0; jj < kKeep; ++jj) {
                             const int j = half + jj * kHalves;
-                            if (j < nchunks) finish(16 * j, ci, e[jj][ci], A);
+                            if (j < nchunks) finish(16 * j, off[ci], e[jj][ci], A);
                         }
                     } else {
                         for (int j = half; j < nchunks; j += kHalves) {
@@ -904,7 +904,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                             ptx::tmem_wait_ld();
                             logits(16 * j, raw, e[0][ci]);
                             exp8(e[0][ci], M[ci]);
-                            finish(16 * j, ci, e[0][ci], A);
+                            finish(16 * j, off[ci], e[0][ci], A);
                         }
                     }
                 }
