@@ -8,7 +8,7 @@ flushed (a 256 MiB write) before every timed step.  Each step is timed with
 CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--precision 3xtf32|tf32|bf16|ffma] [--impl gpu|reference]
+                  [--precision 3xtf32|3xbf16|tf32|bf16|ffma] [--impl gpu|reference]
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (the path shards by batch with no collective on the data path);
@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.BY_NAME))
-    ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "tf32", "bf16", "ffma"])
+    ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "3xbf16", "tf32", "bf16", "ffma"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the CPU baseline sample")
@@ -262,7 +262,8 @@ def run_gpu(args, spec):
     import torch
     import torch.distributed as dist
 
-    from transposed_convolution_convt3d_gb300 import (PREC_3XTF32, PREC_BF16, PREC_FFMA, PREC_TF32, HostPipeline,
+    from transposed_convolution_convt3d_gb300 import (PREC_3XBF16, PREC_3XTF32, PREC_BF16, PREC_FFMA, PREC_TF32,
+                                                      HostPipeline,
                                                       Plan)
 
     world, rank, local = dist_env()
@@ -270,7 +271,8 @@ def run_gpu(args, spec):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    prec = {"3xtf32": PREC_3XTF32, "tf32": PREC_TF32, "bf16": PREC_BF16, "ffma": PREC_FFMA}[args.precision]
+    prec = {"3xtf32": PREC_3XTF32, "3xbf16": PREC_3XBF16, "tf32": PREC_TF32, "bf16": PREC_BF16,
+            "ffma": PREC_FFMA}[args.precision]
 
     if args.io_bf16:
         spec = spec.replace(io_bf16=True)
@@ -390,8 +392,8 @@ def run_gpu(args, spec):
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "peak_source": f"{pk['source']} HBM copy bandwidth",
                 "algorithmic_bytes": info["forward_min_bytes"]}
-    elif prec in (PREC_3XTF32, PREC_TF32, PREC_BF16):
-        bf = prec == PREC_BF16
+    elif prec in (PREC_3XTF32, PREC_TF32, PREC_BF16, PREC_3XBF16):
+        bf = prec in (PREC_BF16, PREC_3XBF16)
         peak = pk["bf16_tflops"] * (1.0 if bf else TF32_OVER_BF16)
         achieved = useful / (gemm_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
@@ -400,6 +402,8 @@ def run_gpu(args, spec):
                 "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak}
         if prec == PREC_3XTF32:
             roof["frac_of_3xtf32_peak"] = achieved / (peak / 3.0)
+        if prec == PREC_3XBF16:
+            roof["frac_of_3xbf16_peak"] = achieved / (peak / 3.0)
     else:
         peak = SMS * FP32_FMA_PER_CLK_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
         achieved = useful / (gemm_avg * 1e-3) / 1e12

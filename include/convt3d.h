@@ -92,10 +92,16 @@ typedef enum {
     CONVT3D_PREC_TF32 = 2,   /* tcgen05 tensor cores, one TF32 product per term: inputs
                                 rounded to TF32 (nearest), fp32 accumulation; results
                                 within the 1e-2 tier of page l2_p49's harness quote */
-    CONVT3D_PREC_BF16 = 3    /* tcgen05 tensor cores, one BF16 product per term (kind::f16):
+    CONVT3D_PREC_BF16 = 3,   /* tcgen05 tensor cores, one BF16 product per term (kind::f16):
                                 inputs rounded to bf16 (nearest even) when staged and
                                 packed, fp32 accumulation and epilogue, fp32 I/O;
                                 same 1e-2 tier                                        */
+    CONVT3D_PREC_3XBF16 = 4  /* tcgen05 tensor cores, split BF16: each operand is
+                                hi = bf16(v) + lo = bf16(v - hi) (nearest even, so
+                                |v - hi - lo| <= 2^-16 |v|), three kind::f16 products
+                                a_hi*b_hi + a_hi*b_lo + a_lo*b_hi per term, fp32
+                                accumulation; fp32 I/O; the 1e-4 tier of 3XTF32 at
+                                half its tensor-core time                              */
 } convt3d_precision_t;
 
 typedef enum {

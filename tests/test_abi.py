@@ -75,6 +75,7 @@ def create(lib, **kw):
     (dict(stride=2, dilation=(2, 2, 2)), 2), (dict(dilation=(16, 1, 1)), 2),
     (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 1, 2), pads=(0, 0, 0), Cout=144), 2),
     (dict(io_bf16=1), 2), (dict(io_bf16=1, precision=2), 2), (dict(io_bf16=1, precision=1), 2),
+    (dict(io_bf16=1, precision=4), 2),
 ])
 def test_plan_validation(lib, kw, status):
     st, h = create(lib, **kw)
@@ -122,7 +123,7 @@ def test_general_shapes_plan_facts(lib, kw, precision):
 
 
 @pytest.mark.parametrize("spec", workloads.ALL, ids=lambda s: s.name)
-@pytest.mark.parametrize("precision", [0, 1])
+@pytest.mark.parametrize("precision", [0, 1, 4])
 def test_plan_facts_for_workloads(lib, spec, precision):
     p = Plan.from_spec(spec, precision=precision)
     dims = [oracle.output_size(v, spec.k, spec.stride, spec.pad, spec.out_pad) for v in (spec.D, spec.H, spec.W)]
@@ -141,7 +142,23 @@ def test_plan_facts_for_workloads(lib, spec, precision):
         assert p.info["issued_mma_flop"] == 2.0 * spec.N * spec.Cout * spec.Cin * spec.k ** 3
         assert p.info["launches_per_forward"] == 2
     else:
-        assert p.info["issued_mma_flop"] >= p.info["useful_flop"] * (3 if precision == 0 else 1) * 0.9
+        assert p.info["issued_mma_flop"] >= p.info["useful_flop"] * (3 if precision in (0, 4) else 1) * 0.9
+
+
+@pytest.mark.parametrize("spec", workloads.ALL, ids=lambda s: s.name)
+def test_split_bf16_planes_are_half_the_split_tf32_planes(lib, spec):
+    """Split BF16 keeps two 2-byte planes where split TF32 keeps two 4-byte
+    planes: the same products are issued and the staged operands need half the
+    workspace and half the GEMM's minimum traffic for them."""
+    t, b = Plan.from_spec(spec, precision=0), Plan.from_spec(spec, precision=4)
+    # a bf16 K step is 64 channels (128-byte rows): below 64 input channels the
+    # padding doubles the elements and the bytes come out equal
+    strict = spec.Cin % 64 == 0
+    assert b.workspace_bytes < t.workspace_bytes if strict else b.workspace_bytes <= t.workspace_bytes
+    if spec.epilogue != workloads.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL:
+        assert b.info["gemm_min_bytes"] <= t.info["gemm_min_bytes"]
+        # bf16 K steps hold 64 channels: padding may add products, never remove them
+        assert b.info["issued_mma_flop"] >= t.info["issued_mma_flop"]
 
 
 def test_parity_classes_tile_every_output_once(lib):

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import workloads as E
-from transposed_convolution_convt3d_gb300 import PREC_3XTF32, PREC_FFMA, Plan, _lib
+from transposed_convolution_convt3d_gb300 import PREC_3XBF16, PREC_3XTF32, PREC_FFMA, Plan, _lib
 
 TOL = 1e-4
 
@@ -49,7 +49,7 @@ def _static_ws_call(plan, d, y):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("precision", [PREC_3XTF32, PREC_FFMA], ids=["3xtf32", "ffma"])
+@pytest.mark.parametrize("precision", [PREC_3XTF32, PREC_3XBF16, PREC_FFMA], ids=["3xtf32", "3xbf16", "ffma"])
 @pytest.mark.parametrize("spec", CASES, ids=lambda s: s.name)
 def test_static_workspace_matches_regular_path_twice(spec, precision):
     dev = torch.device("cuda")

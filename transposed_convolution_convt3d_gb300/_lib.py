@@ -22,6 +22,7 @@ PREC_3XTF32 = 0
 PREC_FFMA = 1
 PREC_TF32 = 2
 PREC_BF16 = 3
+PREC_3XBF16 = 4
 
 STATUS = {
     0: "CONVT3D_OK",

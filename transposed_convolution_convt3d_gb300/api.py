@@ -14,7 +14,7 @@ import torch
 from . import _lib
 from ._lib import (EPI_IDENTITY, EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL,  # noqa: F401
                    EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, EPI_SOFTMAX_SIGMOID, PREC_3XTF32, PREC_FFMA,
-                   PREC_TF32, PREC_BF16, Convt3dError)
+                   PREC_TF32, PREC_BF16, PREC_3XBF16, Convt3dError)
 
 
 def _ptr(t):

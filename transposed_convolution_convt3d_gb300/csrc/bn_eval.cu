@@ -174,8 +174,9 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
         float wv;
         if (P.kmajor) {
             const size_t o = ((size_t)j * P.cout_pad + c) * P.cin_pad + ci;
-            if (P.wbf16)
-                wv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_a)[o]);
+            if (P.wbf16)  // bf16 planes: hi (+ lo, split bf16)
+                wv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_a)[o]) +
+                     (P.w_b ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_b)[o]) : 0.f);
             else  // hi + lo: the fp32 weight, exactly (or its TF32 rounding)
                 wv = P.w_b ? P.w_a[o] + P.w_b[o] : P.w_a[o];
         } else {

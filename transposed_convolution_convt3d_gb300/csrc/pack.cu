@@ -5,7 +5,7 @@
 // per-Cout access strided and re-lays it per output channel.  Here the
 // weight is re-laid per parity class and tap:
 //   tensor-core path: [tap][Cout_pad][Cin_pad] (K-major rows, Cin contiguous),
-//                     split into TF32 hi and lo planes;
+//                     split into TF32 (or bf16) hi and lo planes;
 //   FFMA path:        [tap][Cin_pad][Cout_pad] fp32.
 // The tensor-core path also stages x (NCDHW, or already channels-last) into channels-last
 // [N][D][H][W][Cin_pad] hi/lo planes (one TF32-rounded or bf16 plane for the
@@ -30,6 +30,14 @@ __device__ __forceinline__ float round_tf32(float v) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
     return __uint_as_float(r);
+}
+
+// Split v into a bf16 head and a bf16 tail, both rounded to nearest even:
+// v - hi is exact in fp32 and |v - hi - lo| <= 2^-16 |v| (two 8-bit halves of
+// a 16-bit significand).
+__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
+    hi = __float2bfloat16_rn(v);
+    lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
 struct TapIndex {
@@ -61,7 +69,9 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
             const int64_t src = ((int64_t)ci * cout_g + co % cout_g) * k3 + taps.widx[j];
             v = w16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(w)[src]) : w[src];
         }
-        if (lo) {
+        if (lo && mode == 3) {  // split bf16 planes (2-byte elements)
+            split_bf16(v, reinterpret_cast<__nv_bfloat16 *>(hi)[i], reinterpret_cast<__nv_bfloat16 *>(lo)[i]);
+        } else if (lo) {
             float h, l;
             split_tf32(v, h, l);
             hi[i] = h;
@@ -102,7 +112,11 @@ __global__ void stage_input_kernel(const float *__restrict__ x, float *__restric
         const int64_t s = s0 + ty + j;
         const int c = c0 + tx;
         if (s < S) {
-            if (ln) {
+            if (ln && bf16) {  // split bf16 planes (2-byte elements)
+                const int64_t o = ((int64_t)n * S + s) * cin_pad + c;
+                split_bf16(tile[tx][ty + j], reinterpret_cast<__nv_bfloat16 *>(hi)[o],
+                           reinterpret_cast<__nv_bfloat16 *>(lo)[o]);
+            } else if (ln) {
                 float h, l;
                 split_tf32(tile[tx][ty + j], h, l);
                 hn[s * cin_pad + c] = h;
@@ -129,7 +143,9 @@ __global__ void stage_input_cl_kernel(const float *__restrict__ x, float *__rest
                     : (x16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[r * Cin + c])
                            : __ldg(x + r * Cin + c));
     const int64_t o = r * cin_pad + c;
-    if (lo) {
+    if (lo && bf16) {
+        split_bf16(v, reinterpret_cast<__nv_bfloat16 *>(hi)[o], reinterpret_cast<__nv_bfloat16 *>(lo)[o]);
+    } else if (lo) {
         float h, l;
         split_tf32(v, h, l);
         hi[o] = h;
@@ -151,7 +167,8 @@ cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *
     const int threads = 256;
     const int blocks = (int)((total + threads - 1) / threads < 4096 ? (total + threads - 1) / threads : 4096);
     pack_weights_kernel<<<blocks, threads, 0, s>>>(w, hi, lo, p.g.Cin, p.g.Cout, p.g.kvol, p.g.ntaps, p.cin_pad,
-                                                   p.cout_pad, kmajor, p.bf16 ? 2 : (p.planes == 1 ? 1 : 0),
+                                                   p.cout_pad, kmajor,
+                                                   p.bf16 ? (p.planes == 2 ? 3 : 2) : (p.planes == 1 ? 1 : 0),
                                                    p.g.Cin / p.g.G, p.g.Cout / p.g.G, p.io16, t);
     return cudaGetLastError();
 }

@@ -228,7 +228,7 @@ convt3d_status_t validate(const convt3d_desc_t &d) {
     if (d.Cin % sh.G || d.Cout % sh.G) return fail(CONVT3D_ERR_INVALID_ARG, "conv_groups must divide Cin and Cout");
     if (d.epilogue < CONVT3D_EPI_IDENTITY || d.epilogue > CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
         return fail(CONVT3D_ERR_INVALID_ARG, "unknown epilogue %d", d.epilogue);
-    if (d.precision < CONVT3D_PREC_3XTF32 || d.precision > CONVT3D_PREC_BF16)
+    if (d.precision < CONVT3D_PREC_3XTF32 || d.precision > CONVT3D_PREC_3XBF16)
         return fail(CONVT3D_ERR_INVALID_ARG, "unknown precision %d", d.precision);
     if (d.epilogue == CONVT3D_EPI_RELU_GROUPNORM && (d.groups < 1 || d.Cout % d.groups != 0))
         return fail(CONVT3D_ERR_INVALID_ARG, "groups must divide Cout");
@@ -333,10 +333,11 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
         return fail(CONVT3D_ERR_UNSUPPORTED, "tap table overflow");
     }
     p->tc = desc->precision != CONVT3D_PREC_FFMA;
-    p->planes = desc->precision == CONVT3D_PREC_3XTF32 ? 2 : (p->tc ? 1 : 0);
+    const bool split = desc->precision == CONVT3D_PREC_3XTF32 || desc->precision == CONVT3D_PREC_3XBF16;
+    p->planes = split ? 2 : (p->tc ? 1 : 0);
     p->cl = desc->channels_last != 0;
     p->io16 = desc->io_bf16 != 0;
-    p->bf16 = desc->precision == CONVT3D_PREC_BF16;
+    p->bf16 = desc->precision == CONVT3D_PREC_BF16 || desc->precision == CONVT3D_PREC_3XBF16;
     p->elem_bytes = p->bf16 ? 2 : 4;
     p->chunk = p->tc ? kTcRowBytes / p->elem_bytes : 8;
     p->tile_m = p->tc ? kTcTileM : kFfmaTileM;
@@ -365,12 +366,12 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     p->off_wpk_hi = off;
     off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
     p->off_wpk_lo = off;
-    if (p->planes == 2) off = align_up(off + p->wpk_elems * 4, 256);
+    if (p->planes == 2) off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
     p->xs_elems = (p->tc && !eval_bn) ? (size_t)desc->N * desc->Din * desc->Hin * desc->Win * p->cin_pad : 0;
     p->off_xs_hi = off;
     off = align_up(off + p->xs_elems * p->elem_bytes, 256);
     p->off_xs_lo = off;
-    if (p->planes == 2) off = align_up(off + p->xs_elems * 4, 256);
+    if (p->planes == 2) off = align_up(off + p->xs_elems * p->elem_bytes, 256);
     size_t per_tile = 0, stat = 0;
     if (desc->epilogue == CONVT3D_EPI_RELU_GROUPNORM) {
         per_tile = 2 * (size_t)desc->groups;
@@ -463,7 +464,7 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
     const double out_bytes = (bn || ev) ? 4.0 * d.N * d.Cout : ybytes;
     // Main kernel: reads x (tensor-core path: the staged hi+lo copy) and the packed weights once,
     // writes the output once (BN+pool: nothing but partials).
-    const double planes = p->planes == 2 ? 2.0 : (p->bf16 ? 0.5 : 1.0);  // staged operand bytes / fp32 bytes
+    const double planes = (p->planes == 2 ? 2.0 : 1.0) * p->elem_bytes / 4.0;  // staged operand bytes / fp32 bytes
     info->gemm_min_bytes = planes * xbytes + planes * wbytes + (bn ? 0.0 : ybytes);
     // Whole forward as the pages define it: x and w in, the output out, plus the second pass
     // over y that GroupNorm's global statistics force.

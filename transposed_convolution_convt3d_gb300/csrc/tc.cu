@@ -291,14 +291,15 @@ __device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G,
 // 1, for w-parity pairs with each warp owning one class's channels (8 warps);
 // 0 = the exponentials are recomputed from tensor memory.
 // OPS: operand format, fixed at compile time so that the producer and MMA
-// loops stay branch-free: 0 = split TF32 (hi and lo planes), 1 = TF32, 2 = BF16.
+// loops stay branch-free: 0 = split TF32 (hi and lo planes), 1 = TF32, 2 = BF16,
+// 3 = split BF16 (hi and lo bf16 planes).
 // MERGED: every group is a w-parity pair walked by merged w-taps (GroupDesc::nm):
 // a K step whose w offset both classes have loads the activation slice once,
 // the two classes' weight slices side by side, and issues one MMA of
 // N = 2 * Cout_pad into both accumulators (they are adjacent in tensor memory).
 template <int EPI, int KEEP, int OPS, bool MERGED>
 __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const __grid_constant__ TcParams P) {
-    constexpr int kPlanes = OPS == 0 ? 2 : 1;
+    constexpr int kPlanes = (OPS == 0 || OPS == 3) ? 2 : 1;
     constexpr int kBSlots = MERGED ? 2 : 1;  // weight slices per plane in a stage
     constexpr int kEpiWarps = EpiCfg<EPI>::warps;
     constexpr int kHalves = kEpiWarps / 4;  // warps per tensor-memory lane quarter
@@ -460,10 +461,10 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc =
-                OPS == 2 ? ptx::idesc_bf16((uint32_t)P.cout_pad) : ptx::idesc_tf32((uint32_t)P.cout_pad);
+                OPS >= 2 ? ptx::idesc_bf16((uint32_t)P.cout_pad) : ptx::idesc_tf32((uint32_t)P.cout_pad);
             // merged steps of both classes: N = 2 * Cout_pad
             const uint32_t idesc2 =
-                OPS == 2 ? ptx::idesc_bf16(2u * (uint32_t)P.cout_pad) : ptx::idesc_tf32(2u * (uint32_t)P.cout_pad);
+                OPS >= 2 ? ptx::idesc_bf16(2u * (uint32_t)P.cout_pad) : ptx::idesc_tf32(2u * (uint32_t)P.cout_pad);
             constexpr uint64_t kA16 = kABytes >> 4;                  // one activation plane, 16-byte units
             const uint64_t b16 = (uint64_t)(P.b_bytes >> 4);         // one weight slice
             const uint64_t blo16 = (uint64_t)kBSlots * b16;          // B_lo after the B_hi slots
@@ -499,6 +500,17 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         for (int kk = 0; kk < kChunk / 8; ++kk) {  // 16 bf16 (32 bytes) per MMA
                             const uint64_t a = d0 + 2 * kk;
                             ptx::mma_bf16(d_tmem, a, a + kA16, id, kk ? 1u : first);
+                        }
+                    } else if constexpr (OPS == 3) {
+#pragma unroll
+                        for (int kk = 0; kk < kChunk / 8; ++kk) {  // split bf16: three products
+                            const uint64_t a_hi = d0 + 2 * kk;
+                            const uint64_t a_lo = a_hi + kA16;
+                            const uint64_t b_hi = a_hi + 2 * kA16;
+                            const uint64_t b_lo = b_hi + blo16;
+                            ptx::mma_bf16(d_tmem, a_hi, b_hi, id, kk ? 1u : first);
+                            ptx::mma_bf16(d_tmem, a_hi, b_lo, id, 1u);
+                            ptx::mma_bf16(d_tmem, a_lo, b_hi, id, 1u);
                         }
                     } else {
 #pragma unroll
@@ -574,6 +586,17 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                                     const uint64_t a = d0 + 2 * kk;
                                     ptx::mma_bf16(d_tmem, a, a + kA16, idesc, (s | kk) ? 1u : 0u);
                                 }
+                            } else if constexpr (OPS == 3) {
+#pragma unroll
+                                for (int kk = 0; kk < kChunk / 8; ++kk) {
+                                    const uint64_t a_hi = d0 + 2 * kk;
+                                    const uint64_t a_lo = a_hi + kA16;
+                                    const uint64_t b_hi = a_hi + 2 * kA16;
+                                    const uint64_t b_lo = b_hi + b16;
+                                    ptx::mma_bf16(d_tmem, a_hi, b_hi, idesc, (s | kk) ? 1u : 0u);
+                                    ptx::mma_bf16(d_tmem, a_hi, b_lo, idesc, 1u);
+                                    ptx::mma_bf16(d_tmem, a_lo, b_hi, idesc, 1u);
+                                }
                             } else {
 #pragma unroll
                                 for (int kk = 0; kk < kChunk / 8; ++kk) {
@@ -629,7 +652,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             const GroupDesc &G = s_grp[T.gi];
             const int acc = iter & 1;
             const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
-            if (!ptx::mbar_wait_bounded(tfull0 + 8 * acc, aph, &abort_flag, kWaitNs, 200)) {
+            if (!ptx::mbar_wait_bounded(tfull0 + 8 * acc, aph, &abort_flag, kWaitNs)) {
                 if (lane == 0) record_error(P.status, kErrTimeout, 3);
                 abort_flag = 1;
                 break;
@@ -1177,14 +1200,17 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->cl = p.cl;
         P->io16 = p.io16;
         P->stage_bytes = (uint32_t)p.planes * (kABytes + (p.merged ? 2u : 1u) * P->b_bytes);
-        const int ops = p.planes == 2 ? 0 : (p.bf16 ? 2 : 1);
-        if (p.merged)
-            tc.kern = ops == 0 ? select_kernel<0, true>(p, tc.threads)
-                               : (ops == 1 ? select_kernel<1, true>(p, tc.threads) : select_kernel<2, true>(p, tc.threads));
-        else
-            tc.kern = ops == 0 ? select_kernel<0, false>(p, tc.threads)
-                               : (ops == 1 ? select_kernel<1, false>(p, tc.threads)
-                                           : select_kernel<2, false>(p, tc.threads));
+        const int ops = p.planes == 2 ? (p.bf16 ? 3 : 0) : (p.bf16 ? 2 : 1);
+        switch (ops * 2 + (p.merged ? 1 : 0)) {
+            case 0: tc.kern = select_kernel<0, false>(p, tc.threads); break;
+            case 1: tc.kern = select_kernel<0, true>(p, tc.threads); break;
+            case 2: tc.kern = select_kernel<1, false>(p, tc.threads); break;
+            case 3: tc.kern = select_kernel<1, true>(p, tc.threads); break;
+            case 4: tc.kern = select_kernel<2, false>(p, tc.threads); break;
+            case 5: tc.kern = select_kernel<2, true>(p, tc.threads); break;
+            case 6: tc.kern = select_kernel<3, false>(p, tc.threads); break;
+            default: tc.kern = select_kernel<3, true>(p, tc.threads); break;
+        }
         if (!tc.kern) return cudaErrorInvalidValue;
         // stage ring: as many stages as fit beside the kernel's static shared memory
         cudaFuncAttributes fa;
