@@ -374,8 +374,10 @@ def run_gpu(args, spec):
                 e2e_ms.append(a.elapsed_time(b))
         e2e_chunks = pipe.chunks
         e2e_t = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
+        link_t = host_link_ms(host, y, y_host, stream, dev)
         e2e = {"value": replica_throughput(useful, world, e2e_t), "unit": "TFLOP/s", "ms_per_step": e2e_t,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "host_link_bound_ms": link_t, "host_link_frac": link_t / e2e_t,
                "path": f"HostPipeline, {e2e_chunks} chunk(s) of samples, {args.e2e_copy_streams} copy stream(s) "
                        "per direction, pinned host buffers"}
 
@@ -444,6 +446,37 @@ def run_gpu(args, spec):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def host_link_ms(host, y_dev, y_host, stream, dev, reps=3):
+    """The host link's bound on one end-to-end step: the same bytes copied with
+    nothing else running, the inputs host->device on a second stream while the
+    output goes device->host (median of `reps` after one warm-up)."""
+    import torch
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    scratch = torch.empty(int(h2d), dtype=torch.uint8, device=dev)
+    s_in = torch.cuda.Stream(device=dev)
+    times = []
+    for i in range(reps + 1):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        s_in.wait_event(a)
+        with torch.cuda.stream(s_in):
+            o = 0
+            for t in host.values():
+                if t is None:
+                    continue
+                n = t.numel() * t.element_size()
+                scratch[o:o + n].copy_(t.reshape(-1).view(torch.uint8), non_blocking=True)
+                o += n
+            c.record(s_in)
+        y_host.copy_(y_dev, non_blocking=True)
+        stream.wait_event(c)
+        b.record(stream)
+        b.synchronize()
+        if i > 0:
+            times.append(a.elapsed_time(b))
+    return sorted(times)[len(times) // 2]
 
 
 def main():

@@ -66,7 +66,7 @@ def create(lib, **kw):
     (dict(stride=3, k=3), 2), (dict(k=8), 2), (dict(Cout=257), 2), (dict(k=3, pad=3, Din=9, Hin=9, Win=9), 2),
     (dict(stride=2, k=3, pad=1, Cout=144), 2), (dict(stride=2, k=1), 2),
     (dict(epilogue=4, eps=-1.0), 1), (dict(epilogue=4, scale=float("inf")), 1),
-    (dict(epilogue=4, Hin=200, Win=200), 2),
+    (dict(epilogue=4, Hin=256, Win=256), 2),
     # general shapes
     (dict(dilation=(-1, 1, 1)), 1), (dict(conv_groups=-2), 1), (dict(conv_groups=3), 1),
     (dict(per_dim=1, kdims=(3, 0, 3), strides=(1, 1, 1)), 1),

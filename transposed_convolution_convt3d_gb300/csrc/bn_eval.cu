@@ -11,11 +11,14 @@
 // to o = stride*i - pad + dilation*t per dimension).  Grouped convolution needs
 // nothing more: the packed weight is zero between channels of different groups.  The box is a product of one
 // interval per dimension, so B is three passes of 1-D interval sums:
-//   boxsum_kernel    one block per (n, ci): x once along d into k accumulators
-//                    per (h, w) column, then intervals along h (prefix sums,
-//                    one difference per interval), then along w;
-//   bn_eval_out_kernel  one block per (c, 16 samples): the Cin*k^3 contraction
-//                    with the packed weight, then the formula above in fp64.
+//   boxsum_kernel    one block per (n, ci): x once along d into one
+//                    accumulator per distinct d-interval (taps whose intervals
+//                    coincide share it) per (h, w) column, then intervals along
+//                    h (prefix sums, one difference per interval), then along w;
+//   bn_eval_out_kernel  blocks per (c, 16 samples, K split): the Cin*k^3
+//                    contraction with the packed weight; the last block of a
+//                    (c, samples) pair to finish adds the splits' fp64 partial
+//                    sums in split order and applies the formula above.
 // The work is O(N*Cin*D*H*W*k + N*Cout*Cin*k^3), a read of x and of the weight.
 #include <cuda_bf16.h>
 
@@ -26,14 +29,14 @@ namespace {
 
 constexpr int kMaxK = 7;
 
-__device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+__host__ __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 // Inputs i whose output s*i - p + dil*t lies in [0, out - 1], clamped to [0, in - 1].
 struct Interval {
     int lo, hi;
 };
 
-__device__ __forceinline__ Interval tap_interval(int t, int s, int p, int dil, int in, int out) {
+__host__ __device__ __forceinline__ Interval tap_interval(int t, int s, int p, int dil, int in, int out) {
     Interval r;
     r.lo = -floor_div(-(p - dil * t), s);           // ceil((p - dil*t) / s)
     r.hi = floor_div(out - 1 + p - dil * t, s);
@@ -49,38 +52,43 @@ struct BoxParams {
     int cl;      // channels-last x
     int x16;     // x is a bf16 array
     int kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw;  // kernel, stride, pad, dilation per dimension
+    // distinct d-intervals of the taps along d: nud of them, tap td uses ud_of[td]
+    int nud;
+    int ud_lo[kMaxK], ud_hi[kMaxK], ud_of[kMaxK];
 };
 
-// One block per (n, ci).  fp32 sums: at most D*H*W terms of the input each,
-// far inside the tolerance the contraction's result is held to.
+// One block per (n, ci); NUD = the number of distinct d-intervals (a
+// compile-time count, so that each load feeds exactly that many accumulators).
+// fp32 sums: at most D*H*W terms of the input each, far inside the tolerance
+// the contraction's result is held to.
+template <int NUD>
 __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
     extern __shared__ float sm[];
     const int H = P.H, W = P.W, HW = H * W;
-    float *a1 = sm;                        // [kd][H][W]: sums along d
-    float *a2 = sm + (size_t)P.kd * HW;    // [kd][kh][W]: then along h
+    float *a1 = sm;                        // [nud][H][W]: sums along d, one plane per distinct interval
+    float *a2 = sm + (size_t)P.nud * HW;   // [kd][kh][W]: then along h
     const int n = blockIdx.x / P.Cin, ci = blockIdx.x % P.Cin;
     // element (d, col) of this (n, ci) slab: NCDHW contiguous, or channels-last with stride Cin
     const float *xp = P.cl ? P.x + (size_t)n * P.D * HW * P.Cin + ci : P.x + (size_t)blockIdx.x * P.D * HW;
     const size_t es = P.cl ? (size_t)P.Cin : 1;
 
-    int dlo[kMaxK], dhi[kMaxK];
+    int dlo[NUD], dhi[NUD];
 #pragma unroll
-    for (int t = 0; t < kMaxK; ++t) {
-        const Interval iv = t < P.kd ? tap_interval(t, P.sd, P.pd, P.dd, P.D, P.Do) : Interval{1, 0};
-        dlo[t] = iv.lo;
-        dhi[t] = iv.hi;
+    for (int t = 0; t < NUD; ++t) {
+        dlo[t] = P.ud_lo[t];
+        dhi[t] = P.ud_hi[t];
     }
     if (HW % 4 == 0 && !P.cl && !P.x16) {
         // 128-bit loads: the slab of (n, ci) starts on a 16-byte boundary when H*W % 4 == 0
         for (int c4 = threadIdx.x; c4 < HW / 4; c4 += blockDim.x) {
-            float4 acc[kMaxK];
+            float4 acc[NUD];
 #pragma unroll
-            for (int t = 0; t < kMaxK; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int t = 0; t < NUD; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
             for (int d = 0; d < P.D; ++d) {
                 const float4 v = __ldg(reinterpret_cast<const float4 *>(xp + (size_t)d * HW) + c4);
 #pragma unroll
-                for (int t = 0; t < kMaxK; ++t)
+                for (int t = 0; t < NUD; ++t)
                     if (d >= dlo[t] && d <= dhi[t]) {
                         acc[t].x += v.x;
                         acc[t].y += v.y;
@@ -89,30 +97,28 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
                     }
             }
 #pragma unroll
-            for (int t = 0; t < kMaxK; ++t)
-                if (t < P.kd) reinterpret_cast<float4 *>(a1 + (size_t)t * HW)[c4] = acc[t];
+            for (int t = 0; t < NUD; ++t) reinterpret_cast<float4 *>(a1 + (size_t)t * HW)[c4] = acc[t];
         }
     } else {
         for (int col = threadIdx.x; col < HW; col += blockDim.x) {
-            float acc[kMaxK];
+            float acc[NUD];
 #pragma unroll
-            for (int t = 0; t < kMaxK; ++t) acc[t] = 0.f;
+            for (int t = 0; t < NUD; ++t) acc[t] = 0.f;
             for (int d = 0; d < P.D; ++d) {
                 const size_t xi = ((size_t)d * HW + col) * es;
                 const float v = P.x16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.x)[(xp - P.x) + xi])
                                       : __ldg(xp + xi);
 #pragma unroll
-                for (int t = 0; t < kMaxK; ++t)
+                for (int t = 0; t < NUD; ++t)
                     if (d >= dlo[t] && d <= dhi[t]) acc[t] += v;
             }
 #pragma unroll
-            for (int t = 0; t < kMaxK; ++t)
-                if (t < P.kd) a1[(size_t)t * HW + col] = acc[t];
+            for (int t = 0; t < NUD; ++t) a1[(size_t)t * HW + col] = acc[t];
         }
     }
     __syncthreads();
-    // along h: inclusive prefix sums of each (td, w) column, then one difference per interval
-    for (int col = threadIdx.x; col < P.kd * W; col += blockDim.x) {
+    // along h: inclusive prefix sums of each (interval, w) column, then one difference per interval
+    for (int col = threadIdx.x; col < P.nud * W; col += blockDim.x) {
         float *c = a1 + (size_t)(col / W) * HW + col % W;
         float run = 0.f;
         for (int h = 0; h < H; ++h) {
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
     for (int i = threadIdx.x; i < P.kd * P.kh * W; i += blockDim.x) {
         const int w = i % W, th = (i / W) % P.kh, td = i / (W * P.kh);
         const Interval iv = tap_interval(th, P.sh, P.ph, P.dh, H, P.Ho);
-        const float *c = a1 + (size_t)td * HW + w;
+        const float *c = a1 + (size_t)P.ud_of[td] * HW + w;
         a2[i] = iv.hi < iv.lo ? 0.f : c[(size_t)iv.hi * W] - (iv.lo > 0 ? c[(size_t)(iv.lo - 1) * W] : 0.f);
     }
     __syncthreads();
@@ -146,6 +152,9 @@ constexpr int kOutSamples = 16;  // samples per contraction block
 
 struct OutParams {
     const float *box;
+    double *part;         // [ks][N][Cout] partial sums when the contraction is split (ks > 1)
+    unsigned *counters;   // [N/16 blocks][Cout] blocks finished, reset to 0 by the last one
+    int ks;
     const float *w_a, *w_b;  // tensor-core layout: TF32 hi/lo planes [tap][cout_pad][cin_pad]; FFMA: [tap][cin_pad][cout_pad]
     const float *bias, *gamma, *beta, *rmean, *rvar;
     float *y;
@@ -153,10 +162,12 @@ struct OutParams {
     double inv_vol, scale, eps;
 };
 
-// One block of 512 threads per (c, group of 16 samples): each weight element
-// is read once per block and multiplied into the 16 samples' box sums;
-// per-thread fp32 partial sums, then a block reduction.
-constexpr int kOutThreads = 512;
+// Blocks of 256 threads per (c, group of 16 samples, K split): each weight
+// element is read once per block and multiplied into the 16 samples' box
+// sums; per-thread fp32 partial sums, then a block reduction.  With K split
+// (ks > 1) the last block of a (c, samples) pair to finish adds the splits'
+// fp64 sums in split order.
+constexpr int kOutThreads = 256;
 
 __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParams P,
                                                           const __grid_constant__ TapTable taps) {
@@ -165,11 +176,13 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
     // 16 samples' box sums of one (tap, ci) are consecutive: four 16-byte loads
     const bool vec = nn == kOutSamples && P.N % 4 == 0;
     const int total = P.ntaps * P.Cin;
+    const int ks = blockIdx.z;  // this block's share of the K = taps x Cin products
+    const int i_begin = (int)((int64_t)total * ks / P.ks), i_end = (int)((int64_t)total * (ks + 1) / P.ks);
     float acc[kOutSamples];
 #pragma unroll
     for (int q = 0; q < kOutSamples; ++q) acc[q] = 0.f;
 #pragma unroll 4
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    for (int i = i_begin + threadIdx.x; i < i_end; i += blockDim.x) {
         const int j = i / P.Cin, ci = i - j * P.Cin;
         float wv;
         if (P.kmajor) {
@@ -208,10 +221,32 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
         if (lane == 0) red[q][warp] = v;
     }
     __syncthreads();
+    double S = 0.0;
+    if (threadIdx.x < nn)
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) S += (double)red[threadIdx.x][i];
+    if (P.ks > 1) {
+        // publish this split's sums; the block that finishes last for (c, samples)
+        // adds all splits in split order (a fixed order: results are reproducible)
+        __shared__ bool last;
+        if (threadIdx.x < nn) P.part[((size_t)ks * P.N + n0 + threadIdx.x) * P.Cout + c] = S;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned *cnt = P.counters + (size_t)blockIdx.y * P.Cout + c;
+            last = atomicAdd(cnt, 1u) == (unsigned)P.ks - 1u;
+            if (last) *cnt = 0u;  // ready for the next forward
+        }
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+        if (threadIdx.x < nn) {
+            S = 0.0;
+            for (int k = 0; k < P.ks; ++k)
+                S += __ldcg(P.part + ((size_t)k * P.N + n0 + threadIdx.x) * P.Cout + c);
+        }
+    }
     if (threadIdx.x < nn) {
         const int q = threadIdx.x;
-        double S = 0.0;
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) S += (double)red[q][i];
         const double mean_y = S * P.inv_vol + (P.bias ? (double)P.bias[c] : 0.0);
         const double rstd = 1.0 / sqrt((double)P.rvar[c] + P.eps);
         const float out =
@@ -225,22 +260,65 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
 
 }  // namespace
 
+// Distinct d-intervals of the taps (host): taps whose input intervals along d
+// coincide (for example every tap when no padding crops the output) share one
+// accumulator in boxsum_kernel.
+static int unique_d_intervals(const Geometry &g, int lo[kMaxK], int hi[kMaxK], int of[kMaxK]) {
+    int n = 0;
+    for (int t = 0; t < kMaxK; ++t) {
+        of[t] = 0;
+        if (t >= g.kk[0]) continue;
+        const Interval iv = tap_interval(t, g.ss[0], g.pp[0], g.dil[0], g.Din, g.Do);
+        int u = 0;
+        while (u < n && !(lo[u] == iv.lo && hi[u] == iv.hi)) ++u;
+        if (u == n) {
+            lo[n] = iv.lo;
+            hi[n] = iv.hi;
+            ++n;
+        }
+        of[t] = u;
+    }
+    for (int u = n; u < kMaxK; ++u) lo[u] = 1, hi[u] = 0;
+    return n;
+}
+
 size_t bn_eval_smem_bytes(const convt3d_plan_s &p) {
+    int lo[kMaxK], hi[kMaxK], of[kMaxK];
+    const size_t nud = (size_t)unique_d_intervals(p.g, lo, hi, of);
     const size_t kd = p.g.kk[0], kh = p.g.kk[1];
-    return (kd * p.g.Hin * p.g.Win + kd * kh * p.g.Win) * sizeof(float);
+    return (nud * p.g.Hin * p.g.Win + kd * kh * p.g.Win) * sizeof(float);
+}
+
+// K splits of the contraction: about 2,048 products per block, at most 16 splits.
+int bn_eval_ksplits(int ntaps, int Cin) {
+    const int total = ntaps * Cin;
+    const int ks = (total + 2047) / 2048;
+    return ks < 1 ? 1 : (ks > 16 ? 16 : ks);
 }
 
 cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float *w_a, const float *w_b,
-                           const float *bias, const float *gamma, const float *beta, float *box, float *y,
-                           cudaStream_t s) {
+                           const float *bias, const float *gamma, const float *beta, float *box, double *part,
+                           unsigned *counters, float *y, cudaStream_t s) {
     const Geometry &g = p.g;
     BoxParams bp{x,        box,      g.N,      g.Cin,    g.Din,    g.Hin,    g.Win,    g.Do,     g.Ho,     g.Wo,
                  p.cl,     p.io16,   g.kk[0],  g.kk[1],  g.kk[2],  g.ss[0],  g.ss[1],  g.ss[2],  g.pp[0],
                  g.pp[1],  g.pp[2],  g.dil[0], g.dil[1], g.dil[2]};
+    bp.nud = unique_d_intervals(g, bp.ud_lo, bp.ud_hi, bp.ud_of);
     const size_t smem = bn_eval_smem_bytes(p);
-    cudaError_t e = cudaFuncSetAttribute(boxsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    void (*kern)(const BoxParams) = nullptr;
+    switch (bp.nud) {
+        case 1: kern = boxsum_kernel<1>; break;
+        case 2: kern = boxsum_kernel<2>; break;
+        case 3: kern = boxsum_kernel<3>; break;
+        case 4: kern = boxsum_kernel<4>; break;
+        case 5: kern = boxsum_kernel<5>; break;
+        case 6: kern = boxsum_kernel<6>; break;
+        case 7: kern = boxsum_kernel<7>; break;
+        default: return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    boxsum_kernel<<<(unsigned)(g.N * g.Cin), 256, smem, s>>>(bp);
+    kern<<<(unsigned)(g.N * g.Cin), 256, smem, s>>>(bp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -248,6 +326,9 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
     for (int j = 0; j < kMaxTaps; ++j) t.widx[j] = j < g.ntaps ? g.taps[j].widx : 0;
     OutParams op;
     op.box = box;
+    op.part = part;
+    op.counters = counters;
+    op.ks = p.ev_ks;
     op.w_a = w_a;
     op.w_b = w_b;
     op.bias = bias;
@@ -269,7 +350,7 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
     op.inv_vol = 1.0 / ((double)g.Do * g.Ho * g.Wo);
     op.scale = (double)p.d.scale;
     op.eps = (double)p.d.eps;
-    dim3 grid((unsigned)g.Cout, (unsigned)((g.N + kOutSamples - 1) / kOutSamples));
+    dim3 grid((unsigned)g.Cout, (unsigned)((g.N + kOutSamples - 1) / kOutSamples), (unsigned)p.ev_ks);
     bn_eval_out_kernel<<<grid, kOutThreads, 0, s>>>(op, t);
     return cudaGetLastError();
 }

@@ -192,6 +192,9 @@ struct convt3d_plan_s {
     float *run_var;
     float momentum;
     size_t off_box;         // evaluation-mode BatchNorm: per-tap input box sums
+    int ev_ks;              // evaluation-mode BatchNorm: K splits of the contraction (1 = none)
+    size_t off_evpart;      //   fp64 partial sums [ks][n][c] when ev_ks > 1
+    size_t off_evcnt;       //   per (c, sample block) arrival counters, zeroed by pack_weights
 };
 
 // Kernel launchers (defined in the .cu files); each returns cudaGetLastError().
@@ -212,9 +215,10 @@ cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, co
 cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, double *sums,
                                const float *gamma, const float *beta, float *y, cudaStream_t s);
 cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float *w_a, const float *w_b,
-                           const float *bias, const float *gamma, const float *beta, float *box, float *y,
-                           cudaStream_t s);
+                           const float *bias, const float *gamma, const float *beta, float *box, double *part,
+                           unsigned *counters, float *y, cudaStream_t s);
 size_t bn_eval_smem_bytes(const convt3d_plan_s &p);
+int bn_eval_ksplits(int ntaps, int Cin);
 void tc_cache_free(void *cache);
 void report_error(const char *fmt, ...);
 }  // namespace convt3d

@@ -389,6 +389,11 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     off = align_up(off + p->stat_doubles * 8, 256);
     p->off_box = off;
     if (eval_bn) off = align_up(off + (size_t)desc->N * desc->Cin * p->g.kvol * 4, 256);
+    p->ev_ks = eval_bn ? bn_eval_ksplits(p->g.ntaps, desc->Cin) : 1;
+    p->off_evpart = off;
+    if (p->ev_ks > 1) off = align_up(off + (size_t)p->ev_ks * desc->N * desc->Cout * 8, 256);
+    p->off_evcnt = off;
+    if (p->ev_ks > 1) off = align_up(off + (size_t)desc->Cout * ((desc->N + 15) / 16) * 4, 256);
     p->ws_total = off;
     *out = p;
     return CONVT3D_OK;
@@ -496,6 +501,10 @@ convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const void *wv, void *ws
     char *base = (char *)ws;
     cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing status word");
+    if (p->ev_ks > 1) {  // the split contraction's arrival counters start at zero (each forward resets them)
+        e = cudaMemsetAsync(base + p->off_evcnt, 0, p->ws_total - p->off_evcnt, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing arrival counters");
+    }
     e = launch_pack_weights(*p, w, (float *)(base + p->off_wpk_hi),
                             p->planes == 2 ? (float *)(base + p->off_wpk_lo) : nullptr, p->tc, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack_weights launch");
@@ -536,7 +545,8 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *
         // no convolution: input box sums and a contraction with the packed weight
         e = launch_bn_eval(*p, x, (const float *)(base + p->off_wpk_hi),
                            p->planes == 2 ? (const float *)(base + p->off_wpk_lo) : nullptr, b, gamma, beta,
-                           (float *)(base + p->off_box), y, s);
+                           (float *)(base + p->off_box), (double *)(base + p->off_evpart),
+                           (unsigned *)(base + p->off_evcnt), y, s);
         if (e != cudaSuccess) return cuda_fail(e, "evaluation-mode batchnorm launch");
         return CONVT3D_OK;
     }
