@@ -84,6 +84,55 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
     }
 }
 
+// Tensor-core layout [tap][cout_pad][cin_pad] through a 32 x 32 shared-memory
+// tile per (output channel, 32 taps, 32 input channels): the reads run along
+// the weight's contiguous tap axis, the writes along cin, both coalesced.
+// mode: 0 = split TF32 (fp32 hi/lo planes), 1 = TF32-rounded, 2 = bf16,
+// 3 = split bf16 (bf16 hi/lo planes).
+__global__ void pack_weights_kmajor_kernel(const float *__restrict__ w, float *__restrict__ hi,
+                                           float *__restrict__ lo, int Cin, int Cout, int k3, int ntaps,
+                                           int cin_pad, int cout_pad, int mode, int cin_g, int cout_g, int w16,
+                                           const __grid_constant__ TapIndex taps) {
+    __shared__ float tile[32][33];  // [ci][tap]
+    __shared__ int s_widx[32];      // this block's taps: one parameter read each (lanes that index
+                                    // the parameter table with different taps would serialise)
+    const int ci0 = blockIdx.x * 32, j0 = blockIdx.y * 32, co = blockIdx.z;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    const bool co_ok = co < Cout;
+    if (ty == 0) s_widx[tx] = j0 + tx < ntaps ? taps.widx[j0 + tx] : 0;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 32; r += 8) {
+        const int ci = ci0 + ty + r, j = j0 + tx;
+        float v = 0.0f;
+        if (co_ok && ci < Cin && j < ntaps && ci / cin_g == co / cout_g) {
+            const int64_t src = ((int64_t)ci * cout_g + co % cout_g) * k3 + s_widx[tx];
+            v = w16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(w)[src]) : w[src];
+        }
+        tile[ty + r][tx] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 32; r += 8) {
+        const int j = j0 + ty + r, ci = ci0 + tx;
+        if (j >= ntaps || ci >= cin_pad) continue;
+        const int64_t i = ((int64_t)j * cout_pad + co) * cin_pad + ci;
+        const float v = tile[tx][ty + r];
+        if (mode == 3) {
+            split_bf16(v, reinterpret_cast<__nv_bfloat16 *>(hi)[i], reinterpret_cast<__nv_bfloat16 *>(lo)[i]);
+        } else if (mode == 0) {
+            float h, l;
+            split_tf32(v, h, l);
+            hi[i] = h;
+            lo[i] = l;
+        } else if (mode == 2) {
+            reinterpret_cast<__nv_bfloat16 *>(hi)[i] = __float2bfloat16_rn(v);
+        } else {
+            hi[i] = round_tf32(v);
+        }
+    }
+}
+
 // NCDHW -> NDHWC(+channel padding) transpose of one sample, 32 positions x
 // 32 channels per block through shared memory; both the global read (along
 // positions) and the write (along channels) are 128-byte rows.
@@ -163,6 +212,14 @@ cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *
                                 cudaStream_t s) {
     TapIndex t;
     for (int j = 0; j < kMaxTaps; ++j) t.widx[j] = j < p.g.ntaps ? p.g.taps[j].widx : 0;
+    const int mode = p.bf16 ? (p.planes == 2 ? 3 : 2) : (p.planes == 1 ? 1 : 0);
+    if (kmajor) {  // tensor-core layout (cout_pad rows of every tap; cin_pad is a multiple of 32)
+        dim3 grid((unsigned)(p.cin_pad / 32), (unsigned)((p.g.ntaps + 31) / 32), (unsigned)p.cout_pad);
+        pack_weights_kmajor_kernel<<<grid, dim3(32, 8), 0, s>>>(w, hi, lo, p.g.Cin, p.g.Cout, p.g.kvol, p.g.ntaps,
+                                                                p.cin_pad, p.cout_pad, mode, p.g.Cin / p.g.G,
+                                                                p.g.Cout / p.g.G, p.io16, t);
+        return cudaGetLastError();
+    }
     const int64_t total = (int64_t)p.g.ntaps * p.cin_pad * p.cout_pad;
     const int threads = 256;
     const int blocks = (int)((total + threads - 1) / threads < 4096 ? (total + threads - 1) / threads : 4096);
