@@ -87,6 +87,10 @@ struct GroupDesc {
     int8_t mdw[8];
     uint8_t mmask[8];
     int8_t me[8][2];
+    // The merged walk flattened (tensor-core launch): K steps step0.. in (d-slice,
+    // h-tap, merged w-tap) order, steps_per_a per d-slice, so a tile's trimmed
+    // d-slice range is one contiguous run of steps.
+    int step0, steps_per_a;
 };
 
 // Taps a tile issues.  Along d, a class's taps have decreasing input offsets

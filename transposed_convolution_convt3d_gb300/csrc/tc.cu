@@ -87,6 +87,16 @@ static_assert(kTcChunk % kChunk == 0, "channel padding must be a multiple of the
 constexpr uint32_t kRowBytes = kChunk * 4;
 constexpr uint32_t kABytes = kTcTileM * kRowBytes;  // one 128 x kChunk fp32 activation plane
 
+// One K step of a merged w-parity walk: which class's activation slice (0 or 1
+// within the pair) at offsets (od, oh, ow) from the class's low corner, the
+// weight slices of taps tb0 and (both classes) tb1, and the classes it feeds.
+struct StepDesc {
+    int16_t tb0, tb1;  // tb1 < 0: one class
+    uint8_t cls, mask, ow, oh;
+    uint8_t od, pad_[3];
+};
+constexpr int kMaxSteps = 512;  // <= 4 groups x 4 d-slices x 4 h-taps x 8 merged w-taps
+
 struct TcParams {
     CUtensorMap a_hi[kMaxClasses];
     CUtensorMap a_lo[kMaxClasses];
@@ -112,6 +122,7 @@ struct TcParams {
     GroupDesc grp[kMaxGroups];
     ClassDesc cls[kMaxClasses];
     TapDesc taps[kMaxTaps];
+    StepDesc steps[kMaxSteps];  // merged walks (MERGED kernels)
 };
 
 struct Tile {
@@ -420,21 +431,57 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 const int q0 = T.t * kTcTileM;
                 const int qd0 = q0 / (G.Qh * G.Qw), qh0 = (q0 / G.Qw) % G.Qh, qw0 = q0 % G.Qw;
                 if constexpr (MERGED) {
+                    // the tile's run of the flattened walk (d-slices: the same for both classes)
                     const ClassDesc &C0 = P.cls[G.cls[0]], &C1 = P.cls[G.cls[1]];
-                    const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);  // d-slices: same for both
+                    const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);
                     const int nhw0 = C0.nt_h * C0.nt_w;
                     const int a_begin = tr.begin / nhw0, a_end = (tr.end + nhw0 - 1) / nhw0;
-                    for (int a = a_begin; ok && a < a_end; ++a)
-                        for (int b = 0; ok && b < C0.nt_h; ++b)
-                            for (int m = 0; ok && m < G.nm; ++m) {
-                                const int mask = G.mmask[m];
-                                const int t0 = C0.tap_begin + (a * C0.nt_h + b) * C0.nt_w + G.me[m][0];
-                                const int t1 = C1.tap_begin + (a * C1.nt_h + b) * C1.nt_w + G.me[m][1];
-                                if (mask & 1)
-                                    issue_tap(T, G.cls[0], C0, qd0, qh0, qw0, P.taps[t0], t0, mask == 3 ? t1 : -1);
-                                else
-                                    issue_tap(T, G.cls[1], C1, qd0, qh0, qw0, P.taps[t1], t1, -1);
+                    const int s_end = G.step0 + a_end * G.steps_per_a;
+                    // each class's base pixel of the tile
+                    const int w00 = qw0 + C0.lo_w, h00 = qh0 + C0.lo_h, d00 = qd0 + C0.lo_d;
+                    const int w01 = qw0 + C1.lo_w, h01 = qh0 + C1.lo_h, d01 = qd0 + C1.lo_d;
+                    for (int st = G.step0 + a_begin * G.steps_per_a; ok && st < s_end; ++st) {
+                        const StepDesc e = P.steps[st];
+                        const bool one = e.cls != 0;
+                        const int cls = one ? G.cls[1] : G.cls[0];
+                        const int w0 = one ? w01 : w00, h0 = one ? h01 : h00, d0 = one ? d01 : d00;
+                        const uint32_t nb = e.tb1 >= 0 ? 2u : 1u;
+                        for (int kc = 0; kc < P.kc; ++kc) {
+                            if (!ptx::mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, &abort_flag, kWaitNs)) {
+                                ok = false;
+                                break;
                             }
+                            const uint32_t fb = full0 + 8 * stage;
+                            const uint32_t sb = smem_base + (uint32_t)stage * P.stage_bytes;
+                            ptx::mbar_arrive_expect_tx(fb, (uint32_t)kPlanes * (kABytes + nb * P.b_bytes));
+                            const int c0 = kc * P.chunk;
+                            const uint32_t sbb = sb + (uint32_t)kPlanes * kABytes;
+#if CONVT3D_OFFSETS_DHW
+                            ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, e.od, e.oh, e.ow);
+                            if (kPlanes == 2)
+                                ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, e.od, e.oh,
+                                                        e.ow);
+#else
+                            ptx::tma_load_im2col_5d(sb, &P.a_hi[cls], fb, c0, w0, h0, d0, T.n, e.ow, e.oh, e.od);
+                            if (kPlanes == 2)
+                                ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, e.ow, e.oh,
+                                                        e.od);
+#endif
+                            ptx::tma_load_3d(sbb, &P.b_hi, fb, c0, 0, e.tb0);
+                            if (e.tb1 >= 0) ptx::tma_load_3d(sbb + P.b_bytes, &P.b_hi, fb, c0, 0, e.tb1);
+                            if (kPlanes == 2) {
+                                const uint32_t lo = sbb + (uint32_t)kBSlots * P.b_bytes;
+                                ptx::tma_load_3d(lo, &P.b_lo, fb, c0, 0, e.tb0);
+                                if (e.tb1 >= 0) ptx::tma_load_3d(lo + P.b_bytes, &P.b_lo, fb, c0, 0, e.tb1);
+                            }
+                            armed |= 1u << stage;
+                            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                            if (++stage == P.stages) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                    }
                 } else {
                     for (int ci = 0; ok && ci < G.ncls; ++ci) {
                         const int cls = G.cls[ci];
@@ -544,15 +591,14 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);
                     const int nhw0 = C0.nt_h * C0.nt_w;
                     const int a_begin = tr.begin / nhw0, a_end = (tr.end + nhw0 - 1) / nhw0;
+                    const int s_end = G.step0 + a_end * G.steps_per_a;
                     uint32_t ini = 0;  // bit c: class c's accumulator holds a product
-                    for (int a = a_begin; ok && a < a_end; ++a)
-                        for (int b = 0; ok && b < C0.nt_h; ++b)
-                            for (int m = 0; ok && m < G.nm; ++m) {
-                                const uint32_t mask = G.mmask[m];
-                                const uint32_t d_tmem = acc_base + (mask == 2u ? (uint32_t)P.cout_pad : 0u);
-                                mma_tap(d_tmem, mask == 3u ? idesc2 : idesc, (ini & mask) == 0u);
-                                ini |= mask;
-                            }
+                    for (int st = G.step0 + a_begin * G.steps_per_a; ok && st < s_end; ++st) {
+                        const uint32_t mask = P.steps[st].mask;
+                        const uint32_t d_tmem = acc_base + (mask == 2u ? (uint32_t)P.cout_pad : 0u);
+                        mma_tap(d_tmem, mask == 3u ? idesc2 : idesc, (ini & mask) == 0u);
+                        ini |= mask;
+                    }
                 } else {
                     // flat step loop per class (the issue rate of the MMA-bound shapes depends on it)
                     for (int ci = 0; ok && ci < G.ncls; ++ci) {
@@ -1190,6 +1236,35 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         for (int i = 0; i < p.ngroups; ++i) {
             P->grp[i] = p.grp[i];
             if (p.grp[i].ncls > ncls_max) ncls_max = p.grp[i].ncls;
+        }
+        if (p.merged) {
+            // flatten each pair's merged walk: (d-slice a, h-tap b, merged w-tap m)
+            int ns = 0;
+            for (int gi = 0; gi < p.ngroups; ++gi) {
+                GroupDesc &G = P->grp[gi];
+                const ClassDesc &C0 = g.cls[G.cls[0]], &C1 = g.cls[G.cls[1]];
+                G.step0 = ns;
+                G.steps_per_a = C0.nt_h * G.nm;
+                if (ns + C0.nt_d * G.steps_per_a > kMaxSteps) return cudaErrorInvalidConfiguration;
+                for (int a = 0; a < C0.nt_d; ++a)
+                    for (int b = 0; b < C0.nt_h; ++b)
+                        for (int m = 0; m < G.nm; ++m) {
+                            const int mask = G.mmask[m];
+                            StepDesc e{};
+                            const int t0 = (mask & 1) ? C0.tap_begin + (a * C0.nt_h + b) * C0.nt_w + G.me[m][0] : -1;
+                            const int t1 = (mask & 2) ? C1.tap_begin + (a * C1.nt_h + b) * C1.nt_w + G.me[m][1] : -1;
+                            const ClassDesc &C = (mask & 1) ? C0 : C1;
+                            const TapDesc &td = g.taps[(mask & 1) ? t0 : t1];
+                            e.cls = (mask & 1) ? 0 : 1;
+                            e.mask = (uint8_t)mask;
+                            e.tb0 = (int16_t)((mask & 1) ? t0 : t1);
+                            e.tb1 = (int16_t)(mask == 3 ? t1 : -1);
+                            e.ow = (uint8_t)(td.dw - C.lo_w);
+                            e.oh = (uint8_t)(td.dh - C.lo_h);
+                            e.od = (uint8_t)(td.dd - C.lo_d);
+                            P->steps[ns++] = e;
+                        }
+            }
         }
         for (int i = 0; i < kMaxClasses; ++i) P->cls[i] = g.cls[i];
         for (int i = 0; i < kMaxTaps; ++i) P->taps[i] = g.taps[i];
