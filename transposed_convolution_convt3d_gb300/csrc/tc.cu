@@ -830,9 +830,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 };
                 // sigmoid(f * e) for 8 pairs, with the polynomial's coefficients
                 // pre-multiplied by powers of f (see sigmoid_coefficients), then the stores
-                auto finish = [&](int c0, int row_off, uint64_t (&e)[8], const uint64_t (&A)[4]) {
+                auto sigmoid16 = [](const uint64_t (&e)[8], const uint64_t (&A)[4], float (&o)[16]) {
                     const uint64_t half2 = pack2(0.5f, 0.5f);
-                    float o[16];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint64_t x2 = fmul2(e[k], e[k]);
@@ -841,6 +840,10 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         q = ffma2(q, x2, A[0]);
                         unpack2(ffma2(e[k], q, half2), o[2 * k], o[2 * k + 1]);
                     }
+                };
+                auto finish = [&](int c0, int row_off, uint64_t (&e)[8], const uint64_t (&A)[4]) {
+                    float o[16];
+                    sigmoid16(e, A, o);
                     if (row_off >= 0) store_row16(yn, row_off, c0, o);
                 };
                 if constexpr (KEEP == 2) {
@@ -956,7 +959,44 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         f[ci] = __frcp_rn(sum[ci]);
                     }
                 }
-                // 3) outputs: weight t = f * e in (0, 1], then sigmoid(t)
+                // 3) outputs: weight t = f * e in (0, 1], then sigmoid(t). A w-parity pair's
+                //    two classes are the adjacent columns (2 qw, 2 qw + 1) of one output row:
+                //    with both in this thread, each channel's two outputs go out as one
+                //    8-byte (fp32) or 4-byte (bf16) store, whole sectors per warp.
+                if (KEEP == 1 && G.ncls == 2 && pair_store && !P.cl && off[0] >= 0 && off[1] >= 0) {
+                    uint64_t A0[4], A1[4];
+                    sigmoid_coefficients(f[0], A0);
+                    sigmoid_coefficients(f[1], A1);
+#pragma unroll
+                    for (int jj = 0; jj < kKeep; ++jj) {
+                        const int j = half + jj * kHalves;
+                        if (j >= nchunks) continue;
+                        const int c0 = 16 * j;
+                        float o0[16], o1[16];
+                        sigmoid16(e[jj][0], A0, o0);
+                        sigmoid16(e[jj][1], A1, o1);
+                        if (P.io16) {
+                            __nv_bfloat16 *yh = reinterpret_cast<__nv_bfloat16 *>(P.y) + (int64_t)T.n * C * V;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (c0 + i < C)
+                                    *reinterpret_cast<__nv_bfloat162 *>(yh + (int64_t)(c0 + i) * V + off[0]) =
+                                        __floats2bfloat162_rn(o0[i], o1[i]);
+                        } else {
+                            float *d = yn + (int64_t)c0 * V + off[0];
+                            if (c0 + 16 <= C) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    *reinterpret_cast<float2 *>(d + (int64_t)i * V) = make_float2(o0[i], o1[i]);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (c0 + i < C)
+                                        *reinterpret_cast<float2 *>(d + (int64_t)i * V) = make_float2(o0[i], o1[i]);
+                            }
+                        }
+                    }
+                } else
                 _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
                     uint64_t A[4];
                     sigmoid_coefficients(f[ci], A);
@@ -1193,7 +1233,12 @@ static void (*select_kernel(const convt3d_plan_s &p, int &threads))(const TcPara
             threads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
             // registers hold the exponentials when each warp owns at most
             // kSoftmaxKeepChunks 16-channel chunks
-            if (EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps == 8 && p.g.ss[2] == 2 &&
+            // Stride 2 along w with Cout <= 64, single-product formats: each warp of a
+            // lane quarter owns one class's channels (no exchange; measured faster
+            // there). The split formats, whose longer K steps leave the epilogue more
+            // room, take the channel split below: one (max, sum) exchange per tile
+            // buys each channel's (even, odd) columns stored as one pair.
+            if ((OPS == 1 || OPS == 2) && EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps == 8 && p.g.ss[2] == 2 &&
                 p.cout_pad <= 16 * 2 * kSoftmaxKeepChunks)
                 return convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2, OPS, MERGED>;
             return p.cout_pad <= 16 * kSoftmaxKeepChunks * (EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps / 4)
