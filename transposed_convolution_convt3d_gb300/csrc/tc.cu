@@ -693,7 +693,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             return gn_inline ? ((16 * j) / cpg) % kHalves == half : j % kHalves == half;
         };
         int iter = 0;
-        for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++iter) {
+        int tile = blockIdx.x;
+        for (; tile < P.total_tiles; tile += gridDim.x, ++iter) {
             const Tile T = decode(P, s_grp, tile);
             const GroupDesc &G = s_grp[T.gi];
             const int acc = iter & 1;
@@ -1146,6 +1147,13 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             ptx::tc_fence_before();
             ptx::mbar_arrive(tempty0 + 8 * acc);
         }
+        // Softmax with the channels of a lane quarter split between warps meets its
+        // partner at a named barrier once per tile. A warp whose wait ran out left the
+        // loop early: it still meets that barrier once for every tile it did not
+        // finish, so the partner never waits on a warp that has gone.
+        if constexpr (sm && KEEP != 2 && kHalves > 1)
+            for (; tile < P.total_tiles; tile += gridDim.x)
+                asm volatile("bar.sync %0, %1;" ::"r"(1 + quarter), "r"(32 * kHalves) : "memory");
     }
 
     // ------------------------------------------------------------ teardown
