@@ -22,6 +22,8 @@
 // The work is O(N*Cin*D*H*W*k + N*Cout*Cin*k^3), a read of x and of the weight.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "convt3d_internal.h"
 
 namespace convt3d {
@@ -181,36 +183,63 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
     float acc[kOutSamples];
 #pragma unroll
     for (int q = 0; q < kOutSamples; ++q) acc[q] = 0.f;
+    // The loop over this thread's products, specialised on the box-row access (four
+    // 16-byte loads, or scalars for a partial sample block) and the weight layout
+    // (0: tensor-core fp32 planes, 1: tensor-core bf16 planes, 2: FFMA layout), with
+    // the (tap, ci) index stepped instead of divided per product.
+    auto contract = [&](auto vec_t, auto wm_t) {
+        constexpr bool kVec = decltype(vec_t)::value;
+        constexpr int kWm = decltype(wm_t)::value;
+        const int i0 = i_begin + (int)threadIdx.x;
+        int j = i0 / P.Cin, ci = i0 - j * P.Cin;
+        const int dj = (int)blockDim.x / P.Cin, dci = (int)blockDim.x - dj * P.Cin;
 #pragma unroll 4
-    for (int i = i_begin + threadIdx.x; i < i_end; i += blockDim.x) {
-        const int j = i / P.Cin, ci = i - j * P.Cin;
-        float wv;
-        if (P.kmajor) {
-            const size_t o = ((size_t)j * P.cout_pad + c) * P.cin_pad + ci;
-            if (P.wbf16)  // bf16 planes: hi (+ lo, split bf16)
-                wv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_a)[o]) +
-                     (P.w_b ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_b)[o]) : 0.f);
-            else  // hi + lo: the fp32 weight, exactly (or its TF32 rounding)
-                wv = P.w_b ? P.w_a[o] + P.w_b[o] : P.w_a[o];
-        } else {
-            wv = P.w_a[((size_t)j * P.cin_pad + ci) * P.cout_pad + c];
-        }
-        const float *b = P.box + ((size_t)taps.widx[j] * P.Cin + ci) * P.N + n0;
-        if (vec) {
-#pragma unroll
-            for (int q4 = 0; q4 < kOutSamples / 4; ++q4) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(b) + q4);
-                acc[4 * q4] = fmaf(wv, v.x, acc[4 * q4]);
-                acc[4 * q4 + 1] = fmaf(wv, v.y, acc[4 * q4 + 1]);
-                acc[4 * q4 + 2] = fmaf(wv, v.z, acc[4 * q4 + 2]);
-                acc[4 * q4 + 3] = fmaf(wv, v.w, acc[4 * q4 + 3]);
+        for (int i = i0; i < i_end; i += blockDim.x) {
+            float wv;
+            if constexpr (kWm == 2) {
+                wv = P.w_a[((size_t)j * P.cin_pad + ci) * P.cout_pad + c];
+            } else {
+                const size_t o = ((size_t)j * P.cout_pad + c) * P.cin_pad + ci;
+                if constexpr (kWm == 1)  // bf16 planes: hi (+ lo, split bf16)
+                    wv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_a)[o]) +
+                         (P.w_b ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_b)[o]) : 0.f);
+                else  // hi + lo: the fp32 weight, exactly (or its TF32 rounding)
+                    wv = P.w_b ? P.w_a[o] + P.w_b[o] : P.w_a[o];
             }
-        } else {
+            const float *b = P.box + ((size_t)taps.widx[j] * P.Cin + ci) * P.N + n0;
+            if constexpr (kVec) {
 #pragma unroll
-            for (int q = 0; q < kOutSamples; ++q)
-                if (q < nn) acc[q] = fmaf(wv, b[q], acc[q]);
+                for (int q4 = 0; q4 < kOutSamples / 4; ++q4) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(b) + q4);
+                    acc[4 * q4] = fmaf(wv, v.x, acc[4 * q4]);
+                    acc[4 * q4 + 1] = fmaf(wv, v.y, acc[4 * q4 + 1]);
+                    acc[4 * q4 + 2] = fmaf(wv, v.z, acc[4 * q4 + 2]);
+                    acc[4 * q4 + 3] = fmaf(wv, v.w, acc[4 * q4 + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < kOutSamples; ++q)
+                    if (q < nn) acc[q] = fmaf(wv, __ldg(b + q), acc[q]);
+            }
+            j += dj;
+            ci += dci;
+            if (ci >= P.Cin) {
+                ci -= P.Cin;
+                ++j;
+            }
         }
-    }
+    };
+    using T_ = std::true_type;
+    using F_ = std::false_type;
+    using W0 = std::integral_constant<int, 0>;
+    using W1 = std::integral_constant<int, 1>;
+    using W2 = std::integral_constant<int, 2>;
+    if (!P.kmajor)
+        vec ? contract(T_{}, W2{}) : contract(F_{}, W2{});
+    else if (P.wbf16)
+        vec ? contract(T_{}, W1{}) : contract(F_{}, W1{});
+    else
+        vec ? contract(T_{}, W0{}) : contract(F_{}, W0{});
     __shared__ float red[kOutSamples][kOutThreads / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
