@@ -84,6 +84,20 @@ def test_plan_validation(lib, kw, status):
     assert lib.convt3d_last_error()
 
 
+def test_eval_batchnorm_box_planes_follow_distinct_d_intervals(lib):
+    """Evaluation-mode BN keeps one H x W plane of box sums per distinct d-interval
+    of the taps (shared memory, at most 200 KB per block): unpadded, all three
+    taps of k = 3 cover the whole input along d and share one plane (accepted at
+    200 x 200); with padding 1 the first tap's interval starts one plane later and
+    the last tap's ends one plane earlier, three planes are needed and the same
+    extent is rejected as unsupported."""
+    st, h = create(lib, epilogue=4, k=3, pad=0, Din=4, Hin=200, Win=200)
+    assert st == 0, lib.convt3d_last_error()
+    lib.convt3d_plan_destroy(h)
+    st, h = create(lib, epilogue=4, k=3, pad=1, Din=4, Hin=200, Win=200)
+    assert st == 2 and not h.value
+
+
 def test_ffma_accepts_what_tensor_path_rejects(lib):
     st, h = create(lib, stride=2, k=3, pad=1, Cout=144, precision=1)
     assert st == 0
