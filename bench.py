@@ -429,7 +429,7 @@ def run_gpu(args, spec):
     line = {
         "metric": "useful_tflops", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": compute_dtype(args.precision), "data": "synthetic",
         "config": {"workload": spec.name, "precision": args.precision, "io": "bf16" if args.io_bf16 else "f32", "x": [spec.N, spec.Cin, spec.D, spec.H, spec.W],
                    "w": [spec.Cin, spec.Cout, spec.k, spec.k, spec.k], "stride": spec.stride, "pad": spec.pad,
                    "out_pad": spec.out_pad, "out": list(plan.out_shape), "epilogue": spec.epilogue,
@@ -446,6 +446,13 @@ def run_gpu(args, spec):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def compute_dtype(precision):
+    """The arithmetic type of the products: the split formats (and the FFMA
+    ablation) compute to fp32 accuracy; the single-product formats round their
+    operands to TF32 or bf16."""
+    return {"3xtf32": "f32", "3xbf16": "f32", "ffma": "f32", "tf32": "tf32", "bf16": "bf16"}[precision]
 
 
 def host_link_ms(host, y_dev, y_host, stream, dev, reps=3):

@@ -49,3 +49,10 @@ def test_fastdiv_matches_integer_division(tmp_path):
     bad, checked = (int(v) for v in out.stdout.split())
     assert out.returncode == 0 and bad == 0
     assert checked > 20_000_000
+
+
+def test_bench_reports_the_compute_dtype_of_each_precision():
+    import bench
+    assert bench.compute_dtype("3xtf32") == "f32" and bench.compute_dtype("3xbf16") == "f32"
+    assert bench.compute_dtype("ffma") == "f32"
+    assert bench.compute_dtype("tf32") == "tf32" and bench.compute_dtype("bf16") == "bf16"
