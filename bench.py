@@ -33,7 +33,13 @@ if ROOT not in sys.path:
 
 import workloads  # noqa: E402
 
-DEFAULT_WORKLOAD = workloads.GN.name
+# The largest configuration (l2_p77's module: ConvTranspose3d k=5, x2, BatchNorm3d
+# with batch statistics, AdaptiveAvgPool3d(1); 5.37e11 useful flop per step).
+DEFAULT_WORKLOAD = workloads.BN.name
+# The other configurations, timed GPU-only in the same process for the
+# "configs" key of the line (the bench's own workload is left out).
+OTHER_WORKLOADS = [workloads.TINY, workloads.GN, workloads.BN, workloads.SOFTMAX, workloads.IDENTITY,
+                   workloads.BN_EVAL]
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 / BF16 tensor rates (GB300)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -47,7 +53,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.BY_NAME))
-    ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "3xbf16", "tf32", "bf16", "ffma"])
+    ap.add_argument("--precision", default="3xtf32", choices=["3xtf32", "3xbf16", "tf32", "bf16", "fp16", "ffma"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the CPU baseline sample")
@@ -55,8 +61,14 @@ def parse():
     ap.add_argument("--e2e-chunks", type=int, default=4, help="sample chunks the end-to-end pipeline overlaps")
     ap.add_argument("--io-bf16", action="store_true",
                     help="x, w and y as bf16 tensors (requires --precision bf16)")
+    ap.add_argument("--io-fp16", action="store_true",
+                    help="x, w and y as fp16 tensors (requires --precision fp16)")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="streams per copy direction in the end-to-end pipeline")
+    ap.add_argument("--config-steps", type=int, default=10,
+                    help="timed steps per other configuration in the \"configs\" key (0: leave it out)")
+    ap.add_argument("--config-precisions", default="3xtf32,3xbf16",
+                    help="precisions the other configurations are timed in")
     return ap.parse_args()
 
 
@@ -147,9 +159,9 @@ def kernel_source_sha(precision):
     return h.hexdigest()[:16]
 
 
-def committed_traffic(precision, workload):
-    """DRAM bytes per launch of the main kernel from a committed ncu summary, if the
-    summary was taken on the current kernel source (else None)."""
+def committed_profile_value(precision, workload, field):
+    """A number (`field = value`) from the committed ncu summary of the main
+    kernel, if that summary was taken on the current kernel source (else None)."""
     d = os.path.join(ROOT, "profiles")
     if not os.path.isdir(d):
         return None
@@ -160,12 +172,25 @@ def committed_traffic(precision, workload):
         text = open(os.path.join(d, name)).read()
         m_sha = re.search(r"kernel_source_sha\s*[:=]\s*([0-9a-f]{16})", text)
         m_w = re.search(r"workload\s*[:=]\s*(\S+)", text)
-        m_t = re.search(r"traffic_bytes_per_launch\s*[:=]\s*([0-9.eE+]+)", text)
+        m_t = re.search(field + r"\s*[:=]\s*([0-9.eE+]+)", text)
         m_p = re.search(r"precision\s*[:=]\s*(\S+)", text)
         if m_sha and m_t and m_w and m_sha.group(1) == want and m_w.group(1) == workload and \
                 (not m_p or m_p.group(1) == precision):
             return float(m_t.group(1))
     return None
+
+
+def committed_traffic(precision, workload):
+    """DRAM bytes per launch of the main kernel (ncu dram__bytes_read.sum +
+    dram__bytes_write.sum) from the committed summary, else None."""
+    return committed_profile_value(precision, workload, "traffic_bytes_per_launch")
+
+
+def committed_tensor_active(precision, workload):
+    """ncu's sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of the
+    main kernel from the committed summary, else None."""
+    v = committed_profile_value(precision, workload, "tensor_pipe_active")
+    return None if v is None else (v / 100.0 if v > 1.0 else v)
 
 
 # ------------------------------------------------------------ replicas ----
@@ -256,29 +281,130 @@ def run_reference(args, spec):
     print(json.dumps(line), flush=True)
 
 
+# -------------------------------------------------------------- roofline ----
+
+def roofline(info, precision, useful, kernel_ms, ms_per_step, pk, eval_bn):
+    """Roofline of the main kernel: algorithmic work of one launch over its
+    CUDA-event time, against the measured peak of its bound."""
+    if eval_bn:
+        # two HBM-bound kernels (box sums over x, contraction with the packed weight)
+        achieved = info["forward_min_bytes"] / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": f"{pk['source']} HBM copy bandwidth",
+                "algorithmic_bytes": info["forward_min_bytes"]}
+    elif precision != "ffma":
+        bf = precision in ("bf16", "3xbf16", "fp16")  # kind::f16: the same tensor rate for bf16 and fp16
+        peak = pk["bf16_tflops"] * (1.0 if bf else TF32_OVER_BF16)
+        achieved = useful / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": (f"{pk['source']} bf16 burst" if bf else
+                                f"{pk['source']} bf16 burst x nominal TF32/BF16 ratio {TF32_OVER_BF16:.4f}"),
+                # issued tensor flop (three products per term in the split formats) over that peak;
+                # the peak was measured at a lower clock than these kernels run at, so this can
+                # read above 1: the tensor pipe's own utilisation is tensor_pipe_active (ncu)
+                "issued_frac": info["issued_mma_flop"] / (kernel_ms * 1e-3) / 1e12 / peak}
+        if precision in ("3xtf32", "3xbf16"):
+            roof["frac_of_" + precision + "_peak"] = achieved / (peak / 3.0)
+    else:
+        peak = SMS * FP32_FMA_PER_CLK_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+        achieved = useful / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 flop x max SM clock",
+                "issued_frac": info["issued_mma_flop"] / (kernel_ms * 1e-3) / 1e12 / peak}
+    roof["kernel"] = ("boxsum_kernel + bn_eval_out_kernel" if eval_bn else
+                      "ffma_conv_kernel" if precision == "ffma" else "convt3d_tc_gemm")
+    roof["kernel_ms"] = kernel_ms
+    roof["kernel_share_of_step"] = kernel_ms / ms_per_step
+    roof["min_bytes"] = info["gemm_min_bytes"]
+    return roof
+
+
+def gpu_hold(cycles=300_000):
+    """Keep the GPU busy for ~0.15 ms before a step's start event, so that the
+    host has queued the step's launches by the time the event is recorded: the
+    timed region then holds the device work of the step, not the host's
+    enqueue latency after the previous step's synchronisation."""
+    import torch
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(cycles)
+
+
+PRECISION_CODES = {"3xtf32": 0, "ffma": 1, "tf32": 2, "bf16": 3, "3xbf16": 4, "fp16": 5}
+
+
+def time_config(spec, precision, steps, warmup, dev, stream, flush, pk):
+    """GPU-only timing of one configuration: pack_weights + forward per step,
+    L2 flushed before each, CUDA events on the launching stream (the main
+    kernel's own events from the library's profiling hooks)."""
+    import torch
+
+    from transposed_convolution_convt3d_gb300 import Plan
+    inputs = workloads.make_inputs(spec)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inputs.items()}
+    plan = Plan.from_spec(spec, precision=PRECISION_CODES[precision])
+    info = plan.info
+    ws = plan.new_workspace(dev)
+    y = plan.new_output(dev)
+    eval_bn = spec.epilogue == workloads.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL
+    if eval_bn:
+        plan.set_running_stats(*(t.to(dev) for t in workloads.make_running_stats(spec)))
+    step_ms, kern_ms = [], []
+    for i in range(warmup + steps):
+        flush.fill_(float(i))
+        gpu_hold()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        plan.profile_enable(not eval_bn and i >= warmup)
+        a.record(stream)
+        plan.pack_weights(d["w"], ws, stream)
+        f0.record(stream)
+        plan.forward(d["x"], y, ws, d["bias"], d["gamma"], d["beta"], stream)
+        f1.record(stream)
+        b.record(stream)
+        if i >= warmup:
+            b.synchronize()
+            step_ms.append(a.elapsed_time(b))
+            kern_ms.append(f0.elapsed_time(f1) if eval_bn else plan.profile_read())
+    plan.profile_enable(False)
+    plan.check(ws, stream)
+    ms = sum(step_ms) / len(step_ms)
+    km = sum(kern_ms) / len(kern_ms)
+    useful = spec.useful_flop()
+    roof = roofline(info, precision, useful, km, ms, pk, eval_bn)
+    out = {"workload": spec.name, "precision": precision, "ms_per_step": ms,
+           "useful_tflops": useful / (ms * 1e-3) / 1e12, "kernel": roof["kernel"], "kernel_ms": km,
+           "bound": roof["bound"], "frac": roof["frac"],
+           "hbm_frac_whole_step": info["forward_min_bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    for k in ("issued_frac", "frac_of_3xtf32_peak", "frac_of_3xbf16_peak"):
+        if k in roof:
+            out[k] = roof[k]
+    out["tensor_pipe_active"] = None if eval_bn else committed_tensor_active(precision, spec.name)
+    del ws, y, d
+    torch.cuda.synchronize()
+    return out
+
+
 # ------------------------------------------------------------------ GPU ----
 
 def run_gpu(args, spec):
     import torch
     import torch.distributed as dist
 
-    from transposed_convolution_convt3d_gb300 import (PREC_3XBF16, PREC_3XTF32, PREC_BF16, PREC_FFMA, PREC_TF32,
-                                                      HostPipeline,
-                                                      Plan)
+    from transposed_convolution_convt3d_gb300 import HostPipeline, Plan
 
     world, rank, local = dist_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    prec = {"3xtf32": PREC_3XTF32, "3xbf16": PREC_3XBF16, "tf32": PREC_TF32, "bf16": PREC_BF16,
-            "ffma": PREC_FFMA}[args.precision]
+    prec = PRECISION_CODES[args.precision]
 
-    if args.io_bf16:
-        spec = spec.replace(io_bf16=True)
+    io16 = torch.bfloat16 if args.io_bf16 else (torch.float16 if args.io_fp16 else None)
+    if io16 is not None:
+        spec = spec.replace(io_bf16=args.io_bf16, io_fp16=args.io_fp16)
     inputs = workloads.make_inputs(spec)
-    if args.io_bf16:
-        inputs["x"], inputs["w"] = inputs["x"].to(torch.bfloat16), inputs["w"].to(torch.bfloat16)
+    if io16 is not None:
+        inputs["x"], inputs["w"] = inputs["x"].to(io16), inputs["w"].to(io16)
     d = {k: (v.to(dev) if v is not None else None) for k, v in inputs.items()}
     plan = Plan.from_spec(spec, precision=prec)
     info = plan.info
@@ -324,6 +450,7 @@ def run_gpu(args, spec):
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(float(i))  # evict x, y and the packed weights from L2 between steps
+        gpu_hold()
         ev[i][0].record(stream)
         if eval_bn:
             fwd_ev.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
@@ -356,7 +483,7 @@ def run_gpu(args, spec):
         pipe = HostPipeline(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
                             spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, prec,
                             chunks=args.e2e_chunks, device=dev, copy_streams=args.e2e_copy_streams,
-                            io_bf16=args.io_bf16)
+                            io_bf16=args.io_bf16, io_fp16=args.io_fp16)
         if running is not None:
             pipe.set_running_stats(*running)
         y_host = torch.empty(pipe.full_shape, dtype=pipe.plan.io_dtype).pin_memory()
@@ -388,37 +515,23 @@ def run_gpu(args, spec):
 
     pk = peaks()
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
-    if eval_bn:
-        # two HBM-bound kernels (box sums over x, contraction with the packed weight)
-        achieved = info["forward_min_bytes"] / (gemm_avg * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "peak_source": f"{pk['source']} HBM copy bandwidth",
-                "algorithmic_bytes": info["forward_min_bytes"]}
-    elif prec in (PREC_3XTF32, PREC_TF32, PREC_BF16, PREC_3XBF16):
-        bf = prec in (PREC_BF16, PREC_3XBF16)
-        peak = pk["bf16_tflops"] * (1.0 if bf else TF32_OVER_BF16)
-        achieved = useful / (gemm_avg * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": (f"{pk['source']} bf16 burst" if bf else
-                                f"{pk['source']} bf16 burst x nominal TF32/BF16 ratio {TF32_OVER_BF16:.4f}"),
-                "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak}
-        if prec == PREC_3XTF32:
-            roof["frac_of_3xtf32_peak"] = achieved / (peak / 3.0)
-        if prec == PREC_3XBF16:
-            roof["frac_of_3xbf16_peak"] = achieved / (peak / 3.0)
-    else:
-        peak = SMS * FP32_FMA_PER_CLK_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
-        achieved = useful / (gemm_avg * 1e-3) / 1e12
-        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 flop x max SM clock",
-                "issued_frac": info["issued_mma_flop"] / (gemm_avg * 1e-3) / 1e12 / peak}
-    roof["kernel"] = ("boxsum_kernel + bn_eval_out_kernel" if eval_bn else
-                      "ffma_conv_kernel" if prec == PREC_FFMA else "convt3d_tc_gemm")
-    roof["kernel_ms"] = gemm_avg
-    roof["kernel_share_of_step"] = gemm_avg / ms_per_step
+    roof = roofline(info, args.precision, useful, gemm_avg, ms_per_step, pk, eval_bn)
     roof["traffic"] = committed_traffic(args.precision, spec.name)
-    roof["min_bytes"] = info["gemm_min_bytes"]
     hbm_frac = info["forward_min_bytes"] / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"]
+
+    roof["tensor_pipe_active"] = None if eval_bn else committed_tensor_active(args.precision, spec.name)
+
+    # the other configurations, GPU-only, same process
+    configs = None
+    if args.config_steps > 0 and world == 1:
+        configs = []
+        for cs in OTHER_WORKLOADS:
+            for pr in [p for p in args.config_precisions.split(",") if p]:
+                if cs.name == spec.name and pr == args.precision:
+                    continue
+                if cs.epilogue == workloads.EPI_SCALE_BATCHNORM_EVAL_AVGPOOL and pr != "3xtf32":
+                    continue
+                configs.append(time_config(cs, pr, args.config_steps, 3, dev, stream, flush, pk))
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -430,13 +543,16 @@ def run_gpu(args, spec):
         "metric": "useful_tflops", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": compute_dtype(args.precision), "data": "synthetic",
-        "config": {"workload": spec.name, "precision": args.precision, "io": "bf16" if args.io_bf16 else "f32", "x": [spec.N, spec.Cin, spec.D, spec.H, spec.W],
+        "config": {"workload": spec.name, "precision": args.precision,
+                   "io": "bf16" if args.io_bf16 else ("fp16" if args.io_fp16 else "f32"),
+                   "x": [spec.N, spec.Cin, spec.D, spec.H, spec.W],
                    "w": [spec.Cin, spec.Cout, spec.k, spec.k, spec.k], "stride": spec.stride, "pad": spec.pad,
                    "out_pad": spec.out_pad, "out": list(plan.out_shape), "epilogue": spec.epilogue,
                    "step": "pack_weights + forward (all kernels)", "l2": "flushed (256 MiB write) before each step",
                    "useful_flop_per_step": useful, "parallelism": f"replicas x{world}"},
         "hbm_frac_whole_step": hbm_frac,
         "roofline": roof,
+        "configs": configs,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (info["launches_per_forward"] + info["launches_per_pack"]) * args.steps,
@@ -452,7 +568,7 @@ def compute_dtype(precision):
     """The arithmetic type of the products: the split formats (and the FFMA
     ablation) compute to fp32 accuracy; the single-product formats round their
     operands to TF32 or bf16."""
-    return {"3xtf32": "f32", "3xbf16": "f32", "ffma": "f32", "tf32": "tf32", "bf16": "bf16"}[precision]
+    return {"3xtf32": "f32", "3xbf16": "f32", "ffma": "f32", "tf32": "tf32", "bf16": "bf16", "fp16": "f16"}[precision]
 
 
 def host_link_ms(host, y_dev, y_host, stream, dev, reps=3):

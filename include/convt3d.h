@@ -48,7 +48,7 @@
  *   - Layouts: x [N,Cin,Din,Hin,Win], y [N,Cout,Do,Ho,Wo] (BN+pool: [N,Cout,1,1,1]),
  *     or channels-last x [N,Din,Hin,Win,Cin], y [N,Do,Ho,Wo,Cout] (desc.channels_last),
  *     w [Cin,Cout/G,kd,kh,kw] (PyTorch ConvTranspose3d), bias/gamma/beta [Cout];
- *     fp32 (x, w and y bf16 with desc.io_bf16), contiguous, device memory,
+ *     fp32 (x, w and y bf16 with desc.io_bf16, fp16 with desc.io_fp16), contiguous, device memory,
  *     16-byte aligned.
  *   - Ownership: the caller allocates and owns every device buffer (input,
  *     output, workspace).  The library never allocates or frees device memory
@@ -96,12 +96,16 @@ typedef enum {
                                 inputs rounded to bf16 (nearest even) when staged and
                                 packed, fp32 accumulation and epilogue, fp32 I/O;
                                 same 1e-2 tier                                        */
-    CONVT3D_PREC_3XBF16 = 4  /* tcgen05 tensor cores, split BF16: each operand is
+    CONVT3D_PREC_3XBF16 = 4, /* tcgen05 tensor cores, split BF16: each operand is
                                 hi = bf16(v) + lo = bf16(v - hi) (nearest even, so
                                 |v - hi - lo| <= 2^-16 |v|), three kind::f16 products
                                 a_hi*b_hi + a_hi*b_lo + a_lo*b_hi per term, fp32
                                 accumulation; fp32 I/O; the 1e-4 tier of 3XTF32 at
                                 half its tensor-core time                              */
+    CONVT3D_PREC_FP16 = 5    /* tcgen05 tensor cores, one FP16 product per term (kind::f16
+                                with fp16 operands): inputs rounded to fp16 (nearest
+                                even) when staged and packed, fp32 accumulation and
+                                epilogue; the 1e-2 tier of page l2_p49's harness quote */
 } convt3d_precision_t;
 
 typedef enum {
@@ -145,6 +149,8 @@ typedef struct {
     int io_bf16;          /* non-zero: x, w and y are bf16 (2-byte) arrays; bias,
                              gamma, beta and the running statistics stay fp32;
                              requires precision CONVT3D_PREC_BF16                   */
+    int io_fp16;          /* non-zero: x, w and y are fp16 (IEEE half) arrays, as
+                             io_bf16 otherwise; requires precision CONVT3D_PREC_FP16 */
 } convt3d_desc_t;
 
 typedef struct convt3d_plan_s *convt3d_plan_t;
@@ -217,7 +223,10 @@ convt3d_status_t convt3d_set_running_stats(convt3d_plan_t plan, float *running_m
                                            float momentum);
 
 /* Synchronise `stream`, read and clear the workspace status word: returns OK,
- * TIMEOUT (a device-side bounded wait ran out) or DEVICE_ASSERT. */
+ * TIMEOUT (a device-side bounded wait ran out) or DEVICE_ASSERT.  A NULL
+ * workspace reads the built-in workspace of convt3d_forward_static_workspace
+ * on the current device (the status of the last such call; the next call
+ * clears it when it packs its weights). */
 convt3d_status_t convt3d_check(convt3d_plan_t plan, void *workspace, void *stream);
 
 /* Optional timing of the main GEMM kernel: when enabled, forward records two
@@ -241,7 +250,12 @@ convt3d_status_t convt3d_profile_read(convt3d_plan_t plan, float *gemm_ms);
  * with that device current; make that first call outside any stream capture.
  * All calls share the one array: calls whose GPU work may overlap (other
  * streams, other threads) race on it and must be serialised by the caller.
- * Arguments are as for convt3d_pack_weights and convt3d_forward. */
+ * Device-side conditions (a bounded wait that ran out) are recorded in the
+ * array's status word: read them with convt3d_check(plan, NULL, stream) after
+ * the call and before the next one, which clears the word.  The array's device
+ * address is cached per device for the life of the process: do not call this
+ * after cudaDeviceReset.  Arguments are as for convt3d_pack_weights and
+ * convt3d_forward. */
 convt3d_status_t convt3d_forward_static_workspace(convt3d_plan_t plan, const void *w, const void *x,
                                                   const float *bias, const float *gamma, const float *beta,
                                                   void *y, void *stream);

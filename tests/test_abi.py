@@ -46,7 +46,7 @@ def make_desc(**kw):
     base = dict(N=2, Cin=8, Cout=16, Din=8, Hin=8, Win=8, k=3, stride=1, pad=0, out_pad=0, has_bias=0,
                 epilogue=0, groups=1, eps=1e-5, scale=1.0, precision=0, per_dim=0, kdims=(0, 0, 0),
                 strides=(0, 0, 0), pads=(0, 0, 0), out_pads=(0, 0, 0), dilation=(0, 0, 0), conv_groups=0,
-                channels_last=0, io_bf16=0)
+                channels_last=0, io_bf16=0, io_fp16=0)
     base.update(kw)
     return _lib.Desc(*[base[f] for f, _ in _lib.Desc._fields_])
 
@@ -60,11 +60,11 @@ def create(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(N=0), 1), (dict(Cin=0), 1), (dict(k=0), 1), (dict(stride=0), 1), (dict(pad=-1), 1),
-    (dict(out_pad=1, stride=1), 1), (dict(epilogue=9), 1), (dict(precision=5), 1),
+    (dict(out_pad=1, stride=1), 1), (dict(epilogue=9), 1), (dict(precision=-1), 1),
     (dict(epilogue=1, groups=3), 1), (dict(epilogue=1, groups=4, eps=0.0), 1),
     (dict(Din=1, Hin=1, Win=1, k=1, pad=1), 1),
-    (dict(stride=3, k=3), 2), (dict(k=8), 2), (dict(Cout=257), 2), (dict(k=3, pad=3, Din=9, Hin=9, Win=9), 2),
-    (dict(stride=2, k=3, pad=1, Cout=144), 2), (dict(stride=2, k=1), 2),
+    (dict(stride=3, k=3), 2), (dict(k=8), 2), (dict(Cout=513), 2), (dict(k=3, pad=3, Din=9, Hin=9, Win=9), 2),
+    (dict(stride=2, k=1), 2),
     (dict(epilogue=4, eps=-1.0), 1), (dict(epilogue=4, scale=float("inf")), 1),
     (dict(epilogue=4, Hin=256, Win=256), 2),
     # general shapes
@@ -73,9 +73,10 @@ def create(lib, **kw):
     (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 2, 1), out_pads=(0, 2, 0)), 1),
     (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 1, 3)), 2), (dict(per_dim=1, kdims=(3, 8, 3), strides=(1, 1, 1)), 2),
     (dict(stride=2, dilation=(2, 2, 2)), 2), (dict(dilation=(16, 1, 1)), 2),
-    (dict(per_dim=1, kdims=(3, 3, 3), strides=(1, 1, 2), pads=(0, 0, 0), Cout=144), 2),
     (dict(io_bf16=1), 2), (dict(io_bf16=1, precision=2), 2), (dict(io_bf16=1, precision=1), 2),
     (dict(io_bf16=1, precision=4), 2),
+    (dict(precision=6), 1), (dict(io_fp16=1), 2), (dict(io_fp16=1, precision=3), 2),
+    (dict(io_bf16=1, io_fp16=1, precision=3), 1),
 ])
 def test_plan_validation(lib, kw, status):
     st, h = create(lib, **kw)
@@ -98,9 +99,14 @@ def test_eval_batchnorm_box_planes_follow_distinct_d_intervals(lib):
     assert st == 2 and not h.value
 
 
-def test_ffma_accepts_what_tensor_path_rejects(lib):
-    st, h = create(lib, stride=2, k=3, pad=1, Cout=144, precision=1)
-    assert st == 0
+@pytest.mark.parametrize("precision", [0, 1, 4])
+@pytest.mark.parametrize("kw", [dict(stride=2, k=3, pad=1, Cout=144), dict(Cout=384), dict(Cout=512, epilogue=3),
+                                dict(stride=2, k=4, pad=1, Cout=512, epilogue=2)])
+def test_wide_channels_accepted(lib, kw, precision):
+    """Up to 512 output channels on every path (the tensor-core tile splits N above
+    256 and gives each stride-2 w-parity class its own tile above 128)."""
+    st, h = create(lib, precision=precision, **kw)
+    assert st == 0, lib.convt3d_last_error()
     lib.convt3d_plan_destroy(h)
 
 

@@ -14,7 +14,8 @@ import torch
 
 import oracle
 import workloads
-from transposed_convolution_convt3d_gb300 import PREC_3XBF16, PREC_3XTF32, PREC_BF16, PREC_FFMA, PREC_TF32, Plan
+from transposed_convolution_convt3d_gb300 import (PREC_3XBF16, PREC_3XTF32, PREC_BF16, PREC_FFMA, PREC_FP16,
+                                                  PREC_TF32, Plan)
 
 TOL = 1e-4
 # The fp32-accurate paths, all held to the same 1e-4 bar: split TF32 (the method's),
@@ -38,6 +39,8 @@ def run_gpu(spec, inputs, precision, running=None, momentum=0.1):
         d["x"] = d["x"].permute(0, 2, 3, 4, 1).contiguous()
     if spec.io_bf16:  # x and w handed over as bf16 tensors
         d["x"], d["w"] = d["x"].to(torch.bfloat16), d["w"].to(torch.bfloat16)
+    if spec.io_fp16:  # x and w handed over as fp16 tensors
+        d["x"], d["w"] = d["x"].to(torch.float16), d["w"].to(torch.float16)
     if running is not None:
         rm, rv = (t.to(dev).clone() for t in running)
         plan.set_running_stats(rm, rv, momentum)
@@ -136,8 +139,6 @@ SMALL = [
 @pytest.mark.parametrize("precision", PRECISIONS)
 @pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
 def test_small_cases(spec, precision):
-    if precision != PREC_FFMA and spec.stride == 2 and spec.Cout > 128:
-        pytest.skip("tensor-core stride-2 path holds Cout <= 128")
     inputs = E.make_inputs(spec)
     assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name)
 
@@ -285,7 +286,7 @@ def test_general_shapes_eval_batchnorm(precision):
 # for reduced precision; bf16 inputs can exceed it where K is small and the
 # output cancels.
 TOL_LOW_VS_FP32 = 1e-2
-LOW = [pytest.param(PREC_TF32, id="tf32"), pytest.param(PREC_BF16, id="bf16")]
+LOW = [pytest.param(PREC_TF32, id="tf32"), pytest.param(PREC_BF16, id="bf16"), pytest.param(PREC_FP16, id="fp16")]
 
 
 def round_tf32(a):
@@ -298,8 +299,13 @@ def round_bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).float().numpy()
 
 
+def round_fp16(a):
+    """Nearest IEEE half (ties to even), back in fp32."""
+    return np.ascontiguousarray(a, np.float32).astype(np.float16).astype(np.float32)
+
+
 def rounded_inputs(inputs, precision):
-    rnd = round_tf32 if precision == PREC_TF32 else round_bf16
+    rnd = {PREC_TF32: round_tf32, PREC_BF16: round_bf16, PREC_FP16: round_fp16}[precision]
     out = dict(inputs)
     for k in ("x", "w"):
         out[k] = torch.from_numpy(rnd(inputs[k].numpy()))
@@ -310,8 +316,6 @@ def rounded_inputs(inputs, precision):
 @pytest.mark.parametrize("precision", LOW)
 @pytest.mark.parametrize("spec", SMALL + GENERAL, ids=lambda s: s.name)
 def test_low_precision_small_and_general(spec, precision):
-    if spec.Cout > 128 and (spec.stride == 2 or getattr(spec.stride, "__len__", None) and spec.stride[2] == 2):
-        pytest.skip("tensor-core stride-2 path holds Cout <= 128")
     inputs = E.make_inputs(spec)
     got = run_gpu(spec, inputs, precision)
     assert_close(got, run_oracle(spec, rounded_inputs(inputs, precision)), spec.name)
@@ -405,6 +409,32 @@ def test_bf16_tensors(spec):
     assert_close(got, run_oracle(spec, rounded_inputs(inputs, PREC_BF16)), spec.name, TOL_LOW_VS_FP32)
 
 
+# fp16 tensors at the boundary (x, w, y; bias and affine parameters fp32) with
+# the fp16 tensor-core precision (kind::f16 with fp16 operands), the other
+# format page l2_p49's reduced-precision tier names.  Reference: the oracle on
+# the same fp16-rounded x and w; the output is rounded to fp16 once more
+# (relative 2^-11), inside the 1e-2 tier.
+IO_FP16 = [s.replace(name=s.name.replace("io16", "iofp16"), io_bf16=False, io_fp16=True) for s in IO_BF16]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("spec", IO_FP16, ids=lambda s: s.name)
+def test_fp16_tensors(spec):
+    inputs = E.make_inputs(spec)
+    got = run_gpu(spec, inputs, PREC_FP16)
+    assert_close(got, run_oracle(spec, rounded_inputs(inputs, PREC_FP16)), spec.name, TOL_LOW_VS_FP32)
+
+
+@pytest.mark.gpu
+def test_fp16_tensors_eval_batchnorm():
+    spec = EVAL_CASES[1].replace(name="iofp16_bn_eval", io_fp16=True)
+    inputs = E.make_inputs(spec)
+    running = E.make_running_stats(spec)
+    got, _, _ = run_gpu(spec, inputs, PREC_FP16, running)
+    ref, _, _ = run_oracle(spec, rounded_inputs(inputs, PREC_FP16), running)
+    assert_close(got, ref, spec.name, TOL_LOW_VS_FP32)
+
+
 @pytest.mark.gpu
 def test_bf16_tensors_eval_batchnorm():
     spec = EVAL_CASES[1].replace(name="io16_bn_eval", io_bf16=True)
@@ -430,24 +460,92 @@ def test_long_reduction(cin, precision):
     assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name, 1e-3)
 
 
+# Wide channel counts (up to the 512 output channels of one tensor-memory
+# accumulator): above 256 the tensor-core tile walks its K steps once per N slice
+# of at most 256 columns and keeps a single accumulator; above 128 at stride 2
+# along w the two w-parity classes take separate tiles.  The softmax's row
+# reduction runs over every channel of the row in one tile.
+WIDE = [
+    E.Spec("wide_identity_s1_c384", N=1, Cin=24, Cout=384, D=3, H=4, W=5, k=3, bias=True, seed_index=90),
+    E.Spec("wide_identity_s2_c512", N=1, Cin=16, Cout=512, D=2, H=3, W=4, k=3, stride=2, pad=1, out_pad=1,
+           bias=True, seed_index=91),
+    E.Spec("wide_gn_s1_c512", N=2, Cin=16, Cout=512, D=2, H=3, W=4, k=3, bias=True, epilogue=E.EPI_RELU_GROUPNORM,
+           groups=8, seed_index=92),
+    E.Spec("wide_gn_s2_c384_cpg12", N=1, Cin=20, Cout=384, D=2, H=3, W=3, k=3, stride=2, pad=1, out_pad=1,
+           bias=True, epilogue=E.EPI_RELU_GROUPNORM, groups=32, seed_index=93),
+    E.Spec("wide_bn_s1_c384", N=2, Cin=12, Cout=384, D=2, H=3, W=4, k=3, bias=True,
+           epilogue=E.EPI_SCALE_BATCHNORM_AVGPOOL, scale=2.0, seed_index=94),
+    E.Spec("wide_bn_s2_c512", N=2, Cin=8, Cout=512, D=2, H=3, W=3, k=4, stride=2, pad=1, bias=True,
+           epilogue=E.EPI_SCALE_BATCHNORM_AVGPOOL, scale=0.5, seed_index=95),
+    E.Spec("wide_softmax_s1_c512", N=1, Cin=16, Cout=512, D=2, H=3, W=5, k=3, bias=True,
+           epilogue=E.EPI_SOFTMAX_SIGMOID, seed_index=96),
+    E.Spec("wide_softmax_s2_c384", N=1, Cin=24, Cout=384, D=2, H=3, W=4, k=3, stride=2, pad=1, out_pad=1,
+           bias=True, epilogue=E.EPI_SOFTMAX_SIGMOID, seed_index=97),
+    E.Spec("wide_softmax_s2_c256", N=1, Cin=32, Cout=256, D=2, H=3, W=4, k=3, stride=2, pad=1, out_pad=1,
+           bias=True, epilogue=E.EPI_SOFTMAX_SIGMOID, seed_index=98),
+    # 300 channels: two slices of 160 (Cout_pad rounded to 320), ragged last chunk
+    E.Spec("wide_softmax_s1_c300", N=1, Cin=8, Cout=300, D=2, H=2, W=3, k=2, bias=True,
+           epilogue=E.EPI_SOFTMAX_SIGMOID, seed_index=99),
+]
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("layout", ["cl", "io16", "cl_io16"])
-def test_host_pipeline_layouts(layout):
-    """HostPipeline from pinned host tensors with channels-last and/or bf16 x/w/y."""
-    from transposed_convolution_convt3d_gb300 import HostPipeline
-    cl, io16 = "cl" in layout, "io16" in layout
-    spec = SMALL[7].replace(N=4, channels_last=cl, io_bf16=io16)
-    prec = PREC_BF16 if io16 else PREC_3XTF32
+@pytest.mark.parametrize("precision", PRECISIONS)
+@pytest.mark.parametrize("spec", WIDE, ids=lambda s: s.name)
+def test_wide_channels(spec, precision):
     inputs = E.make_inputs(spec)
-    ref = run_oracle(spec, rounded_inputs(inputs, PREC_BF16) if io16 else inputs)
+    assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name)
+
+
+# Statistics under a large common offset: bias + 100 puts the group / channel
+# means some 250 standard deviations from zero, where a one-pass
+# E[v^2] - mean^2 over fp32 sums would lose most of the variance's digits.  The
+# epilogues sum deviations from each warp's own mean and the finalize kernels
+# combine (count, sum, M2) rows, so the 1e-4 bar holds.
+OFFSET_CASES = [
+    E.Spec("gn_offset", N=2, Cin=16, Cout=32, D=4, H=5, W=6, k=3, bias=True, epilogue=E.EPI_RELU_GROUPNORM,
+           groups=2, seed_index=80),
+    # 12 channels per group: the group statistics take the second pass over tensor memory
+    E.Spec("gn_offset_cpg12", N=2, Cin=16, Cout=48, D=3, H=4, W=5, k=3, bias=True, epilogue=E.EPI_RELU_GROUPNORM,
+           groups=4, seed_index=81),
+    E.Spec("gn_offset_s2", N=2, Cin=16, Cout=32, D=3, H=4, W=4, k=4, stride=2, pad=1, bias=True,
+           epilogue=E.EPI_RELU_GROUPNORM, groups=2, seed_index=82),
+    E.Spec("bn_offset", N=3, Cin=20, Cout=32, D=4, H=6, W=5, k=5, bias=True,
+           epilogue=E.EPI_SCALE_BATCHNORM_AVGPOOL, scale=2.0, seed_index=83),
+    E.Spec("bn_offset_s2", N=2, Cin=8, Cout=16, D=3, H=4, W=5, k=3, stride=2, pad=1, out_pad=1, bias=True,
+           epilogue=E.EPI_SCALE_BATCHNORM_AVGPOOL, scale=0.5, seed_index=84),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("precision", PRECISIONS)
+@pytest.mark.parametrize("spec", OFFSET_CASES, ids=lambda s: s.name)
+def test_statistics_large_offset(spec, precision):
+    inputs = E.make_inputs(spec)
+    inputs["bias"] = inputs["bias"] + 100.0
+    assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("layout", ["cl", "io16", "cl_io16", "iofp16"])
+def test_host_pipeline_layouts(layout):
+    """HostPipeline from pinned host tensors with channels-last and/or 16-bit x/w/y."""
+    from transposed_convolution_convt3d_gb300 import HostPipeline
+    cl, io16, fp16 = "cl" in layout, "io16" in layout, "fp16" in layout
+    spec = SMALL[7].replace(N=4, channels_last=cl, io_bf16=io16, io_fp16=fp16)
+    prec = PREC_BF16 if io16 else (PREC_FP16 if fp16 else PREC_3XTF32)
+    dt = torch.bfloat16 if io16 else torch.float16
+    inputs = E.make_inputs(spec)
+    ref = run_oracle(spec, rounded_inputs(inputs, prec) if (io16 or fp16) else inputs)
     host = {k: (v.pin_memory() if v is not None else None) for k, v in inputs.items()}
     if cl:
         host["x"] = host["x"].permute(0, 2, 3, 4, 1).contiguous().pin_memory()
-    if io16:
-        host["x"], host["w"] = host["x"].to(torch.bfloat16).pin_memory(), host["w"].to(torch.bfloat16).pin_memory()
+    if io16 or fp16:
+        host["x"], host["w"] = host["x"].to(dt).pin_memory(), host["w"].to(dt).pin_memory()
+    io16 = io16 or fp16
     pipe = HostPipeline(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
                         spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, prec, chunks=2,
-                        channels_last=cl, io_bf16=io16)
+                        channels_last=cl, io_bf16=io16 and not fp16, io_fp16=fp16)
     y_host = torch.full(pipe.full_shape, float("nan"), dtype=pipe.plan.io_dtype).pin_memory()
     pipe(host["x"], host["w"], y_host, host["bias"], host["gamma"], host["beta"])
     torch.cuda.synchronize()

@@ -44,6 +44,10 @@ def _static_ws_call(plan, d, y):
     st = lib.convt3d_forward_static_workspace(plan.handle, p(d["w"]), p(d["x"]), p(d["bias"]), p(d["gamma"]),
                                               p(d["beta"]), p(y), stream)
     assert st == 0, lib.convt3d_last_error().decode()
+    # the call's device-side status lives in the built-in workspace: a NULL
+    # workspace makes convt3d_check read (and clear) that one
+    st = lib.convt3d_check(plan.handle, None, stream)
+    assert st == 0, lib.convt3d_last_error().decode()
     torch.cuda.synchronize()
     return y.cpu().numpy()
 

@@ -6,4 +6,4 @@ library; the first Plan does, and fails loudly if it has not been built.
 """
 from .api import (EPI_IDENTITY, EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL,  # noqa: F401
                   EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, EPI_SOFTMAX_SIGMOID, PREC_3XTF32, PREC_FFMA, PREC_TF32,
-                  PREC_BF16, PREC_3XBF16, Convt3dError, HostPipeline, Plan, convt3d)
+                  PREC_BF16, PREC_3XBF16, PREC_FP16, Convt3dError, HostPipeline, Plan, convt3d)

@@ -23,6 +23,7 @@ PREC_FFMA = 1
 PREC_TF32 = 2
 PREC_BF16 = 3
 PREC_3XBF16 = 4
+PREC_FP16 = 5
 
 STATUS = {
     0: "CONVT3D_OK",
@@ -54,6 +55,7 @@ class Desc(ctypes.Structure):
         ("per_dim", ctypes.c_int), ("kdims", ctypes.c_int * 3), ("strides", ctypes.c_int * 3),
         ("pads", ctypes.c_int * 3), ("out_pads", ctypes.c_int * 3), ("dilation", ctypes.c_int * 3),
         ("conv_groups", ctypes.c_int), ("channels_last", ctypes.c_int), ("io_bf16", ctypes.c_int),
+        ("io_fp16", ctypes.c_int),
     ]
 
 

@@ -14,7 +14,7 @@ import torch
 from . import _lib
 from ._lib import (EPI_IDENTITY, EPI_RELU_GROUPNORM, EPI_SCALE_BATCHNORM_AVGPOOL,  # noqa: F401
                    EPI_SCALE_BATCHNORM_EVAL_AVGPOOL, EPI_SOFTMAX_SIGMOID, PREC_3XTF32, PREC_FFMA,
-                   PREC_TF32, PREC_BF16, PREC_3XBF16, Convt3dError)
+                   PREC_TF32, PREC_BF16, PREC_3XBF16, PREC_FP16, Convt3dError)
 
 
 def _ptr(t):
@@ -36,11 +36,11 @@ def _triple(v):
 
 def make_desc(N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False, epilogue=EPI_IDENTITY,
               groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1, conv_groups=1,
-              channels_last=False, io_bf16=False):
+              channels_last=False, io_bf16=False, io_fp16=False):
     """A convt3d_desc_t.  k, stride, pad, out_pad and dilation are an int or
     (d, h, w); conv_groups is the convolution's group count (weight
     [Cin, Cout/conv_groups, kd, kh, kw]); groups is GroupNorm's; channels_last
-    selects NDHWC x and y."""
+    selects NDHWC x and y; io_bf16 / io_fp16 make x, w and y 16-bit tensors."""
     kk, ss, pp, oo, dd = (_triple(v) for v in (k, stride, pad, out_pad, dilation))
     per_dim = any(len(set(t)) > 1 for t in (kk, ss, pp, oo))
     d = _lib.Desc(N, Cin, Cout, D, H, W, kk[0], ss[0], pp[0], oo[0], int(bool(bias)), int(epilogue), int(groups),
@@ -51,6 +51,7 @@ def make_desc(N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False, 
     d.conv_groups = int(conv_groups)
     d.channels_last = int(bool(channels_last))
     d.io_bf16 = int(bool(io_bf16))
+    d.io_fp16 = int(bool(io_fp16))
     return d
 
 
@@ -59,12 +60,13 @@ class Plan:
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, dilation=1,
-                 conv_groups=1, channels_last=False, io_bf16=False):
+                 conv_groups=1, channels_last=False, io_bf16=False, io_fp16=False):
         self.lib = _lib.load()
         self.channels_last = bool(channels_last)
-        self.io_dtype = torch.bfloat16 if io_bf16 else torch.float32  # x, w and y
+        # x, w and y
+        self.io_dtype = torch.bfloat16 if io_bf16 else (torch.float16 if io_fp16 else torch.float32)
         self.desc = make_desc(N, Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale,
-                              precision, dilation, conv_groups, channels_last, io_bf16)
+                              precision, dilation, conv_groups, channels_last, io_bf16, io_fp16)
         h = ctypes.c_void_p()
         _lib.check(self.lib.convt3d_plan_create(ctypes.byref(self.desc), ctypes.byref(h)), self.lib)
         self.handle = h
@@ -84,7 +86,8 @@ class Plan:
     def from_spec(cls, spec, precision=PREC_3XTF32):
         return cls(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
                    spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, precision,
-                   spec.dilation, spec.conv_groups, spec.channels_last, spec.io_bf16)
+                   spec.dilation, spec.conv_groups, spec.channels_last, spec.io_bf16,
+                   getattr(spec, "io_fp16", False))
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -202,13 +205,14 @@ class HostPipeline:
 
     def __init__(self, N, Cin, Cout, D, H, W, k, stride=1, pad=0, out_pad=0, bias=False,
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, chunks=4,
-                 device="cuda", dilation=1, conv_groups=1, copy_streams=1, channels_last=False, io_bf16=False):
+                 device="cuda", dilation=1, conv_groups=1, copy_streams=1, channels_last=False, io_bf16=False,
+                 io_fp16=False):
         if epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) or N % chunks:
             chunks = 1
         self.chunks = chunks
         self.n_chunk = N // chunks
         args = (Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale, precision,
-                dilation, conv_groups, channels_last, io_bf16)
+                dilation, conv_groups, channels_last, io_bf16, io_fp16)
         self.plan = Plan(self.n_chunk, *args)
         dt = self.plan.io_dtype
         self.full_shape = (N,) + self.plan.out_alloc_shape[1:]

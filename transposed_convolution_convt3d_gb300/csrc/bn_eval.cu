@@ -52,7 +52,7 @@ struct BoxParams {
     float *box;  // [kd*kh*kw][Cin][N]: the samples of one (tap, ci) side by side
     int N, Cin, D, H, W, Do, Ho, Wo;
     int cl;      // channels-last x
-    int x16;     // x is a bf16 array
+    int x16;     // x is a 16-bit array of that kind (kBF16 / kF16), 0: fp32
     int kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw;  // kernel, stride, pad, dilation per dimension
     // distinct d-intervals of the taps along d: nud of them, tap td uses ud_of[td]
     int nud;
@@ -108,8 +108,7 @@ __global__ void __launch_bounds__(256) boxsum_kernel(const BoxParams P) {
             for (int t = 0; t < NUD; ++t) acc[t] = 0.f;
             for (int d = 0; d < P.D; ++d) {
                 const size_t xi = ((size_t)d * HW + col) * es;
-                const float v = P.x16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.x)[(xp - P.x) + xi])
-                                      : __ldg(xp + xi);
+                const float v = P.x16 ? ld16(P.x, (xp - P.x) + xi, P.x16) : __ldg(xp + xi);
 #pragma unroll
                 for (int t = 0; t < NUD; ++t)
                     if (d >= dlo[t] && d <= dhi[t]) acc[t] += v;
@@ -160,7 +159,7 @@ struct OutParams {
     const float *w_a, *w_b;  // tensor-core layout: TF32 hi/lo planes [tap][cout_pad][cin_pad]; FFMA: [tap][cin_pad][cout_pad]
     const float *bias, *gamma, *beta, *rmean, *rvar;
     float *y;
-    int N, Cin, Cout, cin_pad, cout_pad, ntaps, k3, kmajor, wbf16, y16;
+    int N, Cin, Cout, cin_pad, cout_pad, ntaps, k3, kmajor, w16, y16;  // w16 / y16: 16-bit kinds (0: fp32)
     double inv_vol, scale, eps;
 };
 
@@ -185,7 +184,8 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
     for (int q = 0; q < kOutSamples; ++q) acc[q] = 0.f;
     // The loop over this thread's products, specialised on the box-row access (four
     // 16-byte loads, or scalars for a partial sample block) and the weight layout
-    // (0: tensor-core fp32 planes, 1: tensor-core bf16 planes, 2: FFMA layout), with
+    // (0: tensor-core fp32 planes, 1: tensor-core bf16 planes, 2: FFMA layout, 3: tensor-core
+    // fp16 plane), with
     // the (tap, ci) index stepped instead of divided per product.
     auto contract = [&](auto vec_t, auto wm_t) {
         constexpr bool kVec = decltype(vec_t)::value;
@@ -201,8 +201,9 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
             } else {
                 const size_t o = ((size_t)j * P.cout_pad + c) * P.cin_pad + ci;
                 if constexpr (kWm == 1)  // bf16 planes: hi (+ lo, split bf16)
-                    wv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_a)[o]) +
-                         (P.w_b ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(P.w_b)[o]) : 0.f);
+                    wv = ld16(P.w_a, (int64_t)o, kBF16) + (P.w_b ? ld16(P.w_b, (int64_t)o, kBF16) : 0.f);
+                else if constexpr (kWm == 3)  // one fp16 plane
+                    wv = ld16(P.w_a, (int64_t)o, kF16);
                 else  // hi + lo: the fp32 weight, exactly (or its TF32 rounding)
                     wv = P.w_b ? P.w_a[o] + P.w_b[o] : P.w_a[o];
             }
@@ -234,9 +235,12 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
     using W0 = std::integral_constant<int, 0>;
     using W1 = std::integral_constant<int, 1>;
     using W2 = std::integral_constant<int, 2>;
+    using W3 = std::integral_constant<int, 3>;
     if (!P.kmajor)
         vec ? contract(T_{}, W2{}) : contract(F_{}, W2{});
-    else if (P.wbf16)
+    else if (P.w16 == kF16)
+        vec ? contract(T_{}, W3{}) : contract(F_{}, W3{});
+    else if (P.w16)
         vec ? contract(T_{}, W1{}) : contract(F_{}, W1{});
     else
         vec ? contract(T_{}, W0{}) : contract(F_{}, W0{});
@@ -280,8 +284,8 @@ __global__ void __launch_bounds__(kOutThreads) bn_eval_out_kernel(const OutParam
         const double rstd = 1.0 / sqrt((double)P.rvar[c] + P.eps);
         const float out =
             (float)((double)P.gamma[c] * (P.scale * mean_y - (double)P.rmean[c]) * rstd + (double)P.beta[c]);
-        if (P.y16)
-            reinterpret_cast<__nv_bfloat16 *>(P.y)[(size_t)(n0 + q) * P.Cout + c] = __float2bfloat16_rn(out);
+        if (P.y16)  // 16-bit output of that kind
+            reinterpret_cast<uint16_t *>(P.y)[(size_t)(n0 + q) * P.Cout + c] = cvt16(out, P.y16);
         else
             P.y[(size_t)(n0 + q) * P.Cout + c] = out;
     }
@@ -374,7 +378,7 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
     op.ntaps = g.ntaps;
     op.k3 = g.kvol;
     op.kmajor = p.tc;
-    op.wbf16 = p.bf16;
+    op.w16 = p.bf16 ? (p.half ? kF16 : kBF16) : kF32;
     op.y16 = p.io16;
     op.inv_vol = 1.0 / ((double)g.Do * g.Ho * g.Wo);
     op.scale = (double)p.d.scale;

@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,6 +19,33 @@ constexpr int kTcTileM = 128;    // output positions per tensor-core tile (TMEM 
 constexpr int kTcChunk = 32;     // fp32 input channels per K step of the tensor-core path (128 B)
 constexpr int kTcRowBytes = 128; // bytes of one operand row per K step (the 128-byte swizzle span)
 constexpr int kTcStatRows = 4;   // partial-statistics rows per tensor-core tile (one per TMEM lane quarter)
+constexpr int kMaxCout = 512;    // output channels: the tensor-memory columns of one accumulator
+constexpr int kTcMaxSliceN = 256;  // largest N of one tcgen05.mma (and one TMA box row count)
+
+// 16-bit element kinds of tensors at the boundary and of operand planes.
+enum : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
+
+// Element i of a 16-bit array of the given kind (kBF16 or kF16), as fp32.
+__device__ __forceinline__ float ld16(const void *p, int64_t i, int kind) {
+    const uint16_t b = reinterpret_cast<const uint16_t *>(p)[i];
+    return kind == kF16 ? __half2float(__ushort_as_half(b)) : __bfloat162float(__ushort_as_bfloat16(b));
+}
+
+// v rounded to nearest even in the given 16-bit kind, as its bit pattern.
+__device__ __forceinline__ uint16_t cvt16(float v, int kind) {
+    return kind == kF16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// Two values as one 32-bit pair (a in the low half).
+__device__ __forceinline__ uint32_t cvt16x2(float a, float b, int kind) {
+    return (uint32_t)cvt16(a, kind) | ((uint32_t)cvt16(b, kind) << 16);
+}
+
+__device__ __forceinline__ float2 ld16x2(uint32_t bits, int kind) {
+    const uint16_t lo = (uint16_t)(bits & 0xFFFFu), hi = (uint16_t)(bits >> 16);
+    if (kind == kF16) return make_float2(__half2float(__ushort_as_half(lo)), __half2float(__ushort_as_half(hi)));
+    return make_float2(__bfloat162float(__ushort_as_bfloat16(lo)), __bfloat162float(__ushort_as_bfloat16(hi)));
+}
 
 // Status word layout at the start of the workspace.
 enum : uint32_t { kErrNone = 0, kErrTimeout = 1, kErrAssert = 2 };
@@ -109,8 +138,7 @@ struct TapRange {
 __host__ __device__ inline TapRange tile_taps(const GroupDesc &G, const ClassDesc &C, int t, int tile_m, int Din) {
     const int q0 = t * tile_m;
     const int q1 = (q0 + tile_m < G.vol ? q0 + tile_m : G.vol) - 1;
-    const int qhw = G.Qh * G.Qw;
-    const int d0 = q0 / qhw, d1 = q1 / qhw;
+    const int d0 = (int)fastdiv((uint32_t)q0, G.div_qhw), d1 = (int)fastdiv((uint32_t)q1, G.div_qhw);
     const int step = C.step_d;
     const int hi = C.lo_d + (C.nt_d - 1) * step;  // offset of d-slice 0
     // live slices a: hi + d0 - (Din - 1) <= a * step <= hi + d1
@@ -170,18 +198,21 @@ struct convt3d_plan_s {
     int tc;                 // 1: tensor-core path, 0: FFMA
     int planes;             // tensor-core operand planes: 2 = split TF32 (hi, lo), 1 = TF32 or BF16
     int cl;                 // channels-last x and y (NDHWC)
-    int io16;               // x, w and y are bf16 arrays (the float pointers below alias them)
+    int io16;               // x, w and y are 16-bit arrays: kBF16 or kF16 (0: fp32)
     int merged;             // w-parity pairs share activation loads and MMAs (see GroupDesc::nm)
-    int bf16;               // tensor-core operands in bf16 (kind::f16 MMA)
+    int bf16;               // tensor-core operands are 16-bit (kind::f16 MMA): bf16, or fp16 when half
+    int half;               // the 16-bit operands are fp16
     int chunk;              // input channels per K step (one 128-byte operand row)
     int elem_bytes;         // bytes per staged / packed operand element
     int cin_pad, cout_pad;
+    int nslices;            // tensor-core path: N slices of cout_pad / nslices (<= 256) columns per tile
     int tile_m;
     int ngroups;
     convt3d::GroupDesc grp[convt3d::kMaxGroups];
     int tiles_per_sample;
     int64_t tiles;
     int stat_rows_per_tile;  // partial-statistics rows each tile writes (tensor-core: one per epilogue warp)
+    int bn_splits;           // BatchNorm: row ranges per sample the first reduction splits into
     // workspace layout (byte offsets, 256-aligned)
     size_t off_wpk_hi, off_wpk_lo, off_xs_hi, off_xs_lo, off_partials, off_stats, ws_total;
     size_t wpk_elems, xs_elems, partial_doubles, stat_doubles;
@@ -215,7 +246,7 @@ cudaError_t launch_tc(convt3d_plan_s &p, const float *xs_hi, const float *xs_lo,
 cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, double *stats,
                                cudaStream_t s);
 cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, const float *gamma,
-                                const float *beta, float *y, cudaStream_t s);
+                                const float *beta, const float *bias, float *y, cudaStream_t s);
 cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, double *sums,
                                const float *gamma, const float *beta, float *y, cudaStream_t s);
 cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float *w_a, const float *w_b,
@@ -224,5 +255,6 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
 size_t bn_eval_smem_bytes(const convt3d_plan_s &p);
 int bn_eval_ksplits(int ntaps, int Cin);
 void tc_cache_free(void *cache);
+void *static_workspace_address();
 void report_error(const char *fmt, ...);
 }  // namespace convt3d

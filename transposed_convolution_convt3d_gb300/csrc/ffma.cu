@@ -11,8 +11,8 @@
 // through shared memory to the epilogue:
 //   identity         store;
 //   softmax+sigmoid  per position over all channels, store;
-//   relu+groupnorm   ReLU, store, per-group (sum, sum of squares) partials;
-//   scale+bn+pool    scale, per-channel (sum, sum of squares) partials, no store.
+//   relu+groupnorm   per-group (count, sum, M2) partials of v = ReLU(conv + b), store v - b;
+//   scale+bn+pool    scale, per-channel (count, sum, M2) partials, no store.
 #include <string.h>
 
 #include "convt3d_internal.h"
@@ -40,6 +40,12 @@ __device__ __forceinline__ TileInfo decode_tile(const FfmaParams &P, int bid) {
     ti.cls = P.grp[gi].cls[0];
     ti.slot = bid;  // == n * tiles_per_sample + r
     return ti;
+}
+
+// ReLU(a + b) in fp64 for the GroupNorm statistics, b = bias[c] (0 without a bias).
+__device__ __forceinline__ double relu_biased(float a, const float *bias, int c) {
+    const float t = a + (bias ? bias[c] : 0.0f);
+    return t > 0.0f ? (double)a + (bias ? (double)bias[c] : 0.0) : 0.0;
 }
 
 template <int CPT>
@@ -84,7 +90,8 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
     int64_t sp[2] = {-1, -1};
     int cur_tap = -1;
     float areg[2];
-    float4 breg[2];
+    constexpr int kBRegs = (kBK * 16 * CPT / 4 + kThreads - 1) / kThreads;  // float4s per thread per weight slice
+    float4 breg[kBRegs];
     const int nb4 = kBK * cpad / 4;  // float4s in one weight slice
 
     auto load_step = [&](int step) {
@@ -107,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
         const float4 *wsrc = reinterpret_cast<const float4 *>(
             P.wpk + ((int64_t)(cl.tap_begin + j) * P.cin_pad + ci0) * cpad);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
+        for (int r = 0; r < kBRegs; ++r) {
             const int idx = tid + r * kThreads;
             if (idx < nb4) breg[r] = __ldg(wsrc + idx);
         }
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
         A[lk * kBM + (tid % 32) + 32] = areg[1];
         float4 *B = reinterpret_cast<float4 *>(Bs + buf * kBK * cpad);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
+        for (int r = 0; r < kBRegs; ++r) {
             const int idx = tid + r * kThreads;
             if (idx < nb4) B[idx] = breg[r];
         }
@@ -159,7 +166,9 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
         for (int j = 0; j < CPT; ++j) {
             const int c = tx * CPT + j;
             const float b = (P.bias && c < P.Cout) ? P.bias[c] : 0.0f;
-            E[(ty * 4 + i) * es + c] = acc[i][j] + b;
+            // GroupNorm keeps the accumulator: its statistics add the bias, and the stored
+            // value is relative to it (see below)
+            E[(ty * 4 + i) * es + c] = P.epilogue == CONVT3D_EPI_RELU_GROUPNORM ? acc[i][j] : acc[i][j] + b;
         }
     if (tid < kBM) {
         const int q = ti.t * kBM + tid;
@@ -177,17 +186,25 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
     const int C = P.Cout;
     float *yn = P.y + (int64_t)ti.n * C * Sout;
     if (P.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL) {
-        double *part = P.partials + (int64_t)ti.slot * 2 * C;
+        // per channel over the tile's valid positions: (count, sum, M2) in fp64, M2 about the tile's mean
+        double *part = P.partials + (int64_t)ti.slot * 3 * C;
         for (int c = tid; c < C; c += kThreads) {
-            double s1 = 0.0, s2 = 0.0;
+            double n = 0.0, s1 = 0.0;
             for (int m = 0; m < kBM; ++m) {
                 if (rowoff[m] < 0) continue;
-                const double z = (double)P.scale * (double)E[m * es + c];
-                s1 += z;
-                s2 += z * z;
+                n += 1.0;
+                s1 += (double)P.scale * (double)E[m * es + c];
             }
-            part[2 * c] = s1;
-            part[2 * c + 1] = s2;
+            const double mu = n > 0.0 ? s1 / n : 0.0;
+            double m2 = 0.0;
+            for (int m = 0; m < kBM; ++m) {
+                if (rowoff[m] < 0) continue;
+                const double d = (double)P.scale * (double)E[m * es + c] - mu;
+                m2 += d * d;
+            }
+            part[3 * c] = n;
+            part[3 * c + 1] = s1;
+            part[3 * c + 2] = m2;
         }
         return;
     }
@@ -207,36 +224,51 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
         __syncthreads();
     }
     if (P.epilogue == CONVT3D_EPI_RELU_GROUPNORM) {
-        for (int idx = tid; idx < kBM * C; idx += kThreads) {
-            const int m = idx % kBM, c = idx / kBM;
-            E[m * es + c] = fmaxf(E[m * es + c], 0.0f);
-        }
-        __syncthreads();
-        // per-group partial sums over the tile's valid positions: one warp per group
+        // E holds the accumulator a; the GroupNorm input is v = ReLU(a + b), and y keeps
+        // r = v - b (a itself where the ReLU passes, else -b) for the normalise pass
+        // per-group (count, sum, M2) over the tile's valid positions in fp64, M2 about
+        // the tile's group mean: one warp per group
         const int G = P.groups, cpg = C / G;
         const int warp = tid / 32, lane = tid % 32;
-        double *part = P.partials + (int64_t)ti.slot * 2 * G;
+        double *part = P.partials + (int64_t)ti.slot * 3 * G;
         for (int g = warp; g < G; g += kThreads / 32) {
-            double s1 = 0.0, s2 = 0.0;
+            double n = 0.0, s1 = 0.0;
+            for (int m = lane; m < kBM; m += 32) {
+                if (rowoff[m] < 0) continue;
+                const float *row = E + m * es + g * cpg;
+                n += cpg;
+                for (int c = 0; c < cpg; ++c) s1 += relu_biased(row[c], P.bias, g * cpg + c);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                n += __shfl_xor_sync(0xffffffffu, n, o);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            }
+            const double mu = n > 0.0 ? s1 / n : 0.0;
+            double m2 = 0.0;
             for (int m = lane; m < kBM; m += 32) {
                 if (rowoff[m] < 0) continue;
                 const float *row = E + m * es + g * cpg;
                 for (int c = 0; c < cpg; ++c) {
-                    const double v = row[c];
-                    s1 += v;
-                    s2 += v * v;
+                    const double d = relu_biased(row[c], P.bias, g * cpg + c) - mu;
+                    m2 += d * d;
                 }
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-                s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-            }
+            for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
             if (lane == 0) {
-                part[2 * g] = s1;
-                part[2 * g + 1] = s2;
+                part[3 * g] = n;
+                part[3 * g + 1] = s1;
+                part[3 * g + 2] = m2;
             }
         }
+        __syncthreads();
+        for (int idx = tid; idx < kBM * C; idx += kThreads) {
+            const int m = idx % kBM, c = idx / kBM;
+            const float a = E[m * es + c], b = P.bias ? P.bias[c] : 0.0f;
+            E[m * es + c] = a + b > 0.0f ? a : -b;
+        }
+        __syncthreads();
     }
     // store (identity, softmax+sigmoid, relu output before normalisation)
     for (int idx = tid; idx < kBM * C; idx += kThreads) {
@@ -291,6 +323,7 @@ cudaError_t launch_ffma(const convt3d_plan_s &p, const float *x, const float *wp
         case 64: return launch_cpt<4>(P, blocks, s);
         case 128: return launch_cpt<8>(P, blocks, s);
         case 256: return launch_cpt<16>(P, blocks, s);
+        case 512: return launch_cpt<32>(P, blocks, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -5,12 +5,13 @@
 // per-Cout access strided and re-lays it per output channel.  Here the
 // weight is re-laid per parity class and tap:
 //   tensor-core path: [tap][Cout_pad][Cin_pad] (K-major rows, Cin contiguous),
-//                     split into TF32 (or bf16) hi and lo planes;
+//                     split into TF32 (or bf16) hi and lo planes, or one TF32,
+//                     bf16 or fp16 plane;
 //   FFMA path:        [tap][Cin_pad][Cout_pad] fp32.
 // The tensor-core path also stages x (NCDHW, or already channels-last) into channels-last
-// [N][D][H][W][Cin_pad] hi/lo planes (one TF32-rounded or bf16 plane for the
-// single-product precisions), the layout its TMA im2col loads read.
-#include <cuda_bf16.h>
+// [N][D][H][W][Cin_pad] hi/lo planes (one TF32-rounded, bf16 or fp16 plane for
+// the single-product precisions), the layout its TMA im2col loads read.
+// x and w may arrive as bf16 or fp16 arrays (kind w16 / x16).
 
 #include "convt3d_internal.h"
 
@@ -67,7 +68,7 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
         float v = 0.0f;
         if (ci < Cin && co < Cout && ci / cin_g == co / cout_g) {
             const int64_t src = ((int64_t)ci * cout_g + co % cout_g) * k3 + taps.widx[j];
-            v = w16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(w)[src]) : w[src];
+            v = w16 ? ld16(w, src, w16) : w[src];
         }
         if (lo && mode == 3) {  // split bf16 planes (2-byte elements)
             split_bf16(v, reinterpret_cast<__nv_bfloat16 *>(hi)[i], reinterpret_cast<__nv_bfloat16 *>(lo)[i]);
@@ -76,8 +77,8 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
             split_tf32(v, h, l);
             hi[i] = h;
             lo[i] = l;
-        } else if (mode == 2) {  // bf16 operands: the plane holds 2-byte elements
-            reinterpret_cast<__nv_bfloat16 *>(hi)[i] = __float2bfloat16_rn(v);
+        } else if (mode == 2 || mode == 4) {  // bf16 / fp16 operands: the plane holds 2-byte elements
+            reinterpret_cast<uint16_t *>(hi)[i] = cvt16(v, mode == 4 ? kF16 : kBF16);
         } else {
             hi[i] = mode == 1 ? round_tf32(v) : v;  // TF32-rounded, or fp32 for the FFMA path
         }
@@ -88,7 +89,7 @@ __global__ void pack_weights_kernel(const float *__restrict__ w, float *__restri
 // tile per (output channel, 32 taps, 32 input channels): the reads run along
 // the weight's contiguous tap axis, the writes along cin, both coalesced.
 // mode: 0 = split TF32 (fp32 hi/lo planes), 1 = TF32-rounded, 2 = bf16,
-// 3 = split bf16 (bf16 hi/lo planes).
+// 3 = split bf16 (bf16 hi/lo planes), 4 = fp16.
 __global__ void pack_weights_kmajor_kernel(const float *__restrict__ w, float *__restrict__ hi,
                                            float *__restrict__ lo, int Cin, int Cout, int k3, int ntaps,
                                            int cin_pad, int cout_pad, int mode, int cin_g, int cout_g, int w16,
@@ -107,7 +108,7 @@ __global__ void pack_weights_kmajor_kernel(const float *__restrict__ w, float *_
         float v = 0.0f;
         if (co_ok && ci < Cin && j < ntaps && ci / cin_g == co / cout_g) {
             const int64_t src = ((int64_t)ci * cout_g + co % cout_g) * k3 + s_widx[tx];
-            v = w16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(w)[src]) : w[src];
+            v = w16 ? ld16(w, src, w16) : w[src];
         }
         tile[ty + r][tx] = v;
     }
@@ -125,8 +126,8 @@ __global__ void pack_weights_kmajor_kernel(const float *__restrict__ w, float *_
             split_tf32(v, h, l);
             hi[i] = h;
             lo[i] = l;
-        } else if (mode == 2) {
-            reinterpret_cast<__nv_bfloat16 *>(hi)[i] = __float2bfloat16_rn(v);
+        } else if (mode == 2 || mode == 4) {
+            reinterpret_cast<uint16_t *>(hi)[i] = cvt16(v, mode == 4 ? kF16 : kBF16);
         } else {
             hi[i] = round_tf32(v);
         }
@@ -138,6 +139,7 @@ __global__ void pack_weights_kmajor_kernel(const float *__restrict__ w, float *_
 // positions) and the write (along channels) are 128-byte rows.
 __global__ void stage_input_kernel(const float *__restrict__ x, float *__restrict__ hi,
                                    float *__restrict__ lo, int Cin, int cin_pad, int64_t S, int bf16, int x16) {
+    // bf16: the 16-bit operand kind (kBF16 / kF16), 0 for fp32 planes; x16: x's kind
     __shared__ float tile[32][33];
     const int n = blockIdx.z;
     const int c0 = blockIdx.y * 32;
@@ -149,9 +151,7 @@ __global__ void stage_input_kernel(const float *__restrict__ x, float *__restric
         const int c = c0 + ty + j;
         const int64_t s = s0 + tx;
         const int64_t i = xb + (int64_t)c * S + s;
-        tile[ty + j][tx] = (c < Cin && s < S)
-                               ? (x16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[i]) : x[i])
-                               : 0.0f;
+        tile[ty + j][tx] = (c < Cin && s < S) ? (x16 ? ld16(x, i, x16) : x[i]) : 0.0f;
     }
     __syncthreads();
     float *hn = hi + (int64_t)n * S * cin_pad;
@@ -170,9 +170,8 @@ __global__ void stage_input_kernel(const float *__restrict__ x, float *__restric
                 split_tf32(tile[tx][ty + j], h, l);
                 hn[s * cin_pad + c] = h;
                 ln[s * cin_pad + c] = l;
-            } else if (bf16) {  // single bf16 plane (2-byte elements)
-                reinterpret_cast<__nv_bfloat16 *>(hi)[((int64_t)n * S + s) * cin_pad + c] =
-                    __float2bfloat16_rn(tile[tx][ty + j]);
+            } else if (bf16) {  // single bf16 or fp16 plane (2-byte elements)
+                reinterpret_cast<uint16_t *>(hi)[((int64_t)n * S + s) * cin_pad + c] = cvt16(tile[tx][ty + j], bf16);
             } else {  // single TF32 plane
                 hn[s * cin_pad + c] = round_tf32(tile[tx][ty + j]);
             }
@@ -188,9 +187,7 @@ __global__ void stage_input_cl_kernel(const float *__restrict__ x, float *__rest
     const int64_t r = (int64_t)blockIdx.x * 8 + threadIdx.y;
     const int c = blockIdx.y * 32 + threadIdx.x;
     if (r >= rows) return;
-    const float v = c >= Cin ? 0.0f
-                    : (x16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[r * Cin + c])
-                           : __ldg(x + r * Cin + c));
+    const float v = c >= Cin ? 0.0f : (x16 ? ld16(x, r * Cin + c, x16) : __ldg(x + r * Cin + c));
     const int64_t o = r * cin_pad + c;
     if (lo && bf16) {
         split_bf16(v, reinterpret_cast<__nv_bfloat16 *>(hi)[o], reinterpret_cast<__nv_bfloat16 *>(lo)[o]);
@@ -200,7 +197,7 @@ __global__ void stage_input_cl_kernel(const float *__restrict__ x, float *__rest
         hi[o] = h;
         lo[o] = l;
     } else if (bf16) {
-        reinterpret_cast<__nv_bfloat16 *>(hi)[o] = __float2bfloat16_rn(v);
+        reinterpret_cast<uint16_t *>(hi)[o] = cvt16(v, bf16);
     } else {
         hi[o] = round_tf32(v);
     }
@@ -212,7 +209,7 @@ cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *
                                 cudaStream_t s) {
     TapIndex t;
     for (int j = 0; j < kMaxTaps; ++j) t.widx[j] = j < p.g.ntaps ? p.g.taps[j].widx : 0;
-    const int mode = p.bf16 ? (p.planes == 2 ? 3 : 2) : (p.planes == 1 ? 1 : 0);
+    const int mode = p.bf16 ? (p.planes == 2 ? 3 : (p.half ? 4 : 2)) : (p.planes == 1 ? 1 : 0);
     if (kmajor) {  // tensor-core layout (cout_pad rows of every tap; cin_pad is a multiple of 32)
         dim3 grid((unsigned)(p.cin_pad / 32), (unsigned)((p.g.ntaps + 31) / 32), (unsigned)p.cout_pad);
         pack_weights_kmajor_kernel<<<grid, dim3(32, 8), 0, s>>>(w, hi, lo, p.g.Cin, p.g.Cout, p.g.kvol, p.g.ntaps,
@@ -224,23 +221,25 @@ cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *
     const int threads = 256;
     const int blocks = (int)((total + threads - 1) / threads < 4096 ? (total + threads - 1) / threads : 4096);
     pack_weights_kernel<<<blocks, threads, 0, s>>>(w, hi, lo, p.g.Cin, p.g.Cout, p.g.kvol, p.g.ntaps, p.cin_pad,
-                                                   p.cout_pad, kmajor,
-                                                   p.bf16 ? (p.planes == 2 ? 3 : 2) : (p.planes == 1 ? 1 : 0),
-                                                   p.g.Cin / p.g.G, p.g.Cout / p.g.G, p.io16, t);
+                                                   p.cout_pad, kmajor, mode, p.g.Cin / p.g.G, p.g.Cout / p.g.G,
+                                                   p.io16, t);
     return cudaGetLastError();
 }
+
+// The staged operand's 16-bit kind (0: fp32 planes).
+static int op16(const convt3d_plan_s &p) { return p.bf16 ? (p.half ? kF16 : kBF16) : kF32; }
 
 cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *hi, float *lo, cudaStream_t s) {
     const int64_t S = (int64_t)p.g.Din * p.g.Hin * p.g.Win;
     if (p.cl) {
         const int64_t rows = S * p.g.N;
         dim3 grid((unsigned)((rows + 7) / 8), (unsigned)(p.cin_pad / 32));
-        stage_input_cl_kernel<<<grid, dim3(32, 8), 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, rows, p.bf16, p.io16);
+        stage_input_cl_kernel<<<grid, dim3(32, 8), 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, rows, op16(p), p.io16);
         return cudaGetLastError();
     }
     dim3 grid((unsigned)((S + 31) / 32), (unsigned)(p.cin_pad / 32), (unsigned)p.g.N);
     dim3 block(32, 8);
-    stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S, p.bf16, p.io16);
+    stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S, op16(p), p.io16);
     return cudaGetLastError();
 }
 

@@ -145,7 +145,9 @@ void build_groups(convt3d_plan_s &p) {
     const int kchunk = p.chunk;
     const int kc = (g.Cin + kchunk - 1) / kchunk;
     p.ngroups = 0;
-    if (p.tc && g.ss[2] == 2) {  // the two w-parity classes of each (rd, rh) share a tile
+    // the two w-parity classes of each (rd, rh) share a tile where both accumulators fit
+    // tensor memory twice (double-buffered): 2 classes x Cout_pad x 2 <= 512 columns
+    if (p.tc && g.ss[2] == 2 && p.cout_pad <= 128) {
         for (int rd = 0; rd < g.ss[0]; ++rd)
             for (int rh = 0; rh < g.ss[1]; ++rh) {
                 GroupDesc &G = p.grp[p.ngroups++];
@@ -228,7 +230,7 @@ convt3d_status_t validate(const convt3d_desc_t &d) {
     if (d.Cin % sh.G || d.Cout % sh.G) return fail(CONVT3D_ERR_INVALID_ARG, "conv_groups must divide Cin and Cout");
     if (d.epilogue < CONVT3D_EPI_IDENTITY || d.epilogue > CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
         return fail(CONVT3D_ERR_INVALID_ARG, "unknown epilogue %d", d.epilogue);
-    if (d.precision < CONVT3D_PREC_3XTF32 || d.precision > CONVT3D_PREC_3XBF16)
+    if (d.precision < CONVT3D_PREC_3XTF32 || d.precision > CONVT3D_PREC_FP16)
         return fail(CONVT3D_ERR_INVALID_ARG, "unknown precision %d", d.precision);
     if (d.epilogue == CONVT3D_EPI_RELU_GROUPNORM && (d.groups < 1 || d.Cout % d.groups != 0))
         return fail(CONVT3D_ERR_INVALID_ARG, "groups must divide Cout");
@@ -238,8 +240,11 @@ convt3d_status_t validate(const convt3d_desc_t &d) {
         return fail(CONVT3D_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (bn_any && !isfinite(d.scale)) return fail(CONVT3D_ERR_INVALID_ARG, "scale must be finite");
     // Limits of this build (valid operations it does not run).
+    if (d.io_bf16 && d.io_fp16) return fail(CONVT3D_ERR_INVALID_ARG, "io_bf16 and io_fp16 are exclusive");
     if (d.io_bf16 && d.precision != CONVT3D_PREC_BF16)
         return fail(CONVT3D_ERR_UNSUPPORTED, "bf16 tensors need precision CONVT3D_PREC_BF16");
+    if (d.io_fp16 && d.precision != CONVT3D_PREC_FP16)
+        return fail(CONVT3D_ERR_UNSUPPORTED, "fp16 tensors need precision CONVT3D_PREC_FP16");
     for (int a = 0; a < 3; ++a) {
         if (sh.ss[a] > 2) return fail(CONVT3D_ERR_UNSUPPORTED, "stride > 2");
         if (sh.kk[a] > 7) return fail(CONVT3D_ERR_UNSUPPORTED, "k > 7");
@@ -248,16 +253,11 @@ convt3d_status_t validate(const convt3d_desc_t &d) {
         if (sh.ss[a] == 2 && (sh.kk[a] < 2 || sh.dil[a] % 2 == 0))
             return fail(CONVT3D_ERR_UNSUPPORTED, "stride 2 needs k >= 2 and an odd dilation (parity classes without taps)");
     }
-    if (d.Cout > 256) return fail(CONVT3D_ERR_UNSUPPORTED, "Cout > 256");
+    if (d.Cout > kMaxCout) return fail(CONVT3D_ERR_UNSUPPORTED, "Cout > 512");
     const int64_t lim = (int64_t)1 << 31;
     if ((int64_t)d.N * d.Cout * out[0] * out[1] * out[2] >= lim || (int64_t)d.N * d.Cin * d.Din * d.Hin * d.Win >= lim / 2 ||
         (int64_t)d.N * 256 * d.Din * d.Hin * d.Win >= ((int64_t)1 << 40))
         return fail(CONVT3D_ERR_UNSUPPORTED, "tensor larger than 2^31 elements");
-    if (d.precision != CONVT3D_PREC_FFMA) {
-        const int cout_pad = round_up(d.Cout, 16);
-        if (sh.ss[2] == 2 && cout_pad > 128)
-            return fail(CONVT3D_ERR_UNSUPPORTED, "3xTF32 with stride 2 along w needs Cout <= 128");
-    }
     return CONVT3D_OK;
 }
 
@@ -336,15 +336,23 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     const bool split = desc->precision == CONVT3D_PREC_3XTF32 || desc->precision == CONVT3D_PREC_3XBF16;
     p->planes = split ? 2 : (p->tc ? 1 : 0);
     p->cl = desc->channels_last != 0;
-    p->io16 = desc->io_bf16 != 0;
-    p->bf16 = desc->precision == CONVT3D_PREC_BF16 || desc->precision == CONVT3D_PREC_3XBF16;
+    p->io16 = desc->io_bf16 ? kBF16 : (desc->io_fp16 ? kF16 : kF32);
+    p->half = desc->precision == CONVT3D_PREC_FP16;
+    p->bf16 = desc->precision == CONVT3D_PREC_BF16 || desc->precision == CONVT3D_PREC_3XBF16 || p->half;
     p->elem_bytes = p->bf16 ? 2 : 4;
     p->chunk = p->tc ? kTcRowBytes / p->elem_bytes : 8;
     p->tile_m = p->tc ? kTcTileM : kFfmaTileM;
     p->cin_pad = round_up(desc->Cin, p->chunk);
     p->cout_pad = round_up(desc->Cout, 16);
-    if (!p->tc)  // the FFMA kernel's register tiles need a power-of-two channel count
+    p->nslices = 1;
+    if (!p->tc) {  // the FFMA kernel's register tiles need a power-of-two channel count
         while (p->cout_pad & (p->cout_pad - 1)) p->cout_pad += 16;
+    } else if (p->cout_pad > kTcMaxSliceN) {
+        // one MMA (and one TMA weight box) spans at most 256 columns: equal slices of
+        // a multiple of 16 columns, walked one after another over the tile's K steps
+        p->nslices = (p->cout_pad + kTcMaxSliceN - 1) / kTcMaxSliceN;
+        p->cout_pad = round_up(desc->Cout, 16 * p->nslices);
+    }
     build_groups(*p);
     // Pairs merge where the combined MMA fits (N = 2 * Cout_pad <= 128): there the
     // instruction count, not the tensor pipe, bounds the main loop.
@@ -373,14 +381,23 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     p->off_xs_lo = off;
     if (p->planes == 2) off = align_up(off + p->xs_elems * p->elem_bytes, 256);
     size_t per_tile = 0, stat = 0;
+    // partial rows hold (count, sum, M2) per group / channel; GroupNorm's statistics are
+    // (mean, rstd) per (n, g), BatchNorm's the (count, sum, M2) per (n, row split, c)
     if (desc->epilogue == CONVT3D_EPI_RELU_GROUPNORM) {
-        per_tile = 2 * (size_t)desc->groups;
+        per_tile = 3 * (size_t)desc->groups;
         stat = (size_t)desc->N * desc->groups * 2;
-    } else if (desc->epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL) {
-        per_tile = 2 * (size_t)desc->Cout;
-        stat = (size_t)desc->N * desc->Cout * 2;
     }
     p->stat_rows_per_tile = p->tc ? kTcStatRows : 1;
+    p->bn_splits = 1;
+    if (desc->epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL) {
+        // the first reduction splits each sample's rows so that its grid has about
+        // 600 blocks of 32 channels (4 per SM), each range at least 8 rows long
+        const int rows = p->tiles_per_sample * p->stat_rows_per_tile;
+        const int blocks = ((desc->Cout + 31) / 32) * desc->N;
+        p->bn_splits = std::max(1, std::min((600 + blocks - 1) / blocks, rows / 8));
+        per_tile = 3 * (size_t)desc->Cout;
+        stat = (size_t)desc->N * p->bn_splits * desc->Cout * 3;
+    }
     p->partial_doubles = per_tile * (size_t)p->tiles * p->stat_rows_per_tile;
     p->stat_doubles = stat;
     p->off_partials = off;
@@ -492,7 +509,7 @@ static convt3d_status_t check_ws(convt3d_plan_t p, void *ws, size_t bytes) {
 convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const void *wv, void *ws, size_t ws_bytes,
                                       void *stream) {
     g_last_error[0] = 0;
-    const float *w = static_cast<const float *>(wv);  // bf16 data when io_bf16: the kernels reinterpret it
+    const float *w = static_cast<const float *>(wv);  // 16-bit data when io_bf16 / io_fp16: the kernels reinterpret it
     if (!p || !w) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan or weight");
     if ((uintptr_t)w % 16) return fail(CONVT3D_ERR_INVALID_ARG, "w must be 16-byte aligned");
     convt3d_status_t st = check_ws(p, ws, ws_bytes);
@@ -515,7 +532,7 @@ convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const void *wv, void *ws
 convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *bias, const float *gamma,
                                  const float *beta, void *yv, void *ws, size_t ws_bytes, void *stream) {
     g_last_error[0] = 0;
-    // bf16 data when io_bf16: the kernels reinterpret these pointers
+    // 16-bit data when io_bf16 / io_fp16: the kernels reinterpret these pointers
     const float *x = static_cast<const float *>(xv);
     float *y = static_cast<float *>(yv);
     if (!p || !x || !y) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan, x or y");
@@ -578,7 +595,7 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *
     if (gn) {
         e = launch_gn_finalize(*p, partials, stats, s);
         if (e != cudaSuccess) return cuda_fail(e, "groupnorm finalize launch");
-        e = launch_gn_normalize(*p, stats, gamma, beta, y, s);
+        e = launch_gn_normalize(*p, stats, gamma, beta, b, y, s);
         if (e != cudaSuccess) return cuda_fail(e, "groupnorm normalize launch");
     } else if (bn) {
         e = launch_bn_finalize(*p, partials, stats, gamma, beta, y, s);
@@ -588,7 +605,11 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *
 }
 
 convt3d_status_t convt3d_check(convt3d_plan_t p, void *ws, void *stream) {
-    if (!p || !ws) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan or workspace");
+    if (!p) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan");
+    if (!ws) {  // the built-in workspace of convt3d_forward_static_workspace on the current device
+        ws = static_workspace_address();
+        if (!ws) return CONVT3D_ERR_CUDA;
+    }
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t word[4] = {0, 0, 0, 0};
     cudaError_t e = cudaStreamSynchronize(s);

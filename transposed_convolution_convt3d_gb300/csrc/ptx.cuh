@@ -156,7 +156,8 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (here both operands bf16), one CTA.
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (both operands bf16, or both
+// fp16: the instruction descriptor names the format), one CTA.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
@@ -215,6 +216,12 @@ __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t n) {
 // code 1 in both operand fields), both K-major, M = 128, N = n.
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16 with FP16 A and B (format code 0 in both
+// operand fields): fp32 accumulator, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t n) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 }  // namespace ptx

@@ -10,7 +10,10 @@
 // The array is kStaticWorkspaceBytes (32 MiB).  Every GPU on which this
 // library's device code is loaded holds those 32 MiB until the process
 // exits.  Problems whose workspace (convt3d_workspace_bytes) is larger are
-// rejected with CONVT3D_ERR_WORKSPACE before anything is launched.
+// rejected with CONVT3D_ERR_WORKSPACE before anything is launched.  A
+// device-side condition of a call (a bounded wait that ran out) lands in the
+// status word at the start of the array; convt3d_check(plan, NULL, stream)
+// reads and clears it, and the next call's weight packing clears it too.
 #include <mutex>
 
 #include "convt3d_internal.h"
@@ -29,6 +32,32 @@ void *g_device_ptr[kMaxDevices];  // device address of g_static_workspace, per d
 
 }  // namespace
 
+namespace convt3d {
+// Device address of the built-in workspace on the current device (looked up
+// with that device current on first use, then cached); NULL on failure, with
+// the reason recorded for convt3d_last_error.  The cached address stays valid
+// for the life of the device's primary context: after cudaDeviceReset the
+// library must not be used again in this process.
+void *static_workspace_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        report_error("no usable current CUDA device");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_device_ptr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+        if (e != cudaSuccess || !p) {
+            report_error("cudaGetSymbolAddress of the built-in workspace: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        g_device_ptr[dev] = p;
+    }
+    return g_device_ptr[dev];
+}
+}  // namespace convt3d
+
 extern "C" convt3d_status_t convt3d_forward_static_workspace(convt3d_plan_t plan, const void *w, const void *x,
                                                              const float *bias, const float *gamma,
                                                              const float *beta, void *y, void *stream) {
@@ -42,26 +71,9 @@ extern "C" convt3d_status_t convt3d_forward_static_workspace(convt3d_plan_t plan
                               kStaticWorkspaceBytes);
         return CONVT3D_ERR_WORKSPACE;
     }
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        convt3d::report_error("no usable current CUDA device");
-        return CONVT3D_ERR_CUDA;
-    }
-    void *ws = nullptr;
-    {
-        // First call on a device: look up the array's device address with that device current.
-        std::lock_guard<std::mutex> lock(g_mutex);
-        if (!g_device_ptr[dev]) {
-            void *p = nullptr;
-            const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
-            if (e != cudaSuccess || !p) {
-                convt3d::report_error("cudaGetSymbolAddress of the built-in workspace: %s", cudaGetErrorString(e));
-                return CONVT3D_ERR_CUDA;
-            }
-            g_device_ptr[dev] = p;
-        }
-        ws = g_device_ptr[dev];
-    }
+    // First call on a device: look up the array's device address with that device current.
+    void *ws = convt3d::static_workspace_address();
+    if (!ws) return CONVT3D_ERR_CUDA;
     // pack_weights clears the status word at the start of the workspace; every
     // other workspace region is fully rewritten by pack_weights and forward.
     convt3d_status_t st = convt3d_pack_weights(plan, w, ws, kStaticWorkspaceBytes, stream);

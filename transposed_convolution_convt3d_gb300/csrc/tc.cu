@@ -95,7 +95,11 @@ struct StepDesc {
     uint8_t cls, mask, ow, oh;
     uint8_t od, pad_[3];
 };
-constexpr int kMaxSteps = 512;  // <= 4 groups x 4 d-slices x 4 h-taps x 8 merged w-taps
+// The pairs' walks hold sum over (rd, rh) of nt_d(rd) * nt_h(rh) * nm steps; every
+// tap lies in exactly one parity class per dimension, so that is kd * kh * nm with
+// nm (distinct w offsets) <= kw: at most 7 * 7 * 7 for the largest kernel.
+constexpr int kMaxSteps = 512;
+static_assert(kMaxSteps >= 7 * 7 * 7, "step table smaller than the largest merged walk");
 
 struct TcParams {
     CUtensorMap a_hi[kMaxClasses];
@@ -115,9 +119,12 @@ struct TcParams {
     uint32_t stage_bytes, b_bytes;
     int planes;  // 2: split TF32 (A and B hi/lo), 1: single TF32 or BF16
     int cl;      // channels-last output
-    int io16;    // y is a bf16 array
-    int bf16;    // operands in bf16 (kind::f16 MMA)
+    int io16;    // y is a 16-bit array: kBF16 or kF16 (0: fp32)
+    int bf16;    // operands are 16-bit (kind::f16 MMA)
+    int half;    // the 16-bit operands are fp16 (else bf16)
     int chunk;   // input channels per K step (one 128-byte row)
+    int nslices, slice_n;  // N slices per tile (Cout_pad > 256: each slice's K walk fills its own columns)
+    int nbuf;              // accumulators in tensor memory: 2 (double-buffered) or 1
     uint32_t tmem_cols, acc_stride;
     GroupDesc grp[kMaxGroups];
     ClassDesc cls[kMaxClasses];
@@ -154,10 +161,35 @@ __device__ __forceinline__ void record_error(uint32_t *status, uint32_t code, ui
     }
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Statistics partial of values spread over the warp's lanes, written as
+// (count n, sum S, M2 = sum of squared deviations from S / n) in fp64.  The
+// lanes hold fp32 sums about a common shift c close to the values' mean --
+// s1 = sum (v - c), s2 = sum (v - c)^2 over cnt values -- so no large common
+// offset enters any fp32 sum, and the butterfly reductions stay in fp32 (this
+// GPU's fp64 rate is a small fraction of its fp32 rate): M2 = sum s2 - (sum s1)^2 / n
+// needs no more, and only S = n c + sum s1, whose terms differ in magnitude, is
+// formed in fp64 (one fused multiply-add on one lane).
+__device__ __forceinline__ void warp_moments(float s1, float s2, int cnt, float c, double *out) {
+    const float t1 = warp_sum_f(s1);
+    const float t2 = warp_sum_f(s2);
+    const int n = warp_sum_i(cnt);
+    if ((threadIdx.x & 31) == 0) {
+        out[0] = (double)n;
+        out[1] = fma((double)n, (double)c, (double)t1);
+        out[2] = n > 0 ? (double)fmaxf(t2 - t1 * t1 * __frcp_rn((float)n), 0.f) : 0.0;
+    }
 }
 
 // Per-channel sums over the 32 lanes for 16 channels held by every lane:
@@ -282,6 +314,11 @@ __device__ __forceinline__ float tree_sum16(const float (&v)[16]) {
     return (a[0] + a[2]) + (a[1] + a[3]);
 }
 
+// Classes (0, 1 or 2) whose row is inside the output, from the two row offsets.
+__device__ __forceinline__ int valid_rows(const int (&off)[2], int ncls) {
+    return (off[0] >= 0 ? 1 : 0) + (ncls > 1 && off[1] >= 0 ? 1 : 0);
+}
+
 // Position of epilogue row m of a tile for one class: output offset within a
 // channel plane, or -1 when the row lies past the q-grid or the output.
 __device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G, const ClassDesc &C, int t, int m) {
@@ -318,12 +355,15 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
-    __shared__ float s_bias[256];                          // bias, zero-padded to 256 channels
-    __shared__ __align__(16) float s_bias_l2e[256];        // bias * log2(e) (softmax)
+    __shared__ float s_bias[kMaxCout];                     // bias, zero-padded to kMaxCout channels
+    __shared__ __align__(16) float s_bias_l2e[kMaxCout];   // bias * log2(e) (softmax)
     __shared__ float s_xchg[sm_exchange_floats<EPI>()];   // softmax (max, sum) exchange, double-buffered
-    // The group and class tables for the epilogue warps.
+    // The group and class tables (and, for merged walks, the step table) in shared
+    // memory: the producer and MMA threads index them per tile and per K step, and
+    // an indexed read of the kernel parameters would go through the constant cache.
     __shared__ GroupDesc s_grp[kMaxGroups];
     __shared__ ClassDesc s_cls[kMaxClasses];
+    __shared__ StepDesc s_steps[MERGED ? kMaxSteps : 1];
 
     // 1024-byte aligned ring of pipeline stages
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -349,12 +389,14 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         ptx::mbar_init(drain, 1);
         ptx::fence_mbar_init();
     }
-    for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+    for (int c = threadIdx.x; c < kMaxCout; c += blockDim.x) {
         s_bias[c] = (P.bias && c < P.Cout) ? P.bias[c] : 0.f;
         s_bias_l2e[c] = s_bias[c] * kLog2e;
     }
     if (threadIdx.x < kMaxGroups) s_grp[threadIdx.x] = P.grp[threadIdx.x];
     if (threadIdx.x < kMaxClasses) s_cls[threadIdx.x] = P.cls[threadIdx.x];
+    if constexpr (MERGED)
+        for (int i = threadIdx.x; i < kMaxSteps; i += blockDim.x) s_steps[i] = P.steps[i];
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), P.tmem_cols);
         ptx::tmem_relinquish();
@@ -384,7 +426,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             // One K step per input-channel chunk of one tap: the activation slice of
             // class `cls` at tap `td`, the weight slice of tap tb0 and, merged, of tap tb1.
             auto issue_tap = [&](const Tile &T, int cls, const ClassDesc &C, int qd0, int qh0, int qw0,
-                                 const TapDesc td, int tb0, int tb1) {
+                                 const TapDesc td, int tb0, int tb1, int row0) {
                 const int w0 = qw0 + C.lo_w, h0 = qh0 + C.lo_h, d0 = qd0 + C.lo_d;
                 const uint16_t ow = (uint16_t)(td.dw - C.lo_w);
                 const uint16_t oh = (uint16_t)(td.dh - C.lo_h);
@@ -410,12 +452,12 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     if (kPlanes == 2)
                         ptx::tma_load_im2col_5d(sb + kABytes, &P.a_lo[cls], fb, c0, w0, h0, d0, T.n, ow, oh, od);
 #endif
-                    ptx::tma_load_3d(sbb, &P.b_hi, fb, c0, 0, tb0);
-                    if (MERGED && tb1 >= 0) ptx::tma_load_3d(sbb + P.b_bytes, &P.b_hi, fb, c0, 0, tb1);
+                    ptx::tma_load_3d(sbb, &P.b_hi, fb, c0, row0, tb0);
+                    if (MERGED && tb1 >= 0) ptx::tma_load_3d(sbb + P.b_bytes, &P.b_hi, fb, c0, row0, tb1);
                     if (kPlanes == 2) {
                         const uint32_t lo = sbb + (uint32_t)kBSlots * P.b_bytes;
-                        ptx::tma_load_3d(lo, &P.b_lo, fb, c0, 0, tb0);
-                        if (MERGED && tb1 >= 0) ptx::tma_load_3d(lo + P.b_bytes, &P.b_lo, fb, c0, 0, tb1);
+                        ptx::tma_load_3d(lo, &P.b_lo, fb, c0, row0, tb0);
+                        if (MERGED && tb1 >= 0) ptx::tma_load_3d(lo + P.b_bytes, &P.b_lo, fb, c0, row0, tb1);
                     }
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -426,13 +468,15 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 }
             };
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
-                const Tile T = decode(P, P.grp, tile);
-                const GroupDesc &G = P.grp[T.gi];
+                const Tile T = decode(P, s_grp, tile);
+                const GroupDesc &G = s_grp[T.gi];
                 const int q0 = T.t * kTcTileM;
-                const int qd0 = q0 / (G.Qh * G.Qw), qh0 = (q0 / G.Qw) % G.Qh, qw0 = q0 % G.Qw;
+                const int qd0 = (int)fastdiv((uint32_t)q0, G.div_qhw);
+                const int qhw = (int)fastdiv((uint32_t)q0, G.div_qw);  // q0 / Qw
+                const int qh0 = qhw - qd0 * G.Qh, qw0 = q0 - qhw * G.Qw;
                 if constexpr (MERGED) {
                     // the tile's run of the flattened walk (d-slices: the same for both classes)
-                    const ClassDesc &C0 = P.cls[G.cls[0]], &C1 = P.cls[G.cls[1]];
+                    const ClassDesc &C0 = s_cls[G.cls[0]], &C1 = s_cls[G.cls[1]];
                     const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);
                     const int nhw0 = C0.nt_h * C0.nt_w;
                     const int a_begin = tr.begin / nhw0, a_end = (tr.end + nhw0 - 1) / nhw0;
@@ -441,7 +485,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     const int w00 = qw0 + C0.lo_w, h00 = qh0 + C0.lo_h, d00 = qd0 + C0.lo_d;
                     const int w01 = qw0 + C1.lo_w, h01 = qh0 + C1.lo_h, d01 = qd0 + C1.lo_d;
                     for (int st = G.step0 + a_begin * G.steps_per_a; ok && st < s_end; ++st) {
-                        const StepDesc e = P.steps[st];
+                        const StepDesc e = s_steps[st];
                         const bool one = e.cls != 0;
                         const int cls = one ? G.cls[1] : G.cls[0];
                         const int w0 = one ? w01 : w00, h0 = one ? h01 : h00, d0 = one ? d01 : d00;
@@ -485,10 +529,12 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 } else {
                     for (int ci = 0; ok && ci < G.ncls; ++ci) {
                         const int cls = G.cls[ci];
-                        const ClassDesc &C = P.cls[cls];
+                        const ClassDesc &C = s_cls[cls];
                         const TapRange tr = tile_taps(G, C, T.t, kTcTileM, P.Din);
-                        for (int j = tr.begin; ok && j < tr.end; ++j)
-                            issue_tap(T, cls, C, qd0, qh0, qw0, P.taps[C.tap_begin + j], C.tap_begin + j, -1);
+                        for (int sl = 0; ok && sl < P.nslices; ++sl)  // the same activation walk per N slice
+                            for (int j = tr.begin; ok && j < tr.end; ++j)
+                                issue_tap(T, cls, C, qd0, qh0, qw0, P.taps[C.tap_begin + j], C.tap_begin + j, -1,
+                                          sl * P.slice_n);
                     }
                 }
             }
@@ -507,11 +553,13 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
     // ---------------------------------------------------------- MMA issuer
     else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc =
-                OPS >= 2 ? ptx::idesc_bf16((uint32_t)P.cout_pad) : ptx::idesc_tf32((uint32_t)P.cout_pad);
+            const uint32_t idesc = OPS >= 2 ? (P.half ? ptx::idesc_f16((uint32_t)P.slice_n)
+                                                      : ptx::idesc_bf16((uint32_t)P.slice_n))
+                                            : ptx::idesc_tf32((uint32_t)P.slice_n);
             // merged steps of both classes: N = 2 * Cout_pad
             const uint32_t idesc2 =
-                OPS >= 2 ? ptx::idesc_bf16(2u * (uint32_t)P.cout_pad) : ptx::idesc_tf32(2u * (uint32_t)P.cout_pad);
+                OPS >= 2 ? (P.half ? ptx::idesc_f16(2u * (uint32_t)P.cout_pad) : ptx::idesc_bf16(2u * (uint32_t)P.cout_pad))
+                         : ptx::idesc_tf32(2u * (uint32_t)P.cout_pad);
             constexpr uint64_t kA16 = kABytes >> 4;                  // one activation plane, 16-byte units
             const uint64_t b16 = (uint64_t)(P.b_bytes >> 4);         // one weight slice
             const uint64_t blo16 = (uint64_t)kBSlots * b16;          // B_lo after the B_hi slots
@@ -574,10 +622,10 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 }
             };
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++iter) {
-                const Tile T = decode(P, P.grp, tile);
-                const GroupDesc &G = P.grp[T.gi];
-                const int acc = iter & 1;
-                const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
+                const Tile T = decode(P, s_grp, tile);
+                const GroupDesc &G = s_grp[T.gi];
+                const int acc = P.nbuf == 2 ? (iter & 1) : 0;
+                const uint32_t aph = (uint32_t)(P.nbuf == 2 ? iter >> 1 : iter) & 1u;
                 if (!ptx::mbar_wait_bounded(tempty0 + 8 * acc, aph ^ 1u, &abort_flag, kWaitNs)) {
                     ok = false;
                     break;
@@ -587,23 +635,24 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 if constexpr (MERGED) {
                     // same walk as the producer; shared offsets come first, so a merged step
                     // never meets one accumulator initialised and the other not
-                    const ClassDesc &C0 = P.cls[G.cls[0]];
+                    const ClassDesc &C0 = s_cls[G.cls[0]];
                     const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);
                     const int nhw0 = C0.nt_h * C0.nt_w;
                     const int a_begin = tr.begin / nhw0, a_end = (tr.end + nhw0 - 1) / nhw0;
                     const int s_end = G.step0 + a_end * G.steps_per_a;
                     uint32_t ini = 0;  // bit c: class c's accumulator holds a product
                     for (int st = G.step0 + a_begin * G.steps_per_a; ok && st < s_end; ++st) {
-                        const uint32_t mask = P.steps[st].mask;
+                        const uint32_t mask = s_steps[st].mask;
                         const uint32_t d_tmem = acc_base + (mask == 2u ? (uint32_t)P.cout_pad : 0u);
                         mma_tap(d_tmem, mask == 3u ? idesc2 : idesc, (ini & mask) == 0u);
                         ini |= mask;
                     }
                 } else {
                     // flat step loop per class (the issue rate of the MMA-bound shapes depends on it)
-                    for (int ci = 0; ok && ci < G.ncls; ++ci) {
-                        const ClassDesc &C = P.cls[G.cls[ci]];
-                        const uint32_t d_tmem = acc_base + (uint32_t)ci * P.cout_pad;
+                    for (int cs = 0; ok && cs < G.ncls * P.nslices; ++cs) {
+                        const int ci = cs / P.nslices, sl = cs - ci * P.nslices;
+                        const ClassDesc &C = s_cls[G.cls[ci]];
+                        const uint32_t d_tmem = acc_base + (uint32_t)ci * P.cout_pad + (uint32_t)(sl * P.slice_n);
                         const TapRange tr = tile_taps(G, C, T.t, kTcTileM, P.Din);  // same taps as the producer
                         const int nsteps = (tr.end - tr.begin) * P.kc;
                         for (int s = 0; s < nsteps; ++s) {
@@ -686,7 +735,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         constexpr bool gn = EPI == CONVT3D_EPI_RELU_GROUPNORM;
         constexpr bool bn = EPI == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
         constexpr bool sm = EPI == CONVT3D_EPI_SOFTMAX_SIGMOID;
-        const int nstat = gn ? 2 * P.groups : (bn ? 2 * C : 0);
+        const int nstat = gn ? 3 * P.groups : (bn ? 3 * C : 0);  // (n, S, M2) per group / channel
         const int cpg = gn ? C / P.groups : 16;
         const bool gn_inline = gn && (cpg % 16 == 0);  // groups made of whole 16-channel chunks
         auto mine = [&](int j) -> bool {                // does this warp own chunk j?
@@ -697,8 +746,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         for (; tile < P.total_tiles; tile += gridDim.x, ++iter) {
             const Tile T = decode(P, s_grp, tile);
             const GroupDesc &G = s_grp[T.gi];
-            const int acc = iter & 1;
-            const uint32_t aph = (uint32_t)(iter >> 1) & 1u;
+            const int acc = P.nbuf == 2 ? (iter & 1) : 0;
+            const uint32_t aph = (uint32_t)(P.nbuf == 2 ? iter >> 1 : iter) & 1u;
             if (!ptx::mbar_wait_bounded(tfull0 + 8 * acc, aph, &abort_flag, kWaitNs)) {
                 if (lane == 0) record_error(P.status, kErrTimeout, 3);
                 abort_flag = 1;
@@ -730,29 +779,26 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     }
                     return;
                 }
-                if (P.io16) {  // bf16 output: same element positions, 2-byte values
-                    __nv_bfloat16 *yh = reinterpret_cast<__nv_bfloat16 *>(P.y) + (int64_t)T.n * C * V;
+                if (P.io16) {  // bf16 / fp16 output: same element positions, 2-byte values
+                    uint16_t *yh = reinterpret_cast<uint16_t *>(P.y) + (int64_t)T.n * C * V;
                     if (P.cl) {
-                        __nv_bfloat16 *dst = yh + (int64_t)off * C + c0;
-                        if (c0 + 16 <= C && (C & 7) == 0) {  // two 16-byte stores of 8 bf16
+                        uint16_t *dst = yh + (int64_t)off * C + c0;
+                        if (c0 + 16 <= C && (C & 7) == 0) {  // two 16-byte stores of 8 values
                             uint32_t w[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-                                w[i] = *reinterpret_cast<const uint32_t *>(&h);
-                            }
+                            for (int i = 0; i < 8; ++i) w[i] = cvt16x2(o[2 * i], o[2 * i + 1], P.io16);
                             reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
                             reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
                         } else {
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
-                                if (c0 + i < C) dst[i] = __float2bfloat16_rn(o[i]);
+                                if (c0 + i < C) dst[i] = cvt16(o[i], P.io16);
                         }
                     } else {
-                        __nv_bfloat16 *dst = yh + (int64_t)c0 * V + off;
+                        uint16_t *dst = yh + (int64_t)c0 * V + off;
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            if (c0 + i < C) dst[(int64_t)i * V] = __float2bfloat16_rn(o[i]);
+                            if (c0 + i < C) dst[(int64_t)i * V] = cvt16(o[i], P.io16);
                     }
                     return;
                 }
@@ -977,12 +1023,12 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         sigmoid16(e[jj][0], A0, o0);
                         sigmoid16(e[jj][1], A1, o1);
                         if (P.io16) {
-                            __nv_bfloat16 *yh = reinterpret_cast<__nv_bfloat16 *>(P.y) + (int64_t)T.n * C * V;
+                            uint16_t *yh = reinterpret_cast<uint16_t *>(P.y) + (int64_t)T.n * C * V;
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 if (c0 + i < C)
-                                    *reinterpret_cast<__nv_bfloat162 *>(yh + (int64_t)(c0 + i) * V + off[0]) =
-                                        __floats2bfloat162_rn(o0[i], o1[i]);
+                                    *reinterpret_cast<uint32_t *>(yh + (int64_t)(c0 + i) * V + off[0]) =
+                                        cvt16x2(o0[i], o1[i], P.io16);
                         } else {
                             float *d = yn + (int64_t)c0 * V + off[0];
                             if (c0 + 16 <= C) {
@@ -1021,7 +1067,9 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 }
             } else {
                 // identity / relu+groupnorm store / batchnorm partial sums, per owned chunk
-                float gs1 = 0.f, gs2 = 0.f;  // running group sums (groups of whole chunks)
+                // running group sums about the shift gc (groups of whole chunks)
+                float gs1 = 0.f, gs2 = 0.f, gc = 0.f;
+                int gcnt = 0;
                 for (int j = 0; j < nchunks; ++j) {
                     if (!mine(j)) continue;
                     const int c0 = 16 * j;
@@ -1033,64 +1081,103 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[1][i] = 0.f;
                     }
+                    // GroupNorm: v = ReLU(conv + b) feeds the statistics; the stored value is
+                    // r = v - b (the accumulator itself where the ReLU passes, else -b), so no
+                    // rounding at the bias's magnitude enters y before the normalise pass
+                    float r[2][16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float b = s_bias[c0 + i];
-                        v[0][i] += b;
-                        v[1][i] += b;
                         if (gn) {
-                            v[0][i] = fmaxf(v[0][i], 0.f);
-                            v[1][i] = fmaxf(v[1][i], 0.f);
+                            const float t0 = v[0][i] + b, t1 = v[1][i] + b;
+                            r[0][i] = t0 > 0.f ? v[0][i] : -b;
+                            r[1][i] = t1 > 0.f ? v[1][i] : -b;
+                            v[0][i] = fmaxf(t0, 0.f);
+                            v[1][i] = fmaxf(t1, 0.f);
+                        } else {
+                            v[0][i] += b;
+                            v[1][i] += b;
                         }
                     }
                     if (bn) {
-                        // per-channel sums of z = scale*(conv + bias) over this warp's 32 rows
-                        float sz = 0.f, sz2 = 0.f;
-                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
-                            const bool valid = off[ci] >= 0;
-                            float z[16], z2[16];
+                        // per channel of z = scale*(conv + bias) over this warp's rows (both
+                        // classes of a pair): count, sum, and the squared deviations from the
+                        // warp's own channel mean (no common offset enters the squares)
+                        const bool val0 = off[0] >= 0, val1 = G.ncls > 1 && off[1] >= 0;
+                        float z[2][16];
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                z[i] = valid ? P.scale * v[ci][i] : 0.f;
-                                z2[i] = z[i] * z[i];
-                            }
-                            sz += transpose_reduce16(z, lane);
-                            sz2 += transpose_reduce16(z2, lane);
+                        for (int i = 0; i < 16; ++i) {
+                            z[0][i] = val0 ? P.scale * v[0][i] : 0.f;
+                            z[1][i] = val1 ? P.scale * v[1][i] : 0.f;
+                        }
+                        float sz = transpose_reduce16(z[0], lane);
+                        if (G.ncls > 1) sz += transpose_reduce16(z[1], lane);
+                        const int nrow = __popc(__ballot_sync(0xffffffffu, val0)) +
+                                         __popc(__ballot_sync(0xffffffffu, val1));
+                        const float mean = nrow > 0 ? sz / (float)nrow : 0.f;  // lanes 2i, 2i+1: channel c0 + i
+                        // deviations from the warp's mean: their sum (the sum of z without the
+                        // offset's rounding) and their squares
+                        float q[2][16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float mi = __shfl_sync(0xffffffffu, mean, 2 * i);
+                            z[0][i] = val0 ? z[0][i] - mi : 0.f;
+                            z[1][i] = val1 ? z[1][i] - mi : 0.f;
+                            q[0][i] = z[0][i] * z[0][i];
+                            q[1][i] = z[1][i] * z[1][i];
+                        }
+                        float sd = transpose_reduce16(z[0], lane), m2 = transpose_reduce16(q[0], lane);
+                        if (G.ncls > 1) {
+                            sd += transpose_reduce16(z[1], lane);
+                            m2 += transpose_reduce16(q[1], lane);
                         }
                         const int c = c0 + (lane >> 1);
                         if ((lane & 1) == 0 && c < C) {
-                            part[2 * c] = (double)sz;
-                            part[2 * c + 1] = (double)sz2;
+                            part[3 * c] = (double)nrow;
+                            part[3 * c + 1] = fma((double)nrow, (double)mean, (double)sd);
+                            part[3 * c + 2] =
+                                nrow > 0 ? (double)fmaxf(m2 - sd * sd * __frcp_rn((float)nrow), 0.f) : 0.0;
                         }
                         continue;
                     }
                     if (gn_inline) {
                         const float m0 = off[0] >= 0 ? 1.f : 0.f, m1 = off[1] >= 0 ? 1.f : 0.f;
+                        const int nval = 16 * ((off[0] >= 0 ? 1 : 0) + (off[1] >= 0 ? 1 : 0));
+                        if (c0 % cpg == 0) {  // first chunk of a group: its warp mean is the group's shift
+                            float sc = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) sc += m0 * v[0][i] + m1 * v[1][i];
+                            sc = warp_sum_f(sc);
+                            const int nc = warp_sum_i(nval);
+                            gc = nc > 0 ? sc / (float)nc : 0.f;
+                            gs1 = gs2 = 0.f;
+                            gcnt = 0;
+                        }
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float a = m0 * v[0][i], b = m1 * v[1][i];
+                            const float a = m0 * (v[0][i] - gc), b = m1 * (v[1][i] - gc);
                             gs1 += a + b;
                             gs2 += a * a + b * b;
                         }
-                        if ((c0 + 16) % cpg == 0) {  // this chunk closes group g (same for all lanes)
-                            const int g = c0 / cpg;
-                            const double t1 = warp_sum_d((double)gs1);
-                            const double t2 = warp_sum_d((double)gs2);
-                            if (lane == 0) {
-                                part[2 * g] = t1;
-                                part[2 * g + 1] = t2;
-                            }
-                            gs1 = gs2 = 0.f;
+                        gcnt += nval;
+                        if ((c0 + 16) % cpg == 0)  // this chunk closes group g (same for all lanes)
+                            warp_moments(gs1, gs2, gcnt, gc, part + 3 * (c0 / cpg));
+                    }
+                    if (gn) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            v[0][i] = r[0][i];
+                            v[1][i] = r[1][i];
                         }
                     }
-                    if (P.io16 && !P.cl && pair_store) {  // bf16 NCDHW: (even, odd) outputs as one bf16x2
+                    if (P.io16 && !P.cl && pair_store) {  // 16-bit NCDHW: (even, odd) outputs as one pair
                         if (off[0] >= 0 && off[1] >= 0) {
-                            __nv_bfloat16 *yh = reinterpret_cast<__nv_bfloat16 *>(P.y) + (int64_t)T.n * C * V;
+                            uint16_t *yh = reinterpret_cast<uint16_t *>(P.y) + (int64_t)T.n * C * V;
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 if (c0 + i < C)
-                                    *reinterpret_cast<__nv_bfloat162 *>(yh + (int64_t)(c0 + i) * V + off[0]) =
-                                        __floats2bfloat162_rn(v[0][i], v[1][i]);
+                                    *reinterpret_cast<uint32_t *>(yh + (int64_t)(c0 + i) * V + off[0]) =
+                                        cvt16x2(v[0][i], v[1][i], P.io16);
                         }
                     } else if (P.cl || P.io16) {
                         _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
@@ -1113,33 +1200,38 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     }
                 }
                 if (gn && !gn_inline) {
-                    // group statistics of the ReLU output: a second pass over tensor memory,
-                    // groups g % 2 == half (all lanes in step; invalid rows contribute nothing)
+                    // group statistics of the ReLU output: passes over tensor memory per group,
+                    // groups g % 2 == half (all lanes in step; invalid rows contribute nothing):
+                    // the warp's mean of the group first, then sums about it
                     for (int g = half; g < P.groups; g += kHalves) {
-                        float s1 = 0.f, s2 = 0.f;
-                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
-                            const bool valid = off[ci] >= 0;
-                            const uint32_t col = acc_col + (uint32_t)ci * P.cout_pad;
-                            for (int c0 = (g * cpg) & ~15; c0 < (g + 1) * cpg; c0 += 16) {
-                                float v[16];
-                                ptx::tmem_ld16(lane_base + col + c0, v);
-                                ptx::tmem_wait_ld();
+                        float c = 0.f, s1 = 0.f, s2 = 0.f;
+                        int cnt = 0;
+                        for (int pass = 0; pass < 2; ++pass) {
+                            _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                                const bool valid = off[ci] >= 0;
+                                const uint32_t col = acc_col + (uint32_t)ci * P.cout_pad;
+                                for (int c0 = (g * cpg) & ~15; c0 < (g + 1) * cpg; c0 += 16) {
+                                    float v[16];
+                                    ptx::tmem_ld16(lane_base + col + c0, v);
+                                    ptx::tmem_wait_ld();
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const int c = c0 + i;
-                                    if (c < g * cpg || c >= (g + 1) * cpg) continue;
-                                    const float val = valid ? fmaxf(v[i] + s_bias[c], 0.f) : 0.f;
-                                    s1 += val;
-                                    s2 += val * val;
+                                    for (int i = 0; i < 16; ++i) {
+                                        const int ch = c0 + i;
+                                        if (!valid || ch < g * cpg || ch >= (g + 1) * cpg) continue;
+                                        const float d = fmaxf(v[i] + s_bias[ch], 0.f) - c;
+                                        s1 += d;
+                                        s2 += d * d;
+                                        cnt += pass;
+                                    }
                                 }
                             }
+                            if (pass == 0) {
+                                const int n = warp_sum_i(valid_rows(off, G.ncls) * cpg);
+                                c = n > 0 ? warp_sum_f(s1) / (float)n : 0.f;
+                                s1 = s2 = 0.f;
+                            }
                         }
-                        const double t1 = warp_sum_d((double)s1);
-                        const double t2 = warp_sum_d((double)s2);
-                        if (lane == 0) {
-                            part[2 * g] = t1;
-                            part[2 * g + 1] = t2;
-                        }
+                        warp_moments(s1, s2, cnt, c, part + 3 * g);
                     }
                 }
             }
@@ -1279,6 +1371,7 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->chunk = kRowBytes / p.elem_bytes;
         P->kc = p.cin_pad / P->chunk;
         P->bf16 = p.bf16;
+        P->half = p.half;
         P->epilogue = p.d.epilogue;
         P->groups = p.d.groups;
         P->scale = p.d.scale;
@@ -1321,9 +1414,14 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         }
         for (int i = 0; i < kMaxClasses; ++i) P->cls[i] = g.cls[i];
         for (int i = 0; i < kMaxTaps; ++i) P->taps[i] = g.taps[i];
-        P->acc_stride = (uint32_t)(ncls_max * p.cout_pad);
-        P->tmem_cols = (uint32_t)round_pow2(2 * ncls_max * p.cout_pad);
-        P->b_bytes = (uint32_t)p.cout_pad * kRowBytes;
+        P->nslices = p.nslices;
+        P->slice_n = p.cout_pad / p.nslices;
+        // double-buffered accumulators where two fit the 512 tensor-memory columns
+        const int acc_cols = ncls_max * p.cout_pad;
+        P->nbuf = 2 * acc_cols <= 512 ? 2 : 1;
+        P->acc_stride = (uint32_t)acc_cols;
+        P->tmem_cols = (uint32_t)round_pow2(P->nbuf * acc_cols);
+        P->b_bytes = (uint32_t)P->slice_n * kRowBytes;
         P->planes = p.planes;
         P->cl = p.cl;
         P->io16 = p.io16;
@@ -1363,7 +1461,8 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
 
     // activation maps: one im2col map per class and plane
     const cuuint64_t eb = (cuuint64_t)p.elem_bytes;
-    const CUtensorMapDataType dt = p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapDataType dt = !p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : (p.half ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
     const cuuint64_t gdim[5] = {(cuuint64_t)p.cin_pad, (cuuint64_t)g.Win, (cuuint64_t)g.Hin, (cuuint64_t)g.Din,
                                 (cuuint64_t)g.N};
     const cuuint64_t gstr[4] = {(cuuint64_t)p.cin_pad * eb, (cuuint64_t)p.cin_pad * eb * g.Win,
@@ -1391,10 +1490,10 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
             }
         }
     }
-    // weight maps: [tap][cout_pad][cin_pad], box 32 x cout_pad x 1
+    // weight maps: [tap][cout_pad][cin_pad], box chunk x slice_n x 1
     const cuuint64_t wdim[3] = {(cuuint64_t)p.cin_pad, (cuuint64_t)p.cout_pad, (cuuint64_t)g.ntaps};
     const cuuint64_t wstr[2] = {(cuuint64_t)p.cin_pad * eb, (cuuint64_t)p.cin_pad * eb * p.cout_pad};
-    const cuuint32_t box[3] = {(cuuint32_t)P->chunk, (cuuint32_t)p.cout_pad, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)P->chunk, (cuuint32_t)P->slice_n, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     for (int plane = 0; plane < p.planes; ++plane) {
         CUresult r = fn.tiled(plane ? &P->b_lo : &P->b_hi, dt, 3,

@@ -54,6 +54,7 @@ class Spec:
     conv_groups: int = 1
     channels_last: bool = False  # x and y in NDHWC memory order (make_inputs still returns NCDHW x)
     io_bf16: bool = False        # x, w and y as bf16 tensors (make_inputs still returns fp32 values)
+    io_fp16: bool = False        # x, w and y as fp16 tensors (likewise)
 
     @property
     def kdims(self):
