@@ -447,17 +447,29 @@ def test_bf16_tensors_eval_batchnorm():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("precision", PRECISIONS)
-@pytest.mark.parametrize("cin", [264, 520])
+@pytest.mark.parametrize("cin", [264, 520, 1024])
 def test_long_reduction(cin, precision):
-    """K = Cin * 27 = 7,128 and 14,040 products per output element with an
-    elementwise epilogue: the tensor cores' fp32 accumulation drifts roughly in
-    proportion to K (1.7e-4 and 2.6e-4 measured after GroupNorm's rescaling,
-    beyond the 1e-4 bar that the workloads' K <= 1,728 meets), so these long
-    reductions are held to 1e-3."""
+    """K = Cin * 27 = 7,128, 14,040 and 27,648 products per output element with an
+    elementwise epilogue, held to the 1e-4 bar.  The tensor cores round the fp32
+    accumulator once per MMA and that error grows with the length of the chain, so
+    the tensor-core kernels accumulate such a tile's K walk in segments of at most
+    64 K steps and add the segments' partial sums in fp32."""
     spec = E.Spec(f"cin{cin}", N=1, Cin=cin, Cout=64, D=2, H=3, W=4, k=3, bias=True,
                   epilogue=E.EPI_RELU_GROUPNORM, groups=8, seed_index=63)
     inputs = E.make_inputs(spec)
-    assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name, 1e-3)
+    assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("precision", PRECISIONS)
+def test_long_reduction_pairs(precision):
+    """The same for w-parity pairs (stride 2 along w, Cout 96: two accumulators per
+    tile, single-buffered beside the running sum) with 12 channels per GroupNorm
+    group (the statistics' second pass over tensor memory): K = 512 * 8 per class."""
+    spec = E.Spec("cin512_s2_pairs", N=1, Cin=512, Cout=96, D=2, H=3, W=4, k=4, stride=2, pad=1, bias=True,
+                  epilogue=E.EPI_RELU_GROUPNORM, groups=8, seed_index=64)
+    inputs = E.make_inputs(spec)
+    assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name)
 
 
 # Wide channel counts (up to the 512 output channels of one tensor-memory

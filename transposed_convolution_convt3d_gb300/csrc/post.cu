@@ -202,25 +202,31 @@ __global__ void bn_reduce_kernel(const double *__restrict__ partials, double *__
 
 // Phase 2: per channel, batch mean and biased variance from the (count, sum,
 // M2) of every (sample, split), then the pooled output from each sample's sum;
-// optionally the running statistics' update (unbiased variance).
-__global__ void bn_finalize_kernel(const double *__restrict__ sums, const float *__restrict__ gamma,
-                                   const float *__restrict__ beta, float *__restrict__ y, int N, int C, int splits,
-                                   double V, double eps, float *__restrict__ rmean, float *__restrict__ rvar,
-                                   double momentum, int y16) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= C) return;
+// optionally the running statistics' update (unbiased variance).  One warp per
+// channel: lanes stride over the rows, butterfly sums in a fixed order.
+constexpr int kBnFinWarps = 4;
+
+__global__ void __launch_bounds__(32 * kBnFinWarps) bn_finalize_kernel(
+    const double *__restrict__ sums, const float *__restrict__ gamma, const float *__restrict__ beta,
+    float *__restrict__ y, int N, int C, int splits, double V, double eps, float *__restrict__ rmean,
+    float *__restrict__ rvar, double momentum, int y16) {
+    const int c = blockIdx.x * kBnFinWarps + threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (c >= C) return;  // whole warps leave together
     const int R = N * splits;
     double cnt = 0.0, S = 0.0;
-    for (int r = 0; r < R; ++r) {
+    for (int r = lane; r < R; r += 32) {
         cnt += sums[((int64_t)r * C + c) * 3];
         S += sums[((int64_t)r * C + c) * 3 + 1];
     }
+    cnt = warp_sum(cnt);
+    S = warp_sum(S);
     const double mean = cnt > 0.0 ? S / cnt : 0.0;
     double m2 = 0.0;
-    for (int r = 0; r < R; ++r) m2 += row_m2(sums + ((int64_t)r * C + c) * 3, mean);
+    for (int r = lane; r < R; r += 32) m2 += row_m2(sums + ((int64_t)r * C + c) * 3, mean);
+    m2 = warp_sum(m2);
     const double var = cnt > 0.0 ? m2 / cnt : 0.0;
     const double rstd = 1.0 / sqrt(var + eps);
-    for (int n = 0; n < N; ++n) {
+    for (int n = lane; n < N; n += 32) {
         double Sn = 0.0;
         for (int k = 0; k < splits; ++k) Sn += sums[(((int64_t)n * splits + k) * C + c) * 3 + 1];
         const float out = (float)((double)gamma[c] * (Sn / V - mean) * rstd + (double)beta[c]);
@@ -229,7 +235,7 @@ __global__ void bn_finalize_kernel(const double *__restrict__ sums, const float 
         else
             y[(int64_t)n * C + c] = out;
     }
-    if (rmean && rvar) {
+    if (lane == 0 && rmean && rvar) {
         const double unbiased = cnt > 1.0 ? var * cnt / (cnt - 1.0) : 0.0;
         rmean[c] = (float)((1.0 - momentum) * (double)rmean[c] + momentum * mean);
         rvar[c] = (float)((1.0 - momentum) * (double)rvar[c] + momentum * unbiased);
@@ -390,8 +396,9 @@ cudaError_t launch_bn_finalize(const convt3d_plan_s &p, const double *partials, 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const double V = (double)p.g.Do * p.g.Ho * p.g.Wo;
-    bn_finalize_kernel<<<(C + 127) / 128, 128, 0, s>>>(sums, gamma, beta, y, N, C, p.bn_splits, V, (double)p.d.eps,
-                                                        p.run_mean, p.run_var, (double)p.momentum, p.io16);
+    bn_finalize_kernel<<<(C + kBnFinWarps - 1) / kBnFinWarps, 32 * kBnFinWarps, 0, s>>>(
+        sums, gamma, beta, y, N, C, p.bn_splits, V, (double)p.d.eps, p.run_mean, p.run_var, (double)p.momentum,
+        p.io16);
     return cudaGetLastError();
 }
 

@@ -75,6 +75,9 @@ constexpr int sm_exchange_floats() {
                                                                       : 1;
 }
 constexpr int kMaxStages = 8;  // the MMA issue dispatches stage indices 0..7
+// Longest accumulation chain of one tensor-memory accumulator, in K steps (32 fp32 /
+// 64 bf16 channels x 12 MMAs each): about 770 roundings of the fp32 accumulator.
+constexpr int kSegSteps = 64;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 // Input channels per K step: 32 (128-byte rows, 128-byte swizzle) or 16
 // (64-byte rows, 64-byte swizzle: half-size stages, twice as many of them).
@@ -125,6 +128,8 @@ struct TcParams {
     int chunk;   // input channels per K step (one 128-byte row)
     int nslices, slice_n;  // N slices per tile (Cout_pad > 256: each slice's K walk fills its own columns)
     int nbuf;              // accumulators in tensor memory: 2 (double-buffered) or 1
+    int seg_steps;         // long K walks: steps per accumulation segment (SEG kernels)
+    uint32_t sum_col;      // tensor-memory column of the segments' running sums (SEG kernels)
     uint32_t tmem_cols, acc_stride;
     GroupDesc grp[kMaxGroups];
     ClassDesc cls[kMaxClasses];
@@ -295,7 +300,7 @@ __device__ __forceinline__ void sigmoid_coefficients(float f, uint64_t (&A)[4]) 
     A[3] = pack2(a3, a3);
 }
 
-// Pairwise reductions of 16 values (4 dependent levels instead of 15).
+// Pairwise maximum of 16 values (4 dependent levels instead of 15).
 __device__ __forceinline__ float tree_max16(const float (&v)[16]) {
     float a[8];
 #pragma unroll
@@ -303,15 +308,6 @@ __device__ __forceinline__ float tree_max16(const float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) a[i] = fmaxf(a[i], a[i + 4]);
     return fmaxf(fmaxf(a[0], a[2]), fmaxf(a[1], a[3]));
-}
-
-__device__ __forceinline__ float tree_sum16(const float (&v)[16]) {
-    float a[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = v[i] + v[i + 8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = a[i] + a[i + 4];
-    return (a[0] + a[2]) + (a[1] + a[3]);
 }
 
 // Classes (0, 1 or 2) whose row is inside the output, from the two row offsets.
@@ -334,6 +330,41 @@ __device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G,
     return (od * P.Ho + oh) * P.Wo + ow;
 }
 
+// Long reductions (SEG kernels, non-merged tiles).  The tensor cores round the
+// fp32 accumulator once per MMA, and the error of a chain of such roundings grows
+// with its length relative to the accumulated value; so a tile whose K walk
+// (class 0's steps, then class 1's) exceeds seg_steps is split into nseg
+// near-equal segments, each accumulated from zero in an accumulator buffer of its
+// own, and the epilogue adds the segments' partial sums in fp32 into a running sum
+// in tensor memory (sum_col).  The MMA thread and the epilogue derive the same plan.
+struct SegPlan {
+    int n[2];  // K steps of class 0 and class 1
+    int total, nseg, len;
+};
+
+__device__ __forceinline__ SegPlan seg_plan(const TcParams &P, const GroupDesc &G, const ClassDesc *cls, int t) {
+    SegPlan sp;
+    sp.total = 0;
+#pragma unroll
+    for (int ci = 0; ci < 2; ++ci) {
+        sp.n[ci] = 0;
+        if (ci < G.ncls) {
+            const TapRange tr = tile_taps(G, cls[G.cls[ci]], t, kTcTileM, P.Din);
+            sp.n[ci] = (tr.end - tr.begin) * P.kc;
+        }
+        sp.total += sp.n[ci];
+    }
+    sp.nseg = sp.total > P.seg_steps ? (sp.total + P.seg_steps - 1) / P.seg_steps : 1;
+    sp.len = (sp.total + sp.nseg - 1) / sp.nseg;
+    return sp;
+}
+
+// Does class ci have K steps in [a, b) of the tile's walk?
+__device__ __forceinline__ bool seg_touches(const SegPlan &sp, int ci, int a, int b) {
+    const int b0 = ci == 0 ? 0 : sp.n[0];
+    return sp.n[ci] > 0 && b0 < b && b0 + sp.n[ci] > a;
+}
+
 // KEEP (softmax only): 1 = each epilogue warp keeps its exponentials in
 // registers (Cout <= 16 * kSoftmaxKeepChunks * warps per lane quarter); 2 = as
 // 1, for w-parity pairs with each warp owning one class's channels (8 warps);
@@ -345,7 +376,8 @@ __device__ __forceinline__ int row_offset(const TcParams &P, const GroupDesc &G,
 // a K step whose w offset both classes have loads the activation slice once,
 // the two classes' weight slices side by side, and issues one MMA of
 // N = 2 * Cout_pad into both accumulators (they are adjacent in tensor memory).
-template <int EPI, int KEEP, int OPS, bool MERGED>
+// SEG: long K walks are accumulated in segments (see SegPlan); split formats only.
+template <int EPI, int KEEP, int OPS, bool MERGED, bool SEG = false>
 __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const __grid_constant__ TcParams P) {
     constexpr int kPlanes = (OPS == 0 || OPS == 3) ? 2 : 1;
     constexpr int kBSlots = MERGED ? 2 : 1;  // weight slices per plane in a stage
@@ -624,14 +656,14 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++iter) {
                 const Tile T = decode(P, s_grp, tile);
                 const GroupDesc &G = s_grp[T.gi];
-                const int acc = P.nbuf == 2 ? (iter & 1) : 0;
+                int acc = P.nbuf == 2 ? (iter & 1) : 0;
                 const uint32_t aph = (uint32_t)(P.nbuf == 2 ? iter >> 1 : iter) & 1u;
                 if (!ptx::mbar_wait_bounded(tempty0 + 8 * acc, aph ^ 1u, &abort_flag, kWaitNs)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t acc_base = tmem_base + (uint32_t)acc * P.acc_stride;
+                uint32_t acc_base = tmem_base + (uint32_t)acc * P.acc_stride;
                 if constexpr (MERGED) {
                     // same walk as the producer; shared offsets come first, so a merged step
                     // never meets one accumulator initialised and the other not
@@ -646,6 +678,62 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         const uint32_t d_tmem = acc_base + (mask == 2u ? (uint32_t)P.cout_pad : 0u);
                         mma_tap(d_tmem, mask == 3u ? idesc2 : idesc, (ini & mask) == 0u);
                         ini |= mask;
+                    }
+                } else if constexpr (SEG) {
+                    // the tile's walk in segments: at each segment boundary the finished
+                    // accumulator goes to the epilogue and the next segment starts from zero
+                    // in the other buffer
+                    const SegPlan sp = seg_plan(P, G, s_cls, T.t);
+                    int k = 0, seg_end = sp.len;
+                    for (int ci = 0; ok && ci < G.ncls; ++ci) {
+                        uint32_t fresh = 1u;  // the next product overwrites class ci's columns
+                        for (int s = 0; s < sp.n[ci]; ++s, ++k) {
+                            if (k == seg_end) {
+                                ptx::mma_commit(tfull0 + 8 * acc);
+                                ++iter;
+                                acc = P.nbuf == 2 ? (iter & 1) : 0;
+                                const uint32_t ph = (uint32_t)(P.nbuf == 2 ? iter >> 1 : iter) & 1u;
+                                if (!ptx::mbar_wait_bounded(tempty0 + 8 * acc, ph ^ 1u, &abort_flag, kWaitNs)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ptx::tc_fence_after();
+                                acc_base = tmem_base + (uint32_t)acc * P.acc_stride;
+                                seg_end += sp.len;
+                                fresh = 1u;
+                            }
+                            const uint32_t d_tmem = acc_base + (uint32_t)ci * P.cout_pad;
+                            if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            const uint64_t d0 =
+                                ptx::sdesc_k_swizzled(smem_base + (uint32_t)stage * P.stage_bytes, kRowBytes);
+#pragma unroll
+                            for (int kk = 0; kk < kChunk / 8; ++kk) {  // split formats: three products
+                                const uint64_t a_hi = d0 + 2 * kk;
+                                const uint64_t a_lo = a_hi + kA16;
+                                const uint64_t b_hi = a_hi + 2 * kA16;
+                                const uint64_t b_lo = b_hi + b16;
+                                const uint32_t first = (fresh && kk == 0) ? 0u : 1u;
+                                if constexpr (OPS == 3) {
+                                    ptx::mma_bf16(d_tmem, a_hi, b_hi, idesc, first);
+                                    ptx::mma_bf16(d_tmem, a_hi, b_lo, idesc, 1u);
+                                    ptx::mma_bf16(d_tmem, a_lo, b_hi, idesc, 1u);
+                                } else {
+                                    ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, first);
+                                    ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+                                    ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                                }
+                            }
+                            fresh = 0u;
+                            ptx::mma_commit(empty0 + 8 * stage);
+                            if (++stage == P.stages) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
                     }
                 } else {
                     // flat step loop per class (the issue rate of the MMA-bound shapes depends on it)
@@ -746,6 +834,67 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         for (; tile < P.total_tiles; tile += gridDim.x, ++iter) {
             const Tile T = decode(P, s_grp, tile);
             const GroupDesc &G = s_grp[T.gi];
+            // SEG: the tile's earlier segments are added into the running sum here; a
+            // class's columns in the last segment's buffer hold its last partial sum
+            // if it has steps there (in_final), and the running sum holds the rest (has_sum)
+            bool has_sum[2] = {false, false}, in_final[2] = {true, true};
+            if constexpr (SEG) {
+                const SegPlan sp = seg_plan(P, G, s_cls, T.t);
+                bool failed = false;
+                for (int sg = 0; sg + 1 < sp.nseg; ++sg, ++iter) {
+                    const int a = P.nbuf == 2 ? (iter & 1) : 0;
+                    const uint32_t ph = (uint32_t)(P.nbuf == 2 ? iter >> 1 : iter) & 1u;
+                    if (!ptx::mbar_wait_bounded(tfull0 + 8 * a, ph, &abort_flag, kWaitNs)) {
+                        failed = true;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    __syncwarp();
+                    const int k0 = sg * sp.len;
+#pragma unroll
+                    for (int ci = 0; ci < 2; ++ci) {
+                        if (!seg_touches(sp, ci, k0, k0 + sp.len)) continue;
+                        for (int j = 0; j < nchunks; ++j) {
+                            if (!mine(j)) continue;
+                            const uint32_t col = (uint32_t)(ci * P.cout_pad + 16 * j);
+                            float v[16], t[16];
+                            ptx::tmem_ld16(lane_base + (uint32_t)a * P.acc_stride + col, v);
+                            if (has_sum[ci]) ptx::tmem_ld16(lane_base + P.sum_col + col, t);
+                            ptx::tmem_wait_ld();
+                            if (has_sum[ci]) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] += t[i];
+                            }
+                            ptx::tmem_st16(lane_base + P.sum_col + col, v);
+                        }
+                        has_sum[ci] = true;
+                    }
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(tempty0 + 8 * a);
+                }
+                if (failed) {
+                    if (lane == 0) record_error(P.status, kErrTimeout, 3);
+                    abort_flag = 1;
+                    break;
+                }
+                const int kf = (sp.nseg - 1) * sp.len;
+#pragma unroll
+                for (int ci = 0; ci < 2; ++ci) in_final[ci] = seg_touches(sp, ci, kf, sp.total);
+            }
+            // a loaded accumulator chunk of class ci at channel c0, completed with the
+            // running sum of the earlier segments (SEG kernels; nothing otherwise)
+            auto seg_fix = [&](int ci, int c0, float (&v)[16]) {
+                if constexpr (SEG) {
+                    if (has_sum[ci]) {
+                        float t[16];
+                        ptx::tmem_ld16(lane_base + P.sum_col + (uint32_t)(ci * P.cout_pad + c0), t);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = (in_final[ci] ? v[i] : 0.f) + t[i];
+                    }
+                }
+            };
             const int acc = P.nbuf == 2 ? (iter & 1) : 0;
             const uint32_t aph = (uint32_t)(P.nbuf == 2 ? iter >> 1 : iter) & 1u;
             if (!ptx::mbar_wait_bounded(tfull0 + 8 * acc, aph, &abort_flag, kWaitNs)) {
@@ -945,6 +1094,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                         for (int jj = 0; jj < kKeep; ++jj) {
                             const int j = half + jj * kHalves;
                             if (j < nchunks) {
+                                seg_fix(ci, 16 * j, raw[jj]);
                                 logits(16 * j, raw[jj], e[jj][ci]);
                                 mx[ci] = fmaxf(mx[ci], max8(e[jj][ci]));
                             }
@@ -963,6 +1113,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                             ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + 16 * j, raw[ci]);
                         ptx::tmem_wait_ld();
                         _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) {
+                            seg_fix(ci, 16 * j, raw[ci]);
                             logits(16 * j, raw[ci], e[0][ci]);
                             const float cm = fmaxf(mx[ci], max8(e[0][ci]));
                             const float old = mx[ci] == -INFINITY ? 0.f : sum[ci] * ex2_approx(mx[ci] - cm);
@@ -1058,6 +1209,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                             float raw[16];
                             ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + 16 * j, raw);
                             ptx::tmem_wait_ld();
+                            seg_fix(ci, 16 * j, raw);
                             logits(16 * j, raw, e[0][ci]);
                             exp8(e[0][ci], M[ci]);
                             finish(16 * j, off[ci], e[0][ci], A);
@@ -1077,6 +1229,9 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls)
                         ptx::tmem_ld16(lane_base + acc_col + (uint32_t)ci * P.cout_pad + c0, v[ci]);
                     ptx::tmem_wait_ld();
+                    if constexpr (SEG) {
+                        _Pragma("unroll") for (int ci = 0; ci < 2; ++ci) if (ci < G.ncls) seg_fix(ci, c0, v[ci]);
+                    }
                     if (G.ncls == 1) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[1][i] = 0.f;
@@ -1214,6 +1369,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                                     float v[16];
                                     ptx::tmem_ld16(lane_base + col + c0, v);
                                     ptx::tmem_wait_ld();
+                                    seg_fix(ci, c0, v);
 #pragma unroll
                                     for (int i = 0; i < 16; ++i) {
                                         const int ch = c0 + i;
@@ -1317,18 +1473,18 @@ void tc_cache_free(void *c) { delete static_cast<TcCache *>(c); }
 
 // The kernel instance for the plan's epilogue, operand format OPS and (for
 // softmax) register-kept exponentials; threads receives its block size.
-template <int OPS, bool MERGED>
+template <int OPS, bool MERGED, bool SEG = false>
 static void (*select_kernel(const convt3d_plan_s &p, int &threads))(const TcParams) {
     switch (p.d.epilogue) {
         case CONVT3D_EPI_IDENTITY:
             threads = EpiCfg<CONVT3D_EPI_IDENTITY>::threads;
-            return convt3d_tc_gemm<CONVT3D_EPI_IDENTITY, 1, OPS, MERGED>;
+            return convt3d_tc_gemm<CONVT3D_EPI_IDENTITY, 1, OPS, MERGED, SEG>;
         case CONVT3D_EPI_RELU_GROUPNORM:
             threads = EpiCfg<CONVT3D_EPI_RELU_GROUPNORM>::threads;
-            return convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM, 1, OPS, MERGED>;
+            return convt3d_tc_gemm<CONVT3D_EPI_RELU_GROUPNORM, 1, OPS, MERGED, SEG>;
         case CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL:
             threads = EpiCfg<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL>::threads;
-            return convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL, 1, OPS, MERGED>;
+            return convt3d_tc_gemm<CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL, 1, OPS, MERGED, SEG>;
         case CONVT3D_EPI_SOFTMAX_SIGMOID:
             threads = EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::threads;
             // registers hold the exponentials when each warp owns at most
@@ -1338,12 +1494,13 @@ static void (*select_kernel(const convt3d_plan_s &p, int &threads))(const TcPara
             // there). The split formats, whose longer K steps leave the epilogue more
             // room, take the channel split below: one (max, sum) exchange per tile
             // buys each channel's (even, odd) columns stored as one pair.
-            if ((OPS == 1 || OPS == 2) && EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps == 8 && p.g.ss[2] == 2 &&
-                p.cout_pad <= 16 * 2 * kSoftmaxKeepChunks)
-                return convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2, OPS, MERGED>;
+            if constexpr ((OPS == 1 || OPS == 2) && !SEG)
+                if (EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps == 8 && p.g.ss[2] == 2 &&
+                    p.cout_pad <= 16 * 2 * kSoftmaxKeepChunks)
+                    return convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2, OPS, MERGED, SEG>;
             return p.cout_pad <= 16 * kSoftmaxKeepChunks * (EpiCfg<CONVT3D_EPI_SOFTMAX_SIGMOID>::warps / 4)
-                       ? convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 1, OPS, MERGED>
-                       : convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 0, OPS, MERGED>;
+                       ? convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 1, OPS, MERGED, SEG>
+                       : convt3d_tc_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 0, OPS, MERGED, SEG>;
     }
     return nullptr;
 }
@@ -1421,13 +1578,45 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->nbuf = 2 * acc_cols <= 512 ? 2 : 1;
         P->acc_stride = (uint32_t)acc_cols;
         P->tmem_cols = (uint32_t)round_pow2(P->nbuf * acc_cols);
+        // Long reductions (split formats, non-merged walks, one N slice): tiles whose walk
+        // exceeds kSegSteps K steps accumulate in segments, with a running-sum region
+        // beside the accumulators (three regions where they fit, else one buffer and the sum).
+        const bool split = p.planes == 2;
+        int max_steps = 0;
+        if (split && !p.merged && p.nslices == 1)
+            for (int gi = 0; gi < p.ngroups; ++gi)
+                for (int t = 0; t < p.grp[gi].tiles; ++t) {
+                    int n = 0;
+                    for (int ci = 0; ci < p.grp[gi].ncls; ++ci) {
+                        const TapRange tr = tile_taps(p.grp[gi], g.cls[p.grp[gi].cls[ci]], t, kTcTileM, g.Din);
+                        n += (tr.end - tr.begin) * P->kc;
+                    }
+                    max_steps = n > max_steps ? n : max_steps;
+                }
+        P->seg_steps = 0;
+        P->sum_col = 0;
+        if (max_steps > kSegSteps) {
+            if (3 * acc_cols <= 512) {
+                P->nbuf = 2;
+                P->sum_col = (uint32_t)(2 * acc_cols);
+                P->tmem_cols = (uint32_t)round_pow2(3 * acc_cols);
+                P->seg_steps = kSegSteps;
+            } else if (2 * acc_cols <= 512) {
+                P->nbuf = 1;
+                P->sum_col = (uint32_t)acc_cols;
+                P->tmem_cols = (uint32_t)round_pow2(2 * acc_cols);
+                P->seg_steps = kSegSteps;
+            }
+        }
         P->b_bytes = (uint32_t)P->slice_n * kRowBytes;
         P->planes = p.planes;
         P->cl = p.cl;
         P->io16 = p.io16;
         P->stage_bytes = (uint32_t)p.planes * (kABytes + (p.merged ? 2u : 1u) * P->b_bytes);
         const int ops = p.planes == 2 ? (p.bf16 ? 3 : 0) : (p.bf16 ? 2 : 1);
-        switch (ops * 2 + (p.merged ? 1 : 0)) {
+        if (P->seg_steps > 0)  // split formats only (ops 0 or 3), never merged
+            tc.kern = ops == 3 ? select_kernel<3, false, true>(p, tc.threads) : select_kernel<0, false, true>(p, tc.threads);
+        else switch (ops * 2 + (p.merged ? 1 : 0)) {
             case 0: tc.kern = select_kernel<0, false>(p, tc.threads); break;
             case 1: tc.kern = select_kernel<0, true>(p, tc.threads); break;
             case 2: tc.kern = select_kernel<1, false>(p, tc.threads); break;
