@@ -133,6 +133,7 @@ struct GroupDesc {
 // still initialises the accumulator.
 struct TapRange {
     int begin, end;
+    int a0, a1;  // the d-slices [a0, a1] (slice 0 alone when none is live)
 };
 
 __host__ __device__ inline TapRange tile_taps(const GroupDesc &G, const ClassDesc &C, int t, int tile_m, int Din) {
@@ -154,9 +155,12 @@ __host__ __device__ inline TapRange tile_taps(const GroupDesc &G, const ClassDes
     if (a0 > a1 || C.ntaps == 0) {
         r.begin = 0;
         r.end = C.ntaps > 0 ? 1 : 0;
+        r.a0 = r.a1 = 0;
     } else {
         r.begin = a0 * nhw;
         r.end = (a1 + 1) * nhw;
+        r.a0 = a0;
+        r.a1 = a1;
     }
     return r;
 }

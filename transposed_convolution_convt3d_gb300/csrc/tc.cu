@@ -118,6 +118,7 @@ struct TcParams {
     int epilogue, groups;
     float scale;
     int ngroups, tiles_per_sample, total_tiles;
+    FastDiv div_tps;  // division by tiles_per_sample
     int stages;
     uint32_t stage_bytes, b_bytes;
     int planes;  // 2: split TF32 (A and B hi/lo), 1: single TF32 or BF16
@@ -149,7 +150,7 @@ struct Tile {
 // the shared-memory copy of the group table.
 __device__ __forceinline__ Tile decode(const TcParams &P, const GroupDesc *grp, int tile) {
     Tile r;
-    r.n = tile / P.tiles_per_sample;
+    r.n = (int)fastdiv((uint32_t)tile, P.div_tps);
     const int rem = tile - r.n * P.tiles_per_sample;
     int gi = 0;
     while (gi + 1 < P.ngroups && rem >= grp[gi + 1].tile_prefix) ++gi;
@@ -510,8 +511,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     // the tile's run of the flattened walk (d-slices: the same for both classes)
                     const ClassDesc &C0 = s_cls[G.cls[0]], &C1 = s_cls[G.cls[1]];
                     const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);
-                    const int nhw0 = C0.nt_h * C0.nt_w;
-                    const int a_begin = tr.begin / nhw0, a_end = (tr.end + nhw0 - 1) / nhw0;
+                    const int a_begin = tr.a0, a_end = tr.a1 + 1;
                     const int s_end = G.step0 + a_end * G.steps_per_a;
                     // each class's base pixel of the tile
                     const int w00 = qw0 + C0.lo_w, h00 = qh0 + C0.lo_h, d00 = qd0 + C0.lo_d;
@@ -669,8 +669,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     // never meets one accumulator initialised and the other not
                     const ClassDesc &C0 = s_cls[G.cls[0]];
                     const TapRange tr = tile_taps(G, C0, T.t, kTcTileM, P.Din);
-                    const int nhw0 = C0.nt_h * C0.nt_w;
-                    const int a_begin = tr.begin / nhw0, a_end = (tr.end + nhw0 - 1) / nhw0;
+                    const int a_begin = tr.a0, a_end = tr.a1 + 1;
                     const int s_end = G.step0 + a_end * G.steps_per_a;
                     uint32_t ini = 0;  // bit c: class c's accumulator holds a product
                     for (int st = G.step0 + a_begin * G.steps_per_a; ok && st < s_end; ++st) {
@@ -682,56 +681,58 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 } else if constexpr (SEG) {
                     // the tile's walk in segments: at each segment boundary the finished
                     // accumulator goes to the epilogue and the next segment starts from zero
-                    // in the other buffer
+                    // in the other buffer; within a segment, each class's steps run as one
+                    // flat loop like the unsegmented walk's
                     const SegPlan sp = seg_plan(P, G, s_cls, T.t);
-                    int k = 0, seg_end = sp.len;
-                    for (int ci = 0; ok && ci < G.ncls; ++ci) {
-                        uint32_t fresh = 1u;  // the next product overwrites class ci's columns
-                        for (int s = 0; s < sp.n[ci]; ++s, ++k) {
-                            if (k == seg_end) {
-                                ptx::mma_commit(tfull0 + 8 * acc);
-                                ++iter;
-                                acc = P.nbuf == 2 ? (iter & 1) : 0;
-                                const uint32_t ph = (uint32_t)(P.nbuf == 2 ? iter >> 1 : iter) & 1u;
-                                if (!ptx::mbar_wait_bounded(tempty0 + 8 * acc, ph ^ 1u, &abort_flag, kWaitNs)) {
-                                    ok = false;
-                                    break;
-                                }
-                                ptx::tc_fence_after();
-                                acc_base = tmem_base + (uint32_t)acc * P.acc_stride;
-                                seg_end += sp.len;
-                                fresh = 1u;
-                            }
-                            const uint32_t d_tmem = acc_base + (uint32_t)ci * P.cout_pad;
-                            if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
+                    for (int sg = 0; ok && sg < sp.nseg; ++sg) {
+                        if (sg > 0) {
+                            ptx::mma_commit(tfull0 + 8 * acc);
+                            ++iter;
+                            acc = P.nbuf == 2 ? (iter & 1) : 0;
+                            const uint32_t ph = (uint32_t)(P.nbuf == 2 ? iter >> 1 : iter) & 1u;
+                            if (!ptx::mbar_wait_bounded(tempty0 + 8 * acc, ph ^ 1u, &abort_flag, kWaitNs)) {
                                 ok = false;
                                 break;
                             }
                             ptx::tc_fence_after();
-                            const uint64_t d0 =
-                                ptx::sdesc_k_swizzled(smem_base + (uint32_t)stage * P.stage_bytes, kRowBytes);
-#pragma unroll
-                            for (int kk = 0; kk < kChunk / 8; ++kk) {  // split formats: three products
-                                const uint64_t a_hi = d0 + 2 * kk;
-                                const uint64_t a_lo = a_hi + kA16;
-                                const uint64_t b_hi = a_hi + 2 * kA16;
-                                const uint64_t b_lo = b_hi + b16;
-                                const uint32_t first = (fresh && kk == 0) ? 0u : 1u;
-                                if constexpr (OPS == 3) {
-                                    ptx::mma_bf16(d_tmem, a_hi, b_hi, idesc, first);
-                                    ptx::mma_bf16(d_tmem, a_hi, b_lo, idesc, 1u);
-                                    ptx::mma_bf16(d_tmem, a_lo, b_hi, idesc, 1u);
-                                } else {
-                                    ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, first);
-                                    ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
-                                    ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                            acc_base = tmem_base + (uint32_t)acc * P.acc_stride;
+                        }
+                        const int k0 = sg * sp.len, k1 = min(k0 + sp.len, sp.total);
+                        for (int ci = 0; ok && ci < G.ncls; ++ci) {
+                            const int b0 = ci == 0 ? 0 : sp.n[0];
+                            const int s0 = max(k0, b0) - b0, s1 = min(k1, b0 + sp.n[ci]) - b0;
+                            const uint32_t d_tmem = acc_base + (uint32_t)ci * P.cout_pad;
+                            for (int s = s0; s < s1; ++s) {
+                                if (!ptx::mbar_wait_bounded(full0 + 8 * stage, phase, &abort_flag, kWaitNs)) {
+                                    ok = false;
+                                    break;
                                 }
-                            }
-                            fresh = 0u;
-                            ptx::mma_commit(empty0 + 8 * stage);
-                            if (++stage == P.stages) {
-                                stage = 0;
-                                phase ^= 1u;
+                                ptx::tc_fence_after();
+                                const uint64_t d0 =
+                                    ptx::sdesc_k_swizzled(smem_base + (uint32_t)stage * P.stage_bytes, kRowBytes);
+#pragma unroll
+                                for (int kk = 0; kk < kChunk / 8; ++kk) {  // split formats: three products
+                                    const uint64_t a_hi = d0 + 2 * kk;
+                                    const uint64_t a_lo = a_hi + kA16;
+                                    const uint64_t b_hi = a_hi + 2 * kA16;
+                                    const uint64_t b_lo = b_hi + b16;
+                                    // the segment's first product of the class overwrites
+                                    const uint32_t first = ((s - s0) | kk) ? 1u : 0u;
+                                    if constexpr (OPS == 3) {
+                                        ptx::mma_bf16(d_tmem, a_hi, b_hi, idesc, first);
+                                        ptx::mma_bf16(d_tmem, a_hi, b_lo, idesc, 1u);
+                                        ptx::mma_bf16(d_tmem, a_lo, b_hi, idesc, 1u);
+                                    } else {
+                                        ptx::mma_tf32(d_tmem, a_hi, b_hi, idesc, first);
+                                        ptx::mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+                                        ptx::mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                                    }
+                                }
+                                ptx::mma_commit(empty0 + 8 * stage);
+                                if (++stage == P.stages) {
+                                    stage = 0;
+                                    phase ^= 1u;
+                                }
                             }
                         }
                     }
@@ -1534,6 +1535,7 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         P->scale = p.d.scale;
         P->ngroups = p.ngroups;
         P->tiles_per_sample = p.tiles_per_sample;
+        P->div_tps = make_fastdiv((uint32_t)p.tiles_per_sample);
         P->total_tiles = (int)p.tiles;
         int ncls_max = 1;
         for (int i = 0; i < p.ngroups; ++i) {
@@ -1582,8 +1584,11 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         // exceeds kSegSteps K steps accumulate in segments, with a running-sum region
         // beside the accumulators (three regions where they fit, else one buffer and the sum).
         const bool split = p.planes == 2;
+        // BatchNorm+pool is left whole: the accumulation error is close to a common
+        // relative factor, which the batch statistics' (z - mean) / sd cancels, and the
+        // pooled mean averages the rest (it meets the bar at K = 8,000 unsegmented)
         int max_steps = 0;
-        if (split && !p.merged && p.nslices == 1)
+        if (split && !p.merged && p.nslices == 1 && p.d.epilogue != CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL)
             for (int gi = 0; gi < p.ngroups; ++gi)
                 for (int t = 0; t < p.grp[gi].tiles; ++t) {
                     int n = 0;
