@@ -187,10 +187,10 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 // GPU's fp64 rate is a small fraction of its fp32 rate): M2 = sum s2 - (sum s1)^2 / n
 // needs no more, and only S = n c + sum s1, whose terms differ in magnitude, is
 // formed in fp64 (one fused multiply-add on one lane).
-__device__ __forceinline__ void warp_moments(float s1, float s2, int cnt, float c, double *out) {
+__device__ __forceinline__ void warp_moments(float s1, float s2, int n, float c, double *out) {
+    // n: the warp's value count (the same in every lane)
     const float t1 = warp_sum_f(s1);
     const float t2 = warp_sum_f(s2);
-    const int n = warp_sum_i(cnt);
     if ((threadIdx.x & 31) == 0) {
         out[0] = (double)n;
         out[1] = fma((double)n, (double)c, (double)t1);
@@ -827,6 +827,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         const int nstat = gn ? 3 * P.groups : (bn ? 3 * C : 0);  // (n, S, M2) per group / channel
         const int cpg = gn ? C / P.groups : 16;
         const bool gn_inline = gn && (cpg % 16 == 0);  // groups made of whole 16-channel chunks
+        const bool has_bias = P.bias != nullptr;
         auto mine = [&](int j) -> bool {                // does this warp own chunk j?
             return gn_inline ? ((16 * j) / cpg) % kHalves == half : j % kHalves == half;
         };
@@ -1222,7 +1223,13 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                 // identity / relu+groupnorm store / batchnorm partial sums, per owned chunk
                 // running group sums about the shift gc (groups of whole chunks)
                 float gs1 = 0.f, gs2 = 0.f, gc = 0.f;
-                int gcnt = 0;
+                // the warp's (row, class) pairs inside the output, and the lane whose row
+                // supplies a group's shift (the first valid row of class 0, else of class 1)
+                const unsigned vb0 = __ballot_sync(0xffffffffu, off[0] >= 0);
+                const unsigned vb1 = __ballot_sync(0xffffffffu, off[1] >= 0);
+                const int rows_valid = __popc(vb0) + __popc(vb1);
+                const bool rows_valid0 = vb0 != 0u;
+                const int shift_lane = vb0 ? __ffs(vb0) - 1 : (vb1 ? __ffs(vb1) - 1 : 0);
                 for (int j = 0; j < nchunks; ++j) {
                     if (!mine(j)) continue;
                     const int c0 = 16 * j;
@@ -1244,12 +1251,15 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float b = s_bias[c0 + i];
-                        if (gn) {
+                        if (gn && has_bias) {
                             const float t0 = v[0][i] + b, t1 = v[1][i] + b;
                             r[0][i] = t0 > 0.f ? v[0][i] : -b;
                             r[1][i] = t1 > 0.f ? v[1][i] : -b;
                             v[0][i] = fmaxf(t0, 0.f);
                             v[1][i] = fmaxf(t1, 0.f);
+                        } else if (gn) {  // no bias: r = v
+                            v[0][i] = fmaxf(v[0][i], 0.f);
+                            v[1][i] = fmaxf(v[1][i], 0.f);
                         } else {
                             v[0][i] += b;
                             v[1][i] += b;
@@ -1298,16 +1308,12 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     }
                     if (gn_inline) {
                         const float m0 = off[0] >= 0 ? 1.f : 0.f, m1 = off[1] >= 0 ? 1.f : 0.f;
-                        const int nval = 16 * ((off[0] >= 0 ? 1 : 0) + (off[1] >= 0 ? 1 : 0));
-                        if (c0 % cpg == 0) {  // first chunk of a group: its warp mean is the group's shift
-                            float sc = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) sc += m0 * v[0][i] + m1 * v[1][i];
-                            sc = warp_sum_f(sc);
-                            const int nc = warp_sum_i(nval);
-                            gc = nc > 0 ? sc / (float)nc : 0.f;
+                        if (c0 % cpg == 0) {
+                            // first chunk of a group: one of its values (the first valid row's
+                            // first channel) is the group's shift, |v - shift| ~ the group's spread
+                            const float mine_v = rows_valid0 ? v[0][0] : v[1][0];
+                            gc = rows_valid ? __shfl_sync(0xffffffffu, mine_v, shift_lane) : 0.f;
                             gs1 = gs2 = 0.f;
-                            gcnt = 0;
                         }
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -1315,11 +1321,10 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                             gs1 += a + b;
                             gs2 += a * a + b * b;
                         }
-                        gcnt += nval;
                         if ((c0 + 16) % cpg == 0)  // this chunk closes group g (same for all lanes)
-                            warp_moments(gs1, gs2, gcnt, gc, part + 3 * (c0 / cpg));
+                            warp_moments(gs1, gs2, rows_valid * cpg, gc, part + 3 * (c0 / cpg));
                     }
-                    if (gn) {
+                    if (gn && has_bias) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             v[0][i] = r[0][i];
@@ -1388,7 +1393,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                                 s1 = s2 = 0.f;
                             }
                         }
-                        warp_moments(s1, s2, cnt, c, part + 3 * g);
+                        warp_moments(s1, s2, warp_sum_i(cnt), c, part + 3 * g);
                     }
                 }
             }
