@@ -170,12 +170,16 @@ typedef struct {
     double issued_mma_flop;      /* tensor/FMA flop the main kernel issues per forward   */
     double gemm_min_bytes;       /* algorithmic HBM bytes of the main kernel             */
     double forward_min_bytes;    /* algorithmic HBM bytes of the whole forward           */
+    int main_kernel;             /* 0: tensor-core GEMM, 1: FFMA kernel (requested, or the
+                                    fallback for shapes the tensor-core loads cannot
+                                    address: TMA im2col corners beyond [-16, 15])       */
 } convt3d_info_t;
 
 /* Validate `desc` and build a plan (host only: no CUDA call, no GPU needed).
  * Returns INVALID_ARG for malformed descriptions, UNSUPPORTED for valid ones
- * this build does not run (for example 3XTF32 with Cout > 256).  *out is set
- * to NULL on failure. */
+ * this build does not run (for example Cout > 512).  A tensor-core precision
+ * whose loads cannot address the shape runs on the FFMA kernel instead
+ * (convt3d_info_t.main_kernel).  *out is set to NULL on failure. */
 convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t *out);
 
 /* Release a plan (NULL is ignored). */

@@ -99,6 +99,18 @@ def test_eval_batchnorm_box_planes_follow_distinct_d_intervals(lib):
     assert st == 2 and not h.value
 
 
+def test_tensor_core_unaddressable_shape_runs_on_ffma(lib):
+    """A dilation of 5 with k = 7 puts the TMA im2col corners at -30 (beyond [-16, 15]):
+    the plan keeps the requested tensor-core precision but runs the FFMA kernel; with
+    16-bit tensors (which the FFMA kernel does not take) the shape is unsupported."""
+    from transposed_convolution_convt3d_gb300 import Plan
+    pl = Plan(1, 8, 16, 2, 3, 3, (7, 3, 3), dilation=(5, 1, 1), precision=0)
+    assert pl.info["main_kernel"] == 1
+    assert Plan(1, 8, 16, 2, 3, 3, 3).info["main_kernel"] == 0
+    st, h = create(lib, per_dim=1, kdims=(7, 3, 3), strides=(1, 1, 1), dilation=(5, 1, 1), precision=3, io_bf16=1)
+    assert st == 2 and not h.value
+
+
 @pytest.mark.parametrize("precision", [0, 1, 4])
 @pytest.mark.parametrize("kw", [dict(stride=2, k=3, pad=1, Cout=144), dict(Cout=384), dict(Cout=512, epilogue=3),
                                 dict(stride=2, k=4, pad=1, Cout=512, epilogue=2)])

@@ -265,6 +265,17 @@ def test_general_shapes(spec, precision):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("precision", PRECISIONS)
+def test_unaddressable_shape_falls_back_to_ffma(precision):
+    """Dilation 5 with k = 7 along d: beyond the TMA im2col corner range, so the
+    tensor-core precisions run the FFMA kernel (same 1e-4 bar)."""
+    spec = E.Spec("fallback_dil5_k7", N=1, Cin=8, Cout=16, D=2, H=3, W=3, k=(7, 3, 3), dilation=(5, 1, 1),
+                  pad=(2, 1, 0), bias=True, epilogue=E.EPI_RELU_GROUPNORM, groups=4, seed_index=47)
+    inputs = E.make_inputs(spec)
+    assert_close(run_gpu(spec, inputs, precision), run_oracle(spec, inputs), spec.name)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("precision", PRECISIONS)
 def test_general_shapes_eval_batchnorm(precision):
     spec = E.Spec("gen_eval_bn", N=2, Cin=12, Cout=20, D=4, H=5, W=6, k=(3, 2, 4), stride=(2, 1, 2),
                   pad=(1, 0, 2), out_pad=(1, 0, 0), dilation=(1, 2, 1), bias=True, conv_groups=2,

@@ -66,6 +66,7 @@ class Info(ctypes.Structure):
         ("tile_m", ctypes.c_int), ("launches_per_forward", ctypes.c_int), ("launches_per_pack", ctypes.c_int),
         ("useful_flop", ctypes.c_double), ("issued_mma_flop", ctypes.c_double),
         ("gemm_min_bytes", ctypes.c_double), ("forward_min_bytes", ctypes.c_double),
+        ("main_kernel", ctypes.c_int),
     ]
 
 

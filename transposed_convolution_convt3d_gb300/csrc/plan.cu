@@ -332,35 +332,45 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
         delete p;
         return fail(CONVT3D_ERR_UNSUPPORTED, "tap table overflow");
     }
-    p->tc = desc->precision != CONVT3D_PREC_FFMA;
-    const bool split = desc->precision == CONVT3D_PREC_3XTF32 || desc->precision == CONVT3D_PREC_3XBF16;
-    p->planes = split ? 2 : (p->tc ? 1 : 0);
-    p->cl = desc->channels_last != 0;
-    p->io16 = desc->io_bf16 ? kBF16 : (desc->io_fp16 ? kF16 : kF32);
-    p->half = desc->precision == CONVT3D_PREC_FP16;
-    p->bf16 = desc->precision == CONVT3D_PREC_BF16 || desc->precision == CONVT3D_PREC_3XBF16 || p->half;
-    p->elem_bytes = p->bf16 ? 2 : 4;
-    p->chunk = p->tc ? kTcRowBytes / p->elem_bytes : 8;
-    p->tile_m = p->tc ? kTcTileM : kFfmaTileM;
-    p->cin_pad = round_up(desc->Cin, p->chunk);
-    p->cout_pad = round_up(desc->Cout, 16);
-    p->nslices = 1;
-    if (!p->tc) {  // the FFMA kernel's register tiles need a power-of-two channel count
-        while (p->cout_pad & (p->cout_pad - 1)) p->cout_pad += 16;
-    } else if (p->cout_pad > kTcMaxSliceN) {
-        // one MMA (and one TMA weight box) spans at most 256 columns: equal slices of
-        // a multiple of 16 columns, walked one after another over the tile's K steps
-        p->nslices = (p->cout_pad + kTcMaxSliceN - 1) / kTcMaxSliceN;
-        p->cout_pad = round_up(desc->Cout, 16 * p->nslices);
-    }
-    build_groups(*p);
-    // Pairs merge where the combined MMA fits (N = 2 * Cout_pad <= 128): there the
-    // instruction count, not the tensor pipe, bounds the main loop.
-    p->merged = p->tc && p->g.ss[2] == 2 && p->cout_pad <= 64;
+    // The main kernel's configuration: tensor cores (tc) or the FFMA kernel.
+    auto configure = [&](bool tc) {
+        p->tc = tc;
+        const bool split = desc->precision == CONVT3D_PREC_3XTF32 || desc->precision == CONVT3D_PREC_3XBF16;
+        p->planes = tc ? (split ? 2 : 1) : 0;
+        p->cl = desc->channels_last != 0;
+        p->io16 = desc->io_bf16 ? kBF16 : (desc->io_fp16 ? kF16 : kF32);
+        p->half = tc && desc->precision == CONVT3D_PREC_FP16;
+        p->bf16 = tc && (desc->precision == CONVT3D_PREC_BF16 || desc->precision == CONVT3D_PREC_3XBF16 || p->half);
+        p->elem_bytes = p->bf16 ? 2 : 4;
+        p->chunk = tc ? kTcRowBytes / p->elem_bytes : 8;
+        p->tile_m = tc ? kTcTileM : kFfmaTileM;
+        p->cin_pad = round_up(desc->Cin, p->chunk);
+        p->cout_pad = round_up(desc->Cout, 16);
+        p->nslices = 1;
+        if (!tc) {  // the FFMA kernel's register tiles need a power-of-two channel count
+            while (p->cout_pad & (p->cout_pad - 1)) p->cout_pad += 16;
+        } else if (p->cout_pad > kTcMaxSliceN) {
+            // one MMA (and one TMA weight box) spans at most 256 columns: equal slices of
+            // a multiple of 16 columns, walked one after another over the tile's K steps
+            p->nslices = (p->cout_pad + kTcMaxSliceN - 1) / kTcMaxSliceN;
+            p->cout_pad = round_up(desc->Cout, 16 * p->nslices);
+        }
+        // Pairs merge where the combined MMA fits (N = 2 * Cout_pad <= 128): there the
+        // instruction count, not the tensor pipe, bounds the main loop.
+        p->merged = tc && p->g.ss[2] == 2 && p->cout_pad <= 64;
+        build_groups(*p);
+    };
+    configure(desc->precision != CONVT3D_PREC_FFMA);
     const bool eval_bn = desc->epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
     if (p->tc && !eval_bn && !im2col_corners_ok(*p)) {
-        delete p;
-        return fail(CONVT3D_ERR_UNSUPPORTED, "shape outside the TMA im2col corner range");
+        // The tensor-core loads cannot address this shape (TMA im2col corners beyond
+        // [-16, 15]): the FFMA kernel runs it instead, in fp32, at least as accurate as any
+        // tensor-core precision; it has no 16-bit tensors at the boundary.
+        if (desc->io_bf16 || desc->io_fp16) {
+            delete p;
+            return fail(CONVT3D_ERR_UNSUPPORTED, "shape outside the TMA im2col corner range (16-bit tensors)");
+        }
+        configure(false);
     }
     if (eval_bn && bn_eval_smem_bytes(*p) > 200 * 1024) {
         delete p;
@@ -453,6 +463,7 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
     for (int c = 0; c < g.nclasses; ++c) ktot += (int64_t)d.Cin * g.cls[c].ntaps;
     info->gemm_k_total = ktot;
     info->tiles = p->tiles;
+    info->main_kernel = p->tc ? 0 : 1;
     info->tile_m = p->tile_m;
     const bool gn = d.epilogue == CONVT3D_EPI_RELU_GROUPNORM;
     const bool bn = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
