@@ -99,6 +99,22 @@ def test_eval_batchnorm_box_planes_follow_distinct_d_intervals(lib):
     assert st == 2 and not h.value
 
 
+def test_check_null_workspace_reads_the_builtin_one(lib):
+    """convt3d_check with a NULL workspace reads the status word of the built-in
+    workspace of convt3d_forward_static_workspace on the current device; without a
+    GPU the device lookup fails and the call reports a CUDA error (it does not
+    treat NULL as an invalid argument any more, and it does not crash)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("checks the no-device path")
+    st, h = create(lib)
+    assert st == 0
+    assert lib.convt3d_check(h, None, None) == 4
+    assert lib.convt3d_last_error()
+    assert lib.convt3d_check(None, None, None) == 1
+    lib.convt3d_plan_destroy(h)
+
+
 def test_tensor_core_unaddressable_shape_runs_on_ffma(lib):
     """A dilation of 5 with k = 7 puts the TMA im2col corners at -30 (beyond [-16, 15]):
     the plan keeps the requested tensor-core precision but runs the FFMA kernel; with
