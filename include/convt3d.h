@@ -170,9 +170,14 @@ typedef struct {
     double issued_mma_flop;      /* tensor/FMA flop the main kernel issues per forward   */
     double gemm_min_bytes;       /* algorithmic HBM bytes of the main kernel             */
     double forward_min_bytes;    /* algorithmic HBM bytes of the whole forward           */
-    int main_kernel;             /* 0: tensor-core GEMM, 1: FFMA kernel (requested, or the
-                                    fallback for shapes the tensor-core loads cannot
-                                    address: TMA im2col corners beyond [-16, 15])       */
+    int main_kernel;             /* 0: tensor-core GEMM on the staged channels-last copy
+                                    of x; 1: FFMA kernel (requested, or the fallback for
+                                    shapes the tensor-core loads cannot address: TMA
+                                    im2col corners beyond [-16, 15]); 2: tensor-core GEMM
+                                    reading NCDHW fp32 x itself, no staging pass (stride
+                                    2 along w, Cin <= 32, Cout <= 64, BF16 or 3XBF16,
+                                    identity or softmax+sigmoid, q-grid rows of 8..128
+                                    positions dividing 128)                            */
 } convt3d_info_t;
 
 /* Validate `desc` and build a plan (host only: no CUDA call, no GPU needed).

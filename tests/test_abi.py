@@ -127,6 +127,28 @@ def test_tensor_core_unaddressable_shape_runs_on_ffma(lib):
     assert st == 2 and not h.value
 
 
+def test_direct_input_kernel_selection():
+    """The softmax workload's shape (stride 2, Cin 32, Cout 64, 32-wide q-rows) runs the
+    kernel that reads NCDHW x itself when the operands are bf16 (split or single), and
+    then needs no staged copy of x in the workspace; split TF32 keeps the staged kernel,
+    and so do shapes outside the direct kernel's range (Cin > 32, q-rows of 12)."""
+    import workloads as E
+    from transposed_convolution_convt3d_gb300 import PREC_3XBF16, PREC_3XTF32, PREC_BF16, Plan
+    spec = E.SOFTMAX
+    direct = Plan.from_spec(spec, precision=PREC_3XBF16)
+    staged = Plan.from_spec(spec, precision=PREC_3XTF32)
+    assert direct.info["main_kernel"] == 2 and Plan.from_spec(spec, precision=PREC_BF16).info["main_kernel"] == 2
+    assert staged.info["main_kernel"] == 0
+    # the staged kernel's workspace holds two bf16 planes of x (channels padded to 64); the direct one's does not
+    staged_cl = Plan.from_spec(spec.replace(channels_last=True), precision=PREC_3XBF16)
+    assert staged_cl.info["main_kernel"] == 0
+    x_planes = 2 * 2 * spec.N * 64 * spec.D * spec.H * spec.W
+    assert staged_cl.workspace_bytes - direct.workspace_bytes >= x_planes
+    assert direct.info["launches_per_forward"] == 1
+    assert Plan.from_spec(spec.replace(Cin=40), precision=PREC_3XBF16).info["main_kernel"] == 0
+    assert Plan.from_spec(spec.replace(W=12), precision=PREC_3XBF16).info["main_kernel"] == 0
+
+
 @pytest.mark.parametrize("precision", [0, 1, 4])
 @pytest.mark.parametrize("kw", [dict(stride=2, k=3, pad=1, Cout=144), dict(Cout=384), dict(Cout=512, epilogue=3),
                                 dict(stride=2, k=4, pad=1, Cout=512, epilogue=2)])

@@ -3,7 +3,7 @@
 odd minimax-style fit of sigmoid - 1/2 on [0, 1] written into the kernel source.
 
 Pins, all against the exact logistic function (numpy exp in fp64), not against
-the fit itself: the constants parsed from the kernel source, evaluated with the
+the fit itself: the constants parsed from the kernels' shared header, evaluated with the
 kernel's fp32 operation order, stay within 2e-7 of sigmoid on a dense grid of
 (0, 1], also with the coefficients pre-scaled by powers of f as the kernel
 does; the leading coefficient is sigmoid'(0) = 1/4 to fit accuracy; and the
@@ -15,7 +15,7 @@ import re
 import numpy as np
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                   "transposed_convolution_convt3d_gb300", "csrc", "tc.cu")
+                   "transposed_convolution_convt3d_gb300", "csrc", "epimath.cuh")
 
 
 def kernel_constants():

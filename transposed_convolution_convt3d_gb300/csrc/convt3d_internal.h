@@ -200,6 +200,7 @@ struct convt3d_plan_s {
     convt3d_desc_t d;
     convt3d::Geometry g;
     int tc;                 // 1: tensor-core path, 0: FFMA
+    int direct;             // tensor-core path reading NCDHW fp32 x directly (no staged copy; direct.cu)
     int planes;             // tensor-core operand planes: 2 = split TF32 (hi, lo), 1 = TF32 or BF16
     int cl;                 // channels-last x and y (NDHWC)
     int io16;               // x, w and y are 16-bit arrays: kBF16 or kF16 (0: fp32)
@@ -227,6 +228,7 @@ struct convt3d_plan_s {
     int ev_created;
     const void *packed_ws;  // workspace that pack_weights last filled for this plan
     void *tc_cache;         // tensor-core launch state (tc.cu)
+    void *direct_cache;     // direct-input tensor-core launch state (direct.cu)
     float *run_mean;        // BatchNorm running statistics (device, Cout each) or NULL
     float *run_var;
     float momentum;
@@ -259,6 +261,10 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
 size_t bn_eval_smem_bytes(const convt3d_plan_s &p);
 int bn_eval_ksplits(int ntaps, int Cin);
 void tc_cache_free(void *cache);
+cudaError_t launch_direct(convt3d_plan_s &p, const float *x, const void *w_hi, const void *w_lo, const float *bias,
+                          float *y, uint32_t *status, cudaStream_t s);
+bool direct_supported(const convt3d_plan_s &p);
+void direct_cache_free(void *cache);
 void *static_workspace_address();
 void report_error(const char *fmt, ...);
 }  // namespace convt3d

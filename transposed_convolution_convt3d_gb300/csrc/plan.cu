@@ -362,7 +362,10 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     };
     configure(desc->precision != CONVT3D_PREC_FFMA);
     const bool eval_bn = desc->epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
-    if (p->tc && !eval_bn && !im2col_corners_ok(*p)) {
+    // Few input channels, stride 2 along w, NCDHW fp32 tensors, bf16 operands: the
+    // kernel that reads x itself (per-slice TMA slabs, operands split on chip).
+    p->direct = p->tc && !eval_bn && direct_supported(*p);
+    if (p->tc && !p->direct && !eval_bn && !im2col_corners_ok(*p)) {
         // The tensor-core loads cannot address this shape (TMA im2col corners beyond
         // [-16, 15]): the FFMA kernel runs it instead, in fp32, at least as accurate as any
         // tensor-core precision; it has no 16-bit tensors at the boundary.
@@ -385,7 +388,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
     p->off_wpk_lo = off;
     if (p->planes == 2) off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
-    p->xs_elems = (p->tc && !eval_bn) ? (size_t)desc->N * desc->Din * desc->Hin * desc->Win * p->cin_pad : 0;
+    p->xs_elems = (p->tc && !eval_bn && !p->direct) ? (size_t)desc->N * desc->Din * desc->Hin * desc->Win * p->cin_pad : 0;
     p->off_xs_hi = off;
     off = align_up(off + p->xs_elems * p->elem_bytes, 256);
     p->off_xs_lo = off;
@@ -429,6 +432,7 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
 void convt3d_plan_destroy(convt3d_plan_t p) {
     if (!p) return;
     if (p->tc_cache) tc_cache_free(p->tc_cache);
+    if (p->direct_cache) direct_cache_free(p->direct_cache);
     if (p->ev_created) {
         cudaEventDestroy(p->ev0);
         cudaEventDestroy(p->ev1);
@@ -463,12 +467,12 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
     for (int c = 0; c < g.nclasses; ++c) ktot += (int64_t)d.Cin * g.cls[c].ntaps;
     info->gemm_k_total = ktot;
     info->tiles = p->tiles;
-    info->main_kernel = p->tc ? 0 : 1;
+    info->main_kernel = p->direct ? 2 : (p->tc ? 0 : 1);
     info->tile_m = p->tile_m;
     const bool gn = d.epilogue == CONVT3D_EPI_RELU_GROUPNORM;
     const bool bn = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
     const bool ev = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
-    info->launches_per_forward = ev ? 2 : (p->tc ? 2 : 1) + (gn ? 2 : 0) + (bn ? 2 : 0);
+    info->launches_per_forward = ev ? 2 : (p->tc && !p->direct ? 2 : 1) + (gn ? 2 : 0) + (bn ? 2 : 0);
     info->launches_per_pack = 1;
     info->useful_flop = 2.0 * d.N * d.Cout * (double)(d.Cin / g.G) * g.kvol * d.Din * d.Hin * d.Win;
     // Issued: every tile runs its class(es)' taps over tile_m rows and cout_pad columns -- the
@@ -495,10 +499,10 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
     const double wbytes = 4.0 * d.Cin * (d.Cout / g.G) * (double)g.kvol;
     const double ybytes = 4.0 * d.N * d.Cout * (double)g.Do * g.Ho * g.Wo;
     const double out_bytes = (bn || ev) ? 4.0 * d.N * d.Cout : ybytes;
-    // Main kernel: reads x (tensor-core path: the staged hi+lo copy) and the packed weights once,
+    // Main kernel: reads x (tensor-core path: the staged hi+lo copy; the direct kernel: x itself) and the packed weights once,
     // writes the output once (BN+pool: nothing but partials).
     const double planes = (p->planes == 2 ? 2.0 : 1.0) * p->elem_bytes / 4.0;  // staged operand bytes / fp32 bytes
-    info->gemm_min_bytes = planes * xbytes + planes * wbytes + (bn ? 0.0 : ybytes);
+    info->gemm_min_bytes = (p->direct ? xbytes : planes * xbytes) + planes * wbytes + (bn ? 0.0 : ybytes);
     // Whole forward as the pages define it: x and w in, the output out, plus the second pass
     // over y that GroupNorm's global statistics force.
     info->forward_min_bytes = xbytes + wbytes + out_bytes + (gn ? 2.0 * ybytes : 0.0);
@@ -585,7 +589,12 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *
             p->ev_created = 1;
         }
     }
-    if (p->tc) {
+    if (p->direct) {
+        const bool two = p->planes == 2;
+        if (p->prof_enabled && (e = cudaEventRecord(p->ev0, s)) != cudaSuccess) return cuda_fail(e, "event");
+        e = launch_direct(*p, x, base + p->off_wpk_hi, two ? base + p->off_wpk_lo : nullptr, b, y, (uint32_t *)base, s);
+        if (e != cudaSuccess) return cuda_fail(e, "direct tensor-core GEMM launch");
+    } else if (p->tc) {
         const bool two = p->planes == 2;
         float *xs_hi = (float *)(base + p->off_xs_hi), *xs_lo = two ? (float *)(base + p->off_xs_lo) : nullptr;
         e = launch_stage_input(*p, x, xs_hi, xs_lo, s);
