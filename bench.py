@@ -149,23 +149,27 @@ class ClockSampler:
 
 # ------------------------------------------------------- traffic from ncu ----
 
-def kernel_source_sha(precision):
+# main kernel of a plan (convt3d_info_t.main_kernel) -> its name and source file
+MAIN_KERNELS = {0: ("convt3d_tc_gemm", "tc.cu"), 1: ("ffma_conv_kernel", "ffma.cu"), 2: ("convt3d_direct_gemm", "direct.cu")}
+
+
+def kernel_source_sha(main_kernel):
     """Fingerprint of the main kernel's sources: its .cu file plus the shared headers."""
     csrc = os.path.join(ROOT, "transposed_convolution_convt3d_gb300", "csrc")
     h = hashlib.sha256()
-    for src in ("ffma.cu" if precision == "ffma" else "tc.cu", "ptx.cuh", "convt3d_internal.h"):
+    for src in (MAIN_KERNELS[main_kernel][1], "epimath.cuh", "ptx.cuh", "convt3d_internal.h"):
         with open(os.path.join(csrc, src), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def committed_profile_value(precision, workload, field):
+def committed_profile_value(precision, workload, field, main_kernel):
     """A number (`field = value`) from the committed ncu summary of the main
     kernel, if that summary was taken on the current kernel source (else None)."""
     d = os.path.join(ROOT, "profiles")
     if not os.path.isdir(d):
         return None
-    want = kernel_source_sha(precision)
+    want = kernel_source_sha(main_kernel)
     for name in sorted(os.listdir(d)):
         if not name.endswith((".md", ".txt")):
             continue
@@ -180,16 +184,16 @@ def committed_profile_value(precision, workload, field):
     return None
 
 
-def committed_traffic(precision, workload):
+def committed_traffic(precision, workload, main_kernel):
     """DRAM bytes per launch of the main kernel (ncu dram__bytes_read.sum +
     dram__bytes_write.sum) from the committed summary, else None."""
-    return committed_profile_value(precision, workload, "traffic_bytes_per_launch")
+    return committed_profile_value(precision, workload, "traffic_bytes_per_launch", main_kernel)
 
 
-def committed_tensor_active(precision, workload):
+def committed_tensor_active(precision, workload, main_kernel):
     """ncu's sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of the
     main kernel from the committed summary, else None."""
-    v = committed_profile_value(precision, workload, "tensor_pipe_active")
+    v = committed_profile_value(precision, workload, "tensor_pipe_active", main_kernel)
     return None if v is None else (v / 100.0 if v > 1.0 else v)
 
 
@@ -305,6 +309,17 @@ def roofline(info, precision, useful, kernel_ms, ms_per_step, pk, eval_bn):
                 "issued_frac": info["issued_mma_flop"] / (kernel_ms * 1e-3) / 1e12 / peak}
         if precision in ("3xtf32", "3xbf16"):
             roof["frac_of_" + precision + "_peak"] = achieved / (peak / 3.0)
+        # Where the kernel's arithmetic intensity (useful flop per algorithmic byte) times the
+        # measured HBM bandwidth is below its useful-flop ceiling (a third of the tensor peak
+        # for the split formats), HBM bounds it (the softmax workload): report that roofline.
+        ceiling = peak / 3.0 if precision in ("3xtf32", "3xbf16") else peak
+        ai = useful / info["gemm_min_bytes"]
+        if ai * pk["hbm_gbs"] * 1e9 < ceiling * 1e12:
+            gbs = info["gemm_min_bytes"] / (kernel_ms * 1e-3) / 1e9
+            tensor = {k: roof[k] for k in ("achieved", "peak", "unit", "frac", "peak_source")}
+            roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                    "peak_source": f"{pk['source']} HBM copy bandwidth", "algorithmic_bytes": info["gemm_min_bytes"],
+                    "tensor": tensor, "issued_frac": roof["issued_frac"]}
     else:
         peak = SMS * FP32_FMA_PER_CLK_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
         achieved = useful / (kernel_ms * 1e-3) / 1e12
@@ -312,7 +327,7 @@ def roofline(info, precision, useful, kernel_ms, ms_per_step, pk, eval_bn):
                 "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 flop x max SM clock",
                 "issued_frac": info["issued_mma_flop"] / (kernel_ms * 1e-3) / 1e12 / peak}
     roof["kernel"] = ("boxsum_kernel + bn_eval_out_kernel" if eval_bn else
-                      "ffma_conv_kernel" if precision == "ffma" else "convt3d_tc_gemm")
+                      MAIN_KERNELS[info["main_kernel"]][0])
     roof["kernel_ms"] = kernel_ms
     roof["kernel_share_of_step"] = kernel_ms / ms_per_step
     roof["min_bytes"] = info["gemm_min_bytes"]
@@ -378,7 +393,7 @@ def time_config(spec, precision, steps, warmup, dev, stream, flush, pk):
     for k in ("issued_frac", "frac_of_3xtf32_peak", "frac_of_3xbf16_peak"):
         if k in roof:
             out[k] = roof[k]
-    out["tensor_pipe_active"] = None if eval_bn else committed_tensor_active(precision, spec.name)
+    out["tensor_pipe_active"] = None if eval_bn else committed_tensor_active(precision, spec.name, info["main_kernel"])
     del ws, y, d
     torch.cuda.synchronize()
     return out
@@ -516,10 +531,10 @@ def run_gpu(args, spec):
     pk = peaks()
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
     roof = roofline(info, args.precision, useful, gemm_avg, ms_per_step, pk, eval_bn)
-    roof["traffic"] = committed_traffic(args.precision, spec.name)
+    roof["traffic"] = committed_traffic(args.precision, spec.name, info["main_kernel"])
     hbm_frac = info["forward_min_bytes"] / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"]
 
-    roof["tensor_pipe_active"] = None if eval_bn else committed_tensor_active(args.precision, spec.name)
+    roof["tensor_pipe_active"] = None if eval_bn else committed_tensor_active(args.precision, spec.name, info["main_kernel"])
 
     # the other configurations, GPU-only, same process
     configs = None

@@ -45,7 +45,7 @@ namespace convt3d {
 namespace {
 
 constexpr int kDirGroups = 4;          // (d, h) parity pairs of a stride-2 problem
-constexpr int kDirMaxSteps = 256;      // merged K steps of all pairs
+constexpr int kDirMaxSteps = 128;      // merged K steps of all pairs
 constexpr int kDirMaxStages = 4;
 constexpr int kDirMaxSlabs = 4;
 constexpr int kDirAccBufs = 4;         // accumulator buffers (all 512 tensor-memory columns)
@@ -103,7 +103,7 @@ struct DirectParams {
     FastDiv div_tps;
     int stages, slabs;
     uint32_t slab_bytes;   // one slab (wfp * hfp * 32 fp32), also its TMA byte count
-    uint32_t slab_stride;  // slab bytes rounded up to 1024
+    uint32_t slab_stride;  // slab bytes rounded up to 128 (the TMA destination alignment)
     uint32_t b_bytes;      // one weight slice: cout_pad rows x 64 bytes
     uint32_t buf_bytes;    // one plane of one activation buffer: max brows x 64 bytes
     uint32_t a_bytes;      // a stage's activation buffers: nm_max x planes x buf_bytes
@@ -708,7 +708,7 @@ bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
     P.hfp = P.TH + span_h;
     if (P.wfp > 256 || P.hfp > 256) return false;
     P.slab_bytes = (uint32_t)(P.wfp * P.hfp * kDirK * 4);
-    P.slab_stride = (P.slab_bytes + 1023u) / 1024u * 1024u;
+    P.slab_stride = (P.slab_bytes + 127u) / 128u * 128u;
     P.tiles_per_sample = prefix;
     P.div_tps = make_fastdiv((uint32_t)(prefix > 0 ? prefix : 1));
     const int64_t total = (int64_t)prefix * g.N;
@@ -717,8 +717,9 @@ bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
     P.buf_bytes = (uint32_t)brows_max * kDirRowBytes;  // a multiple of 512: whole swizzle atoms
     P.a_bytes = ((uint32_t)nm_max * planes * P.buf_bytes + 1023u) / 1024u * 1024u;
     P.stage_bytes = P.a_bytes + (sb_max + 1023u) / 1024u * 1024u;
-    // shared memory beside the static tables (227 KB per block): 1..3 slabs, 2..4 stages
-    const size_t budget = 232448 - 6144 - 1024;
+    // shared memory beside the static tables (under 4 KB) and the alignment slack (227 KB per
+    // block): 1..3 slabs, 2..4 stages
+    const size_t budget = 232448 - 4096 - 1024;
     P.slabs = 3;
     while (P.slabs > 1 && (size_t)P.slabs * P.slab_stride + 2 * (size_t)P.stage_bytes > budget) --P.slabs;
     const size_t used = (size_t)P.slabs * P.slab_stride;
