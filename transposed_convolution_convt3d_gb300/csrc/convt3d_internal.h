@@ -261,9 +261,11 @@ cudaError_t launch_bn_eval(const convt3d_plan_s &p, const float *x, const float 
 size_t bn_eval_smem_bytes(const convt3d_plan_s &p);
 int bn_eval_ksplits(int ntaps, int Cin);
 void tc_cache_free(void *cache);
-cudaError_t launch_direct(convt3d_plan_s &p, const float *x, const void *w_hi, const void *w_lo, const float *bias,
-                          float *y, uint32_t *status, cudaStream_t s);
+cudaError_t launch_direct(convt3d_plan_s &p, const float *x, const void *wdir, const float *bias, float *y,
+                          uint32_t *status, cudaStream_t s);
+cudaError_t launch_direct_pack(convt3d_plan_s &p, const float *w, void *dst, cudaStream_t s);
 bool direct_supported(const convt3d_plan_s &p);
+size_t direct_weight_bytes(const convt3d_plan_s &p);
 void direct_cache_free(void *cache);
 void *static_workspace_address();
 void report_error(const char *fmt, ...);

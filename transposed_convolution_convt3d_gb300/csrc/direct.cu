@@ -84,6 +84,7 @@ struct DGroup {
     int tiles;          // tiles per sample: Qd x nhb
     int tile_prefix;    // tiles of earlier pairs within one sample
     uint32_t sb_bytes;  // weight slices of one d-slice's K steps
+    uint32_t woff;      // its d-slice 0's weight slices in the packed weight (bytes)
     FastDiv div_nhb;
     int8_t dd[8];       // input d offset of each d-slice
     int8_t mdw[8];      // w offset of each activation buffer
@@ -91,13 +92,16 @@ struct DGroup {
 
 struct DirectParams {
     CUtensorMap x_map;  // fp32 [N][Cin][Din][Hin][Win], box (wfp, hfp, 1, 32, 1)
-    CUtensorMap b_hi;   // packed bf16 weight [tap][cout_pad][cin_pad], box (32, cout_pad, 1), 64-byte swizzle
-    CUtensorMap b_lo;
+    // The weight packed for this kernel: per pair and d-slice, the stage image of the
+    // slice's weight slices (bf16 hi [lo] planes, rows of 32 channels, 64-byte swizzled
+    // as the MMA descriptors read them), copied into a stage by one bulk load.
+    const uint8_t *wdir;
     const float *bias;
     float *y;
     uint32_t *status;
     int N, Cout, cout_pad, Din, Do, Ho, Wo, sd, sh, sw;
     int Qw, TH;         // q-grid width, q rows per tile (TH * Qw = 128)
+    int qw_shift;       // log2(Qw)
     int w_lo, wfp, hfp; // slab: first w (a multiple of 4), width, height
     int ngroups, tiles_per_sample, total_tiles;
     FastDiv div_tps;
@@ -108,6 +112,7 @@ struct DirectParams {
     uint32_t buf_bytes;    // one plane of one activation buffer: max brows x 64 bytes
     uint32_t a_bytes;      // a stage's activation buffers: nm_max x planes x buf_bytes
     uint32_t stage_bytes;  // activation buffers + the largest slice's weight slices
+    uint32_t wdir_bytes;   // the packed weight
     DGroup grp[kDirGroups];
     DStep steps[kDirMaxSteps];
 };
@@ -232,8 +237,6 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
     if (warp == 0) {
         if (lane == 0) {
             ptx::prefetch_tmap(&P.x_map);
-            ptx::prefetch_tmap(&P.b_hi);
-            if (kPlanes == 2) ptx::prefetch_tmap(&P.b_lo);
             int st = 0, sl = 0;
             uint32_t sph = 0, lph = 0;
             // per-slot bits: loaded at least once, and the parity of the last load
@@ -258,25 +261,15 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                         sl = 0;
                         lph ^= 1u;
                     }
-                    // the weight slices of its K steps, into the stage's weight area
+                    // the weight slices of its K steps, one bulk copy into the stage's weight area
                     if (!ptx::mbar_wait_bounded(empty0 + 8 * st, sph ^ 1u, &abort_flag, kDirWaitNs)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = fullb0 + 8 * st;
-                    const uint32_t wb = stage_base + (uint32_t)st * P.stage_bytes + P.a_bytes;
                     ptx::mbar_arrive_expect_tx(fb, G.sb_bytes);
-                    for (int j = 0; j < G.spa; ++j) {
-                        const DStep e = s_steps[G.step0 + a * G.spa + j];
-                        const uint32_t nb = e.tb1 >= 0 ? 2u : 1u;
-                        const uint32_t sb = wb + e.boff;
-                        ptx::tma_load_3d(sb, &P.b_hi, fb, 0, 0, e.tb0);
-                        if (e.tb1 >= 0) ptx::tma_load_3d(sb + P.b_bytes, &P.b_hi, fb, 0, 0, e.tb1);
-                        if (kPlanes == 2) {
-                            ptx::tma_load_3d(sb + nb * P.b_bytes, &P.b_lo, fb, 0, 0, e.tb0);
-                            if (e.tb1 >= 0) ptx::tma_load_3d(sb + 3 * P.b_bytes, &P.b_lo, fb, 0, 0, e.tb1);
-                        }
-                    }
+                    ptx::bulk_load(stage_base + (uint32_t)st * P.stage_bytes + P.a_bytes,
+                                   P.wdir + G.woff + (size_t)a * G.sb_bytes, G.sb_bytes, fb);
                     armed_st |= 1u << st;
                     armed_st_ph = (armed_st_ph & ~(1u << st)) | (sph << st);
                     if (++st == P.stages) {
@@ -392,40 +385,48 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                                                                     (size_t)sl * P.slab_stride);
                 uint8_t *stage = smem + (size_t)st * P.stage_bytes;
                 // buffer mi, row r = (h', w): the 32 channels of x at slab row h', column
-                // w + mdw[mi] - w_lo, in range by the slab's construction
-                for (int mi = 0; mi < G.nm; ++mi) {
-                    uint8_t *buf = stage + (size_t)mi * kPlanes * P.buf_bytes;
-                    const int wshift = G.mdw[mi] - P.w_lo;
-                    for (int r = tid; r < G.brows; r += 128) {
-                        const int hp = r / P.Qw, wq = r - hp * P.Qw;
-                        const float *src = slab + hp * P.wfp + (wq + wshift);
-                        float v[32];
+                // w + mdw[mi] - w_lo, in range by the slab's construction.  The rows of all
+                // the slice's buffers are dealt to the 128 threads in turn (no thread has more
+                // than one row above another's); Qw is a power of two.
+                int mi = 0, r = tid;
+                while (mi < G.nm && r >= G.brows) {
+                    r -= G.brows;
+                    ++mi;
+                }
+                for (; mi < G.nm;) {
+                    const int hp = r >> P.qw_shift, wq = r & (P.Qw - 1);
+                    const float *src = slab + hp * P.wfp + (wq + G.mdw[mi] - P.w_lo);
+                    float v[32];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) v[c] = src[c * plane];
-                        uint32_t hi[16], lo[16];
-                        const uint64_t neg1 = pack2(-1.f, -1.f);
+                    for (int c = 0; c < 32; ++c) v[c] = src[c * plane];
+                    uint32_t hi[16], lo[16];
+                    const uint64_t neg1 = pack2(-1.f, -1.f);
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            hi[k] = bf16x2_rn(v[2 * k], v[2 * k + 1]);
-                            if constexpr (kPlanes == 2) {
-                                // residuals v - hi of the pair in one packed fused multiply-add
-                                const uint64_t h2 = pack2(__uint_as_float(hi[k] << 16), __uint_as_float(hi[k] & 0xFFFF0000u));
-                                float r0, r1;
-                                unpack2(ffma2(h2, neg1, pack2(v[2 * k], v[2 * k + 1])), r0, r1);
-                                lo[k] = bf16x2_rn(r0, r1);
-                            }
+                    for (int k = 0; k < 16; ++k) {
+                        hi[k] = bf16x2_rn(v[2 * k], v[2 * k + 1]);
+                        if constexpr (kPlanes == 2) {
+                            // residuals v - hi of the pair in one packed fused multiply-add
+                            const uint64_t h2 = pack2(__uint_as_float(hi[k] << 16), __uint_as_float(hi[k] & 0xFFFF0000u));
+                            float r0, r1;
+                            unpack2(ffma2(h2, neg1, pack2(v[2 * k], v[2 * k + 1])), r0, r1);
+                            lo[k] = bf16x2_rn(r0, r1);
                         }
-                        // 64-byte swizzle: 16-byte chunk j of row r lands at j ^ ((r >> 1) & 3)
-                        uint8_t *row = buf + (size_t)r * kDirRowBytes;
-                        const uint32_t swz = (uint32_t)((r >> 1) & 3);
+                    }
+                    // 64-byte swizzle: 16-byte chunk j of row r lands at j ^ ((r >> 1) & 3)
+                    uint8_t *row = stage + (size_t)mi * kPlanes * P.buf_bytes + (size_t)r * kDirRowBytes;
+                    const uint32_t swz = (uint32_t)((r >> 1) & 3);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t o = ((uint32_t)c ^ swz) << 4;
-                            *reinterpret_cast<uint4 *>(row + o) = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-                            if constexpr (kPlanes == 2)
-                                *reinterpret_cast<uint4 *>(row + P.buf_bytes + o) =
-                                    make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
-                        }
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t o = ((uint32_t)c ^ swz) << 4;
+                        *reinterpret_cast<uint4 *>(row + o) = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+                        if constexpr (kPlanes == 2)
+                            *reinterpret_cast<uint4 *>(row + P.buf_bytes + o) =
+                                make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+                    }
+                    r += 128;
+                    while (mi < G.nm && r >= G.brows) {
+                        r -= G.brows;
+                        ++mi;
                     }
                 }
                 ptx::fence_proxy_async_smem();
@@ -643,11 +644,12 @@ bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
     // rows of whole 8-row swizzle atoms, whole rows per tile: Qw a multiple of 8 dividing 128
     if (P.Qw < 8 || P.Qw > 128 || P.Qw % 8 != 0 || 128 % P.Qw != 0) return false;
     P.TH = 128 / P.Qw;
+    while ((1 << P.qw_shift) < P.Qw) ++P.qw_shift;
     P.ngroups = p.ngroups;
     P.b_bytes = (uint32_t)p.cout_pad * kDirRowBytes;
     const uint32_t planes = (uint32_t)p.planes;
     int dw_min = 1 << 20, dw_max = -(1 << 20), span_h = 0, ns = 0, prefix = 0, nm_max = 1, brows_max = 0;
-    uint32_t sb_max = 0;
+    uint32_t sb_max = 0, woff = 0;
     for (int gi = 0; gi < p.ngroups; ++gi) {
         const GroupDesc &S = p.grp[gi];
         if (S.ncls != 2 || S.Qw != P.Qw || S.nm > 8) return false;
@@ -692,6 +694,8 @@ bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
                     hi_h = td.dh > hi_h ? td.dh : hi_h;
                 }
         sb_max = G.sb_bytes > sb_max ? G.sb_bytes : sb_max;
+        G.woff = woff;
+        woff += (uint32_t)G.nt_d * G.sb_bytes;
         const int sph = hi_h - G.lo_h;
         span_h = sph > span_h ? sph : span_h;
         G.brows = (P.TH + sph) * P.Qw;
@@ -709,6 +713,7 @@ bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
     if (P.wfp > 256 || P.hfp > 256) return false;
     P.slab_bytes = (uint32_t)(P.wfp * P.hfp * kDirK * 4);
     P.slab_stride = (P.slab_bytes + 127u) / 128u * 128u;
+    P.wdir_bytes = woff;
     P.tiles_per_sample = prefix;
     P.div_tps = make_fastdiv((uint32_t)(prefix > 0 ? prefix : 1));
     const int64_t total = (int64_t)prefix * g.N;
@@ -728,14 +733,128 @@ bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
     return P.stages >= 2;
 }
 
+// One weight slice of the packed weight: cout_pad rows of 32 bf16 channels (64
+// bytes, 16-byte chunks stored at chunk ^ ((row >> 1) & 3)) of tap widx, hi or lo.
+struct DPackEntry {
+    uint32_t dst;
+    int16_t widx;
+    uint8_t lo, pad_;
+};
+constexpr int kDirMaxPack = 1024;
+struct DPackParams {
+    const float *w;
+    uint8_t *dst;
+    int Cin, Cout, k3, cout_pad, cin_g, cout_g, split, n;
+    DPackEntry e[kDirMaxPack];
+};
+
+// One block per weight slice, four threads per row: each writes one 16-byte chunk
+// (8 input channels) of the row, split into bf16 hi and lo (rounded to nearest
+// even, lo = bf16(v - hi)).  w is [Cin][Cout/G][taps]; channels of different
+// convolution groups, and rows or channels past Cout or Cin, are zero.
+__global__ void pack_direct_kernel(const __grid_constant__ DPackParams Q) {
+    const DPackEntry E = Q.e[blockIdx.x];
+    const int r = threadIdx.x >> 2, pch = threadIdx.x & 3;
+    if (r >= Q.cout_pad) return;
+    const int jc = pch ^ ((r >> 1) & 3);  // the logical chunk this physical chunk holds
+    const int co = r;
+    uint32_t out[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        float v[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int ci = 8 * jc + e + q;
+            v[q] = 0.f;
+            if (ci < Q.Cin && co < Q.Cout && ci / Q.cin_g == co / Q.cout_g)
+                v[q] = Q.w[((int64_t)ci * Q.cout_g + co % Q.cout_g) * Q.k3 + E.widx];
+        }
+        uint32_t h = bf16x2_rn(v[0], v[1]);
+        if (E.lo) {
+            const float h0 = __uint_as_float(h << 16), h1 = __uint_as_float(h & 0xFFFF0000u);
+            h = bf16x2_rn(v[0] - h0, v[1] - h1);
+        }
+        out[e / 2] = h;
+    }
+    *reinterpret_cast<uint4 *>(Q.dst + E.dst + (size_t)r * kDirRowBytes + (size_t)pch * 16) =
+        make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// The weight slices in the packed weight's order (pair, d-slice, K step, plane,
+// class slot), each placed where the stage image of its slice puts it.
+bool direct_pack_table(const convt3d_plan_s &p, const DirectParams &P, DPackParams &Q) {
+    Q.n = 0;
+    for (int gi = 0; gi < P.ngroups; ++gi) {
+        const DGroup &G = P.grp[gi];
+        for (int a = 0; a < G.nt_d; ++a)
+            for (int j = 0; j < G.spa; ++j) {
+                const DStep &st = P.steps[G.step0 + a * G.spa + j];
+                const uint32_t nb = st.tb1 >= 0 ? 2u : 1u;
+                for (int plane = 0; plane < p.planes; ++plane)
+                    for (uint32_t slot = 0; slot < nb; ++slot) {
+                        if (Q.n >= kDirMaxPack) return false;
+                        DPackEntry &en = Q.e[Q.n++];
+                        en.dst = G.woff + (uint32_t)a * G.sb_bytes + st.boff + ((uint32_t)plane * nb + slot) * P.b_bytes;
+                        en.widx = p.g.taps[slot ? st.tb1 : st.tb0].widx;
+                        en.lo = (uint8_t)plane;
+                    }
+            }
+    }
+    Q.Cin = p.g.Cin;
+    Q.Cout = p.g.Cout;
+    Q.k3 = p.g.kvol;
+    Q.cout_pad = p.cout_pad;
+    Q.cin_g = p.g.Cin / p.g.G;
+    Q.cout_g = p.g.Cout / p.g.G;
+    Q.split = p.planes == 2;
+    return true;
+}
+
 struct DirectCache {
     DirectParams P;
-    const void *key[3];
+    DPackParams Q;
+    const void *key[2];
     void (*kern)(const DirectParams);
     size_t smem;
     int grid;
     bool ready;
 };
+
+// The plan's launch state: tables, kernel instance, shared memory and grid.
+cudaError_t direct_prepare(convt3d_plan_s &p, DirectCache *&out) {
+    if (!p.direct_cache) {
+        DirectCache *c = new (std::nothrow) DirectCache();
+        if (!c) return cudaErrorMemoryAllocation;
+        c->ready = false;
+        p.direct_cache = c;
+    }
+    DirectCache &dc = *static_cast<DirectCache *>(p.direct_cache);
+    out = &dc;
+    if (dc.ready) return cudaSuccess;
+    DirectParams &P = dc.P;
+    cudaError_t e;
+    if (!direct_geometry(p, P)) return cudaErrorInvalidConfiguration;
+    if (!direct_pack_table(p, P, dc.Q)) return cudaErrorInvalidConfiguration;
+    const bool split = p.planes == 2;
+    if (p.d.epilogue == CONVT3D_EPI_SOFTMAX_SIGMOID)
+        dc.kern = split ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 3>
+                        : convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2>;
+    else
+        dc.kern = split ? convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 3> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 2>;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, dc.kern)) != cudaSuccess) return e;
+    dc.smem = 1024 + (size_t)P.stages * P.stage_bytes + (size_t)P.slabs * P.slab_stride;
+    if (dc.smem + fa.sharedSizeBytes > 232448) return cudaErrorInvalidConfiguration;
+    if ((e = cudaFuncSetAttribute(dc.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dc.smem)) != cudaSuccess)
+        return e;
+    int dev = 0, sms = 148;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    dc.grid = P.total_tiles < sms ? P.total_tiles : sms;
+    dc.key[0] = dc.key[1] = nullptr;
+    dc.ready = true;
+    return cudaSuccess;
+}
 
 }  // namespace
 
@@ -747,43 +866,36 @@ bool direct_supported(const convt3d_plan_s &p) {
     return ok;
 }
 
+size_t direct_weight_bytes(const convt3d_plan_s &p) {
+    DirectParams *P = new (std::nothrow) DirectParams();
+    if (!P) return 0;
+    const size_t n = direct_geometry(p, *P) ? P->wdir_bytes : 0;
+    delete P;
+    return n;
+}
+
 void direct_cache_free(void *c) { delete static_cast<DirectCache *>(c); }
 
-cudaError_t launch_direct(convt3d_plan_s &p, const float *x, const void *w_hi, const void *w_lo, const float *bias,
-                          float *y, uint32_t *status, cudaStream_t s) {
+cudaError_t launch_direct_pack(convt3d_plan_s &p, const float *w, void *dst, cudaStream_t s) {
+    static_assert(sizeof(DPackParams) < 32000, "kernel parameter block too large");
+    DirectCache *dc = nullptr;
+    cudaError_t e = direct_prepare(p, dc);
+    if (e != cudaSuccess) return e;
+    dc->Q.w = w;
+    dc->Q.dst = static_cast<uint8_t *>(dst);
+    pack_direct_kernel<<<dc->Q.n, 4 * p.cout_pad, 0, s>>>(dc->Q);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_direct(convt3d_plan_s &p, const float *x, const void *wdir, const float *bias, float *y,
+                          uint32_t *status, cudaStream_t s) {
     static_assert(sizeof(DirectParams) < 32000, "kernel parameter block too large");
-    if (!p.direct_cache) {
-        DirectCache *c = new (std::nothrow) DirectCache();
-        if (!c) return cudaErrorMemoryAllocation;
-        c->ready = false;
-        p.direct_cache = c;
-    }
-    DirectCache &dc = *static_cast<DirectCache *>(p.direct_cache);
+    DirectCache *dcp = nullptr;
+    cudaError_t e = direct_prepare(p, dcp);
+    if (e != cudaSuccess) return e;
+    DirectCache &dc = *dcp;
     DirectParams &P = dc.P;
-    cudaError_t e;
-    if (!dc.ready) {
-        if (!direct_geometry(p, P)) return cudaErrorInvalidConfiguration;
-        const bool split = p.planes == 2;
-        if (p.d.epilogue == CONVT3D_EPI_SOFTMAX_SIGMOID)
-            dc.kern = split ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 3>
-                            : convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2>;
-        else
-            dc.kern = split ? convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 3> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 2>;
-        cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, dc.kern)) != cudaSuccess) return e;
-        dc.smem = 1024 + (size_t)P.stages * P.stage_bytes + (size_t)P.slabs * P.slab_stride;
-        if (dc.smem + fa.sharedSizeBytes > 232448) return cudaErrorInvalidConfiguration;
-        if ((e = cudaFuncSetAttribute(dc.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dc.smem)) !=
-            cudaSuccess)
-            return e;
-        int dev = 0, sms = 148;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        dc.grid = P.total_tiles < sms ? P.total_tiles : sms;
-        dc.key[0] = dc.key[1] = dc.key[2] = nullptr;
-        dc.ready = true;
-    }
-    if (dc.key[0] != x || dc.key[1] != w_hi || dc.key[2] != w_lo) {
+    if (dc.key[0] != x) {
         cudaError_t ferr;
         EncodeTiledFn enc = encode_tiled(ferr);
         if (!enc) return ferr != cudaSuccess ? ferr : cudaErrorNotSupported;
@@ -799,19 +911,9 @@ cudaError_t launch_direct(convt3d_plan_s &p, const float *x, const void *w_hi, c
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        // packed bf16 weights [tap][cout_pad][cin_pad]: a K step reads channels 0..31 of one tap
-        const cuuint64_t wdim[3] = {(cuuint64_t)p.cin_pad, (cuuint64_t)p.cout_pad, (cuuint64_t)g.ntaps};
-        const cuuint64_t wstr[2] = {(cuuint64_t)p.cin_pad * 2, (cuuint64_t)p.cin_pad * 2 * p.cout_pad};
-        const cuuint32_t wbox[3] = {(cuuint32_t)kDirK, (cuuint32_t)p.cout_pad, 1};
-        for (int plane = 0; plane < p.planes; ++plane)
-            if (enc(plane ? &P.b_lo : &P.b_hi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void *)(plane ? w_lo : w_hi),
-                    wdim, wstr, wbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-                return cudaErrorInvalidValue;
         dc.key[0] = x;
-        dc.key[1] = w_hi;
-        dc.key[2] = w_lo;
     }
+    P.wdir = static_cast<const uint8_t *>(wdir);
     P.bias = bias;
     P.y = y;
     P.status = status;

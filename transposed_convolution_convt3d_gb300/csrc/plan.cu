@@ -385,9 +385,14 @@ convt3d_status_t convt3d_plan_create(const convt3d_desc_t *desc, convt3d_plan_t 
     size_t off = kStatusBytes;
     p->wpk_elems = (size_t)p->g.ntaps * p->cin_pad * p->cout_pad;
     p->off_wpk_hi = off;
-    off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
-    p->off_wpk_lo = off;
-    if (p->planes == 2) off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
+    if (p->direct) {  // the direct kernel's own packed layout (both planes, stage images per d-slice)
+        off = align_up(off + direct_weight_bytes(*p), 256);
+        p->off_wpk_lo = off;
+    } else {
+        off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
+        p->off_wpk_lo = off;
+        if (p->planes == 2) off = align_up(off + p->wpk_elems * p->elem_bytes, 256);
+    }
     p->xs_elems = (p->tc && !eval_bn && !p->direct) ? (size_t)desc->N * desc->Din * desc->Hin * desc->Win * p->cin_pad : 0;
     p->off_xs_hi = off;
     off = align_up(off + p->xs_elems * p->elem_bytes, 256);
@@ -537,8 +542,9 @@ convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const void *wv, void *ws
         e = cudaMemsetAsync(base + p->off_evcnt, 0, p->ws_total - p->off_evcnt, s);
         if (e != cudaSuccess) return cuda_fail(e, "clearing arrival counters");
     }
-    e = launch_pack_weights(*p, w, (float *)(base + p->off_wpk_hi),
-                            p->planes == 2 ? (float *)(base + p->off_wpk_lo) : nullptr, p->tc, s);
+    e = p->direct ? launch_direct_pack(*p, w, base + p->off_wpk_hi, s)
+                  : launch_pack_weights(*p, w, (float *)(base + p->off_wpk_hi),
+                                        p->planes == 2 ? (float *)(base + p->off_wpk_lo) : nullptr, p->tc, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack_weights launch");
     p->packed_ws = ws;
     return CONVT3D_OK;
@@ -590,9 +596,8 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *
         }
     }
     if (p->direct) {
-        const bool two = p->planes == 2;
         if (p->prof_enabled && (e = cudaEventRecord(p->ev0, s)) != cudaSuccess) return cuda_fail(e, "event");
-        e = launch_direct(*p, x, base + p->off_wpk_hi, two ? base + p->off_wpk_lo : nullptr, b, y, (uint32_t *)base, s);
+        e = launch_direct(*p, x, base + p->off_wpk_hi, b, y, (uint32_t *)base, s);
         if (e != cudaSuccess) return cuda_fail(e, "direct tensor-core GEMM launch");
     } else if (p->tc) {
         const bool two = p->planes == 2;

@@ -122,6 +122,14 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` (a multiple of 16) from global to shared
+// memory, both addresses 16-byte aligned, completion signalled on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // Make this thread's ordinary shared-memory writes visible to the async proxy
 // (the tensor cores' operand reads) before it signals that they are done.
 __device__ __forceinline__ void fence_proxy_async_smem() {
