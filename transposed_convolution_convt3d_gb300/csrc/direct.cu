@@ -25,8 +25,8 @@
 // CTA roles (persistent, one CTA per SM):
 //   warp 0        TMA producer (one thread): x slabs and weight slices
 //   warp 1        MMA issuer (one thread) + tensor-memory allocation
-//   warps 2..5    converters: slab -> bf16 hi/lo activation buffers
-//   warps 6..17   epilogue, three groups of four warps; group g takes every third
+//   warps 2..7    converters: slab -> bf16 hi/lo activation buffers
+//   warps 8..19   epilogue, three groups of four warps; group g takes every third
 //                 tile of the CTA, one output row (both classes) per thread; the
 //                 tiles rotate through four accumulator buffers, so the MMAs can
 //                 run ahead of the epilogue
@@ -52,7 +52,9 @@ constexpr int kDirAccBufs = 4;         // accumulator buffers (all 512 tensor-me
 constexpr int kDirAccCols = 128;       // tensor-memory columns per buffer (2 x cout_pad <= 128)
 constexpr int kDirEpiGroups = 3;       // epilogue groups of four warps
 constexpr int kDirEpiWarps = 4 * kDirEpiGroups;
-constexpr int kDirThreads = 32 * (2 + 4 + kDirEpiWarps);
+constexpr int kDirConvWarps = 6;       // converter warps (the register budget per thread is the same for 18 and 20 warps)
+constexpr int kDirConvThreads = 32 * kDirConvWarps;
+constexpr int kDirThreads = 32 * (2 + kDirConvWarps + kDirEpiWarps);
 constexpr int kDirK = 32;              // input channels per K step (one 64-byte bf16 row)
 constexpr uint32_t kDirRowBytes = 64;
 constexpr uint64_t kDirWaitNs = 2000000000ull;
@@ -67,6 +69,9 @@ struct DStep {
     uint8_t mask, mi;
     int16_t tb0, tb1;
     uint32_t boff;
+    // the MMA's operand offsets within a stage, in 16-byte units (the descriptors'
+    // start-address unit): activation rows, weight hi slices, and weight lo after hi
+    uint16_t a16, b16, blo16, pad_;
 };
 
 // One w-parity pair: classes (rd, rh, 0) and (rd, rh, 1).
@@ -188,11 +193,11 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
     // integer round trip) so that ordinary loads and stores through it stay shared-memory ones
     uint8_t *smem = dsmem_raw + ((1024u - (ptx::smem_u32(dsmem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t fulla0 = ptx::smem_u32(&bars[0]);                       // stage's buffers built (4 warps)
+    const uint32_t fulla0 = ptx::smem_u32(&bars[0]);                       // stage's buffers built (converter warps)
     const uint32_t fullb0 = ptx::smem_u32(&bars[kDirMaxStages]);           // stage's weights landed (TMA bytes)
     const uint32_t empty0 = ptx::smem_u32(&bars[2 * kDirMaxStages]);       // stage consumed (MMA commit)
     const uint32_t slabf0 = ptx::smem_u32(&bars[3 * kDirMaxStages]);       // slab landed (TMA bytes)
-    const uint32_t slabe0 = slabf0 + 8 * kDirMaxSlabs;                     // slab used (4 warps)
+    const uint32_t slabe0 = slabf0 + 8 * kDirMaxSlabs;                     // slab used (converter warps)
     const uint32_t accf0 = slabe0 + 8 * kDirMaxSlabs;                      // accumulator ready (MMA commit)
     const uint32_t acce0 = accf0 + 8 * kDirAccBufs;                        // accumulator read (128 threads)
     const uint32_t drain = acce0 + 8 * kDirAccBufs;
@@ -202,13 +207,13 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < P.stages; ++s) {
-            ptx::mbar_init(fulla0 + 8 * s, 4);
+            ptx::mbar_init(fulla0 + 8 * s, kDirConvWarps);
             ptx::mbar_init(fullb0 + 8 * s, 1);
             ptx::mbar_init(empty0 + 8 * s, 1);
         }
         for (int s = 0; s < P.slabs; ++s) {
             ptx::mbar_init(slabf0 + 8 * s, 1);
-            ptx::mbar_init(slabe0 + 8 * s, 4);
+            ptx::mbar_init(slabe0 + 8 * s, kDirConvWarps);
         }
         for (int b = 0; b < kDirAccBufs; ++b) {
             ptx::mbar_init(accf0 + 8 * b, 1);
@@ -296,7 +301,6 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
             const uint32_t idesc1 = ptx::idesc_bf16((uint32_t)P.cout_pad);
             const uint32_t idesc2 = ptx::idesc_bf16(2u * (uint32_t)P.cout_pad);
             const uint64_t buf16 = (uint64_t)(P.buf_bytes >> 4);  // one buffer plane, 16-byte units
-            const uint32_t arow = (uint32_t)P.Qw * kDirRowBytes;  // one q-row of a buffer, bytes
             int st = 0, it = 0;
             uint32_t sph = 0;
             bool ok = true;
@@ -320,9 +324,12 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sb = stage_base + (uint32_t)st * P.stage_bytes;
+                    // the stage's descriptor; a step's operands are offsets from it (their start
+                    // addresses stay below 2^18 bytes, so the additions never leave the field)
+                    const uint64_t d0 = ptx::sdesc_k_swizzled(stage_base + (uint32_t)st * P.stage_bytes, kDirRowBytes);
+                    const DStep *sp = s_steps + G.step0 + a * G.spa;
                     for (int j = 0; j < G.spa; ++j) {
-                        const DStep e = s_steps[G.step0 + a * G.spa + j];
+                        const DStep e = sp[j];
                         const uint32_t mask = e.mask;
                         const uint32_t d_tmem = acc + (mask == 2u ? (uint32_t)P.cout_pad : 0u);
                         const uint32_t id = mask == 3u ? idesc2 : idesc1;
@@ -330,10 +337,9 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                         // feeding both classes never finds one initialised and the other not
                         const uint32_t first = (ini & mask) ? 1u : 0u;
                         // buffer mi from row (dh - lo_h) * Qw on: a multiple of 8 rows (512 bytes)
-                        const uint64_t a_hi = ptx::sdesc_k_swizzled(
-                            sb + (uint32_t)e.mi * kPlanes * P.buf_bytes + (uint32_t)(e.dh - G.lo_h) * arow, kDirRowBytes);
-                        const uint64_t b_hi = ptx::sdesc_k_swizzled(sb + P.a_bytes + e.boff, kDirRowBytes);
-                        const uint64_t b_lo = b_hi + (uint64_t)(((e.tb1 >= 0 ? 2u : 1u) * P.b_bytes) >> 4);
+                        const uint64_t a_hi = d0 + e.a16;
+                        const uint64_t b_hi = d0 + e.b16;
+                        const uint64_t b_lo = b_hi + e.blo16;
 #pragma unroll
                         for (int kk = 0; kk < kDirK / 16; ++kk) {  // 16 bf16 (32 bytes) per MMA
                             const uint32_t acc_flag = kk ? 1u : first;
@@ -366,8 +372,8 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
         }
     }
     // ---------------------------------------------------------- converters
-    else if (warp < 6) {
-        const int tid = (warp - 2) * 32 + lane;             // 0..127
+    else if (warp < 2 + kDirConvWarps) {
+        const int tid = (warp - 2) * 32 + lane;             // 0..kDirConvThreads-1
         const uint32_t plane = (uint32_t)(P.hfp * P.wfp);  // floats between channels in a slab
         int st = 0, sl = 0;
         uint32_t sph = 0, lph = 0;
@@ -386,7 +392,7 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                 uint8_t *stage = smem + (size_t)st * P.stage_bytes;
                 // buffer mi, row r = (h', w): the 32 channels of x at slab row h', column
                 // w + mdw[mi] - w_lo, in range by the slab's construction.  The rows of all
-                // the slice's buffers are dealt to the 128 threads in turn (no thread has more
+                // the slice's buffers are dealt to the converter threads in turn (no thread has more
                 // than one row above another's); Qw is a power of two.
                 int mi = 0, r = tid;
                 while (mi < G.nm && r >= G.brows) {
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                             *reinterpret_cast<uint4 *>(row + P.buf_bytes + o) =
                                 make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
                     }
-                    r += 128;
+                    r += kDirConvThreads;
                     while (mi < G.nm && r >= G.brows) {
                         r -= G.brows;
                         ++mi;
@@ -452,7 +458,7 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
     }
     // ------------------------------------------------------------ epilogue
     else {
-        const int ew = warp - 6;
+        const int ew = warp - 2 - kDirConvWarps;
         const int eg = ew >> 2;        // epilogue group
         const int quarter = warp & 3;  // tensor-memory lane quarter this warp may access
         const int m = quarter * 32 + lane;
@@ -722,6 +728,16 @@ bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
     P.buf_bytes = (uint32_t)brows_max * kDirRowBytes;  // a multiple of 512: whole swizzle atoms
     P.a_bytes = ((uint32_t)nm_max * planes * P.buf_bytes + 1023u) / 1024u * 1024u;
     P.stage_bytes = P.a_bytes + (sb_max + 1023u) / 1024u * 1024u;
+    for (int gi = 0; gi < P.ngroups; ++gi) {
+        const DGroup &G = P.grp[gi];
+        for (int j = 0; j < G.nt_d * G.spa; ++j) {
+            DStep &e = P.steps[G.step0 + j];
+            const uint32_t arow = (uint32_t)P.Qw * kDirRowBytes;
+            e.a16 = (uint16_t)(((uint32_t)e.mi * planes * P.buf_bytes + (uint32_t)(e.dh - G.lo_h) * arow) >> 4);
+            e.b16 = (uint16_t)((P.a_bytes + e.boff) >> 4);
+            e.blo16 = (uint16_t)(((e.tb1 >= 0 ? 2u : 1u) * P.b_bytes) >> 4);
+        }
+    }
     // shared memory beside the static tables (under 4 KB) and the alignment slack (227 KB per
     // block): 1..3 slabs, 2..4 stages
     const size_t budget = 232448 - 4096 - 1024;
