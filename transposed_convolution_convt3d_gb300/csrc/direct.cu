@@ -170,6 +170,16 @@ __device__ __forceinline__ float tree_max16_d(const float (&v)[16]) {
     return fmaxf(fmaxf(a[0], a[2]), fmaxf(a[1], a[3]));
 }
 
+// Programmatic dependent launch: let the next grid in the stream (launched with
+// programmatic stream serialization) start before this one completes ...
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ... and, in that grid, wait until the grids it depends on have completed and
+// their memory operations are visible (returns at once without such a launch).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // (lo_elem, hi_elem) rounded to nearest-even bf16 and packed, lo_elem in the low half.
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo_elem, float hi_elem) {
     uint32_t r;
@@ -222,6 +232,10 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
         ptx::mbar_init(drain, 1);
         ptx::fence_mbar_init();
     }
+    // The launch may overlap the end of the work before it in the stream (programmatic
+    // dependent launch: the weight packing kernel lets it start early); no global memory is
+    // read before that work has completed.
+    grid_dependency_wait();
     for (int c = threadIdx.x; c < kDirAccCols; c += blockDim.x) {
         const float b = (P.bias && c < P.Cout) ? P.bias[c] : 0.f;
         s_bias[c] = b;
@@ -769,6 +783,7 @@ struct DPackParams {
 // even, lo = bf16(v - hi)).  w is [Cin][Cout/G][taps]; channels of different
 // convolution groups, and rows or channels past Cout or Cin, are zero.
 __global__ void pack_direct_kernel(const __grid_constant__ DPackParams Q) {
+    grid_launch_dependents();  // the GEMM may launch and set up meanwhile
     const DPackEntry E = Q.e[blockIdx.x];
     const int r = threadIdx.x >> 2, pch = threadIdx.x & 3;
     if (r >= Q.cout_pad) return;
@@ -933,7 +948,22 @@ cudaError_t launch_direct(convt3d_plan_s &p, const float *x, const void *wdir, c
     P.bias = bias;
     P.y = y;
     P.status = status;
-    dc.kern<<<dc.grid, kDirThreads, dc.smem, s>>>(P);
+    // Launched as a programmatic dependent of the work before it in the stream: it may start
+    // once that work lets it (the weight packing kernel does at its start; any other kernel at
+    // its end) and sets up its barriers and tensor memory meanwhile; every thread waits for that
+    // work to complete before its first global-memory read.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)dc.grid);
+    cfg.blockDim = dim3(kDirThreads);
+    cfg.dynamicSmemBytes = dc.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, dc.kern, P);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
