@@ -62,6 +62,16 @@ __device__ __forceinline__ double row_m2(const double *p, double mu) {
     return p[2] + d * d / p[0];
 }
 
+// As row_m2, dividing by the row's count through a table of reciprocals (counts
+// above the table divide).
+constexpr int kRcpTable = 129;
+__device__ __forceinline__ double row_m2_rcp(const double *p, double mu, const double *rcp) {
+    const double n = p[0];
+    if (n <= 0.0) return 0.0;
+    const double d = p[1] - n * mu;
+    return n < (double)kRcpTable ? p[2] + d * d * rcp[(int)n] : p[2] + d * d / n;
+}
+
 __global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const double *__restrict__ partials,
                                                                   double *__restrict__ stats, int N, int G, int T,
                                                                   double eps) {
@@ -158,6 +168,10 @@ __global__ void bn_reduce_kernel(const double *__restrict__ partials, double *__
                                  int T, int splits) {
     __shared__ double red[2][8][33];
     __shared__ double s_mu[32];
+    // 1 / k for the rows' counts (at most one tile's rows, 128): this GPU's fp64 division is
+    // slow, and a row's squared deviation needs one per (row, channel)
+    __shared__ double s_rcp[kRcpTable];
+    for (int i = threadIdx.y * 32 + threadIdx.x; i < kRcpTable; i += 256) s_rcp[i] = i > 0 ? 1.0 / i : 0.0;
     const int n = blockIdx.y, split = blockIdx.z;
     const int c = blockIdx.x * 32 + threadIdx.x;
     const int lane_t = threadIdx.y;
@@ -187,7 +201,7 @@ __global__ void bn_reduce_kernel(const double *__restrict__ partials, double *__
     __syncthreads();  // red is reused
     double m2 = 0.0;
     if (c < C)
-        for (int t = t0 + lane_t; t < t1; t += 8) m2 += row_m2(rows + (int64_t)t * 3 * C, mu);
+        for (int t = t0 + lane_t; t < t1; t += 8) m2 += row_m2_rcp(rows + (int64_t)t * 3 * C, mu, s_rcp);
     red[0][lane_t][threadIdx.x] = m2;
     __syncthreads();
     if (lane_t == 0 && c < C) {
