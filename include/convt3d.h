@@ -175,7 +175,7 @@ typedef struct {
                                     shapes the tensor-core loads cannot address: TMA
                                     im2col corners beyond [-16, 15]); 2: tensor-core GEMM
                                     reading NCDHW fp32 x itself, no staging pass (stride
-                                    2 along w, Cin <= 32, Cout <= 64, BF16 or 3XBF16,
+                                    2 along w, Cin <= 32, Cout <= 64, BF16, 3XBF16 or FP16,
                                     identity or softmax+sigmoid, q-grid rows of 8..128
                                     positions dividing 128)                            */
 } convt3d_info_t;

@@ -133,11 +133,12 @@ def test_direct_input_kernel_selection():
     then needs no staged copy of x in the workspace; split TF32 keeps the staged kernel,
     and so do shapes outside the direct kernel's range (Cin > 32, q-rows of 12)."""
     import workloads as E
-    from transposed_convolution_convt3d_gb300 import PREC_3XBF16, PREC_3XTF32, PREC_BF16, Plan
+    from transposed_convolution_convt3d_gb300 import PREC_3XBF16, PREC_3XTF32, PREC_BF16, PREC_FP16, Plan
     spec = E.SOFTMAX
     direct = Plan.from_spec(spec, precision=PREC_3XBF16)
     staged = Plan.from_spec(spec, precision=PREC_3XTF32)
     assert direct.info["main_kernel"] == 2 and Plan.from_spec(spec, precision=PREC_BF16).info["main_kernel"] == 2
+    assert Plan.from_spec(spec, precision=PREC_FP16).info["main_kernel"] == 2
     assert staged.info["main_kernel"] == 0
     # the staged kernel's workspace holds two bf16 planes of x (channels padded to 64); the direct one's does not
     staged_cl = Plan.from_spec(spec.replace(channels_last=True), precision=PREC_3XBF16)

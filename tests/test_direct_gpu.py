@@ -2,7 +2,7 @@
 
 Plans with stride 2 along w, at most 32 input channels, at most 64 output
 channels, NCDHW fp32 tensors, an identity or softmax+sigmoid epilogue and bf16
-operands (split BF16 or BF16), and q-grid rows of 8, 16, 32, 64 or 128
+operands (split BF16, BF16 or FP16), and q-grid rows of 8, 16, 32, 64 or 128
 positions, read x straight from the caller's tensor: one TMA slab per input
 d-slice, operands built on chip.  The cases cover 16 to 1 q-rows per tile,
 ragged channel counts, w-parity classes of different width, three merged w
@@ -15,7 +15,7 @@ import pytest
 
 import workloads as E
 from test_parity_gpu import TOL, assert_close, rounded_inputs, run_gpu, run_oracle
-from transposed_convolution_convt3d_gb300 import PREC_3XBF16, PREC_BF16, Plan
+from transposed_convolution_convt3d_gb300 import PREC_3XBF16, PREC_BF16, PREC_FP16, Plan
 
 DIRECT = [
     E.Spec("direct_softmax_w8", N=2, Cin=32, Cout=64, D=4, H=6, W=8, k=3, stride=2, pad=1, out_pad=1, bias=True,
@@ -70,6 +70,17 @@ def test_direct_bf16(spec):
     inputs = E.make_inputs(spec)
     got = run_gpu(spec, inputs, PREC_BF16)
     assert_close(got, run_oracle(spec, rounded_inputs(inputs, PREC_BF16)), spec.name, TOL)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("spec", DIRECT[:4] + DIRECT[6:8], ids=lambda s: s.name)
+def test_direct_fp16(spec):
+    """One product of fp16-rounded operands (kind::f16 with fp16 A and B): equal to the
+    oracle on identically rounded x and w within the fp32 tolerance."""
+    assert main_kernel(spec, PREC_FP16) == 2
+    inputs = E.make_inputs(spec)
+    got = run_gpu(spec, inputs, PREC_FP16)
+    assert_close(got, run_oracle(spec, rounded_inputs(inputs, PREC_FP16)), spec.name, TOL)
 
 
 @pytest.mark.gpu

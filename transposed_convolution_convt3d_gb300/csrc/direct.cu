@@ -187,6 +187,16 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo_elem, float hi_elem) {
     return r;
 }
 
+// The same in fp16.
+__device__ __forceinline__ uint32_t f16x2_rn(float lo_elem, float hi_elem) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_elem), "f"(lo_elem));
+    return r;
+}
+
+// EPI: CONVT3D_EPI_SOFTMAX_SIGMOID or CONVT3D_EPI_IDENTITY.  OPS: 2 = BF16 (one product
+// of bf16-rounded operands), 3 = split BF16 (three products), 4 = FP16 (one product of
+// fp16-rounded operands).
 template <int EPI, int OPS>
 __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __grid_constant__ DirectParams P) {
     constexpr int kPlanes = OPS == 3 ? 2 : 1;
@@ -312,8 +322,10 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
     // ---------------------------------------------------------- MMA issuer
     else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc1 = ptx::idesc_bf16((uint32_t)P.cout_pad);
-            const uint32_t idesc2 = ptx::idesc_bf16(2u * (uint32_t)P.cout_pad);
+            const uint32_t idesc1 =
+                OPS == 4 ? ptx::idesc_f16((uint32_t)P.cout_pad) : ptx::idesc_bf16((uint32_t)P.cout_pad);
+            const uint32_t idesc2 =
+                OPS == 4 ? ptx::idesc_f16(2u * (uint32_t)P.cout_pad) : ptx::idesc_bf16(2u * (uint32_t)P.cout_pad);
             const uint64_t buf16 = (uint64_t)(P.buf_bytes >> 4);  // one buffer plane, 16-byte units
             int st = 0, it = 0;
             uint32_t sph = 0;
@@ -423,7 +435,7 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                     const uint64_t neg1 = pack2(-1.f, -1.f);
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
-                        hi[k] = bf16x2_rn(v[2 * k], v[2 * k + 1]);
+                        hi[k] = OPS == 4 ? f16x2_rn(v[2 * k], v[2 * k + 1]) : bf16x2_rn(v[2 * k], v[2 * k + 1]);
                         if constexpr (kPlanes == 2) {
                             // residuals v - hi of the pair in one packed fused multiply-add
                             const uint64_t h2 = pack2(__uint_as_float(hi[k] << 16), __uint_as_float(hi[k] & 0xFFFF0000u));
@@ -646,7 +658,7 @@ int floor4(int v) { return v >= 0 ? v / 4 * 4 : -((-v + 3) / 4 * 4); }
 bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
     const Geometry &g = p.g;
     const int epi = p.d.epilogue;
-    if (!p.tc || !p.merged || p.cl || p.io16 != kF32 || !p.bf16 || p.half || p.nslices != 1) return false;
+    if (!p.tc || !p.merged || p.cl || p.io16 != kF32 || !p.bf16 || p.nslices != 1) return false;
     if (epi != CONVT3D_EPI_SOFTMAX_SIGMOID && epi != CONVT3D_EPI_IDENTITY) return false;
     if (g.Cin > kDirK || g.Win % 4 != 0 || p.cout_pad > 64 || p.ngroups > kDirGroups) return false;
     memset(&P, 0, sizeof(P));
@@ -774,7 +786,7 @@ constexpr int kDirMaxPack = 1024;
 struct DPackParams {
     const float *w;
     uint8_t *dst;
-    int Cin, Cout, k3, cout_pad, cin_g, cout_g, split, n;
+    int Cin, Cout, k3, cout_pad, cin_g, cout_g, split, half, n;
     DPackEntry e[kDirMaxPack];
 };
 
@@ -800,7 +812,7 @@ __global__ void pack_direct_kernel(const __grid_constant__ DPackParams Q) {
             if (ci < Q.Cin && co < Q.Cout && ci / Q.cin_g == co / Q.cout_g)
                 v[q] = Q.w[((int64_t)ci * Q.cout_g + co % Q.cout_g) * Q.k3 + E.widx];
         }
-        uint32_t h = bf16x2_rn(v[0], v[1]);
+        uint32_t h = Q.half ? f16x2_rn(v[0], v[1]) : bf16x2_rn(v[0], v[1]);
         if (E.lo) {
             const float h0 = __uint_as_float(h << 16), h1 = __uint_as_float(h & 0xFFFF0000u);
             h = bf16x2_rn(v[0] - h0, v[1] - h1);
@@ -838,6 +850,7 @@ bool direct_pack_table(const convt3d_plan_s &p, const DirectParams &P, DPackPara
     Q.cin_g = p.g.Cin / p.g.G;
     Q.cout_g = p.g.Cout / p.g.G;
     Q.split = p.planes == 2;
+    Q.half = p.half;
     return true;
 }
 
@@ -867,11 +880,13 @@ cudaError_t direct_prepare(convt3d_plan_s &p, DirectCache *&out) {
     if (!direct_geometry(p, P)) return cudaErrorInvalidConfiguration;
     if (!direct_pack_table(p, P, dc.Q)) return cudaErrorInvalidConfiguration;
     const bool split = p.planes == 2;
-    if (p.d.epilogue == CONVT3D_EPI_SOFTMAX_SIGMOID)
-        dc.kern = split ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 3>
-                        : convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2>;
+    const bool sm = p.d.epilogue == CONVT3D_EPI_SOFTMAX_SIGMOID;
+    if (split)
+        dc.kern = sm ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 3> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 3>;
+    else if (p.half)
+        dc.kern = sm ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 4> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 4>;
     else
-        dc.kern = split ? convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 3> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 2>;
+        dc.kern = sm ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 2>;
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, dc.kern)) != cudaSuccess) return e;
     dc.smem = 1024 + (size_t)P.stages * P.stage_bytes + (size_t)P.slabs * P.slab_stride;
