@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import workloads as E
-from test_parity_gpu import TOL, assert_close, rounded_inputs, run_gpu, run_oracle
+from test_parity_gpu import TOL, TOL_LOW_VS_FP32, assert_close, rounded_inputs, run_gpu, run_oracle
 from transposed_convolution_convt3d_gb300 import PREC_3XBF16, PREC_BF16, PREC_FP16, Plan
 
 DIRECT = [
@@ -81,6 +81,21 @@ def test_direct_fp16(spec):
     inputs = E.make_inputs(spec)
     got = run_gpu(spec, inputs, PREC_FP16)
     assert_close(got, run_oracle(spec, rounded_inputs(inputs, PREC_FP16)), spec.name, TOL)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["bf16", "fp16"])
+@pytest.mark.parametrize("spec", DIRECT[:4] + DIRECT[6:8], ids=lambda s: s.name)
+def test_direct_16bit_tensors(spec, kind):
+    """x, w and y as 16-bit arrays in the operands' format (BF16 / FP16 precision): the slab
+    holds the operands and y is rounded once more on the way out, so the oracle on
+    identically rounded x and w is matched within the 1e-2 tier."""
+    s = spec.replace(name=spec.name + "_io" + kind, io_bf16=kind == "bf16", io_fp16=kind == "fp16")
+    prec = PREC_BF16 if kind == "bf16" else PREC_FP16
+    assert main_kernel(s, prec) == 2
+    inputs = E.make_inputs(s)
+    got = run_gpu(s, inputs, prec)
+    assert_close(got, run_oracle(s, rounded_inputs(inputs, prec)), s.name, TOL_LOW_VS_FP32)
 
 
 @pytest.mark.gpu

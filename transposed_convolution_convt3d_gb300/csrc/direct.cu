@@ -107,7 +107,8 @@ struct DirectParams {
     int N, Cout, cout_pad, Din, Do, Ho, Wo, sd, sh, sw;
     int Qw, TH;         // q-grid width, q rows per tile (TH * Qw = 128)
     int qw_shift;       // log2(Qw)
-    int w_lo, wfp, hfp; // slab: first w (a multiple of 4), width, height
+    int w_lo, wfp, hfp; // slab: first w and width (16-byte multiples), height
+    int io16;           // y's 16-bit kind (kBF16 / kF16) when x and y are 16-bit arrays, else 0
     int ngroups, tiles_per_sample, total_tiles;
     FastDiv div_tps;
     int stages, slabs;
@@ -196,8 +197,9 @@ __device__ __forceinline__ uint32_t f16x2_rn(float lo_elem, float hi_elem) {
 
 // EPI: CONVT3D_EPI_SOFTMAX_SIGMOID or CONVT3D_EPI_IDENTITY.  OPS: 2 = BF16 (one product
 // of bf16-rounded operands), 3 = split BF16 (three products), 4 = FP16 (one product of
-// fp16-rounded operands).
-template <int EPI, int OPS>
+// fp16-rounded operands).  X16: x and y are 16-bit arrays of the operands' own format (BF16
+// or FP16 only): the slab already holds the operands, so the converter only re-lays it.
+template <int EPI, int OPS, bool X16>
 __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __grid_constant__ DirectParams P) {
     constexpr int kPlanes = OPS == 3 ? 2 : 1;
     extern __shared__ __align__(1024) uint8_t dsmem_raw[];
@@ -400,7 +402,7 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
     // ---------------------------------------------------------- converters
     else if (warp < 2 + kDirConvWarps) {
         const int tid = (warp - 2) * 32 + lane;             // 0..kDirConvThreads-1
-        const uint32_t plane = (uint32_t)(P.hfp * P.wfp);  // floats between channels in a slab
+        const uint32_t plane = (uint32_t)(P.hfp * P.wfp);  // elements between channels in a slab
         int st = 0, sl = 0;
         uint32_t sph = 0, lph = 0;
         bool ok = true;
@@ -427,11 +429,19 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                 }
                 for (; mi < G.nm;) {
                     const int hp = r >> P.qw_shift, wq = r & (P.Qw - 1);
-                    const float *src = slab + hp * P.wfp + (wq + G.mdw[mi] - P.w_lo);
+                    const int at = hp * P.wfp + (wq + G.mdw[mi] - P.w_lo);
+                    uint32_t hi[16], lo[16];
+                    if constexpr (X16) {
+                        // the slab holds the operands: 16-bit channel pairs packed as they are
+                        const uint16_t *src = reinterpret_cast<const uint16_t *>(slab) + at;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            hi[k] = (uint32_t)src[(2 * k) * plane] | ((uint32_t)src[(2 * k + 1) * plane] << 16);
+                    } else {
+                    const float *src = slab + at;
                     float v[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) v[c] = src[c * plane];
-                    uint32_t hi[16], lo[16];
                     const uint64_t neg1 = pack2(-1.f, -1.f);
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
@@ -443,6 +453,7 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
                             unpack2(ffma2(h2, neg1, pack2(v[2 * k], v[2 * k + 1])), r0, r1);
                             lo[k] = bf16x2_rn(r0, r1);
                         }
+                    }
                     }
                     // 64-byte swizzle: 16-byte chunk j of row r lands at j ^ ((r >> 1) & 3)
                     uint8_t *row = stage + (size_t)mi * kPlanes * P.buf_bytes + (size_t)r * kDirRowBytes;
@@ -523,6 +534,22 @@ __global__ void __launch_bounds__(kDirThreads, 1) convt3d_direct_gemm(const __gr
             const bool full = C == P.cout_pad;  // no ragged last chunk
             // 16 channels c0.. of the row: class 0 in a, class 1 in b
             auto store16 = [&](int c0, const float (&a)[16], const float (&b)[16]) {
+                if constexpr (X16) {  // 16-bit y: the pair as one 4-byte store
+                    uint16_t *d16 = reinterpret_cast<uint16_t *>(P.y) + (size_t)T.n * C * V + off0;
+                    if (full && valid1 && pairs) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            *reinterpret_cast<uint32_t *>(d16 + (size_t)(c0 + i) * V) = cvt16x2(a[i], b[i], P.io16);
+                        return;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (c0 + i >= C) break;
+                        if (valid0) d16[(size_t)(c0 + i) * V] = cvt16(a[i], P.io16);
+                        if (valid1) d16[(size_t)(c0 + i) * V + 1] = cvt16(b[i], P.io16);
+                    }
+                    return;
+                }
                 if (full && valid1 && pairs) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -651,17 +678,20 @@ EncodeTiledFn encode_tiled(cudaError_t &err) {
     return fn;
 }
 
-int floor4(int v) { return v >= 0 ? v / 4 * 4 : -((-v + 3) / 4 * 4); }
-
 // The kernel's tables and slab geometry for a plan, or false when the plan is
 // outside what the kernel handles.
 bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
     const Geometry &g = p.g;
     const int epi = p.d.epilogue;
-    if (!p.tc || !p.merged || p.cl || p.io16 != kF32 || !p.bf16 || p.nslices != 1) return false;
+    // 16-bit x and y only with the single-product precision of their own format (the plan's
+    // validation pairs io_bf16 with BF16 and io_fp16 with FP16)
+    if (!p.tc || !p.merged || p.cl || !p.bf16 || p.nslices != 1 || (p.io16 != kF32 && p.planes != 1)) return false;
     if (epi != CONVT3D_EPI_SOFTMAX_SIGMOID && epi != CONVT3D_EPI_IDENTITY) return false;
-    if (g.Cin > kDirK || g.Win % 4 != 0 || p.cout_pad > 64 || p.ngroups > kDirGroups) return false;
+    const int eb = p.io16 != kF32 ? 2 : 4;  // bytes per element of x
+    const int al = 16 / eb;                  // elements per 16 bytes: TMA strides and x-coordinates
+    if (g.Cin > kDirK || g.Win % al != 0 || p.cout_pad > 64 || p.ngroups > kDirGroups) return false;
     memset(&P, 0, sizeof(P));
+    P.io16 = p.io16;
     P.N = g.N;
     P.Cout = g.Cout;
     P.cout_pad = p.cout_pad;
@@ -739,11 +769,11 @@ bool direct_geometry(const convt3d_plan_s &p, DirectParams &P) {
         G.tile_prefix = prefix;
         prefix += G.tiles;
     }
-    P.w_lo = floor4(dw_min);
-    P.wfp = (P.Qw + dw_max - P.w_lo + 3) / 4 * 4;
+    P.w_lo = dw_min >= 0 ? dw_min / al * al : -((-dw_min + al - 1) / al * al);
+    P.wfp = (P.Qw + dw_max - P.w_lo + al - 1) / al * al;
     P.hfp = P.TH + span_h;
     if (P.wfp > 256 || P.hfp > 256) return false;
-    P.slab_bytes = (uint32_t)(P.wfp * P.hfp * kDirK * 4);
+    P.slab_bytes = (uint32_t)(P.wfp * P.hfp * kDirK * eb);
     P.slab_stride = (P.slab_bytes + 127u) / 128u * 128u;
     P.wdir_bytes = woff;
     P.tiles_per_sample = prefix;
@@ -786,7 +816,7 @@ constexpr int kDirMaxPack = 1024;
 struct DPackParams {
     const float *w;
     uint8_t *dst;
-    int Cin, Cout, k3, cout_pad, cin_g, cout_g, split, half, n;
+    int Cin, Cout, k3, cout_pad, cin_g, cout_g, split, half, w16, n;
     DPackEntry e[kDirMaxPack];
 };
 
@@ -810,7 +840,10 @@ __global__ void pack_direct_kernel(const __grid_constant__ DPackParams Q) {
             const int ci = 8 * jc + e + q;
             v[q] = 0.f;
             if (ci < Q.Cin && co < Q.Cout && ci / Q.cin_g == co / Q.cout_g)
-                v[q] = Q.w[((int64_t)ci * Q.cout_g + co % Q.cout_g) * Q.k3 + E.widx];
+            {
+                const int64_t src = ((int64_t)ci * Q.cout_g + co % Q.cout_g) * Q.k3 + E.widx;
+                v[q] = Q.w16 ? ld16(Q.w, src, Q.w16) : Q.w[src];
+            }
         }
         uint32_t h = Q.half ? f16x2_rn(v[0], v[1]) : bf16x2_rn(v[0], v[1]);
         if (E.lo) {
@@ -851,6 +884,7 @@ bool direct_pack_table(const convt3d_plan_s &p, const DirectParams &P, DPackPara
     Q.cout_g = p.g.Cout / p.g.G;
     Q.split = p.planes == 2;
     Q.half = p.half;
+    Q.w16 = p.io16;
     return true;
 }
 
@@ -880,13 +914,16 @@ cudaError_t direct_prepare(convt3d_plan_s &p, DirectCache *&out) {
     if (!direct_geometry(p, P)) return cudaErrorInvalidConfiguration;
     if (!direct_pack_table(p, P, dc.Q)) return cudaErrorInvalidConfiguration;
     const bool split = p.planes == 2;
-    const bool sm = p.d.epilogue == CONVT3D_EPI_SOFTMAX_SIGMOID;
+    const bool sm = p.d.epilogue == CONVT3D_EPI_SOFTMAX_SIGMOID, x16 = p.io16 != kF32;
+    constexpr int SM = CONVT3D_EPI_SOFTMAX_SIGMOID, ID = CONVT3D_EPI_IDENTITY;
     if (split)
-        dc.kern = sm ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 3> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 3>;
+        dc.kern = sm ? convt3d_direct_gemm<SM, 3, false> : convt3d_direct_gemm<ID, 3, false>;
     else if (p.half)
-        dc.kern = sm ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 4> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 4>;
+        dc.kern = x16 ? (sm ? convt3d_direct_gemm<SM, 4, true> : convt3d_direct_gemm<ID, 4, true>)
+                      : (sm ? convt3d_direct_gemm<SM, 4, false> : convt3d_direct_gemm<ID, 4, false>);
     else
-        dc.kern = sm ? convt3d_direct_gemm<CONVT3D_EPI_SOFTMAX_SIGMOID, 2> : convt3d_direct_gemm<CONVT3D_EPI_IDENTITY, 2>;
+        dc.kern = x16 ? (sm ? convt3d_direct_gemm<SM, 2, true> : convt3d_direct_gemm<ID, 2, true>)
+                      : (sm ? convt3d_direct_gemm<SM, 2, false> : convt3d_direct_gemm<ID, 2, false>);
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, dc.kern)) != cudaSuccess) return e;
     dc.smem = 1024 + (size_t)P.stages * P.stage_bytes + (size_t)P.slabs * P.slab_stride;
@@ -946,14 +983,19 @@ cudaError_t launch_direct(convt3d_plan_s &p, const float *x, const void *wdir, c
         EncodeTiledFn enc = encode_tiled(ferr);
         if (!enc) return ferr != cudaSuccess ? ferr : cudaErrorNotSupported;
         const Geometry &g = p.g;
-        // x: fp32 NCDHW, box = one slab (all 32 channel planes of the tile's rows and halo)
+        // x: NCDHW (fp32, or the 16-bit operand format), box = one slab (all 32 channel planes of
+        // the tile's rows and halo)
         const cuuint64_t xdim[5] = {(cuuint64_t)g.Win, (cuuint64_t)g.Hin, (cuuint64_t)g.Din, (cuuint64_t)g.Cin,
                                     (cuuint64_t)g.N};
-        const cuuint64_t xstr[4] = {(cuuint64_t)g.Win * 4, (cuuint64_t)g.Win * g.Hin * 4,
-                                    (cuuint64_t)g.Win * g.Hin * g.Din * 4, (cuuint64_t)g.Win * g.Hin * g.Din * g.Cin * 4};
+        const cuuint64_t eb = p.io16 != kF32 ? 2 : 4;
+        const cuuint64_t xstr[4] = {(cuuint64_t)g.Win * eb, (cuuint64_t)g.Win * g.Hin * eb,
+                                    (cuuint64_t)g.Win * g.Hin * g.Din * eb, (cuuint64_t)g.Win * g.Hin * g.Din * g.Cin * eb};
         const cuuint32_t xbox[5] = {(cuuint32_t)P.wfp, (cuuint32_t)P.hfp, 1, (cuuint32_t)kDirK, 1};
         const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-        if (enc(&P.x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, (void *)x, xdim, xstr, xbox, es,
+        const CUtensorMapDataType xdt = p.io16 == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : p.io16 == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        if (enc(&P.x_map, xdt, 5, (void *)x, xdim, xstr, xbox, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;

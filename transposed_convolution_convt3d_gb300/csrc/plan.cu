@@ -500,13 +500,14 @@ convt3d_status_t convt3d_plan_info(convt3d_plan_t p, convt3d_info_t *info) {
         issued += 2.0 * (double)d.N * p->tile_m * p->cout_pad * (double)p->cin_pad * taps;
     }
     info->issued_mma_flop = issued * (p->planes == 2 ? 3.0 : 1.0);
-    const double xbytes = 4.0 * d.N * d.Cin * (double)d.Din * d.Hin * d.Win;
-    const double wbytes = 4.0 * d.Cin * (d.Cout / g.G) * (double)g.kvol;
-    const double ybytes = 4.0 * d.N * d.Cout * (double)g.Do * g.Ho * g.Wo;
-    const double out_bytes = (bn || ev) ? 4.0 * d.N * d.Cout : ybytes;
+    const double eb = p->io16 != kF32 ? 2.0 : 4.0;  // bytes per element of x, w and y at the boundary
+    const double xbytes = eb * d.N * d.Cin * (double)d.Din * d.Hin * d.Win;
+    const double wbytes = eb * d.Cin * (d.Cout / g.G) * (double)g.kvol;
+    const double ybytes = eb * d.N * d.Cout * (double)g.Do * g.Ho * g.Wo;
+    const double out_bytes = (bn || ev) ? eb * d.N * d.Cout : ybytes;
     // Main kernel: reads x (tensor-core path: the staged hi+lo copy; the direct kernel: x itself) and the packed weights once,
     // writes the output once (BN+pool: nothing but partials).
-    const double planes = (p->planes == 2 ? 2.0 : 1.0) * p->elem_bytes / 4.0;  // staged operand bytes / fp32 bytes
+    const double planes = (p->planes == 2 ? 2.0 : 1.0) * p->elem_bytes / eb;  // staged operand bytes / boundary bytes
     info->gemm_min_bytes = (p->direct ? xbytes : planes * xbytes) + planes * wbytes + (bn ? 0.0 : ybytes);
     // Whole forward as the pages define it: x and w in, the output out, plus the second pass
     // over y that GroupNorm's global statistics force.
