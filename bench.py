@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the CPU baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunks", type=int, default=4, help="sample chunks the end-to-end pipeline overlaps")
+    ap.add_argument("--e2e-chunks", type=int, default=8, help="sample chunks the end-to-end pipeline overlaps")
     ap.add_argument("--io-bf16", action="store_true",
                     help="x, w and y as bf16 tensors (requires --precision bf16)")
     ap.add_argument("--io-fp16", action="store_true",

@@ -219,6 +219,31 @@ convt3d_status_t convt3d_forward(convt3d_plan_t plan, const void *x, const float
                                  const float *gamma, const float *beta, void *y,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
+/* convt3d_forward in two parts, so that the main kernel can start on the first
+ * samples of a batch while later ones are still being copied in.  No
+ * counterpart on the pages: a scheduling convenience; the results are those
+ * of convt3d_forward, bit for bit.
+ *
+ * convt3d_forward_samples runs the per-sample work for samples [n0, n1) of
+ * the plan's batch: x and y are the WHOLE batch's tensors (sample n at its
+ * usual offset), only samples n0..n1-1 of x are read and only those of y
+ * (or of the per-tile statistics in the workspace) are written.  After calls
+ * that together cover 0..N-1 once each, convt3d_forward_finish runs the passes
+ * over the whole batch (GroupNorm's normalisation; BatchNorm's statistics,
+ * pooled output and running-statistics update; nothing for IDENTITY and
+ * SOFTMAX_SIGMOID) and y is then that of one convt3d_forward.  Ranges may go on
+ * different streams when the caller orders each one before the finish call.
+ * Errors: INVALID_ARG unless 0 <= n0 < n1 <= N, and as for convt3d_forward;
+ * UNSUPPORTED for SCALE_BATCHNORM_EVAL_AVGPOOL (one pass over the batch) and,
+ * unless [n0, n1) is the whole batch, for plans whose main kernel reads x
+ * directly (convt3d_info_t.main_kernel 2).  gamma/beta as for convt3d_forward. */
+convt3d_status_t convt3d_forward_samples(convt3d_plan_t plan, const void *x, const float *bias, void *y,
+                                         void *workspace, size_t workspace_bytes, int n0, int n1,
+                                         void *stream);
+convt3d_status_t convt3d_forward_finish(convt3d_plan_t plan, const float *bias, const float *gamma,
+                                        const float *beta, void *y, void *workspace, size_t workspace_bytes,
+                                        void *stream);
+
 /* BatchNorm running statistics, device pointers to Cout floats each (page
  * l2_p77: nn.BatchNorm3d with momentum 0.1, eps 1e-5).  With
  * SCALE_BATCHNORM_AVGPOOL, every later forward updates them in place from the

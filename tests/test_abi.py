@@ -277,6 +277,37 @@ def test_groupnorm_requires_affine(lib):
         lib.convt3d_plan_destroy(h)
 
 
+def test_sample_range_validation(lib):
+    """convt3d_forward_samples / convt3d_forward_finish: the range and the epilogue
+    are checked on the host before anything else; a valid range then stops at the
+    unpacked workspace, as convt3d_forward does."""
+    V = ctypes.c_void_p
+    st, h = create(lib, N=4, epilogue=2, has_bias=1)  # training-mode BatchNorm
+    assert st == 0
+    try:
+        rng = lambda n0, n1: lib.convt3d_forward_samples(h, V(1 << 20), V(1 << 23), V(1 << 21), V(1 << 22),  # noqa
+                                                         1 << 30, n0, n1, None)
+        for n0, n1 in ((-1, 2), (0, 5), (2, 2), (3, 1)):
+            assert rng(n0, n1) == 1, (n0, n1)
+        assert rng(1, 3) == 7
+        assert lib.convt3d_forward_samples(h, None, None, V(1 << 21), V(1 << 22), 1 << 30, 0, 4, None) == 1
+        # finish needs gamma and beta for BatchNorm
+        assert lib.convt3d_forward_finish(h, V(1 << 23), None, None, V(1 << 21), V(1 << 22), 1 << 30, None) == 1
+        assert lib.convt3d_forward_finish(h, V(1 << 23), V(1 << 24), V(1 << 25), V(1 << 21), V(1 << 22),
+                                          1 << 30, None) == 7
+    finally:
+        lib.convt3d_plan_destroy(h)
+    st, h = create(lib, N=4, epilogue=4, has_bias=1)  # evaluation-mode BatchNorm: one pass over the batch
+    assert st == 0
+    try:
+        assert lib.convt3d_forward_samples(h, V(1 << 20), V(1 << 23), V(1 << 21), V(1 << 22), 1 << 30, 0, 4,
+                                           None) == 2
+        assert lib.convt3d_forward_finish(h, V(1 << 23), V(1 << 24), V(1 << 25), V(1 << 21), V(1 << 22),
+                                          1 << 30, None) == 2
+    finally:
+        lib.convt3d_plan_destroy(h)
+
+
 def test_running_stats_validation_and_eval_requirement(lib):
     st, h = create(lib, epilogue=4, has_bias=1)
     assert st == 0

@@ -42,6 +42,7 @@ EXPORTS = [
     "convt3d_workspace_bytes", "convt3d_pack_weights", "convt3d_forward", "convt3d_check",
     "convt3d_profile_enable", "convt3d_profile_read", "convt3d_status_string", "convt3d_last_error",
     "convt3d_version", "convt3d_forward_static_workspace", "convt3d_set_running_stats",
+    "convt3d_forward_samples", "convt3d_forward_finish",
 ]
 
 
@@ -123,6 +124,10 @@ def load(path: str | None = None):
         lib.convt3d_forward_static_workspace.argtypes = [V, V, V, V, V, V, V, V]
         lib.convt3d_set_running_stats.restype = I
         lib.convt3d_set_running_stats.argtypes = [V, V, V, ctypes.c_float]
+        lib.convt3d_forward_samples.restype = I
+        lib.convt3d_forward_samples.argtypes = [V, V, V, V, V, S, I, I, V]
+        lib.convt3d_forward_finish.restype = I
+        lib.convt3d_forward_finish.argtypes = [V, V, V, V, V, V, S, V]
         if path is None:
             _lib = lib
         return lib

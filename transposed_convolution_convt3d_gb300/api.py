@@ -111,6 +111,10 @@ class Plan:
             raise TypeError(f"{name} must be a contiguous {dtype} CUDA tensor")
         return t
 
+    def _check_y(self, y):
+        if tuple(y.shape) not in (self.out_shape, self.out_alloc_shape) and y.numel() != _numel(self.out_shape):
+            raise ValueError(f"y has shape {tuple(y.shape)}, expected {self.out_alloc_shape}")
+
     # -- library calls ---------------------------------------------------
     def pack_weights(self, w, workspace, stream=None):
         self._dev(w, "w", self.io_dtype)
@@ -122,11 +126,36 @@ class Plan:
         self._dev(y, "y", self.io_dtype)
         for t, n in ((bias, "bias"), (gamma, "gamma"), (beta, "beta")):
             self._dev(t, n)
-        if tuple(y.shape) not in (self.out_shape, self.out_alloc_shape) and y.numel() != _numel(self.out_shape):
-            raise ValueError(f"y has shape {tuple(y.shape)}, expected {self.out_alloc_shape}")
+        self._check_y(y)
         _lib.check(self.lib.convt3d_forward(self.handle, _ptr(x), _ptr(bias), _ptr(gamma), _ptr(beta),
                                             _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
                    self.lib)
+        return y
+
+    def forward_samples(self, x, y, workspace, n0, n1, bias=None, stream=None):
+        """The per-sample part of forward for samples [n0, n1) of the batch: x and y
+        are the whole batch's tensors, only those samples are read and written.
+        Calls covering every sample once, then forward_finish, give forward's y."""
+        self._dev(x, "x", self.io_dtype)
+        self._dev(y, "y", self.io_dtype)
+        self._dev(bias, "bias")
+        self._check_y(y)
+        if tuple(x.shape)[0] != self.desc.N:
+            raise ValueError(f"x must hold the whole batch of N={self.desc.N} samples")
+        _lib.check(self.lib.convt3d_forward_samples(self.handle, _ptr(x), _ptr(bias), _ptr(y), _ptr(workspace),
+                                                    workspace.numel(), int(n0), int(n1), _stream(stream)),
+                   self.lib)
+        return y
+
+    def forward_finish(self, y, workspace, bias=None, gamma=None, beta=None, stream=None):
+        """The passes over the whole batch after forward_samples (GroupNorm's
+        normalisation, BatchNorm's statistics and pooled output)."""
+        self._dev(y, "y", self.io_dtype)
+        for t, n in ((bias, "bias"), (gamma, "gamma"), (beta, "beta")):
+            self._dev(t, n)
+        self._check_y(y)
+        _lib.check(self.lib.convt3d_forward_finish(self.handle, _ptr(bias), _ptr(gamma), _ptr(beta), _ptr(y),
+                                                   _ptr(workspace), workspace.numel(), _stream(stream)), self.lib)
         return y
 
     def forward_static_workspace(self, w, x, y, bias=None, gamma=None, beta=None, stream=None):
@@ -196,10 +225,13 @@ class HostPipeline:
 
     The batch is split into chunks of samples; chunk i's host->device copy,
     chunk i-1's computation and chunk i-2's device->host copy run at once, each
-    copy split over `copy_streams` streams per direction.  Valid for the epilogues whose result for a sample depends
-    on that sample only (identity, ReLU+GroupNorm, softmax+sigmoid); the
-    BatchNorm epilogues run as one chunk (the training-mode one's batch
-    statistics need the whole batch).  Host tensors should be pinned for the copies to be asynchronous.
+    copy split over `copy_streams` streams per direction.  Epilogues whose result
+    for a sample depends on that sample only (identity, ReLU+GroupNorm,
+    softmax+sigmoid, evaluation-mode BatchNorm) run each chunk as a forward of a
+    chunk-sized plan.  Training-mode BatchNorm, whose statistics cover the whole
+    batch, runs one whole-batch plan: Plan.forward_samples on each chunk as its
+    input arrives, then Plan.forward_finish, and copies the pooled y out at the
+    end.  Host tensors should be pinned for the copies to be asynchronous.
     Device buffers, plans and streams are created once, here.
     """
 
@@ -207,13 +239,17 @@ class HostPipeline:
                  epilogue=EPI_IDENTITY, groups=1, eps=1e-5, scale=1.0, precision=PREC_3XTF32, chunks=4,
                  device="cuda", dilation=1, conv_groups=1, copy_streams=1, channels_last=False, io_bf16=False,
                  io_fp16=False):
-        if epilogue in (EPI_SCALE_BATCHNORM_AVGPOOL, EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) or N % chunks:
+        # training-mode BatchNorm: one whole-batch plan run in sample ranges
+        self.ranges = epilogue == EPI_SCALE_BATCHNORM_AVGPOOL
+        if N % chunks:
             chunks = 1
-        self.chunks = chunks
-        self.n_chunk = N // chunks
         args = (Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale, precision,
                 dilation, conv_groups, channels_last, io_bf16, io_fp16)
-        self.plan = Plan(self.n_chunk, *args)
+        self.plan = Plan(N if self.ranges else N // chunks, *args)
+        if self.ranges and self.plan.info["main_kernel"] == 2:
+            chunks = 1  # that kernel reads the whole batch in one launch
+        self.chunks = chunks
+        self.n_chunk = N // chunks
         dt = self.plan.io_dtype
         self.full_shape = (N,) + self.plan.out_alloc_shape[1:]
         dev = torch.device(device)
@@ -228,6 +264,9 @@ class HostPipeline:
         self.s_in = [torch.cuda.Stream(dev) for _ in range(self.copy_streams)]
         self.s_out = [torch.cuda.Stream(dev) for _ in range(self.copy_streams)]
         self.s_comp = torch.cuda.Stream(dev)
+        # sample ranges alternate between two compute streams, so that a range's main
+        # kernel fills the SMs that the previous range's last wave of tiles leaves idle
+        self.s_comp2 = torch.cuda.Stream(dev)
 
     def set_running_stats(self, running_mean, running_var, momentum=0.1):
         """Device-resident BatchNorm running statistics, as Plan.set_running_stats."""
@@ -237,7 +276,7 @@ class HostPipeline:
         """Run on pinned host tensors; returns y_host.  The work is ordered after
         `stream` (default: current stream) and `stream` waits for its end."""
         caller = stream if stream is not None else torch.cuda.current_stream()
-        for s in self.s_in + self.s_out + [self.s_comp]:
+        for s in self.s_in + self.s_out + [self.s_comp, self.s_comp2]:
             s.wait_stream(caller)
         nc, k = self.n_chunk, self.copy_streams
 
@@ -257,29 +296,41 @@ class HostPipeline:
                     dv[name] = self.vec[name]
                 else:
                     dv[name] = None
-        in_done = []
+        # each chunk's compute is issued right after its copy, so that the GPU can start on
+        # chunk 0 while the host is still issuing the later chunks
+        comp = (self.s_comp, self.s_comp2) if self.ranges else (self.s_comp,)
         for i in range(self.chunks):
-            evs = []
-            for j, d, s_ in pieces(self.x[i * nc:(i + 1) * nc], x_host[i * nc:(i + 1) * nc]):
+            rows = slice(i * nc, (i + 1) * nc)
+            s = comp[i % len(comp)]
+            for j, d, s_ in pieces(self.x[rows], x_host[rows]):
                 with torch.cuda.stream(self.s_in[j]):
                     d.copy_(s_, non_blocking=True)
                     ev = torch.cuda.Event()
                     ev.record(self.s_in[j])
-                    evs.append(ev)
-            in_done.append(evs)
-        for i in range(self.chunks):
-            for ev in in_done[i]:
-                self.s_comp.wait_event(ev)
+                s.wait_event(ev)
             if i == 0:
-                self.plan.pack_weights(self.w, self.ws, self.s_comp)
-            self.plan.forward(self.x[i * nc:(i + 1) * nc], self.y[i * nc:(i + 1) * nc], self.ws, dv["bias"],
-                              dv["gamma"], dv["beta"], self.s_comp)
+                self.plan.pack_weights(self.w, self.ws, s)
+                if len(comp) > 1:
+                    packed = torch.cuda.Event()
+                    packed.record(s)
+                    comp[1].wait_event(packed)
+            if self.ranges:
+                # training-mode BatchNorm: the ranges touch disjoint samples of x, y, the staged
+                # input and the per-tile statistics, so two of them may run at once on the two streams
+                self.plan.forward_samples(self.x, self.y, self.ws, rows.start, rows.stop, dv["bias"], s)
+                continue
+            self.plan.forward(self.x[rows], self.y[rows], self.ws, dv["bias"], dv["gamma"], dv["beta"], s)
             ev = torch.cuda.Event()
-            ev.record(self.s_comp)
-            for j, d, s_ in pieces(y_host[i * nc:(i + 1) * nc], self.y[i * nc:(i + 1) * nc]):
+            ev.record(s)
+            for j, d, s_ in pieces(y_host[rows], self.y[rows]):
                 self.s_out[j].wait_event(ev)
                 with torch.cuda.stream(self.s_out[j]):
                     d.copy_(s_, non_blocking=True)
-        for s in self.s_out + [self.s_comp]:
+        if self.ranges:
+            self.s_comp.wait_stream(self.s_comp2)
+            self.plan.forward_finish(self.y, self.ws, dv["bias"], dv["gamma"], dv["beta"], self.s_comp)
+            with torch.cuda.stream(self.s_comp):
+                y_host.copy_(self.y, non_blocking=True)
+        for s in self.s_out + [self.s_comp, self.s_comp2]:
             caller.wait_stream(s)
         return y_host

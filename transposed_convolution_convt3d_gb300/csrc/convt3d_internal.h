@@ -189,6 +189,7 @@ struct FfmaParams {
     int epilogue, groups;
     float scale;
     int ngroups, tiles_per_sample;
+    int tile_base;           // this launch's first tile (block b runs tile tile_base + b)
     GroupDesc grp[kMaxGroups];
     ClassDesc cls[kMaxClasses];
     TapDesc taps[kMaxTaps];
@@ -242,13 +243,14 @@ struct convt3d_plan_s {
 namespace convt3d {
 cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *hi, float *lo,
                                 int kmajor, cudaStream_t s);
-cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *hi, float *lo,
+// The per-sample launches take the samples [n0, n1) of the batch (all of it: 0, N).
+cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *hi, float *lo, int n0, int n1,
                                cudaStream_t s);
 cudaError_t launch_ffma(const convt3d_plan_s &p, const float *x, const float *wpk, const float *bias,
-                        float *y, double *partials, cudaStream_t s);
+                        float *y, double *partials, int n0, int n1, cudaStream_t s);
 cudaError_t launch_tc(convt3d_plan_s &p, const float *xs_hi, const float *xs_lo,
                       const float *w_hi, const float *w_lo, const float *bias, float *y,
-                      double *partials, uint32_t *status, cudaStream_t s);
+                      double *partials, uint32_t *status, int n0, int n1, cudaStream_t s);
 cudaError_t launch_gn_finalize(const convt3d_plan_s &p, const double *partials, double *stats,
                                cudaStream_t s);
 cudaError_t launch_gn_normalize(const convt3d_plan_s &p, const double *stats, const float *gamma,

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kThreads) ffma_conv_kernel(const __grid_consta
     __shared__ int rowoff[kBM];
 
     const int tid = threadIdx.x;
-    const TileInfo ti = decode_tile(P, blockIdx.x);
+    const TileInfo ti = decode_tile(P, P.tile_base + blockIdx.x);
     const ClassDesc &cl = P.cls[ti.cls];
     const int Qhw = cl.Qh * cl.Qw;
     const int vol = cl.Qd * Qhw;
@@ -294,7 +294,7 @@ cudaError_t launch_cpt(const FfmaParams &P, int blocks, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_ffma(const convt3d_plan_s &p, const float *x, const float *wpk, const float *bias, float *y,
-                        double *partials, cudaStream_t s) {
+                        double *partials, int n0, int n1, cudaStream_t s) {
     FfmaParams P;
     memset(&P, 0, sizeof(P));
     P.x = x; P.wpk = wpk; P.bias = bias; P.y = y; P.partials = partials;
@@ -316,7 +316,10 @@ cudaError_t launch_ffma(const convt3d_plan_s &p, const float *x, const float *wp
     for (int i = 0; i < kMaxGroups; ++i) P.grp[i] = p.grp[i];
     for (int i = 0; i < kMaxClasses; ++i) P.cls[i] = p.g.cls[i];
     for (int i = 0; i < kMaxTaps; ++i) P.taps[i] = p.g.taps[i];
-    const int blocks = (int)p.tiles;
+    // one block per tile, the tiles of samples [n0, n1) (tiles are ordered sample by sample)
+    P.tile_base = n0 * p.tiles_per_sample;
+    const int blocks = (n1 - n0) * p.tiles_per_sample;
+    if (blocks <= 0) return cudaSuccess;
     switch (p.cout_pad) {
         case 16: return launch_cpt<1>(P, blocks, s);
         case 32: return launch_cpt<2>(P, blocks, s);

@@ -229,17 +229,27 @@ cudaError_t launch_pack_weights(const convt3d_plan_s &p, const float *w, float *
 // The staged operand's 16-bit kind (0: fp32 planes).
 static int op16(const convt3d_plan_s &p) { return p.bf16 ? (p.half ? kF16 : kBF16) : kF32; }
 
-cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *hi, float *lo, cudaStream_t s) {
+cudaError_t launch_stage_input(const convt3d_plan_s &p, const float *x, float *hi, float *lo, int n0, int n1,
+                               cudaStream_t s) {
+    // samples [n0, n1): the kernels see the batch from sample n0 on (x and the planes offset by
+    // whole samples; element offsets in units of each array's element)
     const int64_t S = (int64_t)p.g.Din * p.g.Hin * p.g.Win;
+    const int nn = n1 - n0;
+    if (nn <= 0) return cudaSuccess;
+    const int64_t xoff = (int64_t)n0 * p.g.Cin * S * (p.io16 ? 2 : 4);                 // bytes
+    const int64_t poff = (int64_t)n0 * S * p.cin_pad * (op16(p) ? 2 : 4);              // bytes
+    const float *xn = reinterpret_cast<const float *>(reinterpret_cast<const char *>(x) + xoff);
+    float *hn = reinterpret_cast<float *>(reinterpret_cast<char *>(hi) + poff);
+    float *ln = lo ? reinterpret_cast<float *>(reinterpret_cast<char *>(lo) + poff) : nullptr;
     if (p.cl) {
-        const int64_t rows = S * p.g.N;
+        const int64_t rows = S * nn;
         dim3 grid((unsigned)((rows + 7) / 8), (unsigned)(p.cin_pad / 32));
-        stage_input_cl_kernel<<<grid, dim3(32, 8), 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, rows, op16(p), p.io16);
+        stage_input_cl_kernel<<<grid, dim3(32, 8), 0, s>>>(xn, hn, ln, p.g.Cin, p.cin_pad, rows, op16(p), p.io16);
         return cudaGetLastError();
     }
-    dim3 grid((unsigned)((S + 31) / 32), (unsigned)(p.cin_pad / 32), (unsigned)p.g.N);
+    dim3 grid((unsigned)((S + 31) / 32), (unsigned)(p.cin_pad / 32), (unsigned)nn);
     dim3 block(32, 8);
-    stage_input_kernel<<<grid, block, 0, s>>>(x, hi, lo, p.g.Cin, p.cin_pad, S, op16(p), p.io16);
+    stage_input_kernel<<<grid, block, 0, s>>>(xn, hn, ln, p.g.Cin, p.cin_pad, S, op16(p), p.io16);
     return cudaGetLastError();
 }
 

@@ -551,44 +551,34 @@ convt3d_status_t convt3d_pack_weights(convt3d_plan_t p, const void *wv, void *ws
     return CONVT3D_OK;
 }
 
-convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *bias, const float *gamma,
-                                 const float *beta, void *yv, void *ws, size_t ws_bytes, void *stream) {
-    g_last_error[0] = 0;
-    // 16-bit data when io_bf16 / io_fp16: the kernels reinterpret these pointers
-    const float *x = static_cast<const float *>(xv);
-    float *y = static_cast<float *>(yv);
-    if (!p || !x || !y) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan, x or y");
+}  // extern "C"
+
+namespace {
+
+// Argument checks shared by the forward entry points; `affine`: gamma and beta are read.
+convt3d_status_t forward_checks(convt3d_plan_t p, const void *x, const float *bias, const float *gamma,
+                                const float *beta, const void *y, void *ws, size_t ws_bytes, bool affine) {
+    if (!p || !y) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan or y");
     const convt3d_desc_t &d = p->d;
     if (d.has_bias && !bias) return fail(CONVT3D_ERR_INVALID_ARG, "has_bias set but bias is NULL");
-    const bool gn = d.epilogue == CONVT3D_EPI_RELU_GROUPNORM;
-    const bool bn = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL;
-    const bool ev = d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
-    if ((gn || bn || ev) && (!gamma || !beta)) return fail(CONVT3D_ERR_INVALID_ARG, "gamma and beta are required");
-    if (ev && (!p->run_mean || !p->run_var))
-        return fail(CONVT3D_ERR_INVALID_ARG, "evaluation-mode BatchNorm needs convt3d_set_running_stats");
-    for (const void *ptr : {(const void *)x, (const void *)y, (const void *)bias, (const void *)gamma,
-                            (const void *)beta})
+    const bool norm = d.epilogue == CONVT3D_EPI_RELU_GROUPNORM || d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL ||
+                      d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL;
+    if (affine && norm && (!gamma || !beta)) return fail(CONVT3D_ERR_INVALID_ARG, "gamma and beta are required");
+    for (const void *ptr : {x, y, (const void *)bias, (const void *)gamma, (const void *)beta})
         if ((uintptr_t)ptr % 16) return fail(CONVT3D_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
-    if ((const void *)x == (const void *)y) return fail(CONVT3D_ERR_INVALID_ARG, "y must not alias x");
+    if (x && x == y) return fail(CONVT3D_ERR_INVALID_ARG, "y must not alias x");
     convt3d_status_t st = check_ws(p, ws, ws_bytes);
     if (st) return st;
     if (p->packed_ws != ws) return fail(CONVT3D_ERR_NOT_PACKED, "call convt3d_pack_weights on this workspace first");
-    cudaStream_t s = (cudaStream_t)stream;
-    char *base = (char *)ws;
-    const float *b = d.has_bias ? bias : nullptr;
-    double *partials = (double *)(base + p->off_partials);
-    double *stats = (double *)(base + p->off_stats);
-    cudaError_t e;
+    return CONVT3D_OK;
+}
 
-    if (ev) {
-        // no convolution: input box sums and a contraction with the packed weight
-        e = launch_bn_eval(*p, x, (const float *)(base + p->off_wpk_hi),
-                           p->planes == 2 ? (const float *)(base + p->off_wpk_lo) : nullptr, b, gamma, beta,
-                           (float *)(base + p->off_box), (double *)(base + p->off_evpart),
-                           (unsigned *)(base + p->off_evcnt), y, s);
-        if (e != cudaSuccess) return cuda_fail(e, "evaluation-mode batchnorm launch");
-        return CONVT3D_OK;
-    }
+// The per-sample part of the forward for samples [n0, n1): input staging and the main
+// kernel with its fused epilogue (statistics partials land in per-tile slots).
+convt3d_status_t forward_main(convt3d_plan_t p, const float *x, const float *b, float *y, char *base, int n0, int n1,
+                              cudaStream_t s) {
+    cudaError_t e;
+    double *partials = (double *)(base + p->off_partials);
     if (p->prof_enabled) {
         if (!p->ev_created) {
             if ((e = cudaEventCreate(&p->ev0)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
@@ -603,31 +593,102 @@ convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *
     } else if (p->tc) {
         const bool two = p->planes == 2;
         float *xs_hi = (float *)(base + p->off_xs_hi), *xs_lo = two ? (float *)(base + p->off_xs_lo) : nullptr;
-        e = launch_stage_input(*p, x, xs_hi, xs_lo, s);
+        e = launch_stage_input(*p, x, xs_hi, xs_lo, n0, n1, s);
         if (e != cudaSuccess) return cuda_fail(e, "stage_input launch");
         if (p->prof_enabled && (e = cudaEventRecord(p->ev0, s)) != cudaSuccess) return cuda_fail(e, "event");
         e = launch_tc(*p, xs_hi, xs_lo, (const float *)(base + p->off_wpk_hi),
-                      two ? (const float *)(base + p->off_wpk_lo) : nullptr, b, y, partials, (uint32_t *)base, s);
+                      two ? (const float *)(base + p->off_wpk_lo) : nullptr, b, y, partials, (uint32_t *)base, n0, n1,
+                      s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
     } else {
         if (p->prof_enabled && (e = cudaEventRecord(p->ev0, s)) != cudaSuccess) return cuda_fail(e, "event");
-        e = launch_ffma(*p, x, (const float *)(base + p->off_wpk_hi), b, y, partials, s);
+        e = launch_ffma(*p, x, (const float *)(base + p->off_wpk_hi), b, y, partials, n0, n1, s);
         if (e != cudaSuccess) return cuda_fail(e, "FFMA GEMM launch");
     }
     if (p->prof_enabled) {
         if ((e = cudaEventRecord(p->ev1, s)) != cudaSuccess) return cuda_fail(e, "event");
         p->prof_valid = 1;
     }
-    if (gn) {
+    return CONVT3D_OK;
+}
+
+// The passes over the whole batch: GroupNorm's statistics and normalise pass, BatchNorm's
+// statistics, pooled output and running statistics (nothing for the other epilogues).
+convt3d_status_t forward_post(convt3d_plan_t p, const float *b, const float *gamma, const float *beta, float *y,
+                              char *base, cudaStream_t s) {
+    cudaError_t e;
+    double *partials = (double *)(base + p->off_partials);
+    double *stats = (double *)(base + p->off_stats);
+    if (p->d.epilogue == CONVT3D_EPI_RELU_GROUPNORM) {
         e = launch_gn_finalize(*p, partials, stats, s);
         if (e != cudaSuccess) return cuda_fail(e, "groupnorm finalize launch");
         e = launch_gn_normalize(*p, stats, gamma, beta, b, y, s);
         if (e != cudaSuccess) return cuda_fail(e, "groupnorm normalize launch");
-    } else if (bn) {
+    } else if (p->d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_AVGPOOL) {
         e = launch_bn_finalize(*p, partials, stats, gamma, beta, y, s);
         if (e != cudaSuccess) return cuda_fail(e, "batchnorm finalize launch");
     }
     return CONVT3D_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+convt3d_status_t convt3d_forward(convt3d_plan_t p, const void *xv, const float *bias, const float *gamma,
+                                 const float *beta, void *yv, void *ws, size_t ws_bytes, void *stream) {
+    g_last_error[0] = 0;
+    // 16-bit data when io_bf16 / io_fp16: the kernels reinterpret these pointers
+    const float *x = static_cast<const float *>(xv);
+    float *y = static_cast<float *>(yv);
+    if (!p || !x) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan or x");
+    const convt3d_desc_t &d = p->d;
+    if (d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL && (!p->run_mean || !p->run_var))
+        return fail(CONVT3D_ERR_INVALID_ARG, "evaluation-mode BatchNorm needs convt3d_set_running_stats");
+    convt3d_status_t st = forward_checks(p, x, bias, gamma, beta, y, ws, ws_bytes, true);
+    if (st) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *base = (char *)ws;
+    const float *b = d.has_bias ? bias : nullptr;
+    if (d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL) {
+        // no convolution: input box sums and a contraction with the packed weight
+        cudaError_t e = launch_bn_eval(*p, x, (const float *)(base + p->off_wpk_hi),
+                                       p->planes == 2 ? (const float *)(base + p->off_wpk_lo) : nullptr, b, gamma, beta,
+                                       (float *)(base + p->off_box), (double *)(base + p->off_evpart),
+                                       (unsigned *)(base + p->off_evcnt), y, s);
+        if (e != cudaSuccess) return cuda_fail(e, "evaluation-mode batchnorm launch");
+        return CONVT3D_OK;
+    }
+    st = forward_main(p, x, b, y, base, 0, d.N, s);
+    if (st) return st;
+    return forward_post(p, b, gamma, beta, y, base, s);
+}
+
+convt3d_status_t convt3d_forward_samples(convt3d_plan_t p, const void *xv, const float *bias, void *yv, void *ws,
+                                         size_t ws_bytes, int n0, int n1, void *stream) {
+    g_last_error[0] = 0;
+    const float *x = static_cast<const float *>(xv);
+    float *y = static_cast<float *>(yv);
+    if (!p || !x) return fail(CONVT3D_ERR_INVALID_ARG, "NULL plan or x");
+    if (n0 < 0 || n1 > p->d.N || n0 >= n1) return fail(CONVT3D_ERR_INVALID_ARG, "need 0 <= n0 < n1 <= N");
+    if (p->d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
+        return fail(CONVT3D_ERR_UNSUPPORTED, "evaluation-mode BatchNorm runs as one convt3d_forward");
+    if (p->direct && (n0 != 0 || n1 != p->d.N))
+        return fail(CONVT3D_ERR_UNSUPPORTED, "this plan's main kernel (main_kernel 2) runs the whole batch at once");
+    convt3d_status_t st = forward_checks(p, x, bias, nullptr, nullptr, y, ws, ws_bytes, false);
+    if (st) return st;
+    return forward_main(p, x, p->d.has_bias ? bias : nullptr, y, (char *)ws, n0, n1, (cudaStream_t)stream);
+}
+
+convt3d_status_t convt3d_forward_finish(convt3d_plan_t p, const float *bias, const float *gamma, const float *beta,
+                                        void *yv, void *ws, size_t ws_bytes, void *stream) {
+    g_last_error[0] = 0;
+    float *y = static_cast<float *>(yv);
+    if (p && p->d.epilogue == CONVT3D_EPI_SCALE_BATCHNORM_EVAL_AVGPOOL)
+        return fail(CONVT3D_ERR_UNSUPPORTED, "evaluation-mode BatchNorm runs as one convt3d_forward");
+    convt3d_status_t st = forward_checks(p, nullptr, bias, gamma, beta, y, ws, ws_bytes, true);
+    if (st) return st;
+    return forward_post(p, p->d.has_bias ? bias : nullptr, gamma, beta, y, (char *)ws, (cudaStream_t)stream);
 }
 
 convt3d_status_t convt3d_check(convt3d_plan_t p, void *ws, void *stream) {

@@ -119,6 +119,7 @@ struct TcParams {
     int epilogue, groups;
     float scale;
     int ngroups, tiles_per_sample, total_tiles;
+    int tile_begin, tile_end;  // this launch's tiles (a range of whole samples; all of them by default)
     FastDiv div_tps;  // division by tiles_per_sample
     int stages;
     uint32_t stage_bytes, b_bytes;
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     }
                 }
             };
-            for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+            for (int tile = P.tile_begin + blockIdx.x; ok && tile < P.tile_end; tile += gridDim.x) {
                 const Tile T = decode(P, s_grp, tile);
                 const GroupDesc &G = s_grp[T.gi];
                 const int q0 = T.t * kTcTileM;
@@ -595,7 +596,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
                     }
                 }
             };
-            for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++iter) {
+            for (int tile = P.tile_begin + blockIdx.x; ok && tile < P.tile_end; tile += gridDim.x, ++iter) {
                 const Tile T = decode(P, s_grp, tile);
                 const GroupDesc &G = s_grp[T.gi];
                 int acc = P.nbuf == 2 ? (iter & 1) : 0;
@@ -774,8 +775,8 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
             return gn_inline ? ((16 * j) / cpg) % kHalves == half : j % kHalves == half;
         };
         int iter = 0;
-        int tile = blockIdx.x;
-        for (; tile < P.total_tiles; tile += gridDim.x, ++iter) {
+        int tile = P.tile_begin + blockIdx.x;
+        for (; tile < P.tile_end; tile += gridDim.x, ++iter) {
             const Tile T = decode(P, s_grp, tile);
             const GroupDesc &G = s_grp[T.gi];
             // SEG: the tile's earlier segments are added into the running sum here; a
@@ -1348,7 +1349,7 @@ __global__ void __launch_bounds__(EpiCfg<EPI>::threads, 1) convt3d_tc_gemm(const
         // loop early: it still meets that barrier once for every tile it did not
         // finish, so the partner never waits on a warp that has gone.
         if constexpr (sm && KEEP != 2 && kHalves > 1)
-            for (; tile < P.total_tiles; tile += gridDim.x)
+            for (; tile < P.tile_end; tile += gridDim.x)
                 asm volatile("bar.sync %0, %1;" ::"r"(1 + quarter), "r"(32 * kHalves) : "memory");
     }
 
@@ -1594,7 +1595,7 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
         int dev = 0, sms = 148;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        tc.grid = (int)(p.tiles < sms ? p.tiles : sms);
+        tc.grid = sms;
         tc.key[0] = tc.key[1] = tc.key[2] = tc.key[3] = nullptr;
         tc.ready = true;
     }
@@ -1652,7 +1653,7 @@ static cudaError_t tc_setup(convt3d_plan_s &p, TcCache &tc, const float *xs_hi, 
 
 cudaError_t launch_tc(convt3d_plan_s &p, const float *xs_hi, const float *xs_lo, const float *w_hi,
                       const float *w_lo, const float *bias, float *y, double *partials, uint32_t *status,
-                      cudaStream_t s) {
+                      int n0, int n1, cudaStream_t s) {
     static_assert(sizeof(TcParams) < 32000, "kernel parameter block too large");
     if (!p.tc_cache) {
         p.tc_cache = new (std::nothrow) TcCache();
@@ -1666,7 +1667,12 @@ cudaError_t launch_tc(convt3d_plan_s &p, const float *xs_hi, const float *xs_lo,
     tc.P.y = y;
     tc.P.partials = partials;
     tc.P.status = status;
-    tc.kern<<<tc.grid, tc.threads, tc.smem, s>>>(tc.P);
+    // the tiles of samples [n0, n1): tiles are ordered sample by sample
+    tc.P.tile_begin = n0 * tc.P.tiles_per_sample;
+    tc.P.tile_end = n1 * tc.P.tiles_per_sample;
+    const int count = tc.P.tile_end - tc.P.tile_begin;
+    if (count <= 0) return cudaSuccess;
+    tc.kern<<<count < tc.grid ? count : tc.grid, tc.threads, tc.smem, s>>>(tc.P);
     return cudaGetLastError();
 }
 
