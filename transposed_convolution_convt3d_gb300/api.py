@@ -296,9 +296,18 @@ class HostPipeline:
                     dv[name] = self.vec[name]
                 else:
                     dv[name] = None
+            params_in = torch.cuda.Event()
+            params_in.record(self.s_in[0])
+        # the weight is packed while the first chunk of x is still on its way in
+        comp = (self.s_comp, self.s_comp2) if self.ranges else (self.s_comp,)
+        comp[0].wait_event(params_in)
+        self.plan.pack_weights(self.w, self.ws, comp[0])
+        if len(comp) > 1:
+            packed = torch.cuda.Event()
+            packed.record(comp[0])
+            comp[1].wait_event(packed)
         # each chunk's compute is issued right after its copy, so that the GPU can start on
         # chunk 0 while the host is still issuing the later chunks
-        comp = (self.s_comp, self.s_comp2) if self.ranges else (self.s_comp,)
         for i in range(self.chunks):
             rows = slice(i * nc, (i + 1) * nc)
             s = comp[i % len(comp)]
@@ -308,12 +317,6 @@ class HostPipeline:
                     ev = torch.cuda.Event()
                     ev.record(self.s_in[j])
                 s.wait_event(ev)
-            if i == 0:
-                self.plan.pack_weights(self.w, self.ws, s)
-                if len(comp) > 1:
-                    packed = torch.cuda.Event()
-                    packed.record(s)
-                    comp[1].wait_event(packed)
             if self.ranges:
                 # training-mode BatchNorm: the ranges touch disjoint samples of x, y, the staged
                 # input and the per-tile statistics, so two of them may run at once on the two streams
