@@ -150,3 +150,27 @@ def test_host_pipeline_batchnorm_chunks(epilogue, chunks):
         assert_close(y_host.numpy(), ref, spec.name)
         assert_close(rm.cpu().numpy(), ref_rm, spec.name + " running_mean")
         assert_close(rv.cpu().numpy(), ref_rv, spec.name + " running_var")
+
+
+@pytest.mark.gpu
+def test_host_pipeline_batchnorm_uneven_ranges():
+    """Training-mode BatchNorm through HostPipeline with a batch the chunk count does not
+    divide (5 samples in ranges of 2 and 3): y and the running statistics against the oracle."""
+    spec = E.Spec("pipe_bn_uneven", N=5, Cin=12, Cout=16, D=3, H=4, W=5, k=3, bias=True,
+                  epilogue=E.EPI_SCALE_BATCHNORM_AVGPOOL, scale=1.25, seed_index=107)
+    inputs = E.make_inputs(spec)
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in inputs.items()}
+    dev = torch.device("cuda")
+    pipe = HostPipeline(spec.N, spec.Cin, spec.Cout, spec.D, spec.H, spec.W, spec.k, spec.stride, spec.pad,
+                        spec.out_pad, spec.bias, spec.epilogue, spec.groups, spec.eps, spec.scale, chunks=2)
+    assert pipe.chunks == 2
+    rm0, rv0 = E.make_running_stats(spec)
+    rm, rv = rm0.to(dev).clone(), rv0.to(dev).clone()
+    pipe.set_running_stats(rm, rv)
+    y_host = torch.full(pipe.full_shape, float("nan")).pin_memory()
+    pipe(host["x"], host["w"], y_host, host["bias"], host["gamma"], host["beta"])
+    torch.cuda.synchronize()
+    ref, ref_rm, ref_rv = run_oracle(spec, inputs, (rm0, rv0))
+    assert_close(y_host.numpy(), ref, spec.name)
+    assert_close(rm.cpu().numpy(), ref_rm, spec.name + " running_mean")
+    assert_close(rv.cpu().numpy(), ref_rv, spec.name + " running_var")

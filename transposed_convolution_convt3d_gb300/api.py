@@ -241,7 +241,8 @@ class HostPipeline:
                  io_fp16=False):
         # training-mode BatchNorm: one whole-batch plan run in sample ranges
         self.ranges = epilogue == EPI_SCALE_BATCHNORM_AVGPOOL
-        if N % chunks:
+        chunks = max(1, min(int(chunks), N))
+        if N % chunks and not self.ranges:  # chunk-sized plans need equal chunks; ranges need not
             chunks = 1
         args = (Cin, Cout, D, H, W, k, stride, pad, out_pad, bias, epilogue, groups, eps, scale, precision,
                 dilation, conv_groups, channels_last, io_bf16, io_fp16)
@@ -278,7 +279,7 @@ class HostPipeline:
         caller = stream if stream is not None else torch.cuda.current_stream()
         for s in self.s_in + self.s_out + [self.s_comp, self.s_comp2]:
             s.wait_stream(caller)
-        nc, k = self.n_chunk, self.copy_streams
+        nc, k, N = self.n_chunk, self.copy_streams, self.x.shape[0]
 
         def pieces(dst, src):  # the same k contiguous slices of two equally shaped tensors
             d, s_ = dst.view(-1), src.reshape(-1)
@@ -309,7 +310,8 @@ class HostPipeline:
         # each chunk's compute is issued right after its copy, so that the GPU can start on
         # chunk 0 while the host is still issuing the later chunks
         for i in range(self.chunks):
-            rows = slice(i * nc, (i + 1) * nc)
+            rows = slice(i * N // self.chunks, (i + 1) * N // self.chunks) if self.ranges else \
+                slice(i * nc, (i + 1) * nc)
             s = comp[i % len(comp)]
             for j, d, s_ in pieces(self.x[rows], x_host[rows]):
                 with torch.cuda.stream(self.s_in[j]):
