@@ -15,7 +15,8 @@ import torch
 
 import workloads as E
 from test_parity_gpu import PRECISIONS, assert_close, run_oracle
-from transposed_convolution_convt3d_gb300 import PREC_3XBF16, Convt3dError, HostPipeline, Plan
+from transposed_convolution_convt3d_gb300 import (PREC_3XBF16, PREC_BF16, PREC_FP16, Convt3dError, HostPipeline,
+                                                  Plan)
 
 CASES = [
     E.Spec("rng_bn_k5", N=3, Cin=20, Cout=32, D=4, H=6, W=5, k=5, bias=True,
@@ -37,6 +38,9 @@ def device_inputs(spec, inputs, dev):
     d = {k: (v.to(dev) if v is not None else None) for k, v in inputs.items()}
     if spec.channels_last:
         d["x"] = d["x"].permute(0, 2, 3, 4, 1).contiguous()
+    for flag, dt in ((spec.io_bf16, torch.bfloat16), (spec.io_fp16, torch.float16)):
+        if flag:  # x and w handed over as 16-bit tensors
+            d["x"], d["w"] = d["x"].to(dt), d["w"].to(dt)
     return d
 
 
@@ -174,3 +178,19 @@ def test_host_pipeline_batchnorm_uneven_ranges():
     assert_close(y_host.numpy(), ref, spec.name)
     assert_close(rm.cpu().numpy(), ref_rm, spec.name + " running_mean")
     assert_close(rv.cpu().numpy(), ref_rv, spec.name + " running_var")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["bf16", "fp16"])
+@pytest.mark.parametrize("spec", [CASES[0], CASES[2], CASES[4]], ids=lambda s: s.name)
+def test_sample_ranges_16bit_tensors(spec, kind):
+    """Ranges over 16-bit x and y (staging offsets in 2-byte elements): bitwise the one-call
+    forward, BatchNorm's running statistics included."""
+    s = spec.replace(name=spec.name + "_io" + kind, io_bf16=kind == "bf16", io_fp16=kind == "fp16")
+    prec = PREC_BF16 if kind == "bf16" else PREC_FP16
+    assert Plan.from_spec(s, precision=prec).info["main_kernel"] == 0
+    _, ((y1, st1), (y2, st2)) = run_both(s, prec, split_of(s.N))
+    assert np.all(np.isfinite(y1))
+    assert np.array_equal(y1, y2)
+    if st1 is not None:
+        assert np.array_equal(st1[0], st2[0]) and np.array_equal(st1[1], st2[1])
